@@ -1,0 +1,345 @@
+"""Float64 CPU oracle for SANATAN p=1 root-parity gated angular attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+module.  The product path (the CUDA library and its Python binding) never
+imports, links or calls anything here, and this module imports nothing from the
+product package: the two share no code.
+
+Every function is a plain, slow restatement of the method's definitions, taken
+from "SANATAN: Root-Parity Gated Angular Attention with an Exact Constant-State
+Recurrent Form" as summarised by its reading notes (page "SANATAN：根标签门控的
+角度核、精确递推与修订后的实验证据", cited below as *Notes*) and by the author's
+own post (cited as *Post*).  Section / equation numbers in brackets are those
+of the paper as the notes give them.
+
+Conventions (the readings taken where the pages leave a step open):
+  * Shapes: q, k [B, H, T, d]; v [B, H, T, dv]; gamma [H]; omega, phi [H, d].
+  * Positions are t = pos0 + i for the i-th token of the sequence.
+  * Feature index inside Phi is 6*a + c with channel order
+    c = 0..5 -> [1, cos th_rot, sin th_rot, r, r cos th_rot, r sin th_rot].
+  * The causal mask includes the current token (state update, then read).
+  * eps is added to the denominator in raw score units and defaults to 0.
+  * omega is shared by q and k of a head; phi (the rotation rate, lambda on
+    the pages) is a per-(head, dim) input, so any parameterisation of it
+    (0.01 tanh(lambda_raw), 10000^(-a/d), ...) happens before this module.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, invariants, brute force, finite differences and an independent
+torch float64 autograd).  None is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# Feature map: Notes §2.2-§2.3 [paper §§3.1-3.3, eqs. (2)-(6)]
+# ---------------------------------------------------------------------------
+
+N_CHANNELS = 6
+
+
+def squash(u):
+    """Angle squash theta = pi*u / (1 + |u|)  (Notes §2.2, eq. (2)).
+
+    Maps every real component into the open interval (-pi, pi); it is close
+    to pi*u near 0 and saturates towards +-pi for large |u|.
+    """
+    u = np.asarray(u, dtype=np.float64)
+    return np.pi * u / (1.0 + np.abs(u))
+
+
+def soft_root(theta, gamma, omega):
+    """Soft root label r = tanh(gamma*(cos(theta+omega) - sin(theta+omega)))
+    (Notes §2.2, eq. (3)).  ``theta`` is the content angle BEFORE the temporal
+    rotation: the label is not recomputed after the rotation (Notes §2.2,
+    the remark after eq. (4))."""
+    x = np.asarray(theta, dtype=np.float64) + omega
+    return np.tanh(gamma * (np.cos(x) - np.sin(x)))
+
+
+def rotate(theta, t, phi):
+    """Temporal rotation theta_rot = theta + t*phi  (Notes §2.2, eq. (4)).
+
+    ``t`` is an integer position, promoted exactly to float64; ``phi`` is the
+    per-dimension rate (lambda on the pages)."""
+    return np.asarray(theta, dtype=np.float64) + np.asarray(t, dtype=np.float64) * phi
+
+
+def features_from_angles(theta_rot, r):
+    """Six-channel block per dimension (Notes §2.3, eq. (6)):
+    [1, cos th_rot, sin th_rot, r, r cos th_rot, r sin th_rot], concatenated
+    over the dimensions so that channel c of dimension a sits at 6a + c."""
+    c = np.cos(theta_rot)
+    s = np.sin(theta_rot)
+    one = np.ones_like(c)
+    blk = np.stack([one, c, s, r, r * c, r * s], axis=-1)  # [..., d, 6]
+    return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * N_CHANNELS,))
+
+
+def positions(T, pos0):
+    """t = pos0 + i, i = 0..T-1 (integer valued, exact in float64)."""
+    return np.arange(T, dtype=np.int64) + np.int64(pos0)
+
+
+def featurize(u, gamma, omega, phi, pos0=0):
+    """Phi(u) for a [B, H, T, d] tensor of query or key components.
+
+    gamma [H], omega [H, d], phi [H, d]; returns float64 [B, H, T, 6d].
+    Steps: eq. (2) squash -> eq. (3) soft root from the un-rotated angle ->
+    eq. (4) rotation by t*phi -> eq. (6) six channels."""
+    u = np.asarray(u, dtype=np.float64)
+    B, H, T, d = u.shape
+    g = np.asarray(gamma, dtype=np.float64).reshape(1, H, 1, 1)
+    om = np.asarray(omega, dtype=np.float64).reshape(1, H, 1, d)
+    ph = np.asarray(phi, dtype=np.float64).reshape(1, H, 1, d)
+    t = positions(T, pos0).astype(np.float64).reshape(1, 1, T, 1)
+    theta = squash(u)
+    r = soft_root(theta, g, om)
+    th_rot = rotate(theta, t, ph)
+    return features_from_angles(th_rot, r)
+
+
+def pair_kernel(phi_q, phi_k):
+    """Score s = <Phi(q), Phi(k)> (Notes §2.3, eq. (7)); the pages show it
+    equals sum_a (1 + r_q r_k)(1 + cos(dtheta_a)), so 0 <= s <= 4d."""
+    return np.asarray(phi_q) @ np.asarray(phi_k).T
+
+
+# ---------------------------------------------------------------------------
+# p = 1 causal normalised attention: Notes §2.6-§2.7 [paper §§3.4-3.5,
+# eqs. (8)-(9)]
+# ---------------------------------------------------------------------------
+
+
+def _heads(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def attn_quadratic(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None):
+    """Parallel (quadratic) causal form at p = 1 (Notes §2.6, eq. (8) with p=1):
+
+        o_t = sum_{j<=t} s_tj v_j / (sum_{j<=t} s_tj + eps),  s_tj = Phi(q_t).Phi(k_j)
+
+    plus, when an initial state (S0 [B,H,6d,dv], z0 [B,H,6d]) is given, the
+    history it summarises: Phi(q_t).S0 is added to the numerator and
+    Phi(q_t).z0 to the denominator (Notes §2.7: the state is the sum of the
+    outer products of all earlier tokens).
+
+    Returns o [B,H,T,dv] and the denominator D [B,H,T] (without eps)."""
+    pq = featurize(q, gamma, omega, phi, pos0)
+    pk = featurize(k, gamma, omega, phi, pos0)
+    v = _heads(v)
+    B, H, T, _ = pq.shape
+    dv = v.shape[-1]
+    mask = np.tril(np.ones((T, T)))
+    o = np.zeros((B, H, T, dv))
+    D = np.zeros((B, H, T))
+    for b in range(B):
+        for h in range(H):
+            s = pair_kernel(pq[b, h], pk[b, h]) * mask
+            num = s @ v[b, h]
+            den = s.sum(axis=1)
+            if S0 is not None:
+                num = num + pq[b, h] @ _heads(S0)[b, h]
+                den = den + pq[b, h] @ _heads(z0)[b, h]
+            o[b, h] = num / (den + eps)[:, None]
+            D[b, h] = den
+    return o, D
+
+
+def attn_recurrent(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None):
+    """Constant-state recurrent form (Notes §2.7, eq. (9)):
+
+        S_t = S_{t-1} + Phi(k_t) v_t^T,   z_t = z_{t-1} + Phi(k_t),
+        o_t = Phi(q_t)^T S_t / (Phi(q_t)^T z_t + eps)
+
+    starting from zero (or from S0, z0).  The update precedes the read, which
+    is the j <= t mask.  Returns o, D, and the final S [B,H,6d,dv], z [B,H,6d].
+    """
+    pq = featurize(q, gamma, omega, phi, pos0)
+    pk = featurize(k, gamma, omega, phi, pos0)
+    v = _heads(v)
+    B, H, T, F = pq.shape
+    dv = v.shape[-1]
+    S = np.zeros((B, H, F, dv)) if S0 is None else _heads(S0).copy()
+    z = np.zeros((B, H, F)) if z0 is None else _heads(z0).copy()
+    o = np.zeros((B, H, T, dv))
+    D = np.zeros((B, H, T))
+    for t in range(T):
+        S += pk[:, :, t, :, None] * v[:, :, t, None, :]
+        z += pk[:, :, t, :]
+        num = np.einsum("bhf,bhfe->bhe", pq[:, :, t, :], S)
+        den = np.einsum("bhf,bhf->bh", pq[:, :, t, :], z)
+        o[:, :, t, :] = num / (den + eps)[..., None]
+        D[:, :, t] = den
+    return o, D, S, z
+
+
+def final_state(k, v, gamma, omega, phi, pos0=0, S0=None, z0=None):
+    """S_T = S0 + sum_t Phi(k_t) v_t^T and z_T = z0 + sum_t Phi(k_t)
+    (Notes §2.7: the definition of the state as a sum, written directly)."""
+    pk = featurize(k, gamma, omega, phi, pos0)
+    S = np.einsum("bhtf,bhte->bhfe", pk, _heads(v))
+    z = pk.sum(axis=2)
+    if S0 is not None:
+        S = S + _heads(S0)
+        z = z + _heads(z0)
+    return S, z
+
+
+def attn_rows(q, k, v, gamma, omega, phi, rows, pos0=0, eps=0.0, b=0, h=0):
+    """o_t and D_t of one (batch, head) at the selected row indices only,
+    each computed straight from the definition of eq. (8) at p = 1 over its
+    own causal prefix.  Used to check large problems one output at a time."""
+    q1 = _heads(q)[b:b + 1, h:h + 1]
+    k1 = _heads(k)[b:b + 1, h:h + 1]
+    v1 = _heads(v)[b, h]
+    g1 = np.asarray(gamma, dtype=np.float64)[h:h + 1]
+    om1 = np.asarray(omega, dtype=np.float64)[h:h + 1]
+    ph1 = np.asarray(phi, dtype=np.float64)[h:h + 1]
+    pk = featurize(k1, g1, om1, ph1, pos0)[0, 0]
+    out_o, out_D = [], []
+    for i in rows:
+        qi = q1[:, :, i:i + 1, :]
+        pqi = featurize(qi, g1, om1, ph1, pos0 + i)[0, 0, 0]
+        s = pk[: i + 1] @ pqi
+        den = s.sum()
+        out_o.append((s @ v1[: i + 1]) / (den + eps))
+        out_D.append(den)
+    return np.array(out_o), np.array(out_D)
+
+
+def decode_step(S, z, q, k, v, gamma, omega, phi, pos, eps=0.0):
+    """One token of the recurrence of eq. (9) for N independent slots.
+
+    S [N, 6d, dv], z [N, 6d]; q, k [N, d]; v [N, dv]; gamma [N];
+    omega, phi [N, d]; pos [N] integer positions.  Returns (S', z', o)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    N, d = q.shape
+    g = np.asarray(gamma, dtype=np.float64).reshape(N, 1)
+    om = np.asarray(omega, dtype=np.float64)
+    ph = np.asarray(phi, dtype=np.float64)
+    t = np.asarray(pos, dtype=np.int64).astype(np.float64).reshape(N, 1)
+
+    def phi_of(u):
+        th = squash(u)
+        return features_from_angles(rotate(th, t, ph), soft_root(th, g, om))
+
+    pq, pk = phi_of(q), phi_of(k)
+    S = _heads(S) + pk[:, :, None] * np.asarray(v, dtype=np.float64)[:, None, :]
+    z = _heads(z) + pk
+    num = np.einsum("nf,nfe->ne", pq, S)
+    den = np.einsum("nf,nf->n", pq, z)
+    return S, z, num / (den + eps)[:, None]
+
+
+# ---------------------------------------------------------------------------
+# Backward.  The pages give no gradient; this is the chain rule through
+# eqs. (2)-(4), (6) and (8) at p = 1, written for the quadratic causal form.
+# ---------------------------------------------------------------------------
+
+
+def _feature_parts(u, gamma, omega, phi, pos0):
+    u = np.asarray(u, dtype=np.float64)
+    B, H, T, d = u.shape
+    g = np.asarray(gamma, dtype=np.float64).reshape(1, H, 1, 1)
+    om = np.asarray(omega, dtype=np.float64).reshape(1, H, 1, d)
+    ph = np.asarray(phi, dtype=np.float64).reshape(1, H, 1, d)
+    t = positions(T, pos0).astype(np.float64).reshape(1, 1, T, 1)
+    theta = squash(u)
+    x = theta + om
+    gx = np.cos(x) - np.sin(x)            # the pre-tanh coefficient of eq. (3)
+    gpx = -np.sin(x) - np.cos(x)          # its derivative in theta (and omega)
+    r = np.tanh(g * gx)
+    th_rot = rotate(theta, t, ph)
+    return dict(u=u, g=g, gx=gx, gpx=gpx, r=r, c=np.cos(th_rot), s=np.sin(th_rot), t=t)
+
+
+def _feature_vjp(parts, dphi):
+    """Pull dPhi [B,H,T,6d] back to du and the parameter gradients."""
+    B, H, T, F = dphi.shape
+    d = F // N_CHANNELS
+    dp = dphi.reshape(B, H, T, d, N_CHANNELS)
+    r, c, s = parts["r"], parts["c"], parts["s"]
+    dc = dp[..., 1] + r * dp[..., 4]
+    ds = dp[..., 2] + r * dp[..., 5]
+    dr = dp[..., 3] + c * dp[..., 4] + s * dp[..., 5]
+    dth_rot = -s * dc + c * ds                       # d/dtheta of (cos, sin)
+    sech2 = 1.0 - r * r                              # tanh' = 1 - tanh^2
+    dpre = dr * sech2                                # grad of gamma*g(theta+omega)
+    dtheta = dth_rot + dpre * parts["g"] * parts["gpx"]
+    u = parts["u"]
+    du = dtheta * np.pi / (1.0 + np.abs(u)) ** 2     # d squash / du
+    dgamma = (dpre * parts["gx"]).sum(axis=(0, 2, 3))
+    domega = (dpre * parts["g"] * parts["gpx"]).sum(axis=(0, 2))
+    dphi_rate = (dth_rot * parts["t"]).sum(axis=(0, 2))
+    return du, dgamma, domega, dphi_rate
+
+
+def attn_backward(q, k, v, gamma, omega, phi, dO, pos0=0, eps=0.0, S0=None, z0=None):
+    """Gradients of sum(o * dO) for the quadratic form of ``attn_quadratic``.
+
+    With N_t = sum_j s_tj v_j (+ Phi(q_t) S0), D_t = sum_j s_tj (+ Phi(q_t) z0),
+    Dh_t = D_t + eps and o_t = N_t / Dh_t:
+        dN_t = dO_t / Dh_t,          dD_t = -(dO_t . o_t) / Dh_t,
+        ds_tj = [j <= t] (dN_t . v_j + dD_t),
+        dv_j = sum_t [j <= t] s_tj dN_t,
+        dPhi(q_t) = sum_j ds_tj Phi(k_j) (+ S0 dN_t + z0 dD_t),
+        dPhi(k_j) = sum_t ds_tj Phi(q_t),
+    then through the feature map.  Returns a dict with dq, dk, dv, dgamma,
+    domega and dphi (the rate gradient)."""
+    pq = featurize(q, gamma, omega, phi, pos0)
+    pk = featurize(k, gamma, omega, phi, pos0)
+    v = _heads(v)
+    dO = _heads(dO)
+    B, H, T, F = pq.shape
+    mask = np.tril(np.ones((T, T)))
+    dpq = np.zeros_like(pq)
+    dpk = np.zeros_like(pk)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            s = pair_kernel(pq[b, h], pk[b, h]) * mask
+            num = s @ v[b, h]
+            den = s.sum(axis=1)
+            if S0 is not None:
+                num = num + pq[b, h] @ _heads(S0)[b, h]
+                den = den + pq[b, h] @ _heads(z0)[b, h]
+            dh = den + eps
+            o = num / dh[:, None]
+            dN = dO[b, h] / dh[:, None]
+            dD = -(dO[b, h] * o).sum(axis=1) / dh
+            ds = (dN @ v[b, h].T + dD[:, None]) * mask
+            dv[b, h] = s.T @ dN
+            dpq[b, h] = ds @ pk[b, h]
+            if S0 is not None:
+                dpq[b, h] += dN @ _heads(S0)[b, h].T + np.outer(dD, _heads(z0)[b, h])
+            dpk[b, h] = ds.T @ pq[b, h]
+    dq, dg_q, dom_q, dph_q = _feature_vjp(_feature_parts(q, gamma, omega, phi, pos0), dpq)
+    dk, dg_k, dom_k, dph_k = _feature_vjp(_feature_parts(k, gamma, omega, phi, pos0), dpk)
+    return dict(dq=dq, dk=dk, dv=dv, dgamma=dg_q + dg_k, domega=dom_q + dom_k,
+                dphi=dph_q + dph_k)
+
+
+# ---------------------------------------------------------------------------
+# Memory accounting: Notes §4.5 [paper §4.4]
+# ---------------------------------------------------------------------------
+
+
+def state_bytes(layers, heads, d, dv, bytes_per_float=4):
+    """Recurrent state of one sequence: per head S (6d x dv) and z (6d)."""
+    return layers * heads * (6 * d * dv + 6 * d) * bytes_per_float
+
+
+def kv_cache_bytes(n, layers, model_dim, bytes_per_float=4):
+    """Softmax KV cache for context n: keys and values of every layer."""
+    return 2 * n * layers * model_dim * bytes_per_float
+
+
+def kv_crossover(layers, heads, d, dv, model_dim, bytes_per_float=4):
+    """Smallest integer context n whose KV cache is at least the state size."""
+    st = state_bytes(layers, heads, d, dv, bytes_per_float)
+    per_token = kv_cache_bytes(1, layers, model_dim, bytes_per_float)
+    return int(np.ceil(st / per_token))

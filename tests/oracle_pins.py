@@ -1,0 +1,330 @@
+"""Checks that pin the float64 oracle to facts fixed by the SANATAN pages and by
+mathematics, independently of the oracle's own code.
+
+Each ``check_*`` function raises AssertionError when the oracle disagrees.
+``test_oracle_pins.py`` runs them all; ``test_oracle_mutations.py`` plants
+plausible mistakes in the oracle and shows that at least one check fails for
+each, so a dropped term, a wrong sign or index, or a transposed operand does
+not go unnoticed.
+"""
+import math
+import os
+
+import numpy as np
+
+import oracle.sanatan_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+def _small_case(seed=0, B=1, H=2, T=9, d=3, dv=2, phi_scale=0.3):
+    g = _rng(seed)
+    return dict(
+        q=g.standard_normal((B, H, T, d)),
+        k=g.standard_normal((B, H, T, d)),
+        v=g.standard_normal((B, H, T, dv)),
+        gamma=g.uniform(1.0, 5.0, H),
+        omega=g.uniform(-math.pi, math.pi, (H, d)),
+        phi=g.uniform(0.0, phi_scale, (H, d)),
+    )
+
+
+# --------------------------------------------------------------------------
+# eq. (2): angle squash
+# --------------------------------------------------------------------------
+
+def check_squash_closed_forms():
+    # u = 0, +-1, +-1/3, 3 give 0, +-pi/2, +-pi/4, 3pi/4 (pi*u/(1+|u|) by hand)
+    u = np.array([0.0, 1.0, -1.0, 1.0 / 3.0, -1.0 / 3.0, 3.0])
+    want = np.array([0.0, math.pi / 2, -math.pi / 2, math.pi / 4, -math.pi / 4, 3 * math.pi / 4])
+    assert np.allclose(O.squash(u), want, rtol=0, atol=1e-15), O.squash(u)
+    # near the origin the map is pi*u to first order; it stays inside (-pi, pi)
+    x = np.array([1e-9, -1e-9])
+    assert np.allclose(O.squash(x) / x, math.pi, rtol=1e-8)
+    big = np.array([1e6, -1e6, 3e7])
+    th = O.squash(big)
+    assert np.all(np.abs(th) < math.pi) and np.allclose(np.abs(th), math.pi, rtol=1e-5)
+    grid = np.linspace(-20, 20, 4001)
+    assert np.all(np.diff(O.squash(grid)) > 0)  # strictly increasing
+
+
+# --------------------------------------------------------------------------
+# eq. (3): soft root label
+# --------------------------------------------------------------------------
+
+def check_soft_root_closed_forms():
+    th = np.linspace(-3.1, 3.1, 257)
+    for gamma in (0.5, 4.0, 10.0):
+        # with omega = pi/4 the coefficient is -sqrt(2) sin(theta)
+        r = O.soft_root(th, gamma, math.pi / 4)
+        assert np.allclose(r, np.tanh(-gamma * math.sqrt(2.0) * np.sin(th)), rtol=0, atol=1e-14)
+        # sign of the root is opposite to the sign of a nonzero theta in (-pi, pi)
+        nz = np.abs(th) > 1e-3
+        assert np.all(np.sign(r[nz]) == -np.sign(th[nz]))
+    # the root boundary: theta = pi/4 - omega (mod pi) gives r = 0
+    for omega in (-2.0, -0.3, 0.0, 0.7, 2.9):
+        for m in (-1, 0, 1):
+            b = math.pi / 4 - omega + m * math.pi
+            assert abs(O.soft_root(b, 7.0, omega)) < 1e-13
+    # omega -> omega + pi swaps every label (r -> -r)
+    om = np.linspace(-3, 3, 13)
+    a = O.soft_root(0.37, 3.0, om)
+    b = O.soft_root(0.37, 3.0, om + math.pi)
+    assert np.allclose(a, -b, atol=1e-13)
+    # a large gamma makes the root hard (+-1)
+    hard = O.soft_root(np.array([0.5, -0.5]), 200.0, math.pi / 4)
+    assert np.allclose(hard, [-1.0, 1.0], atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# eq. (6)-(7): six-channel features and the factorised kernel
+# --------------------------------------------------------------------------
+
+def check_feature_channels():
+    g = _rng(1)
+    th = g.uniform(-7, 7, (5, 4))
+    r = g.uniform(-1, 1, (5, 4))
+    f = O.features_from_angles(th, r).reshape(5, 4, 6)
+    assert np.all(f[..., 0] == 1.0)
+    assert np.allclose(f[..., 1], np.cos(th), atol=1e-15)
+    assert np.allclose(f[..., 2], np.sin(th), atol=1e-15)
+    assert np.allclose(f[..., 3], r, atol=1e-15)
+    assert np.allclose(f[..., 4], r * np.cos(th), atol=1e-15)
+    assert np.allclose(f[..., 5], r * np.sin(th), atol=1e-15)
+
+
+def check_factorisation_bruteforce():
+    """<Phi_a(q), Phi_a(k)> = (1 + r_q r_k)(1 + cos(th_q - th_k)) summed over a."""
+    g = _rng(2)
+    for d in (1, 2, 3, 5):
+        for _ in range(20):
+            tq, tk = g.uniform(-10, 10, d), g.uniform(-10, 10, d)
+            rq, rk = g.uniform(-1, 1, d), g.uniform(-1, 1, d)
+            fq = O.features_from_angles(tq, rq)
+            fk = O.features_from_angles(tk, rk)
+            got = float(O.pair_kernel(fq[None], fk[None])[0, 0])
+            want = sum((1 + rq[a] * rk[a]) * (1 + math.cos(tq[a] - tk[a])) for a in range(d))
+            assert abs(got - want) < 1e-12 * max(1.0, abs(want))
+            assert -1e-12 <= got <= 4 * d + 1e-12
+    # hard roots: the per-dimension gate is 0 (labels differ) or 2 (labels agree)
+    for rq, rk, gate in ((1, 1, 2), (-1, -1, 2), (1, -1, 0), (-1, 1, 0)):
+        f1 = O.features_from_angles(np.array([0.4]), np.array([float(rq)]))
+        f2 = O.features_from_angles(np.array([0.4]), np.array([float(rk)]))
+        assert abs(float(O.pair_kernel(f1[None], f2[None])[0, 0]) - gate * 2.0) < 1e-14
+
+
+def check_kernel_range_from_inputs():
+    c = _small_case(3, H=2, T=40, d=6)
+    pq = O.featurize(c["q"], c["gamma"], c["omega"], c["phi"])
+    pk = O.featurize(c["k"], c["gamma"], c["omega"], c["phi"])
+    for h in range(2):
+        s = O.pair_kernel(pq[0, h], pk[0, h])
+        assert s.min() >= -1e-12 and s.max() <= 4 * 6 + 1e-12
+
+
+# --------------------------------------------------------------------------
+# A worked example derived by hand from eqs. (2)-(4), (6), (8)-(9)
+# --------------------------------------------------------------------------
+
+def worked_example():
+    """d = 1, T = 2, gamma = 1, omega = pi/4, phi = pi/2, pos0 = 0.
+
+    u_q = (1/3, 1)   -> theta_q = (pi/4, pi/2)
+    u_k = (-1/3, 0)  -> theta_k = (-pi/4, 0)
+    roots from the UN-rotated angles, r = tanh(-sqrt(2) sin theta):
+      r_q = (tanh(-1), tanh(-sqrt 2)),  r_k = (tanh(1), 0)
+    rotated angles theta + t*pi/2: q -> (pi/4, pi), k -> (-pi/4, pi/2)
+      s_00 = (1 - tanh(1)^2) (1 + cos(pi/2))            = sech(1)^2
+      s_10 = (1 - tanh(sqrt 2) tanh(1)) (1 + cos(5pi/4)) = (1 - th2 th1)(1 - sqrt(2)/2)
+      s_11 = (1 + 0) (1 + cos(pi/2))                      = 1
+    v = (2, -1):  o_0 = 2,  o_1 = (2 s_10 - s_11) / (s_10 + s_11)
+    """
+    th1, th2 = math.tanh(1.0), math.tanh(math.sqrt(2.0))
+    s00 = 1.0 - th1 * th1
+    s10 = (1.0 - th2 * th1) * (1.0 - math.sqrt(2.0) / 2.0)
+    s11 = 1.0
+    inputs = dict(
+        q=np.array([1.0 / 3.0, 1.0]).reshape(1, 1, 2, 1),
+        k=np.array([-1.0 / 3.0, 0.0]).reshape(1, 1, 2, 1),
+        v=np.array([2.0, -1.0]).reshape(1, 1, 2, 1),
+        gamma=np.array([1.0]), omega=np.array([[math.pi / 4]]), phi=np.array([[math.pi / 2]]),
+    )
+    o = np.array([2.0, (2.0 * s10 - s11) / (s10 + s11)])
+    D = np.array([s00, s10 + s11])
+    return inputs, o, D, (s00, s10, s11)
+
+
+def check_worked_example():
+    inp, o_want, D_want, (s00, s10, s11) = worked_example()
+    pq = O.featurize(inp["q"], inp["gamma"], inp["omega"], inp["phi"])[0, 0]
+    pk = O.featurize(inp["k"], inp["gamma"], inp["omega"], inp["phi"])[0, 0]
+    s = O.pair_kernel(pq, pk)
+    assert abs(s[0, 0] - s00) < 1e-14 and abs(s[1, 0] - s10) < 1e-14 and abs(s[1, 1] - s11) < 1e-14
+    for fn in (O.attn_quadratic, O.attn_recurrent):
+        res = fn(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["omega"], inp["phi"])
+        assert np.allclose(res[0].ravel(), o_want, rtol=0, atol=1e-14), (fn.__name__, res[0].ravel())
+        assert np.allclose(res[1].ravel(), D_want, rtol=0, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# eq. (8)-(9): quadratic form, recurrent form and their invariants
+# --------------------------------------------------------------------------
+
+def check_quadratic_equals_recurrent():
+    for seed, eps, with_state in ((4, 0.0, False), (5, 0.37, False), (6, 0.0, True)):
+        c = _small_case(seed, B=2, H=2, T=11, d=3, dv=2)
+        S0 = z0 = None
+        if with_state:
+            S0, z0 = O.final_state(c["k"] * 0.5 + 0.1, c["v"][:, :, ::-1], c["gamma"], c["omega"],
+                                   c["phi"], pos0=-11)
+        a = O.attn_quadratic(**c, pos0=3, eps=eps, S0=S0, z0=z0)
+        b = O.attn_recurrent(**c, pos0=3, eps=eps, S0=S0, z0=z0)
+        assert np.allclose(a[0], b[0], rtol=1e-12, atol=1e-12)
+        assert np.allclose(a[1], b[1], rtol=1e-12, atol=1e-12)
+        S, z = O.final_state(c["k"], c["v"], c["gamma"], c["omega"], c["phi"], pos0=3, S0=S0, z0=z0)
+        assert np.allclose(S, b[2], rtol=1e-12, atol=1e-12) and np.allclose(z, b[3], rtol=1e-12, atol=1e-12)
+
+
+def check_single_token():
+    c = _small_case(7, B=2, H=3, T=1, d=4, dv=3)
+    o, D = O.attn_quadratic(**c)
+    assert np.allclose(o, c["v"], rtol=0, atol=1e-14)
+    o2, _, _, _ = O.attn_recurrent(**c)
+    assert np.allclose(o2, c["v"], rtol=0, atol=1e-14)
+    assert np.all(D > 0)
+
+
+def check_constant_values():
+    c = _small_case(8, B=1, H=2, T=17, d=3, dv=4)
+    c["v"] = np.broadcast_to(np.array([0.5, -2.0, 3.0, 1e-3]), c["v"].shape).copy()
+    o, _ = O.attn_quadratic(**c)
+    assert np.allclose(o, c["v"], rtol=1e-13, atol=1e-13)
+
+
+def check_relative_position():
+    c = _small_case(9, B=1, H=2, T=13, d=3, dv=2, phi_scale=0.9)
+    o_a, D_a = O.attn_quadratic(**c, pos0=0)
+    o_b, D_b = O.attn_quadratic(**c, pos0=12345)
+    assert np.allclose(o_a, o_b, rtol=1e-9, atol=1e-9) and np.allclose(D_a, D_b, rtol=1e-9, atol=1e-9)
+    # the state itself does depend on the absolute position
+    S_a, _ = O.final_state(c["k"], c["v"], c["gamma"], c["omega"], c["phi"], pos0=0)
+    S_b, _ = O.final_state(c["k"], c["v"], c["gamma"], c["omega"], c["phi"], pos0=12345)
+    assert not np.allclose(S_a, S_b)
+
+
+def check_state_channel_zero():
+    c = _small_case(10, B=2, H=2, T=23, d=5, dv=3)
+    _, _, S, z = O.attn_recurrent(**c)
+    d = 5
+    for a in range(d):
+        assert np.allclose(S[:, :, 6 * a, :], c["v"].sum(axis=2), rtol=1e-13, atol=1e-13)
+        assert np.allclose(z[:, :, 6 * a], 23.0, rtol=0, atol=1e-12)
+    # denominator positivity with soft roots
+    _, D = O.attn_quadratic(**c)
+    assert np.all(D > 0)
+
+
+def check_rows_and_decode():
+    c = _small_case(11, B=1, H=2, T=15, d=3, dv=2)
+    o, D = O.attn_quadratic(**c, pos0=5, eps=0.01)
+    rows = [0, 3, 14]
+    for h in range(2):
+        oo, dd = O.attn_rows(c["q"], c["k"], c["v"], c["gamma"], c["omega"], c["phi"], rows,
+                             pos0=5, eps=0.01, b=0, h=h)
+        assert np.allclose(oo, o[0, h, rows], rtol=1e-12, atol=1e-12)
+        assert np.allclose(dd, D[0, h, rows], rtol=1e-12, atol=1e-12)
+    # token-by-token decode over the sequence reproduces the recurrent form
+    H, F, dv = 2, 18, 2
+    S = np.zeros((H, F, dv))
+    z = np.zeros((H, F))
+    for t in range(15):
+        S, z, ot = O.decode_step(S, z, c["q"][0, :, t], c["k"][0, :, t], c["v"][0, :, t],
+                                 c["gamma"], c["omega"], c["phi"], np.full(H, 5 + t), eps=0.01)
+        assert np.allclose(ot, o[0, :, t], rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Backward: central finite differences in float64
+# --------------------------------------------------------------------------
+
+def _loss(c, dO, pos0, eps, S0, z0):
+    o, _ = O.attn_quadratic(c["q"], c["k"], c["v"], c["gamma"], c["omega"], c["phi"],
+                            pos0=pos0, eps=eps, S0=S0, z0=z0)
+    return float((o * dO).sum())
+
+
+def check_backward_finite_differences():
+    c = _small_case(12, B=1, H=2, T=7, d=2, dv=2, phi_scale=0.8)
+    g = _rng(13)
+    dO = g.standard_normal(c["v"].shape)
+    S0, z0 = O.final_state(g.standard_normal(c["k"].shape), g.standard_normal(c["v"].shape),
+                           c["gamma"], c["omega"], c["phi"], pos0=-7)
+    for pos0, eps, st in ((2, 0.0, False), (0, 0.25, True)):
+        S = S0 if st else None
+        Z = z0 if st else None
+        grads = O.attn_backward(c["q"], c["k"], c["v"], c["gamma"], c["omega"], c["phi"], dO,
+                                pos0=pos0, eps=eps, S0=S, z0=Z)
+        h = 1e-6
+        for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("gamma", "dgamma"),
+                            ("omega", "domega"), ("phi", "dphi")):
+            x = c[name]
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                old = x[idx]
+                x[idx] = old + h
+                lp = _loss(c, dO, pos0, eps, S, Z)
+                x[idx] = old - h
+                lm = _loss(c, dO, pos0, eps, S, Z)
+                x[idx] = old
+                num[idx] = (lp - lm) / (2 * h)
+            err = np.abs(num - grads[gname]).max() / max(1e-3, np.abs(num).max())
+            assert err < 1e-6, (name, err)
+
+
+# --------------------------------------------------------------------------
+# Memory accounting printed by the pages (golden fixture)
+# --------------------------------------------------------------------------
+
+def read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *vals = line.split()
+            out.setdefault(key, []).append([float(x) for x in vals])
+    return out
+
+
+def check_memory_accounting():
+    g = read_golden("memory_accounting.txt")
+    total = O.state_bytes(12, 12, 64, 64)
+    assert total == int(g["state_bytes_total"][0][0])
+    assert O.state_bytes(1, 1, 64, 64) == int(g["state_bytes_per_head"][0][0])
+    assert round(total / 1e6, 1) == g["state_mb_decimal"][0][0]
+    assert O.kv_crossover(12, 12, 64, 64, 768) == int(g["kv_crossover_n"][0][0])
+    for n, mb in g["kv_mb"]:
+        assert round(O.kv_cache_bytes(int(n), 12, 768) / 1e6, 1) == mb, (n, mb)
+
+
+ALL_CHECKS = [
+    check_squash_closed_forms,
+    check_soft_root_closed_forms,
+    check_feature_channels,
+    check_factorisation_bruteforce,
+    check_kernel_range_from_inputs,
+    check_worked_example,
+    check_quadratic_equals_recurrent,
+    check_single_token,
+    check_constant_values,
+    check_relative_position,
+    check_state_channel_zero,
+    check_rows_and_decode,
+    check_backward_finite_differences,
+    check_memory_accounting,
+]

@@ -1,0 +1,186 @@
+"""Plant plausible mistakes in the float64 oracle (on the CPU, through
+monkeypatching) and show that the pins of ``oracle_pins`` catch every one.
+
+A pin set that cannot tell the oracle from a subtly wrong variant would not
+pin it; each mutation below is a mistake that a transcription of the pages
+could plausibly make."""
+import numpy as np
+import pytest
+
+import oracle.sanatan_oracle as O
+import oracle_pins as P
+
+_orig = {n: getattr(O, n) for n in ("squash", "soft_root", "rotate", "features_from_angles",
+                                     "attn_quadratic", "attn_recurrent", "attn_backward",
+                                     "_feature_vjp", "state_bytes", "featurize")}
+
+
+def m_squash_no_abs(u):
+    u = np.asarray(u, dtype=np.float64)
+    return np.pi * u / (1.0 + u)
+
+
+def m_squash_square(u):
+    u = np.asarray(u, dtype=np.float64)
+    return np.pi * u / (1.0 + u * u)
+
+
+def m_root_sign(theta, gamma, omega):
+    x = np.asarray(theta, dtype=np.float64) + omega
+    return np.tanh(gamma * (np.sin(x) - np.cos(x)))
+
+
+def m_root_no_omega(theta, gamma, omega):
+    x = np.asarray(theta, dtype=np.float64)
+    return np.tanh(gamma * (np.cos(x) - np.sin(x)))
+
+
+def m_rotate_minus(theta, t, phi):
+    return np.asarray(theta, dtype=np.float64) - np.asarray(t, dtype=np.float64) * phi
+
+
+def m_rotate_scaled(theta, t, phi):
+    return np.asarray(theta, dtype=np.float64) + 2.0 * np.asarray(t, dtype=np.float64) * phi
+
+
+def m_features_dropped(theta_rot, r):
+    c, s = np.cos(theta_rot), np.sin(theta_rot)
+    blk = np.stack([np.ones_like(c), c, s, r, r * c, 0.0 * s], axis=-1)
+    return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * 6,))
+
+
+def m_features_swapped(theta_rot, r):
+    c, s = np.cos(theta_rot), np.sin(theta_rot)
+    blk = np.stack([np.ones_like(c), s, c, r, r * s, r * c], axis=-1)
+    return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * 6,))
+
+
+def m_featurize_root_after_rotation(u, gamma, omega, phi, pos0=0):
+    u = np.asarray(u, dtype=np.float64)
+    B, H, T, d = u.shape
+    g = np.asarray(gamma, dtype=np.float64).reshape(1, H, 1, 1)
+    om = np.asarray(omega, dtype=np.float64).reshape(1, H, 1, d)
+    ph = np.asarray(phi, dtype=np.float64).reshape(1, H, 1, d)
+    t = O.positions(T, pos0).astype(np.float64).reshape(1, 1, T, 1)
+    th_rot = O.rotate(O.squash(u), t, ph)
+    return O.features_from_angles(th_rot, O.soft_root(th_rot, g, om))
+
+
+def _quadratic_mask(offset):
+    def f(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None):
+        pq = O.featurize(q, gamma, omega, phi, pos0)
+        pk = O.featurize(k, gamma, omega, phi, pos0)
+        v = np.asarray(v, dtype=np.float64)
+        B, H, T, _ = pq.shape
+        mask = np.tril(np.ones((T, T)), offset)
+        o = np.zeros(v.shape[:3] + (v.shape[-1],))
+        D = np.zeros((B, H, T))
+        for b in range(B):
+            for h in range(H):
+                s = O.pair_kernel(pq[b, h], pk[b, h]) * mask
+                num, den = s @ v[b, h], s.sum(1)
+                if S0 is not None:
+                    num = num + pq[b, h] @ S0[b, h]
+                    den = den + pq[b, h] @ z0[b, h]
+                o[b, h] = num / (den + eps)[:, None]
+                D[b, h] = den
+        return o, D
+    return f
+
+
+def m_recurrent_read_first(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None):
+    pq = O.featurize(q, gamma, omega, phi, pos0)
+    pk = O.featurize(k, gamma, omega, phi, pos0)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, T, F = pq.shape
+    S = np.zeros((B, H, F, v.shape[-1])) if S0 is None else S0.copy()
+    z = np.zeros((B, H, F)) if z0 is None else z0.copy()
+    o = np.zeros((B, H, T, v.shape[-1]))
+    D = np.zeros((B, H, T))
+    for t in range(T):
+        num = np.einsum("bhf,bhfe->bhe", pq[:, :, t], S)
+        den = np.einsum("bhf,bhf->bh", pq[:, :, t], z)
+        o[:, :, t] = num / (den + eps + 1e-300)[..., None]
+        D[:, :, t] = den
+        S = S + pk[:, :, t, :, None] * v[:, :, t, None, :]
+        z = z + pk[:, :, t]
+    return o, D, S, z
+
+
+def m_eps_outside(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None):
+    o, D = _orig["attn_quadratic"](q, k, v, gamma, omega, phi, pos0, 0.0, S0, z0)
+    return o + eps, D
+
+
+def _vjp_mutant(kind):
+    def f(parts, dphi):
+        B, H, T, F = dphi.shape
+        d = F // 6
+        dp = dphi.reshape(B, H, T, d, 6)
+        r, c, s = parts["r"], parts["c"], parts["s"]
+        dc = dp[..., 1] + r * dp[..., 4]
+        ds = dp[..., 2] + r * dp[..., 5]
+        dr = dp[..., 3] + c * dp[..., 4] + s * dp[..., 5]
+        if kind == "rot_sign":
+            dth_rot = s * dc - c * ds
+        else:
+            dth_rot = -s * dc + c * ds
+        sech2 = 1.0 if kind == "no_sech2" else 1.0 - r * r
+        dpre = dr * sech2
+        dtheta = dth_rot + dpre * parts["g"] * parts["gpx"]
+        u = parts["u"]
+        if kind == "squash_deriv":
+            du = dtheta * np.pi / (1.0 + np.abs(u))
+        else:
+            du = dtheta * np.pi / (1.0 + np.abs(u)) ** 2
+        dgamma = (dpre * parts["gx"]).sum(axis=(0, 2, 3))
+        domega = (dpre * parts["g"] * parts["gpx"]).sum(axis=(0, 2))
+        dphi_rate = (dth_rot * parts["t"]).sum(axis=(0, 2))
+        return du, dgamma, domega, dphi_rate
+    return f
+
+
+def m_backward_sign_error(q, k, v, gamma, omega, phi, dO, pos0=0, eps=0.0, S0=None, z0=None):
+    # a sign slip on the upstream gradient everywhere but dv
+    g = _orig["attn_backward"](q, k, v, gamma, omega, phi, -np.asarray(dO), pos0, eps, S0, z0)
+    g["dv"] = -g["dv"]
+    return g
+
+
+def m_state_bytes_no_z(layers, heads, d, dv, bytes_per_float=4):
+    return layers * heads * (6 * d * dv) * bytes_per_float
+
+
+MUTANTS = {
+    "squash_no_abs": ("squash", m_squash_no_abs),
+    "squash_square": ("squash", m_squash_square),
+    "root_sign": ("soft_root", m_root_sign),
+    "root_no_omega": ("soft_root", m_root_no_omega),
+    "rotate_minus": ("rotate", m_rotate_minus),
+    "rotate_scaled": ("rotate", m_rotate_scaled),
+    "features_dropped_channel": ("features_from_angles", m_features_dropped),
+    "features_swapped_cos_sin": ("features_from_angles", m_features_swapped),
+    "root_from_rotated_angle": ("featurize", m_featurize_root_after_rotation),
+    "mask_strict": ("attn_quadratic", _quadratic_mask(-1)),
+    "mask_one_future": ("attn_quadratic", _quadratic_mask(1)),
+    "recurrent_read_before_write": ("attn_recurrent", m_recurrent_read_first),
+    "eps_outside_ratio": ("attn_quadratic", m_eps_outside),
+    "vjp_rotation_sign": ("_feature_vjp", _vjp_mutant("rot_sign")),
+    "vjp_missing_sech2": ("_feature_vjp", _vjp_mutant("no_sech2")),
+    "vjp_squash_derivative": ("_feature_vjp", _vjp_mutant("squash_deriv")),
+    "backward_flipped_upstream": ("attn_backward", m_backward_sign_error),
+    "state_bytes_without_z": ("state_bytes", m_state_bytes_no_z),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutation_is_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(O, attr, fn)
+    caught = []
+    for check in P.ALL_CHECKS:
+        try:
+            check()
+        except (AssertionError, FloatingPointError, ZeroDivisionError, ValueError):
+            caught.append(check.__name__)
+    assert caught, f"no pin detects the planted mistake {name}"
