@@ -1,0 +1,151 @@
+// C ABI of libsanatan.so: host-side validation and dispatch (see sanatan.h).
+#include <cstdint>
+#include <cstring>
+
+#include "sanatan_internal.h"
+
+namespace {
+
+using namespace sanatan;
+
+constexpr int kAbiVersion = 1;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+bool ok_nullable(const void* p) { return p == nullptr || aligned16(p); }
+bool ok_dtype(int t) { return t == SANATAN_F32 || t == SANATAN_BF16; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? SANATAN_OK : SANATAN_ERR_CUDA; }
+
+// The kernels are built for sm_103a only; refuse any other device before a
+// launch could fail with "no kernel image".
+int check_arch() {
+  static int cached[64];  // 0 unknown, 1 ok, 2 wrong arch
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SANATAN_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && cached[dev] != 0) return cached[dev] == 1 ? SANATAN_OK : SANATAN_ERR_ARCH;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return SANATAN_ERR_CUDA;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) cached[dev] = ok ? 1 : 2;
+  return ok ? SANATAN_OK : SANATAN_ERR_ARCH;
+}
+
+int check_sizes(int B, int H, int T, int d, int dv) {
+  if (B < 0 || H < 0 || T < 0 || d < 0 || dv < 0) return SANATAN_ERR_INVALID;
+  if (d != 64 || dv != 64) return SANATAN_ERR_UNSUPPORTED;
+  // Element counts index with 64-bit arithmetic; CTA counts must fit a grid.
+  if (static_cast<int64_t>(B) * H > (1LL << 31) - 1) return SANATAN_ERR_UNSUPPORTED;
+  return SANATAN_OK;
+}
+
+int check_params(const float* gamma, const float* omega, const float* phi) {
+  if (!ok_ptr(gamma) || !ok_ptr(omega) || !ok_ptr(phi)) return SANATAN_ERR_INVALID;
+  return SANATAN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sanatan_status_string(int status) {
+  switch (status) {
+    case SANATAN_OK: return "ok";
+    case SANATAN_ERR_INVALID: return "invalid argument (null or misaligned pointer, negative size, bad enum)";
+    case SANATAN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case SANATAN_ERR_CUDA: return "CUDA runtime error";
+    case SANATAN_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case SANATAN_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int sanatan_abi_version(void) { return kAbiVersion; }
+
+size_t sanatan_state_bytes(int layers, int heads, int d, int dv) {
+  if (layers < 0 || heads < 0 || d < 0 || dv < 0) return 0;
+  return static_cast<size_t>(layers) * heads * (6ull * d * dv + 6ull * d) * sizeof(float);
+}
+
+int sanatan_featurize(const void* u, int u_dtype, const float* gamma, const float* omega,
+                      const float* phi, int B, int H, int T, int d, int64_t pos0, void* out,
+                      int out_dtype, void* stream) {
+  if (!ok_dtype(u_dtype) || !ok_dtype(out_dtype)) return SANATAN_ERR_INVALID;
+  if (B < 0 || H < 0 || T < 0 || d <= 0) return SANATAN_ERR_INVALID;
+  if (d != 64) return SANATAN_ERR_UNSUPPORTED;
+  const int64_t n = static_cast<int64_t>(B) * H * T;
+  if (n == 0) return SANATAN_OK;
+  if (!ok_ptr(u) || !ok_ptr(out)) return SANATAN_ERR_INVALID;
+  if (int s = check_params(gamma, omega, phi)) return s;
+  if (n * d / 256 + 1 > 0x7fffffffLL) return SANATAN_ERR_UNSUPPORTED;
+  if (int s = check_arch()) return s;
+  return from_cuda(featurize_launch(u, u_dtype, gamma, omega, phi, B, H, T, d, pos0, out,
+                                    out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+size_t sanatan_chunk_fwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype) {
+  (void)B; (void)H; (void)T; (void)d; (void)dv; (void)in_dtype;
+  return 0;
+}
+
+int sanatan_chunk_fwd(const void* q, const void* k, const void* v, int in_dtype,
+                      const float* gamma, const float* omega, const float* phi, int B, int H,
+                      int T, int d, int dv, int64_t pos0, float eps, const float* S0,
+                      const float* z0, float* o, float* D, float* S_out, float* z_out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ok_dtype(in_dtype)) return SANATAN_ERR_INVALID;
+  if (int s = check_sizes(B, H, T, d, dv)) return s;
+  if ((S0 == nullptr) != (z0 == nullptr)) return SANATAN_ERR_INVALID;
+  if ((S_out == nullptr) != (z_out == nullptr)) return SANATAN_ERR_INVALID;
+  if (!ok_nullable(S0) || !ok_nullable(z0) || !ok_nullable(S_out) || !ok_nullable(z_out) ||
+      !ok_nullable(D) || !ok_nullable(workspace))
+    return SANATAN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * H == 0) return SANATAN_OK;
+  if (T > 0 && (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(o))) return SANATAN_ERR_INVALID;
+  if (int s = check_params(gamma, omega, phi)) return s;
+  if (workspace_bytes < sanatan_chunk_fwd_workspace_size(B, H, T, d, dv, in_dtype))
+    return SANATAN_ERR_INVALID;
+  if (int s = check_arch()) return s;
+  ChunkFwdArgs a{q, k, v, in_dtype, gamma, omega, phi, B, H, T, d, dv, pos0, eps,
+                 S0, z0, o, D, S_out, z_out, workspace, workspace_bytes};
+  return from_cuda(chunk_fwd_simt_launch(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t sanatan_chunk_bwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype) {
+  (void)B; (void)H; (void)T; (void)d; (void)dv; (void)in_dtype;
+  return 0;
+}
+
+int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
+                      const float* gamma, const float* omega, const float* phi, int B, int H,
+                      int T, int d, int dv, int64_t pos0, float eps, const float* S0,
+                      const float* z0, const float* o, const float* D, const void* dO,
+                      int grad_dtype, void* dq, void* dk, void* dv_out, float* dgamma,
+                      float* domega, float* dphi, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  (void)q; (void)k; (void)v; (void)in_dtype; (void)gamma; (void)omega; (void)phi; (void)B;
+  (void)H; (void)T; (void)d; (void)dv; (void)pos0; (void)eps; (void)S0; (void)z0; (void)o;
+  (void)D; (void)dO; (void)grad_dtype; (void)dq; (void)dk; (void)dv_out; (void)dgamma;
+  (void)domega; (void)dphi; (void)workspace; (void)workspace_bytes; (void)stream;
+  return SANATAN_ERR_UNSUPPORTED;
+}
+
+int sanatan_decode_step(float* S, float* z, const float* q, const float* k, const float* v,
+                        const float* gamma, const float* omega, const float* phi,
+                        const int64_t* pos, int N, int G, int d, int dv, float eps, float* o,
+                        void* stream) {
+  if (N < 0 || G <= 0 || d < 0 || dv < 0) return SANATAN_ERR_INVALID;
+  if (d != 64 || dv != 64) return SANATAN_ERR_UNSUPPORTED;
+  if (N == 0) return SANATAN_OK;
+  if (!ok_ptr(S) || !ok_ptr(z) || !ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(pos) ||
+      !ok_ptr(o))
+    return SANATAN_ERR_INVALID;
+  if (int s = check_params(gamma, omega, phi)) return s;
+  if (int s = check_arch()) return s;
+  return from_cuda(decode_step_launch(S, z, q, k, v, gamma, omega, phi, pos, N, G, eps, o,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// Internal launch interfaces between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sanatan.h"
+
+namespace sanatan {
+
+struct ChunkFwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int in_dtype;
+  const float* gamma;
+  const float* omega;
+  const float* phi;
+  int B, H, T, d, dv;
+  int64_t pos0;
+  float eps;
+  const float* S0;
+  const float* z0;
+  float* o;
+  float* D;
+  float* S_out;
+  float* z_out;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+struct ChunkBwdArgs {
+  ChunkFwdArgs f;
+  const float* o;
+  const float* Dn;
+  const void* dO;
+  int grad_dtype;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dgamma;
+  float* domega;
+  float* dphi;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+cudaError_t featurize_launch(const void* u, int u_dtype, const float* gamma, const float* omega,
+                             const float* phi, int B, int H, int T, int d, int64_t pos0,
+                             void* out, int out_dtype, cudaStream_t st);
+
+cudaError_t decode_step_launch(float* S, float* z, const float* q, const float* k,
+                               const float* v, const float* gamma, const float* omega,
+                               const float* phi, const int64_t* pos, int N, int G, float eps,
+                               float* o, cudaStream_t st);
+
+size_t chunk_fwd_simt_smem_bytes();
+cudaError_t chunk_fwd_simt_launch(const ChunkFwdArgs& a, cudaStream_t st);
+
+}  // namespace sanatan

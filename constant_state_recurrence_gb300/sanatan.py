@@ -1,0 +1,244 @@
+"""Thin ctypes binding of libsanatan.so (C ABI declared in include/sanatan.h).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and the current CUDA
+stream.  The library is loaded on first use; if it has not been built, every
+call raises RuntimeError (there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libsanatan.so")
+
+SANATAN_F32 = 0
+SANATAN_BF16 = 1
+_DT = {torch.float32: SANATAN_F32, torch.bfloat16: SANATAN_BF16}
+
+_c_int, _c_i64, _c_f, _c_sz, _c_p = (ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                     ctypes.c_size_t, ctypes.c_void_p)
+
+_SIGS = {
+    "sanatan_status_string": (ctypes.c_char_p, [_c_int]),
+    "sanatan_abi_version": (_c_int, []),
+    "sanatan_state_bytes": (_c_sz, [_c_int] * 4),
+    "sanatan_featurize": (_c_int, [_c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
+                                   _c_i64, _c_p, _c_int, _c_p]),
+    "sanatan_chunk_fwd_workspace_size": (_c_sz, [_c_int] * 6),
+    "sanatan_chunk_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int,
+                                   _c_int, _c_int, _c_int, _c_i64, _c_f, _c_p, _c_p, _c_p, _c_p,
+                                   _c_p, _c_p, _c_p, _c_sz, _c_p]),
+    "sanatan_chunk_bwd_workspace_size": (_c_sz, [_c_int] * 6),
+    "sanatan_chunk_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int,
+                                   _c_int, _c_int, _c_int, _c_i64, _c_f, _c_p, _c_p, _c_p, _c_p,
+                                   _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_sz,
+                                   _c_p]),
+    "sanatan_decode_step": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int,
+                                     _c_int, _c_int, _c_int, _c_f, _c_p, _c_p]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library with argument types set (raises if not built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with "
+                        "`python -m constant_state_recurrence_gb300.build` (there is no fallback)")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in _SIGS.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+class SanatanError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        msg = lib().sanatan_status_string(status).decode()
+        super().__init__(f"{fn} failed with status {status}: {msg}")
+
+
+def _check(fn, status):
+    if status != 0:
+        raise SanatanError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(dev):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _need(t, name, dtypes=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def state_bytes(layers, heads, d=64, dv=64):
+    return int(lib().sanatan_state_bytes(layers, heads, d, dv))
+
+
+def sanatan_featurize(u, gamma, omega, phi, pos0=0, out_dtype=None, out=None):
+    """Phi(u) [B, H, T, 6d] (index 6a + c) for u [B, H, T, d]."""
+    _need(u, "u", (torch.float32, torch.bfloat16))
+    B, H, T, d = u.shape
+    odt = out_dtype or torch.float32
+    if out is None:
+        out = torch.empty(B, H, T, 6 * d, dtype=odt, device=u.device)
+    _need(out, "out", (torch.float32, torch.bfloat16), (B, H, T, 6 * d))
+    for n, t in (("gamma", gamma), ("omega", omega), ("phi", phi)):
+        _need(t, n, (torch.float32,))
+    st = lib().sanatan_featurize(_ptr(u), _DT[u.dtype], _ptr(gamma), _ptr(omega), _ptr(phi),
+                                 B, H, T, d, int(pos0), _ptr(out), _DT[out.dtype],
+                                 _stream(u.device))
+    _check("sanatan_featurize", st)
+    return out
+
+
+def chunk_fwd_workspace_size(B, H, T, d=64, dv=64, dtype=torch.bfloat16):
+    return int(lib().sanatan_chunk_fwd_workspace_size(B, H, T, d, dv, _DT[dtype]))
+
+
+def sanatan_chunk_fwd(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None,
+                      want_D=True, want_state=False, out=None, workspace=None):
+    """Causal p=1 attention over [B, H, T] sequences.
+
+    Returns (o [B,H,T,dv] f32, D [B,H,T] f32 or None, S [B,H,6d,dv] or None,
+    z [B,H,6d] or None)."""
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    B, H, T, d = q.shape
+    _need(k, "k", (q.dtype,), (B, H, T, d))
+    _need(v, "v", (q.dtype,))
+    dv = v.shape[-1]
+    _need(v, "v", (q.dtype,), (B, H, T, dv))
+    for n, t in (("gamma", gamma), ("omega", omega), ("phi", phi)):
+        _need(t, n, (torch.float32,))
+    dev = q.device
+    F = 6 * d
+    o = out if out is not None else torch.empty(B, H, T, dv, dtype=torch.float32, device=dev)
+    _need(o, "o", (torch.float32,), (B, H, T, dv))
+    D = torch.empty(B, H, T, dtype=torch.float32, device=dev) if want_D else None
+    S = z = None
+    if want_state:
+        S = torch.empty(B, H, F, dv, dtype=torch.float32, device=dev)
+        z = torch.empty(B, H, F, dtype=torch.float32, device=dev)
+    if S0 is not None:
+        _need(S0, "S0", (torch.float32,), (B, H, F, dv))
+        _need(z0, "z0", (torch.float32,), (B, H, F))
+    ws_size = int(lib().sanatan_chunk_fwd_workspace_size(B, H, T, d, dv, _DT[q.dtype]))
+    if workspace is None and ws_size > 0:
+        workspace = torch.empty(ws_size, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().sanatan_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(gamma),
+                                 _ptr(omega), _ptr(phi), B, H, T, d, dv, int(pos0), float(eps),
+                                 _ptr(S0), _ptr(z0), _ptr(o), _ptr(D), _ptr(S), _ptr(z),
+                                 _ptr(workspace), ws_bytes, _stream(dev))
+    _check("sanatan_chunk_fwd", st)
+    return o, D, S, z
+
+
+def chunk_bwd_workspace_size(B, H, T, d=64, dv=64, dtype=torch.bfloat16):
+    return int(lib().sanatan_chunk_bwd_workspace_size(B, H, T, d, dv, _DT[dtype]))
+
+
+def sanatan_chunk_bwd(q, k, v, gamma, omega, phi, o, D, dO, pos0=0, eps=0.0, S0=None, z0=None,
+                      want_dphi=False, workspace=None):
+    """Gradients of sum(o * dO): dict(dq, dk, dv, dgamma, domega, dphi)."""
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    _need(k, "k", (q.dtype,), (B, H, T, d))
+    _need(v, "v", (q.dtype,), (B, H, T, dv))
+    _need(o, "o", (torch.float32,), (B, H, T, dv))
+    _need(D, "D", (torch.float32,), (B, H, T))
+    _need(dO, "dO", (torch.float32, torch.bfloat16), (B, H, T, dv))
+    dev = q.device
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dvv = torch.empty_like(v)
+    dgamma = torch.empty(H, dtype=torch.float32, device=dev)
+    domega = torch.empty(H, d, dtype=torch.float32, device=dev)
+    dphi = torch.empty(H, d, dtype=torch.float32, device=dev) if want_dphi else None
+    ws_size = int(lib().sanatan_chunk_bwd_workspace_size(B, H, T, d, dv, _DT[q.dtype]))
+    if workspace is None and ws_size > 0:
+        workspace = torch.empty(ws_size, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().sanatan_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(gamma),
+                                 _ptr(omega), _ptr(phi), B, H, T, d, dv, int(pos0), float(eps),
+                                 _ptr(S0), _ptr(z0), _ptr(o), _ptr(D), _ptr(dO), _DT[dO.dtype],
+                                 _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(dgamma), _ptr(domega),
+                                 _ptr(dphi), _ptr(workspace), ws_bytes, _stream(dev))
+    _check("sanatan_chunk_bwd", st)
+    return dict(dq=dq, dk=dk, dv=dvv, dgamma=dgamma, domega=domega, dphi=dphi)
+
+
+def sanatan_decode_step(S, z, q, k, v, gamma, omega, phi, pos, eps=0.0, out=None):
+    """One decode token for N slots; S [N,6d,dv] and z [N,6d] are updated in
+    place.  Returns o [N, dv] f32."""
+    _need(q, "q", (torch.float32,))
+    N, d = q.shape
+    _need(k, "k", (torch.float32,), (N, d))
+    _need(v, "v", (torch.float32,))
+    dv = v.shape[-1]
+    F = 6 * d
+    _need(S, "S", (torch.float32,), (N, F, dv))
+    _need(z, "z", (torch.float32,), (N, F))
+    _need(pos, "pos", (torch.int64,), (N,))
+    G = gamma.shape[0]
+    _need(gamma, "gamma", (torch.float32,), (G,))
+    _need(omega, "omega", (torch.float32,), (G, d))
+    _need(phi, "phi", (torch.float32,), (G, d))
+    o = out if out is not None else torch.empty(N, dv, dtype=torch.float32, device=q.device)
+    _need(o, "o", (torch.float32,), (N, dv))
+    st = lib().sanatan_decode_step(_ptr(S), _ptr(z), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
+                                   _ptr(omega), _ptr(phi), _ptr(pos), N, G, d, dv, float(eps),
+                                   _ptr(o), _stream(q.device))
+    _check("sanatan_decode_step", st)
+    return o
+
+
+class SanatanAttention(torch.autograd.Function):
+    """autograd wrapper: forward = sanatan_chunk_fwd, backward = sanatan_chunk_bwd."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, gamma, omega, phi, pos0=0, eps=0.0):
+        o, D, _, _ = sanatan_chunk_fwd(q, k, v, gamma, omega, phi, pos0=pos0, eps=eps)
+        ctx.save_for_backward(q, k, v, gamma, omega, phi, o, D)
+        ctx.pos0, ctx.eps = pos0, eps
+        return o
+
+    @staticmethod
+    def backward(ctx, dO):
+        q, k, v, gamma, omega, phi, o, D = ctx.saved_tensors
+        g = sanatan_chunk_bwd(q, k, v, gamma, omega, phi, o, D, dO.contiguous(), pos0=ctx.pos0,
+                              eps=ctx.eps, want_dphi=True)
+        return g["dq"], g["dk"], g["dv"], g["dgamma"], g["domega"], g["dphi"], None, None

@@ -1,0 +1,157 @@
+/*
+ * sanatan.h -- C ABI of libsanatan.so: SANATAN p=1 root-parity gated angular
+ * attention on NVIDIA GB300 (sm_103a).
+ *
+ * The method is that of "SANATAN: Root-Parity Gated Angular Attention with an
+ * Exact Constant-State Recurrent Form" (B. Patel), as summarised by its reading
+ * notes (cited as "Notes") and the author's post.  Each query/key component u
+ * of a head becomes an angle theta = pi u / (1 + |u|) (Notes §2.2, eq. (2)); a
+ * soft root label r = tanh(gamma (cos(theta+omega) - sin(theta+omega))) is
+ * taken from that un-rotated angle (eq. (3)); the angle is rotated by
+ * t * phi_a (eq. (4)); the six channels
+ *     Phi_a = [1, cos theta_rot, sin theta_rot, r, r cos theta_rot, r sin theta_rot]
+ * are concatenated over the d dimensions (eq. (6), Notes §2.3).  Attention at
+ * p = 1 is causal and normalised (eq. (9), Notes §2.7):
+ *     S_t = S_{t-1} + Phi(k_t) v_t^T,   z_t = z_{t-1} + Phi(k_t),
+ *     o_t = Phi(q_t)^T S_t / (Phi(q_t)^T z_t + eps),
+ * the update preceding the read (the mask includes the current token).
+ *
+ * Conventions shared by every call
+ *  - Every pointer is DEVICE memory owned by the caller, unless stated.
+ *    The library allocates no device memory and keeps no state between calls
+ *    except cached device attributes.
+ *  - Tensors are dense and row-major (C order) with the shapes given below;
+ *    pointers must be 16-byte aligned (SANATAN_ERR_INVALID otherwise).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  No call synchronises the device; a status of SANATAN_OK means
+ *    the launches were enqueued without a launch error.
+ *  - Feature index inside the 6d axis is 6*a + c, channel order as above.
+ *  - Positions: token i of a sequence sits at t = pos0 + i.
+ *  - eps is added to the denominator in raw score units (default 0).
+ *  - gamma [H], omega [H, d], phi [H, d] are float32; omega is shared by q and k
+ *    of a head; phi is the per-dimension rotation rate.
+ *  - d = dv = 64 is the supported head size (SANATAN_ERR_UNSUPPORTED otherwise).
+ *  - Arguments are validated on the host before anything is launched; on an
+ *    error status nothing has been enqueued (except SANATAN_ERR_CUDA, which
+ *    reports a failed launch).
+ */
+#ifndef SANATAN_H_
+#define SANATAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SANATAN_API __attribute__((visibility("default")))
+#else
+#define SANATAN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum sanatan_status {
+  SANATAN_OK = 0,
+  SANATAN_ERR_INVALID = 1,     /* null/misaligned pointer, negative size, bad enum */
+  SANATAN_ERR_UNSUPPORTED = 2, /* a shape or dtype this build does not handle     */
+  SANATAN_ERR_CUDA = 3,        /* a CUDA runtime error (launch or attribute query) */
+  SANATAN_ERR_ARCH = 4,        /* the current device is not sm_103 / sm_100 family  */
+  SANATAN_ERR_TIMEOUT = 5      /* a device-side bounded wait gave up                */
+};
+
+/* Element types of q, k, v (and of dq, dk, dv, dO where stated). */
+enum sanatan_dtype { SANATAN_F32 = 0, SANATAN_BF16 = 1 };
+
+/* Human-readable text of a status code (static storage, never NULL). */
+SANATAN_API const char* sanatan_status_string(int status);
+
+/* ABI version of this library (increments when a signature changes). */
+SANATAN_API int sanatan_abi_version(void);
+
+/* Bytes of recurrent state of one sequence with `layers` x `heads` heads:
+ * per head S (6d x dv) and z (6d) float32 (Notes §4.5, paper §4.4:
+ * 12 x 12 x (6*64*64 + 6*64) x 4 = 14,376,960 bytes). Host-only arithmetic. */
+SANATAN_API size_t sanatan_state_bytes(int layers, int heads, int d, int dv);
+
+/*
+ * sanatan_featurize -- the feature map Phi of eqs. (2)-(6) (Notes §2.2-§2.3).
+ *   u       [B, H, T, d]   u_dtype (SANATAN_F32 or SANATAN_BF16)
+ *   gamma   [H] f32, omega [H, d] f32, phi [H, d] f32
+ *   out     [B, H, T, 6d]  out_dtype; out[..., 6a + c] is channel c of dim a
+ * Float32 output is computed with correctly rounded division and libm-grade
+ * sin/cos/tanh; bf16 output is the float32 value rounded to nearest even.
+ */
+SANATAN_API int sanatan_featurize(const void* u, int u_dtype, const float* gamma, const float* omega,
+                      const float* phi, int B, int H, int T, int d, int64_t pos0, void* out,
+                      int out_dtype, void* stream);
+
+/*
+ * sanatan_chunk_fwd -- causal normalised attention at p = 1 over whole
+ * sequences (eq. (9) evaluated chunk-parallel; the exact re-association of the
+ * sums in Notes §2.7), optionally continuing from a state (S0, z0).
+ *   q, k    [B, H, T, d]   in_dtype;   v [B, H, T, dv] in_dtype
+ *   S0      [B, H, 6d, dv] f32 or NULL (zero state); z0 [B, H, 6d] f32 or NULL
+ *           (S0 and z0 are both NULL or both non-NULL)
+ *   o       [B, H, T, dv]  f32 output
+ *   D       [B, H, T]      f32 output or NULL: the denominator Phi(q_t)^T z_t
+ *           (without eps), kept for the backward
+ *   S_out   [B, H, 6d, dv] f32 output or NULL: the state after token T-1
+ *   z_out   [B, H, 6d]     f32 output or NULL (both or neither with S_out)
+ *   workspace / workspace_bytes: device scratch of at least
+ *           sanatan_chunk_fwd_workspace_size(...) bytes (may be NULL if that
+ *           size is 0); its contents on entry do not matter.
+ * bf16 inputs run on the tensor cores (bf16 operands, f32 accumulation);
+ * f32 inputs run an all-f32 CUDA-core path.  T = 0 is valid and does nothing
+ * but copy (S0, z0) (or zeros) to (S_out, z_out).
+ */
+SANATAN_API size_t sanatan_chunk_fwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype);
+SANATAN_API int sanatan_chunk_fwd(const void* q, const void* k, const void* v, int in_dtype,
+                      const float* gamma, const float* omega, const float* phi, int B, int H,
+                      int T, int d, int dv, int64_t pos0, float eps, const float* S0,
+                      const float* z0, float* o, float* D, float* S_out, float* z_out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * sanatan_chunk_bwd -- gradients of sum(o * dO) for sanatan_chunk_fwd.
+ * The chain rule through eqs. (2)-(4), (6), (9); the pages give no backward.
+ *   q, k, v, gamma, omega, phi, sizes, pos0, eps, S0, z0: as for the forward
+ *   o       [B, H, T, dv] f32 and D [B, H, T] f32: the forward's outputs
+ *   dO      [B, H, T, dv] in grad_dtype (SANATAN_F32 or SANATAN_BF16)
+ *   dq, dk  [B, H, T, d]  in_dtype outputs;  dv_out [B, H, T, dv] in_dtype
+ *   dgamma  [H] f32 output, domega [H, d] f32 output (overwritten, summed over
+ *           the batch and both q and k), dphi [H, d] f32 output or NULL
+ *   workspace: at least sanatan_chunk_bwd_workspace_size(...) bytes.
+ */
+SANATAN_API size_t sanatan_chunk_bwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype);
+SANATAN_API int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
+                      const float* gamma, const float* omega, const float* phi, int B, int H,
+                      int T, int d, int dv, int64_t pos0, float eps, const float* S0,
+                      const float* z0, const float* o, const float* D, const void* dO,
+                      int grad_dtype, void* dq, void* dk, void* dv_out, float* dgamma,
+                      float* domega, float* dphi, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
+ * sanatan_decode_step -- one token of the constant-state recurrence of eq. (9)
+ * (Notes §2.7) for N independent state slots, updating the state IN PLACE.
+ *   S       [N, 6d, dv] f32, read and written;  z [N, 6d] f32, read and written
+ *   q, k    [N, d] f32;  v [N, dv] f32
+ *   gamma [G] f32, omega [G, d] f32, phi [G, d] f32: slot n uses row g = n % G
+ *           (G = layers x heads when slots are ordered sequence-major)
+ *   pos     [N] int64: the position t of this token in each slot's sequence
+ *   o       [N, dv] f32 output
+ * The state written is S + Phi(k) v^T, z + Phi(k); the read uses the updated
+ * state.
+ */
+SANATAN_API int sanatan_decode_step(float* S, float* z, const float* q, const float* k, const float* v,
+                        const float* gamma, const float* omega, const float* phi,
+                        const int64_t* pos, int N, int G, int d, int dv, float eps, float* o,
+                        void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SANATAN_H_ */
