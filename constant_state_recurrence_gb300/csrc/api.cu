@@ -86,8 +86,9 @@ int sanatan_featurize(const void* u, int u_dtype, const float* gamma, const floa
 }
 
 size_t sanatan_chunk_fwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype) {
-  (void)B; (void)H; (void)T; (void)d; (void)dv; (void)in_dtype;
-  return 0;
+  if (B < 0 || H < 0 || T < 0 || d != 64 || dv != 64) return 0;
+  if (in_dtype != SANATAN_BF16) return 0;
+  return chunk_fwd_tc_workspace_bytes(B, H, T);
 }
 
 int sanatan_chunk_fwd(const void* q, const void* k, const void* v, int in_dtype,
@@ -110,7 +111,9 @@ int sanatan_chunk_fwd(const void* q, const void* k, const void* v, int in_dtype,
   if (int s = check_arch()) return s;
   ChunkFwdArgs a{q, k, v, in_dtype, gamma, omega, phi, B, H, T, d, dv, pos0, eps,
                  S0, z0, o, D, S_out, z_out, workspace, workspace_bytes};
-  return from_cuda(chunk_fwd_simt_launch(a, static_cast<cudaStream_t>(stream)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (in_dtype == SANATAN_BF16) return from_cuda(chunk_fwd_tc_launch(a, st));
+  return from_cuda(chunk_fwd_simt_launch(a, st));
 }
 
 size_t sanatan_chunk_bwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype) {
@@ -130,6 +133,13 @@ int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
   (void)D; (void)dO; (void)grad_dtype; (void)dq; (void)dk; (void)dv_out; (void)dgamma;
   (void)domega; (void)dphi; (void)workspace; (void)workspace_bytes; (void)stream;
   return SANATAN_ERR_UNSUPPORTED;
+}
+
+int sanatan_device_status(void* stream) {
+  if (int s = check_arch()) return s;
+  const int h = tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
+  if (h < 0) return SANATAN_ERR_CUDA;
+  return h ? SANATAN_ERR_TIMEOUT : SANATAN_OK;
 }
 
 int sanatan_decode_step(float* S, float* z, const float* q, const float* k, const float* v,

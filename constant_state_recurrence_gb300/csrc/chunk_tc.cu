@@ -1,0 +1,751 @@
+// Chunked forward on the tensor cores (tcgen05 + TMEM), bf16 operands with
+// f32 accumulation, for sequences of bf16 q, k, v.
+//
+// The method (reading notes §2.3 and §2.7, paper eqs. (6), (7), (9)):
+//   o_t = Phi(q_t)^T S_t / (Phi(q_t)^T z_t + eps),  S_t = sum_{j<=t} Phi(k_j) v_j^T.
+// Per chunk of kC = 128 tokens this is evaluated as
+//   P      = PhiQ PhiK^T (+ the ones channel, below), masked to j <= t
+//   O_ext  = PhiQ [S | z]_prev + P [V | 1]     (columns 0..63: numerator, 64: denominator)
+//   [S|z] += PhiK^T [V | 1]
+// which is the recurrence re-associated by chunks (the sums are identical).
+//
+// Feature layout.  Channel 0 of every dimension is the constant 1, so its 64
+// features are the same for every token: they contribute exactly 64 to every
+// score and 64 * sum(v) to every numerator.  The tensor cores therefore see
+// only the 320 non-constant features, ordered channel-major
+// (f = (c-1)*64 + a for c = 1..5 = cos, sin, r, r cos, r sin); the constant
+// channel is added back in the epilogues.  The running sum of v and the token
+// count live in an extra state row (row 320) produced by a ones feature of
+// PhiK, so they accumulate in f32 on the tensor core with the rest of the
+// state.
+//
+// Roles (416 threads): warps 0-7 featurise q, k and stage v into shared
+// memory; warps 8-11 drain TMEM (mask + split the scores into bf16 hi/lo
+// parts, snapshot the state to bf16 for the next chunk, normalise and store
+// the outputs); one thread of warp 12 issues every tcgen05.mma.  All hand-offs
+// are mbarriers with bounded waits.
+//
+// Shared-memory operands use the canonical no-swizzle layout (8 x 16-byte
+// core matrices); TMEM holds P (128 cols), O_ext (80) and the f32 state
+// (3 tiles x 80).
+#include "sanatan_internal.h"
+#include "sanatan_math.cuh"
+#include "tc_ptx.cuh"
+
+namespace sanatan {
+
+__device__ int g_tc_error;  // set when a bounded wait gives up
+
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 64;
+constexpr int kC = 128;              // tokens per chunk (= MMA M)
+constexpr int kNF = 320;             // non-constant features
+constexpr int kSCRows = kNF + 1;     // + the [sum v | count] row
+constexpr int kSCCols = 80;          // compact state row stride (floats)
+constexpr int kXQ = 40 * 128;        // bytes per 8-token group of PhiQ
+constexpr int kXK = 41 * 128;        // PhiK: + the ones feature group (fg 40)
+constexpr int kNG = 9;               // stored 8-column groups of [V | 1 | 0]
+constexpr int kLBO_SV = kNG * 128;   // K-direction core stride of S'bf16 and V
+constexpr int kN = 80;               // N of the value-side products
+
+constexpr uint32_t kTP = 0;          // TMEM columns: P / P-tilde
+constexpr uint32_t kTO = 128;        // O_ext
+constexpr uint32_t kTS = 208;        // state tiles at 208, 288, 368
+constexpr uint32_t kTL = 448;         // low bf16 halves of P-tilde
+constexpr uint32_t kTmemCols = 512;
+
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + 16 * kXQ;
+constexpr int kOffS = kOffK + 16 * kXK;
+constexpr int kOffV = kOffS + 40 * kLBO_SV;
+// The MMAs read up to 128 B past S'bf16 and V (ignored padding columns); the
+// pad keeps those reads inside this layout and away from the mbarriers.
+constexpr int kOffMisc = kOffV + 16 * kLBO_SV + 128;
+
+enum Bar {
+  kFeatFull = 0, kPFull, kPTilde, kQFree, kStateDone, kPVDone, kSnapReady, kOFree, kDrain,
+  kNumBars
+};
+
+struct Misc {
+  uint64_t bar[kNumBars];
+  uint32_t tmem_base;
+  int abort_flag;
+  int pad[2];
+  float vs[68];      // state row 320 before the current chunk: sum v (64), count
+  float a0[68];      // constant-channel part of S0: sum_a S0[6a] (64), sum_a z0[6a]
+  float4 dimc[64];   // per dim: gamma*sqrt2*cos(omega+pi/4), gamma*sqrt2*sin(omega+pi/4),
+                     //          cos(8 phi), sin(8 phi)
+};
+constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
+static_assert(kSmemBytes <= 232448, "shared memory layout exceeds 227 KB");
+
+constexpr int kThreads = 416;
+constexpr int kFeatWarps = 8;
+constexpr int kEpiWarp0 = 8;
+constexpr int kMmaWarp = 12;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
+
+struct TcParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const float* gamma;
+  const float* omega;
+  const float* phi;
+  int H, T;
+  int64_t pos0;
+  float eps;
+  int nseg;         // segments per sequence
+  int seg_grid;     // CTAs per sequence in this launch
+  int nchunks;      // chunks per sequence
+  const float* init_sc;  // compact initial states [B*H][nseg][321][80] or null (zero)
+  const float* S0;       // full initial state (export of constant rows) or null
+  const float* z0;
+  float* o;
+  float* Dn;
+  float* S_out;
+  float* z_out;
+  float* delta_out;      // state-only mode: compact per-segment sums
+};
+
+__device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
+  if (*reinterpret_cast<volatile int*>(&m.abort_flag)) return false;
+  if (mbar_wait_bounded(&m.bar[b], parity, kWaitNs)) return true;
+  m.abort_flag = 1;
+  atomicOr(&g_tc_error, 1);
+  return false;
+}
+
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void feat_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+
+// Eight dimensions of one token: the five non-constant channels, packed as
+// bf16 pairs (out[c][j/2] holds dims j, j+1 of channel c).
+__device__ __forceinline__ void features8(uint4 raw, const float4* __restrict__ dimc,
+                                          const float (&cb)[8], const float (&sb)[8],
+                                          uint32_t (&out)[5][4]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    float ch[5][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = 2 * p + h;
+      const float u = __uint_as_float((h == 0 ? (w[p] << 16) : (w[p] & 0xffff0000u)));
+      const float th = kPi * __fdividef(u, 1.0f + fabsf(u));
+      float s, c;
+      __sincosf(th, &s, &c);
+      const float4 kc = dimc[j];
+      const float r = tanh_fast(fmaf(kc.x, c, -kc.y * s));
+      const float cr = fmaf(c, cb[j], -s * sb[j]);
+      const float sr = fmaf(s, cb[j], c * sb[j]);
+      ch[0][h] = cr;
+      ch[1][h] = sr;
+      ch[2][h] = r;
+      ch[3][h] = r * cr;
+      ch[4][h] = r * sr;
+    }
+#pragma unroll
+    for (int c = 0; c < 5; ++c) out[c][p] = pack_bf16x2(ch[c][0], ch[c][1]);
+  }
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+template <bool kStateOnly>
+__global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
+  const uint32_t sQ = smem_u32(smem + kOffQ);
+  const uint32_t sK = smem_u32(smem + kOffK);
+  const uint32_t sS = smem_u32(smem + kOffS);
+  const uint32_t sV = smem_u32(smem + kOffV);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int bh = blockIdx.x / prm.seg_grid;
+  const int seg = blockIdx.x % prm.seg_grid;
+  const int h = bh % prm.H;
+  const int c_begin = static_cast<int>(static_cast<int64_t>(seg) * prm.nchunks / prm.nseg);
+  const int c_end = static_cast<int>(static_cast<int64_t>(seg + 1) * prm.nchunks / prm.nseg);
+  const int nloc = c_end - c_begin;
+  const int64_t seq_row0 = static_cast<int64_t>(bh) * prm.T;  // first token row of the sequence
+  const bool last_seg = (seg == prm.nseg - 1);
+
+  if (warp == kMmaWarp) {
+    tmem_alloc(&m.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int b = 0; b < kNumBars; ++b) {
+      const uint32_t cnt = (b == kFeatFull) ? kFeatWarps
+                           : (b == kPTilde || b == kSnapReady || b == kOFree) ? 4u : 1u;
+      mbar_init(&m.bar[b], cnt);
+    }
+    m.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (tid < kD) {
+    const float g = prm.gamma[h] * 1.41421356237309515f;
+    float sw, cw;
+    sincosf(prm.omega[h * kD + tid] + 0.785398163397448310f, &sw, &cw);
+    float s8, c8;
+    sincosf(phase_mod_2pi(8, prm.phi[h * kD + tid]), &s8, &c8);
+    m.dimc[tid] = make_float4(g * cw, g * sw, c8, s8);
+  }
+  if (tid >= 64 && tid < 64 + 68) {
+    const int e = tid - 64;
+    float acc = 0.f;
+    if (prm.S0 != nullptr && e < 64) {
+      const float* s0 = prm.S0 + static_cast<int64_t>(bh) * 384 * 64;
+      for (int a = 0; a < kD; ++a) acc += s0[(6 * a) * 64 + e];
+    } else if (prm.z0 != nullptr && e == 64) {
+      const float* z0 = prm.z0 + static_cast<int64_t>(bh) * 384;
+      for (int a = 0; a < kD; ++a) acc += z0[6 * a];
+    }
+    m.a0[e] = acc;
+  }
+  // Constant part of [V | 1 | 0]: column 64 is one, 65..71 zero.
+  if (tid < 16 * 8) {
+    const int kg = tid >> 3, row = tid & 7;
+    st_shared_v4(sV + kg * kLBO_SV + 8 * 128 + row * 16, 0x3F80u, 0u, 0u, 0u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+
+  if (warp < kFeatWarps) {
+    // ------------------------------------------------------------ featuriser
+    const int r = lane & 7;
+    const int ag = (lane >> 3) + 4 * (warp & 1);      // dimension group (8 dims)
+    const int tq = 32 * (warp >> 1) + r;              // first of this thread's 4 tokens
+    const float4* dimc = &m.dimc[8 * ag];
+    const float* phi_h = prm.phi + h * kD + 8 * ag;
+    for (int ci = 0; ci < nloc; ++ci) {
+      const int chunk = c_begin + ci;
+      const int tok0 = chunk * kC;
+      float cb0[8], sb0[8];
+      {
+        const int64_t tabs = prm.pos0 + tok0 + tq;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) __sincosf(phase_mod_2pi(tabs, phi_h[j]), &sb0[j], &cb0[j]);
+      }
+      if constexpr (!kStateOnly) {
+        uint32_t qf[4][5][4];
+        float cb[8], sb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { cb[j] = cb0[j]; sb[j] = sb0[j]; }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = tq + 8 * i;
+          if (tok0 + t < prm.T) {
+            const uint4 raw = ldg_nc_v4(prm.q + (seq_row0 + tok0 + t) * kD + 8 * ag);
+            features8(raw, dimc, cb, sb, qf[i]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 5; ++c)
+#pragma unroll
+              for (int p = 0; p < 4; ++p) qf[i][c][p] = 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 kc = dimc[j];
+            const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
+            sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
+            cb[j] = nc;
+          }
+        }
+        if (ci > 0) wait_bar(m, kQFree, (ci - 1) & 1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = tq + 8 * i;
+          const uint32_t base = sQ + (t >> 3) * kXQ + (t & 7) * 16;
+#pragma unroll
+          for (int c = 0; c < 5; ++c)
+            st_shared_v4(base + (c * 8 + ag) * 128, qf[i][c][0], qf[i][c][1], qf[i][c][2],
+                         qf[i][c][3]);
+        }
+      }
+      // keys
+      if (ci > 0) wait_bar(m, kStateDone, (ci - 1) & 1);
+      {
+        float cb[8], sb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { cb[j] = cb0[j]; sb[j] = sb0[j]; }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = tq + 8 * i;
+          const bool valid = tok0 + t < prm.T;
+          uint32_t kf[5][4];
+          if (valid) {
+            const uint4 raw = ldg_nc_v4(prm.k + (seq_row0 + tok0 + t) * kD + 8 * ag);
+            features8(raw, dimc, cb, sb, kf);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 5; ++c)
+#pragma unroll
+              for (int p = 0; p < 4; ++p) kf[c][p] = 0u;
+          }
+          const uint32_t base = sK + (t >> 3) * kXK + (t & 7) * 16;
+#pragma unroll
+          for (int c = 0; c < 5; ++c)
+            st_shared_v4(base + (c * 8 + ag) * 128, kf[c][0], kf[c][1], kf[c][2], kf[c][3]);
+          if (ag == 0) st_shared_v4(base + 40 * 128, valid ? 0x3F80u : 0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 kc = dimc[j];
+            const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
+            sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
+            cb[j] = nc;
+          }
+        }
+      }
+      // values: 8 columns (dimension group ag) of each of the 4 tokens
+      if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = tq + 8 * i;
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (tok0 + t < prm.T) raw = ldg_nc_v4(prm.v + (seq_row0 + tok0 + t) * kD + 8 * ag);
+        st_shared_v4(sV + (t >> 3) * kLBO_SV + ag * 128 + (t & 7) * 16, raw.x, raw.y, raw.z,
+                     raw.w);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.bar[kFeatFull]);
+    }
+  } else if (warp < kMmaWarp) {
+    // ------------------------------------------------------------ TMEM epilogue
+    const int qd = warp - kEpiWarp0;           // TMEM lane quarter
+    const int row = 32 * qd + lane;            // TMEM lane = token row / feature row in tile
+    const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
+    // Initial state -> TMEM tiles (and the bf16 snapshot for the first chunk).
+    {
+      const float* src = nullptr;
+      if (prm.init_sc != nullptr)
+        src = prm.init_sc + (static_cast<int64_t>(bh) * prm.nseg + seg) * kSCRows * kSCCols;
+      for (int mt = 0; mt < 3; ++mt) {
+        const int f = mt * 128 + row;
+        if (mt == 2 && qd == 3) continue;  // rows 352..383 are never used
+        float val[80];
+#pragma unroll
+        for (int e = 0; e < 80; ++e) val[e] = 0.f;
+        if (src != nullptr && f < kSCRows) {
+          const float4* s4 = reinterpret_cast<const float4*>(src + f * kSCCols);
+#pragma unroll
+          for (int e4 = 0; e4 < 17; ++e4) {
+            const float4 x = s4[e4];
+            val[4 * e4] = x.x; val[4 * e4 + 1] = x.y; val[4 * e4 + 2] = x.z; val[4 * e4 + 3] = x.w;
+          }
+#pragma unroll
+          for (int e = 65; e < 68; ++e) val[e] = 0.f;
+        }
+#pragma unroll
+        for (int blk = 0; blk < 5; ++blk) {
+          uint32_t rr[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(val[16 * blk + i]);
+          tmem_st16(tmem + lane_off + kTS + mt * kN + 16 * blk, rr);
+        }
+        if constexpr (!kStateOnly) {
+          if (f < kNF) {
+            const uint32_t base = sS + (f >> 3) * kLBO_SV + (f & 7) * 16;
+#pragma unroll
+            for (int ng = 0; ng < kNG; ++ng)
+              st_shared_v4(base + ng * 128, pack_bf16x2(val[8 * ng], val[8 * ng + 1]),
+                           pack_bf16x2(val[8 * ng + 2], val[8 * ng + 3]),
+                           pack_bf16x2(val[8 * ng + 4], val[8 * ng + 5]),
+                           pack_bf16x2(val[8 * ng + 6], val[8 * ng + 7]));
+          } else if (f == kNF) {
+#pragma unroll
+            for (int e = 0; e < 65; ++e) m.vs[e] = val[e];
+          }
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      epi_sync();
+      if (lane == 0) {
+        mbar_arrive(&m.bar[kSnapReady]);
+        mbar_arrive(&m.bar[kOFree]);
+      }
+    }
+    if constexpr (!kStateOnly) {
+      for (int ci = 0; ci < nloc; ++ci) {
+        const int tok0 = (c_begin + ci) * kC;
+        // E1: mask the scores, add the constant channel, split into bf16 hi + lo.
+        // Keys are taken 32 at a time; the hi halves overwrite P in place (their
+        // columns hold keys that were already read), the lo halves go to kTL.
+        wait_bar(m, kPFull, ci & 1);
+        tc_fence_after();
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          uint32_t hi[16], lo[16];
+          if (b > qd) {  // every key of this block is after every row of this warp
+#pragma unroll
+            for (int i = 0; i < 16; ++i) { hi[i] = 0u; lo[i] = 0u; }
+          } else {
+            float p[32];
+            tmem_ld16(tmem + lane_off + kTP + 32 * b, *reinterpret_cast<float(*)[16]>(&p[0]));
+            tmem_ld16(tmem + lane_off + kTP + 32 * b + 16, *reinterpret_cast<float(*)[16]>(&p[16]));
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j0 = 32 * b + 2 * i;
+              const float x0 = (j0 <= row) ? p[2 * i] + 64.0f : 0.0f;
+              const float x1 = (j0 + 1 <= row) ? p[2 * i + 1] + 64.0f : 0.0f;
+              const uint32_t hpk = pack_bf16x2(x0, x1);
+              hi[i] = hpk;
+              lo[i] = pack_bf16x2(x0 - __uint_as_float(hpk << 16),
+                                  x1 - __uint_as_float(hpk & 0xffff0000u));
+            }
+          }
+          tmem_st16(tmem + lane_off + kTP + 16 * b, hi);
+          tmem_st16(tmem + lane_off + kTL + 16 * b, lo);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m.bar[kPTilde]);
+
+        // E3: outputs of this chunk (state row 320 in m.vs is still the pre-chunk one).
+        wait_bar(m, kPVDone, ci & 1);
+        tc_fence_after();
+        {
+          float ov[80];
+#pragma unroll
+          for (int blk = 0; blk < 5; ++blk) {
+            float x[16];
+            tmem_ld16(tmem + lane_off + kTO + 16 * blk, x);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[16 * blk + i] = x[i];
+          }
+          tmem_ld_wait();
+          const int64_t tok = tok0 + row;
+          if (tok < prm.T) {
+            const float den = ov[64] + 64.0f * m.vs[64] + m.a0[64];
+            const float inv = 1.0f / (den + prm.eps);
+            float4* orow = reinterpret_cast<float4*>(prm.o + (seq_row0 + tok) * kD);
+#pragma unroll
+            for (int e4 = 0; e4 < 16; ++e4) {
+              float4 y;
+              y.x = (ov[4 * e4 + 0] + 64.0f * m.vs[4 * e4 + 0] + m.a0[4 * e4 + 0]) * inv;
+              y.y = (ov[4 * e4 + 1] + 64.0f * m.vs[4 * e4 + 1] + m.a0[4 * e4 + 1]) * inv;
+              y.z = (ov[4 * e4 + 2] + 64.0f * m.vs[4 * e4 + 2] + m.a0[4 * e4 + 2]) * inv;
+              y.w = (ov[4 * e4 + 3] + 64.0f * m.vs[4 * e4 + 3] + m.a0[4 * e4 + 3]) * inv;
+              orow[e4] = y;
+            }
+            if (prm.Dn != nullptr) prm.Dn[seq_row0 + tok] = den;
+          }
+        }
+        tc_fence_before();
+        epi_sync();  // every epilogue thread is done with m.vs and O
+        if (lane == 0) mbar_arrive(&m.bar[kOFree]);
+
+        // E2: snapshot of the state after this chunk, for the next chunk.
+        wait_bar(m, kStateDone, ci & 1);
+        tc_fence_after();
+        if (ci + 1 < nloc) {
+          for (int mt = 0; mt < 3; ++mt) {
+            if (mt == 2 && qd >= 3) continue;
+            const int f = mt * 128 + row;
+            float val[72];
+#pragma unroll
+            for (int blk = 0; blk < 5; ++blk) {
+              float x[16];
+              tmem_ld16(tmem + lane_off + kTS + mt * kN + 16 * blk, x);
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (16 * blk + i < 72) val[16 * blk + i] = x[i];
+            }
+            tmem_ld_wait();
+            if (f < kNF) {
+              const uint32_t base = sS + (f >> 3) * kLBO_SV + (f & 7) * 16;
+#pragma unroll
+              for (int ng = 0; ng < kNG; ++ng)
+                st_shared_v4(base + ng * 128, pack_bf16x2(val[8 * ng], val[8 * ng + 1]),
+                             pack_bf16x2(val[8 * ng + 2], val[8 * ng + 3]),
+                             pack_bf16x2(val[8 * ng + 4], val[8 * ng + 5]),
+                             pack_bf16x2(val[8 * ng + 6], val[8 * ng + 7]));
+            } else if (f == kNF) {
+#pragma unroll
+              for (int e = 0; e < 65; ++e) m.vs[e] = val[e];
+            }
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          epi_sync();
+          if (lane == 0) mbar_arrive(&m.bar[kSnapReady]);
+        }
+      }
+    } else {
+      // One wait on the single-phase drain barrier: a wait on the last
+      // state_done phase could alias an earlier phase of the same parity.
+      wait_bar(m, kDrain, 0);
+      tc_fence_after();
+    }
+    // Final state of the segment: the sequence's S_out / z_out (last segment of
+    // a full pass) or the per-segment sums (state-only pass).
+    const bool want_export = kStateOnly ? (prm.delta_out != nullptr)
+                                        : (last_seg && prm.S_out != nullptr);
+    if (want_export) {
+      for (int mt = 0; mt < 3; ++mt) {
+        if (mt == 2 && qd >= 3) continue;
+        const int f = mt * 128 + row;
+        float val[80];
+#pragma unroll
+        for (int blk = 0; blk < 5; ++blk) {
+          float x[16];
+          tmem_ld16(tmem + lane_off + kTS + mt * kN + 16 * blk, x);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) val[16 * blk + i] = x[i];
+        }
+        tmem_ld_wait();
+        if (kStateOnly) {
+          if (f < kSCRows) {
+            float4* dst = reinterpret_cast<float4*>(
+                prm.delta_out + (static_cast<int64_t>(bh) * prm.nseg + seg) * kSCRows * kSCCols +
+                f * kSCCols);
+#pragma unroll
+            for (int e4 = 0; e4 < 17; ++e4)
+              dst[e4] = make_float4(val[4 * e4], val[4 * e4 + 1], val[4 * e4 + 2], val[4 * e4 + 3]);
+          }
+        } else {
+          if (f < kNF) {
+            const int c = f / kD + 1, a = f % kD;
+            float4* dst = reinterpret_cast<float4*>(prm.S_out + (static_cast<int64_t>(bh) * 384 +
+                                                                 6 * a + c) * 64);
+#pragma unroll
+            for (int e4 = 0; e4 < 16; ++e4)
+              dst[e4] = make_float4(val[4 * e4], val[4 * e4 + 1], val[4 * e4 + 2], val[4 * e4 + 3]);
+            prm.z_out[static_cast<int64_t>(bh) * 384 + 6 * a + c] = val[64];
+          } else if (f == kNF) {
+#pragma unroll
+            for (int e = 0; e < 65; ++e) m.vs[e] = val[e];
+          }
+        }
+      }
+      if (!kStateOnly) {
+        epi_sync();
+        // constant-channel rows: S0[6a] + sum v, z0[6a] + count
+        const int et = tid - 32 * kEpiWarp0;
+        for (int idx = et; idx < kD * 65; idx += 128) {
+          const int a = idx / 65, e = idx % 65;
+          const int64_t rowi = static_cast<int64_t>(bh) * 384 + 6 * a;
+          if (e < 64) {
+            const float base = prm.S0 ? prm.S0[rowi * 64 + e] : 0.f;
+            prm.S_out[rowi * 64 + e] = base + m.vs[e];
+          } else {
+            const float base = prm.z0 ? prm.z0[rowi] : 0.f;
+            prm.z_out[rowi] = base + m.vs[64];
+          }
+        }
+      }
+    }
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idQK = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idIN = idesc_bf16_f32(128, kN, false, true);
+    constexpr uint32_t idST = idesc_bf16_f32(128, kN, true, true);
+    constexpr uint32_t idPV = idesc_bf16_f32(128, kN, false, true);
+    for (int ci = 0; ci < nloc; ++ci) {
+      wait_bar(m, kFeatFull, ci & 1);
+      tc_fence_after();
+      if constexpr (!kStateOnly) {
+        for (int s = 0; s < 20; ++s)
+          mma_ss(tmem + kTP, smem_desc(sQ + s * 256, 128, kXQ), smem_desc(sK + s * 256, 128, kXK),
+                 idQK, s > 0);
+        mma_commit(&m.bar[kPFull]);
+        wait_bar(m, kSnapReady, ci & 1);  // bf16 state snapshot of the previous chunk
+        wait_bar(m, kOFree, ci & 1);      // previous outputs drained from TMEM
+        tc_fence_after();
+        for (int s = 0; s < 20; ++s)
+          mma_ss(tmem + kTO, smem_desc(sQ + s * 256, 128, kXQ),
+                 smem_desc(sS + s * 2 * kLBO_SV, kLBO_SV, 128), idIN, s > 0);
+        mma_commit(&m.bar[kQFree]);
+      } else if (ci == 0) {
+        wait_bar(m, kSnapReady, 0);  // initial state is in TMEM
+        tc_fence_after();
+      }
+      for (int mt = 0; mt < 3; ++mt)
+        for (int s = 0; s < 8; ++s)
+          mma_ss(tmem + kTS + mt * kN, smem_desc(sK + mt * 2048 + s * 2 * kXK, kXK, 128),
+                 smem_desc(sV + s * 2 * kLBO_SV, kLBO_SV, 128), idST, true);
+      mma_commit(&m.bar[kStateDone]);
+      if constexpr (!kStateOnly) {
+        wait_bar(m, kPTilde, ci & 1);
+        tc_fence_after();
+        for (int s = 0; s < 8; ++s) {
+          const uint64_t bd = smem_desc(sV + s * 2 * kLBO_SV, kLBO_SV, 128);
+          mma_ts(tmem + kTO, tmem + kTP + 8 * s, bd, idPV, true);
+          mma_ts(tmem + kTO, tmem + kTL + 8 * s, bd, idPV, true);
+        }
+      }
+      mma_commit(&m.bar[kPVDone]);
+    }
+    // Nothing may still be in flight when TMEM is released.
+    mma_commit(&m.bar[kDrain]);
+    wait_bar(m, kDrain, 0);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Exclusive scan over segments of the per-segment state sums, seeded with the
+// caller's initial state in compact form.  In place: W[bh][p] <- init_p.
+__global__ void __launch_bounds__(256) seg_scan_kernel(const float* __restrict__ S0,
+                                                       const float* __restrict__ z0,
+                                                       float* __restrict__ W, int nseg,
+                                                       int has_delta) {
+  const int bh = blockIdx.y;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= kSCRows * 65) return;
+  const int row = e / 65, col = e % 65;
+  float acc = 0.f;
+  if (S0 != nullptr && row < kNF) {
+    const int c = row / kD + 1, a = row % kD;
+    acc = (col < 64) ? S0[(static_cast<int64_t>(bh) * 384 + 6 * a + c) * 64 + col]
+                     : z0[static_cast<int64_t>(bh) * 384 + 6 * a + c];
+  }
+  float* w = W + static_cast<int64_t>(bh) * nseg * kSCRows * kSCCols + row * kSCCols + col;
+  for (int p = 0; p < nseg; ++p) {
+    float* cell = w + static_cast<int64_t>(p) * kSCRows * kSCCols;
+    const float d = (has_delta && p < nseg - 1) ? *cell : 0.f;
+    *cell = acc;
+    acc += d;
+  }
+}
+
+int sm_count() {
+  static int cached = 0;
+  if (cached == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      cached = n;
+    else
+      return 152;
+  }
+  return cached;
+}
+
+}  // namespace
+
+int tc_segments(int B, int H, int T) {
+  const int64_t bhn = static_cast<int64_t>(B) * H;
+  const int nchunks = (T + kC - 1) / kC;
+  if (bhn <= 0 || nchunks <= 1) return 1;
+  const int64_t per = sm_count() / bhn;
+  if (per <= 1) return 1;
+  return static_cast<int>(per < nchunks ? per : nchunks);
+}
+
+size_t chunk_fwd_tc_workspace_bytes(int B, int H, int T) {
+  const int nseg = tc_segments(B, H, T);
+  return static_cast<size_t>(B) * H * nseg * kSCRows * kSCCols * sizeof(float);
+}
+
+cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st) {
+  const int nchunks = (a.T + kC - 1) / kC;
+  const int nseg = tc_segments(a.B, a.H, a.T);
+  const int bhn = a.B * a.H;
+  float* W = static_cast<float*>(a.workspace);
+  const bool use_ws = (nseg > 1) || (a.S0 != nullptr);
+  {
+    cudaError_t e = cudaFuncSetAttribute(sanatan_tc_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(sanatan_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  TcParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.k = static_cast<const __nv_bfloat16*>(a.k);
+  p.v = static_cast<const __nv_bfloat16*>(a.v);
+  p.gamma = a.gamma;
+  p.omega = a.omega;
+  p.phi = a.phi;
+  p.H = a.H;
+  p.T = a.T;
+  p.pos0 = a.pos0;
+  p.eps = a.eps;
+  p.nseg = nseg;
+  p.nchunks = nchunks;
+  p.S0 = a.S0;
+  p.z0 = a.z0;
+  if (nseg > 1) {
+    TcParams d = p;
+    d.seg_grid = nseg - 1;  // the last segment's sum is never needed
+    d.delta_out = W;        // segment p of sequence bh -> W[bh][p]
+    d.init_sc = nullptr;
+    d.o = nullptr;
+    sanatan_tc_kernel<true><<<bhn * (nseg - 1), kThreads, kSmemBytes, st>>>(d);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (use_ws) {
+    dim3 grid((kSCRows * 65 + 255) / 256, bhn);
+    seg_scan_kernel<<<grid, 256, 0, st>>>(a.S0, a.z0, W, nseg, nseg > 1 ? 1 : 0);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  p.seg_grid = nseg;
+  p.init_sc = use_ws ? W : nullptr;
+  p.o = a.o;
+  p.Dn = a.D;
+  p.S_out = a.S_out;
+  p.z_out = a.z_out;
+  sanatan_tc_kernel<false><<<bhn * nseg, kThreads, kSmemBytes, st>>>(p);
+  return cudaGetLastError();
+}
+
+int tc_read_and_clear_error(cudaStream_t st) {
+  int h = 0;
+  if (cudaMemcpyFromSymbolAsync(&h, g_tc_error, sizeof(int), 0, cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return -1;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_tc_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) !=
+        cudaSuccess)
+      return -1;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+  }
+  return h;
+}
+
+}  // namespace sanatan

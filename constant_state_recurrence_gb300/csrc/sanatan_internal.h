@@ -58,3 +58,10 @@ size_t chunk_fwd_simt_smem_bytes();
 cudaError_t chunk_fwd_simt_launch(const ChunkFwdArgs& a, cudaStream_t st);
 
 }  // namespace sanatan
+
+namespace sanatan {
+int tc_segments(int B, int H, int T);
+size_t chunk_fwd_tc_workspace_bytes(int B, int H, int T);
+cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st);
+int tc_read_and_clear_error(cudaStream_t st);
+}  // namespace sanatan

@@ -38,6 +38,7 @@ _SIGS = {
                                    _c_int, _c_int, _c_int, _c_i64, _c_f, _c_p, _c_p, _c_p, _c_p,
                                    _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_sz,
                                    _c_p]),
+    "sanatan_device_status": (_c_int, [_c_p]),
     "sanatan_decode_step": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int,
                                      _c_int, _c_int, _c_int, _c_f, _c_p, _c_p]),
 }
@@ -101,6 +102,13 @@ def _need(t, name, dtypes=None, shape=None):
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     return t
+
+
+def device_status(device=None):
+    """Synchronise the current stream and raise if a kernel of the library gave
+    up a bounded device-side wait since the last check."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check("sanatan_device_status", lib().sanatan_device_status(_stream(dev)))
 
 
 def state_bytes(layers, heads, d=64, dv=64):

@@ -57,7 +57,7 @@ enum sanatan_status {
   SANATAN_ERR_INVALID = 1,     /* null/misaligned pointer, negative size, bad enum */
   SANATAN_ERR_UNSUPPORTED = 2, /* a shape or dtype this build does not handle     */
   SANATAN_ERR_CUDA = 3,        /* a CUDA runtime error (launch or attribute query) */
-  SANATAN_ERR_ARCH = 4,        /* the current device is not sm_103 / sm_100 family  */
+  SANATAN_ERR_ARCH = 4,        /* the current device is not sm_103 (GB300)          */
   SANATAN_ERR_TIMEOUT = 5      /* a device-side bounded wait gave up                */
 };
 
@@ -132,6 +132,15 @@ SANATAN_API int sanatan_chunk_bwd(const void* q, const void* k, const void* v, i
                       int grad_dtype, void* dq, void* dk, void* dv_out, float* dgamma,
                       float* domega, float* dphi, void* workspace, size_t workspace_bytes,
                       void* stream);
+
+/*
+ * sanatan_device_status -- synchronises `stream`, then reports whether any
+ * kernel of this library gave up a bounded device-side wait since the last
+ * call (SANATAN_ERR_TIMEOUT; the flag is cleared) or not (SANATAN_OK).  The
+ * tensor-core kernels never spin without a time limit: a lost hand-off makes
+ * them skip their remaining waits and return, with undefined outputs.
+ */
+SANATAN_API int sanatan_device_status(void* stream);
 
 /*
  * sanatan_decode_step -- one token of the constant-state recurrence of eq. (9)

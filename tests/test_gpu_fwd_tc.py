@@ -1,0 +1,118 @@
+"""The bf16 tensor-core chunked forward against the float64 oracle
+(max abs error <= 5e-3 on outputs: bf16 operands, f32 accumulation).
+
+The oracle consumes the same bf16-rounded inputs promoted to float64."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.sanatan_oracle as O
+from constant_state_recurrence_gb300 import sanatan as S
+from constant_state_recurrence_gb300 import workloads as W
+from gpu_util import dev, f64, max_abs, ref_args, rel_fro, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 5e-3      # outputs, max abs
+TOL_STATE = 5e-3     # emitted S, z: relative Frobenius
+TOL_DEN = 2e-3       # denominator, relative Frobenius
+
+
+def run(x, **kw):
+    g = to_dev(x)
+    out = S.sanatan_chunk_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"],
+                              want_state=True, **kw)
+    S.device_status()
+    return out
+
+
+def check_full(x, pos0=0, eps=0.0, S0=None, z0=None):
+    o, D, Sx, zx = run(x, pos0=pos0, eps=eps,
+                       S0=None if S0 is None else S0.to(dev()),
+                       z0=None if z0 is None else z0.to(dev()))
+    ra = ref_args(x)
+    S0r = None if S0 is None else f64(S0)
+    z0r = None if z0 is None else f64(z0)
+    o_ref, D_ref = O.attn_quadratic(**ra, pos0=pos0, eps=eps, S0=S0r, z0=z0r)
+    S_ref, z_ref = O.final_state(ra["k"], ra["v"], ra["gamma"], ra["omega"], ra["phi"], pos0=pos0,
+                                 S0=S0r, z0=z0r)
+    err = max_abs(f64(o), o_ref)
+    assert err <= TOL_BF16, err
+    assert rel_fro(f64(D), D_ref) <= TOL_DEN
+    assert rel_fro(f64(Sx), S_ref) <= TOL_STATE
+    assert rel_fro(f64(zx), z_ref) <= TOL_STATE
+    return err
+
+
+@pytest.mark.parametrize("T", [1, 64, 127, 128, 129, 300])
+def test_short_sequences(T):
+    x = W.make(W.LAYER, B=1, H=2, T=T)
+    check_full(x)
+
+
+def test_many_segments_one_sequence():
+    # 16 chunks spread over 16 segments (delta pass + scan + main pass)
+    x = W.make(W.LAYER, B=1, H=1, T=2000)
+    check_full(x)
+
+
+def test_single_segment_many_sequences():
+    # more sequences than SMs: one segment per sequence, no workspace traffic
+    x = W.make(W.LAYER, B=2, H=80, T=200)
+    o, D, Sx, zx = run(x)
+    ra = ref_args(x)
+    for b, h in ((0, 0), (1, 79), (0, 41)):
+        sl = {n: ra[n][b:b + 1, h:h + 1] for n in ("q", "k", "v")}
+        o_ref, _ = O.attn_quadratic(**sl, gamma=ra["gamma"][h:h + 1], omega=ra["omega"][h:h + 1],
+                                    phi=ra["phi"][h:h + 1])
+        assert max_abs(f64(o)[b, h], o_ref[0, 0]) <= TOL_BF16
+
+
+def test_initial_state_eps_and_offset():
+    x = W.make(W.LAYER, B=2, H=3, T=257)
+    rng = np.random.default_rng(3)
+    kp = rng.standard_normal((2, 3, 100, 64))
+    vp = rng.standard_normal((2, 3, 100, 64))
+    S0, z0 = O.final_state(kp, vp, f64(x["gamma"]), f64(x["omega"]), f64(x["phi"]), pos0=900)
+    check_full(x, pos0=1000, eps=0.75, S0=torch.tensor(S0, dtype=torch.float32),
+               z0=torch.tensor(z0, dtype=torch.float32))
+
+
+def test_outputs_do_not_depend_on_position_offset():
+    x = W.make(W.LAYER, B=1, H=2, T=400)
+    o1, _, _, _ = run(x, pos0=0)
+    o2, _, _, _ = run(x, pos0=50000)
+    assert max_abs(f64(o1), f64(o2)) <= 2 * TOL_BF16
+
+
+def _sampled_rows_check(x, rows_per_head, heads):
+    o, D, Sx, zx = run(x)
+    ra = ref_args(x)
+    worst = 0.0
+    for (b, h) in heads:
+        oo, dd = O.attn_rows(ra["q"], ra["k"], ra["v"], ra["gamma"], ra["omega"], ra["phi"],
+                             rows_per_head, b=b, h=h)
+        worst = max(worst, max_abs(f64(o)[b, h, rows_per_head], oo))
+        assert rel_fro(f64(D)[b, h, rows_per_head], dd) <= TOL_DEN
+        kb = ra["k"][b:b + 1, h:h + 1]
+        vb = ra["v"][b:b + 1, h:h + 1]
+        S_ref, z_ref = O.final_state(kb, vb, ra["gamma"][h:h + 1], ra["omega"][h:h + 1],
+                                     ra["phi"][h:h + 1])
+        assert rel_fro(f64(Sx)[b, h], S_ref[0, 0]) <= TOL_STATE
+        assert rel_fro(f64(zx)[b, h], z_ref[0, 0]) <= TOL_STATE
+    assert worst <= TOL_BF16, worst
+
+
+def test_layer_forward_full_size_sampled():
+    """B=4, H=12, T=2048 in the benchmarked launch configuration; rows checked
+    one by one against the definition (first, chunk edges, ragged middle, last)."""
+    x = W.make(W.LAYER, device="cpu")
+    rows = [0, 1, 2, 63, 127, 128, 129, 1000, 1023, 1024, 2046, 2047]
+    _sampled_rows_check(x, rows, [(0, 0), (1, 5), (3, 11), (2, 7)])
+
+
+def test_long_prefill_full_size_sampled():
+    """B=1, H=12, T=32768, with the final S, z of sampled heads."""
+    x = W.make(W.LONG, device="cpu")
+    rows = [0, 5, 127, 128, 4095, 4096, 16383, 20000, 32766, 32767]
+    _sampled_rows_check(x, rows, [(0, 0), (0, 6), (0, 11)])
