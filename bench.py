@@ -1,0 +1,490 @@
+#!/usr/bin/env python
+"""Benchmark of SANATAN p=1 attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one sanatan_chunk_fwd call over the layer-forward workload
+(B=4, H=12, T=2048, d=dv=64, bf16 q/k/v): the whole prefill path (load,
+feature map, intra-chunk scores, value products, state carry, segment scan,
+normalisation, stores).  `value` is prefill tokens/s (B*T per step, all heads),
+timed with CUDA events on the launching stream, L2 flushed (256 MiB write)
+before every timed step.  The same line also carries the long-prefill,
+decode and training measurements (each timed the same way), the roofline of
+the dominant kernel, an end-to-end figure through the C ABI with pinned host
+buffers, the float64 oracle timed on the host cores, and the SM clocks
+sampled during the timed region.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload (the
+sequences are independent: weak scaling, no collective on the data path);
+`value` is the tokens of all ranks divided by the slowest rank's time.
+
+`--impl reference` times the float64 oracle (the only reference this method
+has) on the host cores, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from constant_state_recurrence_gb300 import workloads as W  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "sanatan_tc_kernel": os.path.join(ROOT, "constant_state_recurrence_gb300", "csrc", "chunk_tc.cu"),
+}
+
+# Algorithmic work per token-head (d = dv = 64, F = 6d = 384, C = 64), the
+# figures of the hot-path scope table: forward flops 2CF + 2C dv + 4F dv,
+# forward bytes 3*64*2 (bf16 q, k, v) + 64*4 (o) + 4 (D); decode bytes per
+# slot: read + write of S and z plus q, k, v, o.
+FWD_FLOPS_PER_TOKEN_HEAD = 2 * 64 * 384 + 2 * 64 * 64 + 4 * 384 * 64        # 155,648
+FWD_BYTES_PER_TOKEN_HEAD = 3 * 64 * 2 + 64 * 4 + 4                          # 644
+BWD_FLOPS_PER_TOKEN_HEAD = 6 * 64 * 384 + 4 * 64 * 64 + 10 * 384 * 64       # 409,600
+DECODE_BYTES_PER_SLOT = 2 * (384 * 64 + 384) * 4 + 4 * 64 * 4               # 200,704
+
+FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p["bf16_tflops_sustained"]), source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel, workload):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernel source
+    is unchanged since the counters were taken; otherwise None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        rec = t[kernel][workload]
+        if rec["source_sha256_16"] != source_hash(KERNEL_SOURCES[kernel]):
+            return None
+        return float(rec["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def timed_steps(step, steps, flush, stream, profile=None):
+    """Run `steps` steps, each after an L2 flush; return per-step ms (whole
+    step) and, if `profile` is given, per-step ms of the dominant kernel."""
+    from constant_state_recurrence_gb300 import sanatan as S
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)] if profile else None
+    for i in range(steps):
+        flush.zero_()
+        if profile:
+            S.set_profile_events(*kev[i])
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    if profile:
+        S.set_profile_events(None, None)
+    torch.cuda.synchronize()
+    whole = [a.elapsed_time(b) for a, b in ev]
+    kern = [a.elapsed_time(b) for a, b in kev] if profile else None
+    return whole, kern
+
+
+def prefill_case(w, dev, flush, steps, warmup, stream):
+    from constant_state_recurrence_gb300 import sanatan as S
+    x = W.make(w, device=dev)
+    g = {n: x[n] for n in ("q", "k", "v", "gamma", "omega", "phi")}
+    B, H, T = x["B"], x["H"], x["T"]
+    o = torch.empty(B, H, T, 64, dtype=torch.float32, device=dev)
+    D = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    ws_n = S.chunk_fwd_workspace_size(B, H, T)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    segs, launches = S.chunk_fwd_plan(B, H, T)
+
+    def step(_i):
+        S.sanatan_chunk_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], out=o,
+                            D_out=D, workspace=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step(0)
+    torch.cuda.synchronize()
+    S.device_status()
+    return dict(step=step, B=B, H=H, T=T, segs=segs, launches=launches, x=x, o=o, D=D, ws=ws,
+                g=g)
+
+
+def e2e_prefill(case, dev, steps, stream):
+    """tokens/s through the public call with pinned host buffers: H2D of q, k, v,
+    the chunked forward, D2H of o, every step."""
+    from constant_state_recurrence_gb300 import sanatan as S
+    g, o, D, ws = case["g"], case["o"], case["D"], case["ws"]
+    hq, hk, hv = (case["x"][n].to("cpu").pin_memory() for n in ("q", "k", "v"))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size()
+
+    def run():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        S.sanatan_chunk_fwd(dq, dk, dv, g["gamma"], g["omega"], g["phi"], out=o, D_out=D,
+                            workspace=ws)
+        ho.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return dict(ms=ms, h2d=h2d, d2h=d2h)
+
+
+def decode_case(batch, dev, flush, steps, warmup, stream):
+    """Decode workload: 12 layers x 12 heads = 144 state slots per sequence,
+    state built by a bf16 chunked prefill of 4096 N(0,1) tokens, then
+    single-token steps with fresh f32 N(0,1) q, k, v at positions 4096, ..."""
+    from constant_state_recurrence_gb300 import sanatan as S
+    w = W.DECODE
+    G = 144
+    x = W.make(w, device=dev, B=batch)
+    _, _, Sx, zx = S.sanatan_chunk_fwd(x["q"], x["k"], x["v"], x["gamma"], x["omega"], x["phi"],
+                                       want_D=False, want_state=True)
+    del x["q"], x["k"], x["v"]
+    N = batch * G
+    Sd = Sx.reshape(N, 384, 64)
+    zd = zx.reshape(N, 384)
+    gen = W.generator(w.seed + 100 * batch, dev)
+    nsteps = steps + warmup
+    q, k, v = W.decode_tokens(N, 64, 64, nsteps, gen)
+    pos = [torch.full((N,), 4096 + i, dtype=torch.int64, device=dev) for i in range(nsteps)]
+    o = torch.empty(N, 64, dtype=torch.float32, device=dev)
+
+    def step(i):
+        S.sanatan_decode_step(Sd, zd, q[i], k[i], v[i], x["gamma"], x["omega"], x["phi"], pos[i],
+                              out=o)
+
+    for i in range(warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    return dict(step=lambda i: step(warmup + i), N=N)
+
+
+def oracle_prefill_sample(batch=4, T=2048):
+    """The float64 oracle's recurrent form on B x 12 heads x T tokens of the
+    layer-forward workload; returns (tokens/s, seconds, threads)."""
+    import numpy as np
+    import oracle.sanatan_oracle as O
+    x = W.make(W.LAYER, device="cpu", B=batch, T=T)
+    f = W.to_f64
+    args = [f(x[n]) for n in ("q", "k", "v", "gamma", "omega", "phi")]
+    t0 = time.perf_counter()
+    O.attn_recurrent(*args)
+    dt = time.perf_counter() - t0
+    threads = None
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max((i.get("num_threads") or 0) for i in threadpool_info()) or None
+    except Exception:
+        pass
+    del np
+    return batch * T / dt, dt, threads or os.cpu_count()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, dev):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    T_sample = 256
+    vals = []
+    for _ in range(args.warmup):
+        oracle_prefill_sample(batch=1, T=T_sample)
+    secs = 0.0
+    threads = os.cpu_count()
+    for _ in range(args.steps):
+        tps, dt, threads = oracle_prefill_sample(batch=1, T=T_sample)
+        vals.append(tps)
+        secs += dt
+    value = args.steps * T_sample / secs
+    line = {
+        "impl": "reference", "metric": "SANATAN p=1 prefill tokens/s", "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": W.LAYER.name, "B": 4, "H": 12, "T": 2048,
+                   "sample_per_step": f"batch element 0, all 12 heads, first {T_sample} tokens"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"recurrent float64 form, 1 x 12 heads x {T_sample} tokens "
+                                   "per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["layer", "long", "decode"], default=None,
+                    help="run one workload only (profiling); the JSON line keeps its keys")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    from constant_state_recurrence_gb300 import sanatan as S
+    S.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    pk = peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    steps, warm = args.steps, args.warmup
+
+    want = (lambda name: args.only is None or args.only == name)
+    lp_steps = max(4, steps // 5)
+    d64_steps = max(4, steps // 5)
+    layer = prefill_case(W.LAYER, dev, flush, steps, warm, stream) if want("layer") else None
+    longp = prefill_case(W.LONG, dev, flush, lp_steps, warm, stream) if want("long") else None
+    dec1 = decode_case(1, dev, flush, steps, warm, stream) if want("decode") else None
+    dec64 = decode_case(64, dev, flush, d64_steps, warm, stream) if want("decode") else None
+
+    gpu_idx = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_idx = int(vis.split(",")[local])
+        except ValueError:
+            pass
+    barrier(world)
+    torch.cuda.synchronize()
+    nan = float("nan")
+    l_whole = l_kern = lp_whole = lp_kern = d1_whole = d64_whole = [nan]
+    with ClockSampler(gpu_idx) as clk:
+        t_wall0 = time.perf_counter()
+        if layer:
+            l_whole, l_kern = timed_steps(layer["step"], steps, flush, stream, profile=True)
+        if longp:
+            lp_whole, lp_kern = timed_steps(longp["step"], lp_steps, flush, stream, profile=True)
+        if dec1:
+            d1_whole, _ = timed_steps(dec1["step"], steps, flush, stream)
+            d64_whole, _ = timed_steps(dec64["step"], d64_steps, flush, stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    S.device_status()
+
+    L = layer or dict(B=4, H=12, T=2048, segs=None, launches=0)
+    LP = longp or dict(B=1, H=12, T=32768, segs=None)
+    D1 = dec1 or dict(N=144)
+    D64 = dec64 or dict(N=9216)
+    ms = statistics.mean(l_whole)
+    ms = max_over_ranks(ms, world, dev)
+    tokens_per_step = L["B"] * L["T"]
+    value = world * tokens_per_step / (ms * 1e-3)
+    kern_ms = statistics.mean(l_kern)
+    th_layer = L["B"] * L["H"] * L["T"]
+    achieved_tf = FWD_FLOPS_PER_TOKEN_HEAD * th_layer / (kern_ms * 1e-3) / 1e12
+    achieved_gbs = FWD_BYTES_PER_TOKEN_HEAD * th_layer / (kern_ms * 1e-3) / 1e9
+    traffic = traffic_for("sanatan_tc_kernel", W.LAYER.name)
+
+    lp_ms = statistics.mean(lp_whole)
+    lp_kms = statistics.mean(lp_kern)
+    th_long = LP["B"] * LP["H"] * LP["T"]
+    d1_us = 1e3 * statistics.mean(d1_whole)
+    d64_us = 1e3 * statistics.mean(d64_whole)
+
+    e2e = e2e_prefill(layer, dev, steps, stream) if layer else dict(ms=nan, h2d=0, d2h=0)
+    layer, longp, dec1, dec64 = L, LP, D1, D64
+
+    line = {
+        "metric": "SANATAN p=1 prefill tokens/s (layer forward B=4 H=12 T=2048)",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v; gamma=4; omega~U(-pi,pi); "
+                "phi_a=10000^(-a/64))",
+        "config": {"workload": W.LAYER.name, "B": 4, "H": 12, "T": 2048, "d": 64, "dv": 64,
+                   "chunk": 128, "segments_per_sequence": layer["segs"],
+                   "parallelism": f"{world} independent replica(s), sequences sharded by rank",
+                   "l2": "256 MiB flush write before every timed step"},
+        "gpu_launches": steps * layer["launches"],
+        "roofline": {"bound": "tensor", "kernel": "sanatan_tc_kernel (main pass)",
+                     "achieved": achieved_tf, "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": achieved_tf / pk["bf16"],
+                     "peak_source": f"{pk['source']} bf16 burst",
+                     "flops_per_token_head": FWD_FLOPS_PER_TOKEN_HEAD,
+                     "kernel_ms": kern_ms,
+                     "traffic": traffic},
+        "roofline_hbm": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": achieved_gbs / pk["hbm"],
+                         "bytes_per_token_head": FWD_BYTES_PER_TOKEN_HEAD},
+        "e2e": {"value": world * tokens_per_step / (e2e["ms"] * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": e2e["ms"]},
+        "long_prefill": {
+            "workload": W.LONG.name, "tokens_per_s": longp["B"] * longp["T"] / (lp_ms * 1e-3),
+            "ms_per_step": lp_ms, "kernel_ms": lp_kms,
+            "tc_frac": FWD_FLOPS_PER_TOKEN_HEAD * th_long / (lp_kms * 1e-3) / 1e12 / pk["bf16"],
+            "hbm_frac": FWD_BYTES_PER_TOKEN_HEAD * th_long / (lp_kms * 1e-3) / 1e9 / pk["hbm"],
+            "segments_per_sequence": longp["segs"], "steps": lp_steps},
+        "decode": {
+            "B1": {"slots": dec1["N"], "us_per_step": d1_us,
+                   "achieved_gbs": DECODE_BYTES_PER_SLOT * dec1["N"] / (d1_us * 1e-6) / 1e9,
+                   "hbm_frac": DECODE_BYTES_PER_SLOT * dec1["N"] / (d1_us * 1e-6) / 1e9 / pk["hbm"],
+                   "note": "14.4 MB state; L2 flushed before each step"},
+            "B64": {"slots": dec64["N"], "us_per_step": d64_us,
+                    "achieved_gbs": DECODE_BYTES_PER_SLOT * dec64["N"] / (d64_us * 1e-6) / 1e9,
+                    "hbm_frac": DECODE_BYTES_PER_SLOT * dec64["N"] / (d64_us * 1e-6) / 1e9 / pk["hbm"],
+                    "steps": d64_steps},
+            "bytes_per_slot": DECODE_BYTES_PER_SLOT},
+        "timed_region_wall_s": t_wall,
+    }
+    clocks = clk.summary()
+    if clocks:
+        line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, dt, threads = oracle_prefill_sample(batch=4, T=2048)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"recurrent float64 oracle on the full layer-forward "
+                                          f"workload (4 x 12 heads x 2048 tokens), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -48,6 +48,13 @@ int check_params(const float* gamma, const float* omega, const float* phi) {
 
 }  // namespace
 
+namespace sanatan {
+ProfileEvents& profile_events() {
+  static thread_local ProfileEvents ev;
+  return ev;
+}
+}  // namespace sanatan
+
 extern "C" {
 
 const char* sanatan_status_string(int status) {
@@ -89,6 +96,26 @@ size_t sanatan_chunk_fwd_workspace_size(int B, int H, int T, int d, int dv, int 
   if (B < 0 || H < 0 || T < 0 || d != 64 || dv != 64) return 0;
   if (in_dtype != SANATAN_BF16) return 0;
   return chunk_fwd_tc_workspace_bytes(B, H, T);
+}
+
+int sanatan_chunk_fwd_plan(int B, int H, int T, int in_dtype, int has_initial_state,
+                           int* segments, int* launches) {
+  if (!ok_dtype(in_dtype) || B < 0 || H < 0 || T < 0 || segments == nullptr || launches == nullptr)
+    return SANATAN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * H == 0) {
+    *segments = 0;
+    *launches = 0;
+    return SANATAN_OK;
+  }
+  if (in_dtype == SANATAN_F32) {
+    *segments = 1;
+    *launches = 1;
+    return SANATAN_OK;
+  }
+  const int nseg = tc_segments(B, H, T);
+  *segments = nseg;
+  *launches = 1 + (nseg > 1 ? 2 : (has_initial_state ? 1 : 0));
+  return SANATAN_OK;
 }
 
 int sanatan_chunk_fwd(const void* q, const void* k, const void* v, int in_dtype,
@@ -133,6 +160,13 @@ int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
   (void)D; (void)dO; (void)grad_dtype; (void)dq; (void)dk; (void)dv_out; (void)dgamma;
   (void)domega; (void)dphi; (void)workspace; (void)workspace_bytes; (void)stream;
   return SANATAN_ERR_UNSUPPORTED;
+}
+
+int sanatan_set_profile_events(void* start, void* stop) {
+  if ((start == nullptr) != (stop == nullptr)) return SANATAN_ERR_INVALID;
+  profile_events().start = static_cast<cudaEvent_t>(start);
+  profile_events().stop = static_cast<cudaEvent_t>(stop);
+  return SANATAN_OK;
 }
 
 int sanatan_device_status(void* stream) {

@@ -156,10 +156,14 @@ cudaError_t launch(const ChunkFwdArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  const ProfileEvents& pe = profile_events();
+  if (pe.start != nullptr) cudaEventRecord(pe.start, st);
   kern<<<a.B * a.H, kThreads, smem, st>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
       a.gamma, a.omega, a.phi, a.H, a.T, a.pos0, a.eps, a.S0, a.z0, a.o, a.D, a.S_out, a.z_out);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (pe.stop != nullptr) cudaEventRecord(pe.stop, st);
+  return e;
 }
 
 }  // namespace

@@ -728,8 +728,12 @@ cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st) {
   p.Dn = a.D;
   p.S_out = a.S_out;
   p.z_out = a.z_out;
+  const ProfileEvents& pe = profile_events();
+  if (pe.start != nullptr) cudaEventRecord(pe.start, st);
   sanatan_tc_kernel<false><<<bhn * nseg, kThreads, kSmemBytes, st>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (pe.stop != nullptr) cudaEventRecord(pe.stop, st);
+  return e;
 }
 
 int tc_read_and_clear_error(cudaStream_t st) {

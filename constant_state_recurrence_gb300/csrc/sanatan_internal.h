@@ -45,6 +45,14 @@ struct ChunkBwdArgs {
   size_t workspace_bytes;
 };
 
+// Events recorded around the dominant kernel of a chunk_fwd / chunk_bwd call
+// (bench instrumentation; null when unused).
+struct ProfileEvents {
+  cudaEvent_t start = nullptr;
+  cudaEvent_t stop = nullptr;
+};
+ProfileEvents& profile_events();
+
 cudaError_t featurize_launch(const void* u, int u_dtype, const float* gamma, const float* omega,
                              const float* phi, int B, int H, int T, int d, int64_t pos0,
                              void* out, int out_dtype, cudaStream_t st);

@@ -30,6 +30,7 @@ _SIGS = {
     "sanatan_featurize": (_c_int, [_c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
                                    _c_i64, _c_p, _c_int, _c_p]),
     "sanatan_chunk_fwd_workspace_size": (_c_sz, [_c_int] * 6),
+    "sanatan_chunk_fwd_plan": (_c_int, [_c_int] * 5 + [_c_p, _c_p]),
     "sanatan_chunk_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int,
                                    _c_int, _c_int, _c_int, _c_i64, _c_f, _c_p, _c_p, _c_p, _c_p,
                                    _c_p, _c_p, _c_p, _c_sz, _c_p]),
@@ -39,6 +40,7 @@ _SIGS = {
                                    _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_sz,
                                    _c_p]),
     "sanatan_device_status": (_c_int, [_c_p]),
+    "sanatan_set_profile_events": (_c_int, [_c_p, _c_p]),
     "sanatan_decode_step": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int,
                                      _c_int, _c_int, _c_int, _c_f, _c_p, _c_p]),
 }
@@ -111,6 +113,17 @@ def device_status(device=None):
     _check("sanatan_device_status", lib().sanatan_device_status(_stream(dev)))
 
 
+def set_profile_events(start=None, stop=None):
+    """Record torch.cuda.Event `start`/`stop` around the dominant kernel of the
+    following chunk_fwd / chunk_bwd calls of this thread (None, None: off)."""
+    for ev in (start, stop):
+        if ev is not None and ev.cuda_event == 0:
+            ev.record()  # torch creates the CUDA event lazily, on first record
+    a = None if start is None else ctypes.c_void_p(start.cuda_event)
+    b = None if stop is None else ctypes.c_void_p(stop.cuda_event)
+    _check("sanatan_set_profile_events", lib().sanatan_set_profile_events(a, b))
+
+
 def state_bytes(layers, heads, d=64, dv=64):
     return int(lib().sanatan_state_bytes(layers, heads, d, dv))
 
@@ -136,8 +149,17 @@ def chunk_fwd_workspace_size(B, H, T, d=64, dv=64, dtype=torch.bfloat16):
     return int(lib().sanatan_chunk_fwd_workspace_size(B, H, T, d, dv, _DT[dtype]))
 
 
+def chunk_fwd_plan(B, H, T, dtype=torch.bfloat16, has_initial_state=False):
+    """(segments per sequence, kernel launches per call) of sanatan_chunk_fwd."""
+    seg, nl = ctypes.c_int(0), ctypes.c_int(0)
+    _check("sanatan_chunk_fwd_plan",
+           lib().sanatan_chunk_fwd_plan(B, H, T, _DT[dtype], int(bool(has_initial_state)),
+                                        ctypes.byref(seg), ctypes.byref(nl)))
+    return seg.value, nl.value
+
+
 def sanatan_chunk_fwd(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None,
-                      want_D=True, want_state=False, out=None, workspace=None):
+                      want_D=True, want_state=False, out=None, D_out=None, workspace=None):
     """Causal p=1 attention over [B, H, T] sequences.
 
     Returns (o [B,H,T,dv] f32, D [B,H,T] f32 or None, S [B,H,6d,dv] or None,
@@ -154,7 +176,11 @@ def sanatan_chunk_fwd(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=N
     F = 6 * d
     o = out if out is not None else torch.empty(B, H, T, dv, dtype=torch.float32, device=dev)
     _need(o, "o", (torch.float32,), (B, H, T, dv))
-    D = torch.empty(B, H, T, dtype=torch.float32, device=dev) if want_D else None
+    D = D_out
+    if D is None and want_D:
+        D = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    if D is not None:
+        _need(D, "D", (torch.float32,), (B, H, T))
     S = z = None
     if want_state:
         S = torch.empty(B, H, F, dv, dtype=torch.float32, device=dev)

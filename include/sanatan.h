@@ -107,6 +107,11 @@ SANATAN_API int sanatan_featurize(const void* u, int u_dtype, const float* gamma
  * but copy (S0, z0) (or zeros) to (S_out, z_out).
  */
 SANATAN_API size_t sanatan_chunk_fwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype);
+/* How sanatan_chunk_fwd splits a problem: *segments = segments per sequence
+ * (the long-sequence split of the tensor-core path), *launches = kernels one
+ * call enqueues.  Host-only arithmetic (reads the current device's SM count). */
+SANATAN_API int sanatan_chunk_fwd_plan(int B, int H, int T, int in_dtype, int has_initial_state,
+                                       int* segments, int* launches);
 SANATAN_API int sanatan_chunk_fwd(const void* q, const void* k, const void* v, int in_dtype,
                       const float* gamma, const float* omega, const float* phi, int B, int H,
                       int T, int d, int dv, int64_t pos0, float eps, const float* S0,
@@ -132,6 +137,16 @@ SANATAN_API int sanatan_chunk_bwd(const void* q, const void* k, const void* v, i
                       int grad_dtype, void* dq, void* dk, void* dv_out, float* dgamma,
                       float* domega, float* dphi, void* workspace, size_t workspace_bytes,
                       void* stream);
+
+/*
+ * sanatan_set_profile_events -- instrumentation for benchmarks.  When both
+ * are non-NULL, the calling thread's subsequent sanatan_chunk_fwd and
+ * sanatan_chunk_bwd calls record `start` (a cudaEvent_t) on their stream just
+ * before their dominant kernel launch and `stop` just after it, so the caller
+ * can time that kernel alone.  Pass NULL, NULL to turn it off.  Thread-local;
+ * the events stay owned by the caller.
+ */
+SANATAN_API int sanatan_set_profile_events(void* start, void* stop);
 
 /*
  * sanatan_device_status -- synchronises `stream`, then reports whether any
