@@ -34,6 +34,10 @@ _SIGS = {
     "sanatan_chunk_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int,
                                    _c_int, _c_int, _c_int, _c_i64, _c_f, _c_p, _c_p, _c_p, _c_p,
                                    _c_p, _c_p, _c_p, _c_sz, _c_p]),
+    "sanatan_chunk_fwd_noalloc_max_scratch_bytes": (_c_sz, []),
+    "sanatan_chunk_fwd_noalloc": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int,
+                                           _c_int, _c_int, _c_int, _c_i64, _c_f, _c_p, _c_p, _c_p,
+                                           _c_p, _c_p, _c_p, _c_p]),
     "sanatan_chunk_bwd_workspace_size": (_c_sz, [_c_int] * 6),
     "sanatan_chunk_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int,
                                    _c_int, _c_int, _c_int, _c_i64, _c_f, _c_p, _c_p, _c_p, _c_p,
@@ -197,6 +201,32 @@ def sanatan_chunk_fwd(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=N
                                  _ptr(S0), _ptr(z0), _ptr(o), _ptr(D), _ptr(S), _ptr(z),
                                  _ptr(workspace), ws_bytes, _stream(dev))
     _check("sanatan_chunk_fwd", st)
+    return o, D, S, z
+
+
+def sanatan_chunk_fwd_noalloc(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None,
+                              want_D=True, want_state=False):
+    """sanatan_chunk_fwd for bf16 inputs without a workspace: the library uses
+    its own fixed 16 MiB device scratch instead (for callers that cannot
+    allocate).  Calls must not overlap on the GPU.  Returns (o, D, S, z)."""
+    _need(q, "q", (torch.bfloat16,))
+    B, H, T, d = q.shape
+    _need(k, "k", (torch.bfloat16,), (B, H, T, d))
+    dv = v.shape[-1]
+    _need(v, "v", (torch.bfloat16,), (B, H, T, dv))
+    dev = q.device
+    F = 6 * d
+    o = torch.empty(B, H, T, dv, dtype=torch.float32, device=dev)
+    D = torch.empty(B, H, T, dtype=torch.float32, device=dev) if want_D else None
+    S = z = None
+    if want_state:
+        S = torch.empty(B, H, F, dv, dtype=torch.float32, device=dev)
+        z = torch.empty(B, H, F, dtype=torch.float32, device=dev)
+    st = lib().sanatan_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(omega),
+                                         _ptr(phi), B, H, T, d, dv, int(pos0), float(eps),
+                                         _ptr(S0), _ptr(z0), _ptr(o), _ptr(D), _ptr(S), _ptr(z),
+                                         _stream(dev))
+    _check("sanatan_chunk_fwd_noalloc", st)
     return o, D, S, z
 
 

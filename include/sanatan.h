@@ -119,6 +119,36 @@ SANATAN_API int sanatan_chunk_fwd(const void* q, const void* k, const void* v, i
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sanatan_chunk_fwd_noalloc -- sanatan_chunk_fwd for bf16 inputs that takes no
+ * workspace and allocates nothing.  The paper has no counterpart: this entry
+ * exists for callers that cannot hand the library device scratch memory, e.g.
+ * a plugin that only receives its input and output buffers from a host
+ * framework, or code running where cudaMalloc is off limits because it
+ * implicitly synchronises the device or because a pool owns all device memory.
+ *   Arguments and results are those of sanatan_chunk_fwd with in_dtype =
+ *   SANATAN_BF16 and without the workspace pair.
+ *   Scratch: a fixed array inside the library, 16 MiB per device
+ *   (sanatan_chunk_fwd_noalloc_max_scratch_bytes()), held by every GPU that
+ *   loads the library until the process exits.  Problems whose workspace
+ *   (sanatan_chunk_fwd_workspace_size) would exceed it return
+ *   SANATAN_ERR_UNSUPPORTED; on one GB300 these are the problems with more
+ *   than 163 sequences (B * H > 163).
+ *   The first call on a device looks up the array's device address (no
+ *   allocation); make that first call before any stream capture.
+ *   Calls share the array: two calls whose kernels overlap on the GPU (other
+ *   streams, other threads) race on it and give undefined results.  The
+ *   kernels overwrite every scratch byte before reading it, so nothing needs
+ *   clearing between calls.
+ */
+SANATAN_API size_t sanatan_chunk_fwd_noalloc_max_scratch_bytes(void);
+SANATAN_API int sanatan_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
+                                          const float* gamma, const float* omega,
+                                          const float* phi, int B, int H, int T, int d, int dv,
+                                          int64_t pos0, float eps, const float* S0,
+                                          const float* z0, float* o, float* D, float* S_out,
+                                          float* z_out, void* stream);
+
+/*
  * sanatan_chunk_bwd -- gradients of sum(o * dO) for sanatan_chunk_fwd.
  * The chain rule through eqs. (2)-(4), (6), (9); the pages give no backward.
  *   q, k, v, gamma, omega, phi, sizes, pos0, eps, S0, z0: as for the forward
