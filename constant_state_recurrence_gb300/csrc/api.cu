@@ -155,11 +155,39 @@ int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
                       int grad_dtype, void* dq, void* dk, void* dv_out, float* dgamma,
                       float* domega, float* dphi, void* workspace, size_t workspace_bytes,
                       void* stream) {
-  (void)q; (void)k; (void)v; (void)in_dtype; (void)gamma; (void)omega; (void)phi; (void)B;
-  (void)H; (void)T; (void)d; (void)dv; (void)pos0; (void)eps; (void)S0; (void)z0; (void)o;
-  (void)D; (void)dO; (void)grad_dtype; (void)dq; (void)dk; (void)dv_out; (void)dgamma;
-  (void)domega; (void)dphi; (void)workspace; (void)workspace_bytes; (void)stream;
-  return SANATAN_ERR_UNSUPPORTED;
+  if (!ok_dtype(in_dtype) || !ok_dtype(grad_dtype)) return SANATAN_ERR_INVALID;
+  if (int s = check_sizes(B, H, T, d, dv)) return s;
+  if ((S0 == nullptr) != (z0 == nullptr)) return SANATAN_ERR_INVALID;
+  if (!ok_nullable(S0) || !ok_nullable(z0) || !ok_nullable(dphi) || !ok_nullable(workspace))
+    return SANATAN_ERR_INVALID;
+  if (H > 0 && (!ok_ptr(dgamma) || !ok_ptr(domega))) return SANATAN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * H * T > 0 &&
+      (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(o) || !ok_ptr(D) || !ok_ptr(dO) ||
+       !ok_ptr(dq) || !ok_ptr(dk) || !ok_ptr(dv_out)))
+    return SANATAN_ERR_INVALID;
+  if (H > 0) {
+    if (int s = check_params(gamma, omega, phi)) return s;
+  }
+  if (workspace_bytes < sanatan_chunk_bwd_workspace_size(B, H, T, d, dv, in_dtype))
+    return SANATAN_ERR_INVALID;
+  if (H == 0) return SANATAN_OK;
+  if (int s = check_arch()) return s;
+  ChunkBwdArgs a{};
+  a.f = ChunkFwdArgs{q, k, v, in_dtype, gamma, omega, phi, B, H, T, d, dv, pos0, eps,
+                     S0, z0, nullptr, nullptr, nullptr, nullptr, workspace, workspace_bytes};
+  a.o = o;
+  a.Dn = D;
+  a.dO = dO;
+  a.grad_dtype = grad_dtype;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv_out;
+  a.dgamma = dgamma;
+  a.domega = domega;
+  a.dphi = dphi;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  return from_cuda(chunk_bwd_simt_launch(a, static_cast<cudaStream_t>(stream)));
 }
 
 int sanatan_set_profile_events(void* start, void* stop) {

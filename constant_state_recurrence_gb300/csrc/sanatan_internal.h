@@ -63,6 +63,8 @@ cudaError_t decode_step_launch(float* S, float* z, const float* q, const float* 
                                float* o, cudaStream_t st);
 
 size_t chunk_fwd_simt_smem_bytes();
+size_t chunk_bwd_simt_smem_bytes();
+cudaError_t chunk_bwd_simt_launch(const ChunkBwdArgs& a, cudaStream_t st);
 cudaError_t chunk_fwd_simt_launch(const ChunkFwdArgs& a, cudaStream_t st);
 
 }  // namespace sanatan
