@@ -19,11 +19,14 @@
 // PhiK, so they accumulate in f32 on the tensor core with the rest of the
 // state.
 //
-// Roles (416 threads): warps 0-7 featurise q, k and stage v into shared
-// memory; warps 8-11 drain TMEM (mask + split the scores into bf16 hi/lo
-// parts, snapshot the state to bf16 for the next chunk, normalise and store
-// the outputs); one thread of warp 12 issues every tcgen05.mma.  All hand-offs
-// are mbarriers with bounded waits.
+// Roles (512 threads, four warpgroups): warps 0-7 featurise q, k and stage v
+// into shared memory (168 registers each after setmaxnreg); warps 8-11 drain
+// TMEM (mask + split the scores into bf16 hi/lo parts, snapshot the state to
+// bf16 for the next chunk, normalise and store the outputs; 144 registers);
+// one thread of warp 12 issues every tcgen05.mma (warps 12-15 keep 32
+// registers).  All hand-offs are mbarriers with bounded waits.  The next
+// chunk's q, k, v are bulk-prefetched into L2 while the current one runs, and
+// output rows leave through bulk asynchronous copies.
 //
 // Shared-memory operands use the canonical no-swizzle layout (8 x 16-byte
 // core matrices); TMEM holds P (128 cols), O_ext (80) and the f32 state
@@ -71,19 +74,31 @@ enum Bar {
 };
 
 struct Misc {
+  float4 dimc[64];   // per dim: gamma*sqrt2*cos(omega+pi/4), gamma*sqrt2*sin(omega+pi/4),
+                     //          cos(8 phi), sin(8 phi)
+  float vs[68];      // state row 320 before the current chunk: sum v (64), count
+  float a0[68];      // constant-channel part of S0: sum_a S0[6a] (64), sum_a z0[6a]
   uint64_t bar[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
-  int pad[2];
-  float vs[68];      // state row 320 before the current chunk: sum v (64), count
-  float a0[68];      // constant-channel part of S0: sum_a S0[6a] (64), sum_a z0[6a]
-  float4 dimc[64];   // per dim: gamma*sqrt2*cos(omega+pi/4), gamma*sqrt2*sin(omega+pi/4),
-                     //          cos(8 phi), sin(8 phi)
 };
+// Output staging for the bulk row stores: rows of 256 B at a 272-B pitch (the
+// extra 16 B spread consecutive rows over the banks).  It lives in the bf16
+// state snapshot buffer, which is free between the chunk's Phi(Q)[S|z]
+// product and the next snapshot.
+constexpr int kStagePitch = 272;
+static_assert(kC * kStagePitch <= 40 * kLBO_SV, "output staging must fit the snapshot buffer");
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kSmemBytes <= 232448, "shared memory layout exceeds 227 KB");
 
-constexpr int kThreads = 416;
+constexpr int kThreads = 512;
+// Register split: 256 x 168 + 128 x 144 + 128 x 32 = 65,536 = 512 x 128, the
+// registers the block is launched with.
+constexpr uint32_t kRegFeat = 168;
+constexpr uint32_t kRegEpi = 144;
+constexpr uint32_t kRegMma = 32;
+static_assert(256 * kRegFeat + 128 * kRegEpi + 128 * kRegMma <= kThreads * 128,
+              "setmaxnreg split must fit the launch allocation");
 constexpr int kFeatWarps = 8;
 constexpr int kEpiWarp0 = 8;
 constexpr int kMmaWarp = 12;
@@ -102,7 +117,7 @@ struct TcParams {
   int nseg;         // segments per sequence
   int seg_grid;     // CTAs per sequence in this launch
   int nchunks;      // chunks per sequence
-  const float* init_sc;  // compact initial states [B*H][nseg][321][80] or null (zero)
+  const float* deltas;   // per-segment state sums [B*H][nseg][321][80] (slots 0..nseg-2) or null
   const float* S0;       // full initial state (export of constant rows) or null
   const float* z0;
   float* o;
@@ -127,7 +142,6 @@ __device__ __forceinline__ float tanh_fast(float x) {
 }
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void feat_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
 
 // Eight dimensions of one token: the five non-constant channels, packed as
 // bf16 pairs (out[c][j/2] holds dims j, j+1 of channel c).
@@ -175,6 +189,19 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// L2 prefetch of one chunk's rows of q (unless state-only), k and v.
+template <bool kStateOnly>
+__device__ __forceinline__ void prefetch_chunk(const TcParams& prm, int64_t seq_row0, int chunk) {
+  const int tok0 = chunk * kC;
+  const int n = min(kC, prm.T - tok0);
+  if (n <= 0) return;
+  const int64_t off = (seq_row0 + tok0) * kD;
+  const uint32_t bytes = static_cast<uint32_t>(n) * kD * 2;
+  if (!kStateOnly) prefetch_l2_bulk(prm.q + off, bytes);
+  prefetch_l2_bulk(prm.k + off, bytes);
+  prefetch_l2_bulk(prm.v + off, bytes);
+}
+
 // ---------------------------------------------------------------------------
 template <bool kStateOnly>
 __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
@@ -197,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
   const int64_t seq_row0 = static_cast<int64_t>(bh) * prm.T;  // first token row of the sequence
   const bool last_seg = (seg == prm.nseg - 1);
 
+  if (tid == 0 && nloc > 0) prefetch_chunk<kStateOnly>(prm, seq_row0, c_begin);
   if (warp == kMmaWarp) {
     tmem_alloc(&m.tmem_base, kTmemCols);
     tmem_relinquish();
@@ -242,20 +270,36 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
 
   if (warp < kFeatWarps) {
     // ------------------------------------------------------------ featuriser
+    setmaxnreg_inc<kRegFeat>();
     const int r = lane & 7;
     const int ag = (lane >> 3) + 4 * (warp & 1);      // dimension group (8 dims)
     const int tq = 32 * (warp >> 1) + r;              // first of this thread's 4 tokens
     const float4* dimc = &m.dimc[8 * ag];
-    const float* phi_h = prm.phi + h * kD + 8 * ag;
+    float phi_r[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) phi_r[j] = prm.phi[h * kD + 8 * ag + j];
     for (int ci = 0; ci < nloc; ++ci) {
       const int chunk = c_begin + ci;
       const int tok0 = chunk * kC;
+      if (tid == 0 && ci + 1 < nloc) prefetch_chunk<kStateOnly>(prm, seq_row0, chunk + 1);
+      // All raw loads of the chunk go out together (they hit L2 after the prefetch).
+      uint4 rq[4], rk[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = tq + 8 * i;
+        const bool valid = tok0 + t < prm.T;
+        const int64_t off = (seq_row0 + tok0 + t) * kD + 8 * ag;
+        rk[i] = valid ? ldg_nc_v4(prm.k + off) : make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (!kStateOnly)
+          rq[i] = valid ? ldg_nc_v4(prm.q + off) : make_uint4(0u, 0u, 0u, 0u);
+      }
       float cb0[8], sb0[8];
       {
         const int64_t tabs = prm.pos0 + tok0 + tq;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) __sincosf(phase_mod_2pi(tabs, phi_h[j]), &sb0[j], &cb0[j]);
+        for (int j = 0; j < 8; ++j) __sincosf(phase_mod_2pi(tabs, phi_r[j]), &sb0[j], &cb0[j]);
       }
+      uint4 rv[4];
       if constexpr (!kStateOnly) {
         uint32_t qf[4][5][4];
         float cb[8], sb[8];
@@ -263,10 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         for (int j = 0; j < 8; ++j) { cb[j] = cb0[j]; sb[j] = sb0[j]; }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int t = tq + 8 * i;
-          if (tok0 + t < prm.T) {
-            const uint4 raw = ldg_nc_v4(prm.q + (seq_row0 + tok0 + t) * kD + 8 * ag);
-            features8(raw, dimc, cb, sb, qf[i]);
+          if (tok0 + tq + 8 * i < prm.T) {
+            features8(rq[i], dimc, cb, sb, qf[i]);
           } else {
 #pragma unroll
             for (int c = 0; c < 5; ++c)
@@ -281,6 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
             cb[j] = nc;
           }
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = tq + 8 * i;
+          rv[i] = (tok0 + t < prm.T) ? ldg_nc_v4(prm.v + (seq_row0 + tok0 + t) * kD + 8 * ag)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+        }
         if (ci > 0) wait_bar(m, kQFree, (ci - 1) & 1);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -290,6 +338,13 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           for (int c = 0; c < 5; ++c)
             st_shared_v4(base + (c * 8 + ag) * 128, qf[i][c][0], qf[i][c][1], qf[i][c][2],
                          qf[i][c][3]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = tq + 8 * i;
+          rv[i] = (tok0 + t < prm.T) ? ldg_nc_v4(prm.v + (seq_row0 + tok0 + t) * kD + 8 * ag)
+                                     : make_uint4(0u, 0u, 0u, 0u);
         }
       }
       // keys
@@ -304,8 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           const bool valid = tok0 + t < prm.T;
           uint32_t kf[5][4];
           if (valid) {
-            const uint4 raw = ldg_nc_v4(prm.k + (seq_row0 + tok0 + t) * kD + 8 * ag);
-            features8(raw, dimc, cb, sb, kf);
+            features8(rk[i], dimc, cb, sb, kf);
           } else {
 #pragma unroll
             for (int c = 0; c < 5; ++c)
@@ -331,10 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int t = tq + 8 * i;
-        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-        if (tok0 + t < prm.T) raw = ldg_nc_v4(prm.v + (seq_row0 + tok0 + t) * kD + 8 * ag);
-        st_shared_v4(sV + (t >> 3) * kLBO_SV + ag * 128 + (t & 7) * 16, raw.x, raw.y, raw.z,
-                     raw.w);
+        st_shared_v4(sV + (t >> 3) * kLBO_SV + ag * 128 + (t & 7) * 16, rv[i].x, rv[i].y,
+                     rv[i].z, rv[i].w);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -342,26 +394,42 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ TMEM epilogue
+    setmaxnreg_inc<kRegEpi>();
     const int qd = warp - kEpiWarp0;           // TMEM lane quarter
     const int row = 32 * qd + lane;            // TMEM lane = token row / feature row in tile
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
-    // Initial state -> TMEM tiles (and the bf16 snapshot for the first chunk).
+    // Initial state -> TMEM tiles (and the bf16 snapshot for the first chunk):
+    // the caller's state (S0, z0) plus the sums of all earlier segments.
     {
-      const float* src = nullptr;
-      if (prm.init_sc != nullptr)
-        src = prm.init_sc + (static_cast<int64_t>(bh) * prm.nseg + seg) * kSCRows * kSCCols;
       for (int mt = 0; mt < 3; ++mt) {
         const int f = mt * 128 + row;
         if (mt == 2 && qd == 3) continue;  // rows 352..383 are never used
         float val[80];
 #pragma unroll
         for (int e = 0; e < 80; ++e) val[e] = 0.f;
-        if (src != nullptr && f < kSCRows) {
-          const float4* s4 = reinterpret_cast<const float4*>(src + f * kSCCols);
+        if (!kStateOnly && f < kNF && prm.S0 != nullptr) {
+          const int c = f / kD + 1, a = f % kD;
+          const int64_t rowi = static_cast<int64_t>(bh) * 384 + 6 * a + c;
+          const float4* s4 = reinterpret_cast<const float4*>(prm.S0 + rowi * 64);
 #pragma unroll
-          for (int e4 = 0; e4 < 17; ++e4) {
+          for (int e4 = 0; e4 < 16; ++e4) {
             const float4 x = s4[e4];
             val[4 * e4] = x.x; val[4 * e4 + 1] = x.y; val[4 * e4 + 2] = x.z; val[4 * e4 + 3] = x.w;
+          }
+          val[64] = prm.z0[rowi];
+        }
+        if (!kStateOnly && f < kSCRows && prm.deltas != nullptr) {
+          const float* d0 = prm.deltas + static_cast<int64_t>(bh) * prm.nseg * kSCRows * kSCCols +
+                            f * kSCCols;
+          for (int sp = 0; sp < seg; ++sp) {
+            const float4* s4 = reinterpret_cast<const float4*>(d0 + static_cast<int64_t>(sp) *
+                                                                         kSCRows * kSCCols);
+#pragma unroll
+            for (int e4 = 0; e4 < 17; ++e4) {
+              const float4 x = s4[e4];
+              val[4 * e4] += x.x; val[4 * e4 + 1] += x.y; val[4 * e4 + 2] += x.z;
+              val[4 * e4 + 3] += x.w;
+            }
           }
 #pragma unroll
           for (int e = 65; e < 68; ++e) val[e] = 0.f;
@@ -436,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         if (lane == 0) mbar_arrive(&m.bar[kPTilde]);
 
         // E3: outputs of this chunk (state row 320 in m.vs is still the pre-chunk one).
+        // Each row is normalised in registers, staged in the free snapshot buffer
+        // and written to global memory by one 256-byte bulk copy.
         wait_bar(m, kPVDone, ci & 1);
         tc_fence_after();
         {
@@ -452,21 +522,28 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           if (tok < prm.T) {
             const float den = ov[64] + 64.0f * m.vs[64] + m.a0[64];
             const float inv = 1.0f / (den + prm.eps);
-            float4* orow = reinterpret_cast<float4*>(prm.o + (seq_row0 + tok) * kD);
+            const float4* vs4 = reinterpret_cast<const float4*>(m.vs);
+            const float4* a04 = reinterpret_cast<const float4*>(m.a0);
+            const uint32_t srow = sS + row * kStagePitch;
 #pragma unroll
             for (int e4 = 0; e4 < 16; ++e4) {
-              float4 y;
-              y.x = (ov[4 * e4 + 0] + 64.0f * m.vs[4 * e4 + 0] + m.a0[4 * e4 + 0]) * inv;
-              y.y = (ov[4 * e4 + 1] + 64.0f * m.vs[4 * e4 + 1] + m.a0[4 * e4 + 1]) * inv;
-              y.z = (ov[4 * e4 + 2] + 64.0f * m.vs[4 * e4 + 2] + m.a0[4 * e4 + 2]) * inv;
-              y.w = (ov[4 * e4 + 3] + 64.0f * m.vs[4 * e4 + 3] + m.a0[4 * e4 + 3]) * inv;
-              orow[e4] = y;
+              const float4 w = vs4[e4];
+              const float4 c = a04[e4];
+              st_shared_v4(srow + 16 * e4,
+                           __float_as_uint((fmaf(64.0f, w.x, ov[4 * e4 + 0]) + c.x) * inv),
+                           __float_as_uint((fmaf(64.0f, w.y, ov[4 * e4 + 1]) + c.y) * inv),
+                           __float_as_uint((fmaf(64.0f, w.z, ov[4 * e4 + 2]) + c.z) * inv),
+                           __float_as_uint((fmaf(64.0f, w.w, ov[4 * e4 + 3]) + c.w) * inv));
             }
+            fence_proxy_async_smem();
+            bulk_store_s2g(prm.o + (seq_row0 + tok) * kD, srow, kD * 4);
+            bulk_commit();
             if (prm.Dn != nullptr) prm.Dn[seq_row0 + tok] = den;
           }
         }
+        bulk_wait_read_all();  // this thread's staged rows have been read by the copy engine
         tc_fence_before();
-        epi_sync();  // every epilogue thread is done with m.vs and O
+        epi_sync();  // all staged rows read, every thread done with m.vs and O
         if (lane == 0) mbar_arrive(&m.bar[kOFree]);
 
         // E2: snapshot of the state after this chunk, for the next chunk.
@@ -569,41 +646,64 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         }
       }
     }
-  } else if (lane == 0) {
+  } else {
+    setmaxnreg_dec<kRegMma>();
+  }
+  if (warp == kMmaWarp && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idQK = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idIN = idesc_bf16_f32(128, kN, false, true);
     constexpr uint32_t idST = idesc_bf16_f32(128, kN, true, true);
     constexpr uint32_t idPV = idesc_bf16_f32(128, kN, false, true);
+    // Descriptor bases; an operand at byte offset o from its base is base + o/16
+    // (the start-address field is the low 14 bits and never overflows here).
+    // The issue stream is fully unrolled: a rolled loop costs the single
+    // issuing thread more cycles per MMA than the tensor core needs.
+    const uint64_t dQ = smem_desc(sQ, 128, kXQ);          // PhiQ, K-major A
+    const uint64_t dKb = smem_desc(sK, 128, kXK);         // PhiK, K-major B (scores)
+    const uint64_t dKa = smem_desc(sK, kXK, 128);         // PhiK^T, MN-major A (state)
+    const uint64_t dS = smem_desc(sS, kLBO_SV, 128);      // S' bf16, MN-major B
+    const uint64_t dV = smem_desc(sV, kLBO_SV, 128);      // [V | 1], MN-major B
     for (int ci = 0; ci < nloc; ++ci) {
+      // Opaque copies of the bases keep the descriptor arithmetic of each group
+      // next to its MMAs instead of hoisted (80 live descriptors would not fit
+      // this warpgroup's registers).
+      uint64_t dQl = dQ, dKbl = dKb, dKal = dKa, dSl = dS, dVl = dV;
+      asm volatile("" : "+l"(dQl), "+l"(dKbl), "+l"(dKal), "+l"(dSl), "+l"(dVl));
       wait_bar(m, kFeatFull, ci & 1);
       tc_fence_after();
       if constexpr (!kStateOnly) {
+#pragma unroll
         for (int s = 0; s < 20; ++s)
-          mma_ss(tmem + kTP, smem_desc(sQ + s * 256, 128, kXQ), smem_desc(sK + s * 256, 128, kXK),
-                 idQK, s > 0);
+          mma_ss(tmem + kTP, dQl + 16 * s, dKbl + 16 * s, idQK, s > 0);
         mma_commit(&m.bar[kPFull]);
         wait_bar(m, kSnapReady, ci & 1);  // bf16 state snapshot of the previous chunk
         wait_bar(m, kOFree, ci & 1);      // previous outputs drained from TMEM
         tc_fence_after();
+        asm volatile("" : "+l"(dQl), "+l"(dSl));
+#pragma unroll
         for (int s = 0; s < 20; ++s)
-          mma_ss(tmem + kTO, smem_desc(sQ + s * 256, 128, kXQ),
-                 smem_desc(sS + s * 2 * kLBO_SV, kLBO_SV, 128), idIN, s > 0);
+          mma_ss(tmem + kTO, dQl + 16 * s, dSl + (2 * kLBO_SV / 16) * s, idIN, s > 0);
         mma_commit(&m.bar[kQFree]);
       } else if (ci == 0) {
         wait_bar(m, kSnapReady, 0);  // initial state is in TMEM
         tc_fence_after();
       }
-      for (int mt = 0; mt < 3; ++mt)
-        for (int s = 0; s < 8; ++s)
-          mma_ss(tmem + kTS + mt * kN, smem_desc(sK + mt * 2048 + s * 2 * kXK, kXK, 128),
-                 smem_desc(sV + s * 2 * kLBO_SV, kLBO_SV, 128), idST, true);
+      asm volatile("" : "+l"(dKal), "+l"(dVl));
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+#pragma unroll
+        for (int mt = 0; mt < 3; ++mt)
+          mma_ss(tmem + kTS + mt * kN, dKal + (2048 / 16) * mt + (2 * kXK / 16) * s,
+                 dVl + (2 * kLBO_SV / 16) * s, idST, true);
       mma_commit(&m.bar[kStateDone]);
       if constexpr (!kStateOnly) {
         wait_bar(m, kPTilde, ci & 1);
         tc_fence_after();
+        asm volatile("" : "+l"(dVl));
+#pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint64_t bd = smem_desc(sV + s * 2 * kLBO_SV, kLBO_SV, 128);
+          const uint64_t bd = dVl + (2 * kLBO_SV / 16) * s;
           mma_ts(tmem + kTO, tmem + kTP + 8 * s, bd, idPV, true);
           mma_ts(tmem + kTO, tmem + kTL + 8 * s, bd, idPV, true);
         }
@@ -615,36 +715,12 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     wait_bar(m, kDrain, 0);
   }
 
+  if (warp >= kEpiWarp0 && warp < kMmaWarp) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// Exclusive scan over segments of the per-segment state sums, seeded with the
-// caller's initial state in compact form.  In place: W[bh][p] <- init_p.
-__global__ void __launch_bounds__(256) seg_scan_kernel(const float* __restrict__ S0,
-                                                       const float* __restrict__ z0,
-                                                       float* __restrict__ W, int nseg,
-                                                       int has_delta) {
-  const int bh = blockIdx.y;
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= kSCRows * 65) return;
-  const int row = e / 65, col = e % 65;
-  float acc = 0.f;
-  if (S0 != nullptr && row < kNF) {
-    const int c = row / kD + 1, a = row % kD;
-    acc = (col < 64) ? S0[(static_cast<int64_t>(bh) * 384 + 6 * a + c) * 64 + col]
-                     : z0[static_cast<int64_t>(bh) * 384 + 6 * a + c];
-  }
-  float* w = W + static_cast<int64_t>(bh) * nseg * kSCRows * kSCCols + row * kSCCols + col;
-  for (int p = 0; p < nseg; ++p) {
-    float* cell = w + static_cast<int64_t>(p) * kSCRows * kSCCols;
-    const float d = (has_delta && p < nseg - 1) ? *cell : 0.f;
-    *cell = acc;
-    acc += d;
   }
 }
 
@@ -682,7 +758,6 @@ cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st) {
   const int nseg = tc_segments(a.B, a.H, a.T);
   const int bhn = a.B * a.H;
   float* W = static_cast<float*>(a.workspace);
-  const bool use_ws = (nseg > 1) || (a.S0 != nullptr);
   {
     cudaError_t e = cudaFuncSetAttribute(sanatan_tc_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -707,23 +782,21 @@ cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st) {
   p.S0 = a.S0;
   p.z0 = a.z0;
   if (nseg > 1) {
+    // State-only pass: the sum of each segment but the last -> W[bh][p].  The
+    // main pass then starts segment p from S0 plus the sums of segments < p.
     TcParams d = p;
-    d.seg_grid = nseg - 1;  // the last segment's sum is never needed
-    d.delta_out = W;        // segment p of sequence bh -> W[bh][p]
-    d.init_sc = nullptr;
+    d.seg_grid = nseg - 1;
+    d.delta_out = W;
+    d.deltas = nullptr;
+    d.S0 = nullptr;
+    d.z0 = nullptr;
     d.o = nullptr;
     sanatan_tc_kernel<true><<<bhn * (nseg - 1), kThreads, kSmemBytes, st>>>(d);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if (use_ws) {
-    dim3 grid((kSCRows * 65 + 255) / 256, bhn);
-    seg_scan_kernel<<<grid, 256, 0, st>>>(a.S0, a.z0, W, nseg, nseg > 1 ? 1 : 0);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   p.seg_grid = nseg;
-  p.init_sc = use_ws ? W : nullptr;
+  p.deltas = nseg > 1 ? W : nullptr;
   p.o = a.o;
   p.Dn = a.D;
   p.S_out = a.S_out;

@@ -24,9 +24,18 @@ constexpr float kC2 = 0.0019350051879882812f;
 constexpr float kC3 = 3.019916050561733e-07f;
 constexpr double kTwoPiD = 6.283185307179586476925286766559;
 
+// Float64 reduction for positions or rates outside the float fast range.
+// Kept out of line: float64 is far slower than float32 on this GPU, and an
+// inlined copy could be evaluated (if-converted) even when not taken.
+static __device__ __noinline__ float phase_mod_2pi_f64(int64_t t, float phi) {
+  const double p = static_cast<double>(t) * static_cast<double>(phi);
+  const double k = rint(p * (1.0 / kTwoPiD));
+  return static_cast<float>(fma(-k, kTwoPiD, p));
+}
+
 // t * phi reduced into [-pi, pi] to about 3e-7 rad.  The product is kept as an
 // exact float pair (FMA two-product) and reduced by the three-part 2*pi above;
-// positions or rates outside the float fast range take a float64 path.
+// positions or rates outside the float fast range take the float64 path.
 __device__ __forceinline__ float phase_mod_2pi(int64_t t, float phi) {
   if (t > -(1LL << 24) && t < (1LL << 24)) {
     const float tf = static_cast<float>(t);
@@ -39,9 +48,7 @@ __device__ __forceinline__ float phase_mod_2pi(int64_t t, float phi) {
       return r + fmaf(-k, kC3, p_lo);
     }
   }
-  const double p = static_cast<double>(t) * static_cast<double>(phi);
-  const double k = rint(p / kTwoPiD);
-  return static_cast<float>(fma(-k, kTwoPiD, p));
+  return phase_mod_2pi_f64(t, phi);
 }
 
 // theta = pi u / (1 + |u|), correctly rounded division.
