@@ -48,6 +48,15 @@ constexpr int kC = 128;              // tokens per chunk (= MMA M)
 constexpr int kNF = 320;             // non-constant features
 constexpr int kSCRows = kNF + 1;     // + the [sum v | count] row
 constexpr int kSCCols = 80;          // compact state row stride (floats)
+// Per-segment state sums in the workspace: 68 columns (S, z, 3 pad) of 321
+// rows, stored per 128-row tile column-major with the row index fastest, so
+// that the threads of a warp (one row each) read and write consecutive words.
+constexpr int kSCUsedCols = 68;
+__host__ __device__ constexpr int sc_tile_rows(int mt) { return mt < 2 ? 128 : kSCRows - 256; }
+__host__ __device__ constexpr int sc_index(int f, int col) {
+  return kSCUsedCols * (f & ~127) + col * sc_tile_rows(f >> 7) + (f & 127);
+}
+static_assert(kSCUsedCols * kSCRows <= kSCRows * kSCCols, "slot layout must fit the slot");
 constexpr int kXQ = 40 * 128;        // bytes per 8-token group of PhiQ
 constexpr int kXK = 41 * 128;        // PhiK: + the ones feature group (fg 40)
 constexpr int kNG = 9;               // stored 8-column groups of [V | 1 | 0]
@@ -224,7 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
   const int64_t seq_row0 = static_cast<int64_t>(bh) * prm.T;  // first token row of the sequence
   const bool last_seg = (seg == prm.nseg - 1);
 
-  if (tid == 0 && nloc > 0) prefetch_chunk<kStateOnly>(prm, seq_row0, c_begin);
+  if (tid == 0) {
+    if (nloc > 0) prefetch_chunk<kStateOnly>(prm, seq_row0, c_begin);
+    if (nloc > 1) prefetch_chunk<kStateOnly>(prm, seq_row0, c_begin + 1);
+  }
   if (warp == kMmaWarp) {
     tmem_alloc(&m.tmem_base, kTmemCols);
     tmem_relinquish();
@@ -278,21 +290,27 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     float phi_r[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) phi_r[j] = prm.phi[h * kD + 8 * ag + j];
-    for (int ci = 0; ci < nloc; ++ci) {
-      const int chunk = c_begin + ci;
+    // Raw q / k of chunk `chunk` for this thread's four tokens (zero past the end).
+    auto load_raw = [&](const __nv_bfloat16* src, int chunk, uint4 (&dst)[4]) {
       const int tok0 = chunk * kC;
-      if (tid == 0 && ci + 1 < nloc) prefetch_chunk<kStateOnly>(prm, seq_row0, chunk + 1);
-      // All raw loads of the chunk go out together (they hit L2 after the prefetch).
-      uint4 rq[4], rk[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int t = tq + 8 * i;
-        const bool valid = tok0 + t < prm.T;
-        const int64_t off = (seq_row0 + tok0 + t) * kD + 8 * ag;
-        rk[i] = valid ? ldg_nc_v4(prm.k + off) : make_uint4(0u, 0u, 0u, 0u);
-        if constexpr (!kStateOnly)
-          rq[i] = valid ? ldg_nc_v4(prm.q + off) : make_uint4(0u, 0u, 0u, 0u);
+        dst[i] = (chunk < c_end && tok0 + t < prm.T)
+                     ? ldg_nc_v4(src + (seq_row0 + tok0 + t) * kD + 8 * ag)
+                     : make_uint4(0u, 0u, 0u, 0u);
       }
+    };
+    // q and k are loaded one chunk ahead: the loads of chunk c+1 are issued as
+    // soon as those of chunk c are consumed, so their latency hides behind the
+    // rest of chunk c and the hand-offs with the tensor core.
+    uint4 rq[4], rk[4];
+    if constexpr (!kStateOnly) load_raw(prm.q, c_begin, rq);
+    load_raw(prm.k, c_begin, rk);
+    for (int ci = 0; ci < nloc; ++ci) {
+      const int chunk = c_begin + ci;
+      const int tok0 = chunk * kC;
+      if (tid == 0 && ci + 2 < nloc) prefetch_chunk<kStateOnly>(prm, seq_row0, chunk + 2);
       float cb0[8], sb0[8];
       {
         const int64_t tabs = prm.pos0 + tok0 + tq;
@@ -329,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           rv[i] = (tok0 + t < prm.T) ? ldg_nc_v4(prm.v + (seq_row0 + tok0 + t) * kD + 8 * ag)
                                      : make_uint4(0u, 0u, 0u, 0u);
         }
+        load_raw(prm.q, chunk + 1, rq);
         if (ci > 0) wait_bar(m, kQFree, (ci - 1) & 1);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -380,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           }
         }
       }
+      load_raw(prm.k, chunk + 1, rk);
       // values: 8 columns (dimension group ag) of each of the 4 tokens
       if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
 #pragma unroll
@@ -419,20 +439,12 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           val[64] = prm.z0[rowi];
         }
         if (!kStateOnly && f < kSCRows && prm.deltas != nullptr) {
-          const float* d0 = prm.deltas + static_cast<int64_t>(bh) * prm.nseg * kSCRows * kSCCols +
-                            f * kSCCols;
+          const float* d0 = prm.deltas + static_cast<int64_t>(bh) * prm.nseg * kSCRows * kSCCols;
           for (int sp = 0; sp < seg; ++sp) {
-            const float4* s4 = reinterpret_cast<const float4*>(d0 + static_cast<int64_t>(sp) *
-                                                                         kSCRows * kSCCols);
+            const float* ds = d0 + static_cast<int64_t>(sp) * kSCRows * kSCCols;
 #pragma unroll
-            for (int e4 = 0; e4 < 17; ++e4) {
-              const float4 x = s4[e4];
-              val[4 * e4] += x.x; val[4 * e4 + 1] += x.y; val[4 * e4 + 2] += x.z;
-              val[4 * e4 + 3] += x.w;
-            }
+            for (int e = 0; e < 65; ++e) val[e] += ds[sc_index(f, e)];
           }
-#pragma unroll
-          for (int e = 65; e < 68; ++e) val[e] = 0.f;
         }
 #pragma unroll
         for (int blk = 0; blk < 5; ++blk) {
@@ -607,12 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         tmem_ld_wait();
         if (kStateOnly) {
           if (f < kSCRows) {
-            float4* dst = reinterpret_cast<float4*>(
-                prm.delta_out + (static_cast<int64_t>(bh) * prm.nseg + seg) * kSCRows * kSCCols +
-                f * kSCCols);
+            float* dst = prm.delta_out + (static_cast<int64_t>(bh) * prm.nseg + seg) * kSCRows * kSCCols;
 #pragma unroll
-            for (int e4 = 0; e4 < 17; ++e4)
-              dst[e4] = make_float4(val[4 * e4], val[4 * e4 + 1], val[4 * e4 + 2], val[4 * e4 + 3]);
+            for (int e = 0; e < 65; ++e) dst[sc_index(f, e)] = val[e];
           }
         } else {
           if (f < kNF) {
