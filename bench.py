@@ -260,6 +260,34 @@ def decode_case(batch, dev, flush, steps, warmup, stream):
     return dict(step=lambda i: step(warmup + i), N=N)
 
 
+def train_case(dev, flush, steps, warmup, stream):
+    """Training step of the B=8, H=12, T=4096 workload: the chunked forward
+    (keeping o and D) then the backward to dq, dk, dv, dgamma, domega, dphi."""
+    from constant_state_recurrence_gb300 import sanatan as S
+    x = W.make(W.TRAIN, device=dev, with_grad_out=True)
+    g = {n: x[n] for n in ("q", "k", "v", "gamma", "omega", "phi", "dO")}
+    B, H, T = x["B"], x["H"], x["T"]
+    o = torch.empty(B, H, T, 64, dtype=torch.float32, device=dev)
+    D = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(S.chunk_fwd_workspace_size(B, H, T), 16), dtype=torch.uint8, device=dev)
+    bws_n = S.chunk_bwd_workspace_size(B, H, T)
+    bws = torch.empty(max(bws_n, 16), dtype=torch.uint8, device=dev) if bws_n else None
+    _, fwd_launches = S.chunk_fwd_plan(B, H, T)
+
+    def step(_i):
+        S.sanatan_chunk_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], out=o,
+                            D_out=D, workspace=ws)
+        S.sanatan_chunk_bwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], o, D,
+                            g["dO"], want_dphi=True, workspace=bws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step(0)
+    torch.cuda.synchronize()
+    S.device_status()
+    return dict(step=step, B=B, H=H, T=T, fwd_launches=fwd_launches)
+
+
 def oracle_prefill_sample(batch=4, T=2048):
     """The float64 oracle's recurrent form on B x 12 heads x T tokens of the
     layer-forward workload; returns (tokens/s, seconds, threads)."""
@@ -346,7 +374,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["layer", "long", "decode"], default=None,
+    ap.add_argument("--only", choices=["layer", "long", "decode", "train"], default=None,
                     help="run one workload only (profiling); the JSON line keeps its keys")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -371,6 +399,8 @@ def main():
     longp = prefill_case(W.LONG, dev, flush, lp_steps, warm, stream) if want("long") else None
     dec1 = decode_case(1, dev, flush, steps, warm, stream) if want("decode") else None
     dec64 = decode_case(64, dev, flush, d64_steps, warm, stream) if want("decode") else None
+    tr_steps = max(3, steps // 10)
+    train = train_case(dev, flush, tr_steps, warm, stream) if want("train") else None
 
     gpu_idx = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -392,6 +422,9 @@ def main():
         if dec1:
             d1_whole, _ = timed_steps(dec1["step"], steps, flush, stream)
             d64_whole, _ = timed_steps(dec64["step"], d64_steps, flush, stream)
+        tr_whole, tr_kern = [nan], [nan]
+        if train:
+            tr_whole, tr_kern = timed_steps(train["step"], tr_steps, flush, stream, profile=True)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
     barrier(world)
@@ -468,6 +501,15 @@ def main():
                     "hbm_frac": DECODE_BYTES_PER_SLOT * dec64["N"] / (d64_us * 1e-6) / 1e9 / pk["hbm"],
                     "steps": d64_steps},
             "bytes_per_slot": DECODE_BYTES_PER_SLOT},
+        "train": {
+            "workload": W.TRAIN.name, "steps": tr_steps,
+            "tokens_per_s": 8 * 4096 / (statistics.mean(tr_whole) * 1e-3),
+            "ms_per_step": statistics.mean(tr_whole),
+            "bwd_kernel_ms": statistics.mean(tr_kern),
+            "tc_frac_step": (FWD_FLOPS_PER_TOKEN_HEAD + BWD_FLOPS_PER_TOKEN_HEAD) * 8 * 12 * 4096
+                            / (statistics.mean(tr_whole) * 1e-3) / 1e12 / pk["bf16"],
+            "flops_per_token_head": FWD_FLOPS_PER_TOKEN_HEAD + BWD_FLOPS_PER_TOKEN_HEAD,
+            "note": "forward + backward per step; bwd_kernel_ms times the backward's dominant kernel"},
         "timed_region_wall_s": t_wall,
     }
     clocks = clk.summary()
