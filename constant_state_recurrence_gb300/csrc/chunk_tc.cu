@@ -34,6 +34,7 @@
 #include "sanatan_internal.h"
 #include "sanatan_math.cuh"
 #include "tc_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace sanatan {
 
@@ -42,26 +43,7 @@ __device__ int g_tc_error;  // set when a bounded wait gives up
 namespace {
 
 using namespace tc;
-
-constexpr int kD = 64;
-constexpr int kC = 128;              // tokens per chunk (= MMA M)
-constexpr int kNF = 320;             // non-constant features
-constexpr int kSCRows = kNF + 1;     // + the [sum v | count] row
-constexpr int kSCCols = 80;          // compact state row stride (floats)
-// Per-segment state sums in the workspace: 68 columns (S, z, 3 pad) of 321
-// rows, stored per 128-row tile column-major with the row index fastest, so
-// that the threads of a warp (one row each) read and write consecutive words.
-constexpr int kSCUsedCols = 68;
-__host__ __device__ constexpr int sc_tile_rows(int mt) { return mt < 2 ? 128 : kSCRows - 256; }
-__host__ __device__ constexpr int sc_index(int f, int col) {
-  return kSCUsedCols * (f & ~127) + col * sc_tile_rows(f >> 7) + (f & 127);
-}
-static_assert(kSCUsedCols * kSCRows <= kSCRows * kSCCols, "slot layout must fit the slot");
-constexpr int kXQ = 40 * 128;        // bytes per 8-token group of PhiQ
-constexpr int kXK = 41 * 128;        // PhiK: + the ones feature group (fg 40)
-constexpr int kNG = 9;               // stored 8-column groups of [V | 1 | 0]
-constexpr int kLBO_SV = kNG * 128;   // K-direction core stride of S'bf16 and V
-constexpr int kN = 80;               // N of the value-side products
+using namespace tcc;
 
 constexpr uint32_t kTP = 0;          // TMEM columns: P / P-tilde
 constexpr uint32_t kTO = 128;        // O_ext
@@ -134,7 +116,17 @@ struct TcParams {
   float* S_out;
   float* z_out;
   float* delta_out;      // state-only mode: compact per-segment sums
+  // Modes used by the backward (all off for the forward):
+  int reverse;           // process token u as row T-1-u (anti-causal attention)
+  int normalize;         // 0: write the numerator N_t instead of N_t / (D_t + eps)
+  int out_bf16;          // write o as bf16 instead of f32
+  const float* extra;    // per-token value of the ones column of [V | 1] (null: 1)
 };
+
+// Row of the sequence that processing position u stands for.
+__device__ __forceinline__ int orow(const TcParams& prm, int u) {
+  return prm.reverse ? prm.T - 1 - u : u;
+}
 
 __device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
   if (*reinterpret_cast<volatile int*>(&m.abort_flag)) return false;
@@ -144,59 +136,7 @@ __device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
   return false;
 }
 
-__device__ __forceinline__ float tanh_fast(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// Eight dimensions of one token: the five non-constant channels, packed as
-// bf16 pairs (out[c][j/2] holds dims j, j+1 of channel c).
-__device__ __forceinline__ void features8(uint4 raw, const float4* __restrict__ dimc,
-                                          const float (&cb)[8], const float (&sb)[8],
-                                          uint32_t (&out)[5][4]) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    float ch[5][2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = 2 * p + h;
-      const float u = __uint_as_float((h == 0 ? (w[p] << 16) : (w[p] & 0xffff0000u)));
-      const float th = kPi * __fdividef(u, 1.0f + fabsf(u));
-      float s, c;
-      __sincosf(th, &s, &c);
-      const float4 kc = dimc[j];
-      const float r = tanh_fast(fmaf(kc.x, c, -kc.y * s));
-      const float cr = fmaf(c, cb[j], -s * sb[j]);
-      const float sr = fmaf(s, cb[j], c * sb[j]);
-      ch[0][h] = cr;
-      ch[1][h] = sr;
-      ch[2][h] = r;
-      ch[3][h] = r * cr;
-      ch[4][h] = r * sr;
-    }
-#pragma unroll
-    for (int c = 0; c < 5; ++c) out[c][p] = pack_bf16x2(ch[c][0], ch[c][1]);
-  }
-}
-
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
 
 // L2 prefetch of one chunk's rows of q (unless state-only), k and v.
 template <bool kStateOnly>
@@ -204,7 +144,7 @@ __device__ __forceinline__ void prefetch_chunk(const TcParams& prm, int64_t seq_
   const int tok0 = chunk * kC;
   const int n = min(kC, prm.T - tok0);
   if (n <= 0) return;
-  const int64_t off = (seq_row0 + tok0) * kD;
+  const int64_t off = (seq_row0 + (prm.reverse ? prm.T - tok0 - n : tok0)) * kD;
   const uint32_t bytes = static_cast<uint32_t>(n) * kD * 2;
   if (!kStateOnly) prefetch_l2_bulk(prm.q + off, bytes);
   prefetch_l2_bulk(prm.k + off, bytes);
@@ -256,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     sincosf(prm.omega[h * kD + tid] + 0.785398163397448310f, &sw, &cw);
     float s8, c8;
     sincosf(phase_mod_2pi(8, prm.phi[h * kD + tid]), &s8, &c8);
-    m.dimc[tid] = make_float4(g * cw, g * sw, c8, s8);
+    // In reverse mode consecutive processing positions step back by one row.
+    m.dimc[tid] = make_float4(g * cw, g * sw, c8, prm.reverse ? -s8 : s8);
   }
   if (tid >= 64 && tid < 64 + 68) {
     const int e = tid - 64;
@@ -275,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     const int kg = tid >> 3, row = tid & 7;
     st_shared_v4(sV + kg * kLBO_SV + 8 * 128 + row * 16, 0x3F80u, 0u, 0u, 0u);
   }
+  if (tid < 8) st_shared_v4(sV + 16 * kLBO_SV + 16 * tid, 0u, 0u, 0u, 0u);  // over-read pad
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -297,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       for (int i = 0; i < 4; ++i) {
         const int t = tq + 8 * i;
         dst[i] = (chunk < c_end && tok0 + t < prm.T)
-                     ? ldg_nc_v4(src + (seq_row0 + tok0 + t) * kD + 8 * ag)
+                     ? ldg_nc_v4(src + (seq_row0 + orow(prm, tok0 + t)) * kD + 8 * ag)
                      : make_uint4(0u, 0u, 0u, 0u);
       }
     };
@@ -313,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       if (tid == 0 && ci + 2 < nloc) prefetch_chunk<kStateOnly>(prm, seq_row0, chunk + 2);
       float cb0[8], sb0[8];
       {
-        const int64_t tabs = prm.pos0 + tok0 + tq;
+        const int64_t tabs = prm.pos0 + orow(prm, tok0 + tq);
 #pragma unroll
         for (int j = 0; j < 8; ++j) __sincosf(phase_mod_2pi(tabs, phi_r[j]), &sb0[j], &cb0[j]);
       }
@@ -344,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int t = tq + 8 * i;
-          rv[i] = (tok0 + t < prm.T) ? ldg_nc_v4(prm.v + (seq_row0 + tok0 + t) * kD + 8 * ag)
+          rv[i] = (tok0 + t < prm.T) ? ldg_nc_v4(prm.v + (seq_row0 + orow(prm, tok0 + t)) * kD + 8 * ag)
                                      : make_uint4(0u, 0u, 0u, 0u);
         }
         load_raw(prm.q, chunk + 1, rq);
@@ -355,14 +297,14 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           const uint32_t base = sQ + (t >> 3) * kXQ + (t & 7) * 16;
 #pragma unroll
           for (int c = 0; c < 5; ++c)
-            st_shared_v4(base + (c * 8 + ag) * 128, qf[i][c][0], qf[i][c][1], qf[i][c][2],
-                         qf[i][c][3]);
+            st_shared_v4(base + feat_group(ag, c + 1) * 128, qf[i][c][0], qf[i][c][1],
+                         qf[i][c][2], qf[i][c][3]);
         }
       } else {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int t = tq + 8 * i;
-          rv[i] = (tok0 + t < prm.T) ? ldg_nc_v4(prm.v + (seq_row0 + tok0 + t) * kD + 8 * ag)
+          rv[i] = (tok0 + t < prm.T) ? ldg_nc_v4(prm.v + (seq_row0 + orow(prm, tok0 + t)) * kD + 8 * ag)
                                      : make_uint4(0u, 0u, 0u, 0u);
         }
       }
@@ -388,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           const uint32_t base = sK + (t >> 3) * kXK + (t & 7) * 16;
 #pragma unroll
           for (int c = 0; c < 5; ++c)
-            st_shared_v4(base + (c * 8 + ag) * 128, kf[c][0], kf[c][1], kf[c][2], kf[c][3]);
+            st_shared_v4(base + feat_group(ag, c + 1) * 128, kf[c][0], kf[c][1], kf[c][2], kf[c][3]);
           if (ag == 0) st_shared_v4(base + 40 * 128, valid ? 0x3F80u : 0u, 0u, 0u, 0u);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -407,6 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         const int t = tq + 8 * i;
         st_shared_v4(sV + (t >> 3) * kLBO_SV + ag * 128 + (t & 7) * 16, rv[i].x, rv[i].y,
                      rv[i].z, rv[i].w);
+        if (prm.extra != nullptr && ag == 0) {
+          const float x = (tok0 + t < prm.T) ? prm.extra[seq_row0 + orow(prm, tok0 + t)] : 0.f;
+          st_shared_v4(sV + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16,
+                       __bfloat16_as_ushort(__float2bfloat16_rn(x)), 0u, 0u, 0u);
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -428,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
 #pragma unroll
         for (int e = 0; e < 80; ++e) val[e] = 0.f;
         if (!kStateOnly && f < kNF && prm.S0 != nullptr) {
-          const int c = f / kD + 1, a = f % kD;
+          int a, c;
+          feat_dim_chan(f, a, c);
           const int64_t rowi = static_cast<int64_t>(bh) * 384 + 6 * a + c;
           const float4* s4 = reinterpret_cast<const float4*>(prm.S0 + rowi * 64);
 #pragma unroll
@@ -533,24 +481,40 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           const int64_t tok = tok0 + row;
           if (tok < prm.T) {
             const float den = ov[64] + 64.0f * m.vs[64] + m.a0[64];
-            const float inv = 1.0f / (den + prm.eps);
+            const float inv = prm.normalize ? 1.0f / (den + prm.eps) : 1.0f;
             const float4* vs4 = reinterpret_cast<const float4*>(m.vs);
             const float4* a04 = reinterpret_cast<const float4*>(m.a0);
             const uint32_t srow = sS + row * kStagePitch;
+            const int64_t grow = seq_row0 + orow(prm, static_cast<int>(tok));
 #pragma unroll
             for (int e4 = 0; e4 < 16; ++e4) {
               const float4 w = vs4[e4];
               const float4 c = a04[e4];
-              st_shared_v4(srow + 16 * e4,
-                           __float_as_uint((fmaf(64.0f, w.x, ov[4 * e4 + 0]) + c.x) * inv),
-                           __float_as_uint((fmaf(64.0f, w.y, ov[4 * e4 + 1]) + c.y) * inv),
-                           __float_as_uint((fmaf(64.0f, w.z, ov[4 * e4 + 2]) + c.z) * inv),
-                           __float_as_uint((fmaf(64.0f, w.w, ov[4 * e4 + 3]) + c.w) * inv));
+              ov[4 * e4 + 0] = (fmaf(64.0f, w.x, ov[4 * e4 + 0]) + c.x) * inv;
+              ov[4 * e4 + 1] = (fmaf(64.0f, w.y, ov[4 * e4 + 1]) + c.y) * inv;
+              ov[4 * e4 + 2] = (fmaf(64.0f, w.z, ov[4 * e4 + 2]) + c.z) * inv;
+              ov[4 * e4 + 3] = (fmaf(64.0f, w.w, ov[4 * e4 + 3]) + c.w) * inv;
             }
-            fence_proxy_async_smem();
-            bulk_store_s2g(prm.o + (seq_row0 + tok) * kD, srow, kD * 4);
+            if (prm.out_bf16) {
+#pragma unroll
+              for (int e8 = 0; e8 < 8; ++e8)
+                st_shared_v4(srow + 16 * e8, pack_bf16x2(ov[8 * e8], ov[8 * e8 + 1]),
+                             pack_bf16x2(ov[8 * e8 + 2], ov[8 * e8 + 3]),
+                             pack_bf16x2(ov[8 * e8 + 4], ov[8 * e8 + 5]),
+                             pack_bf16x2(ov[8 * e8 + 6], ov[8 * e8 + 7]));
+              fence_proxy_async_smem();
+              bulk_store_s2g(reinterpret_cast<__nv_bfloat16*>(prm.o) + grow * kD, srow, kD * 2);
+            } else {
+#pragma unroll
+              for (int e4 = 0; e4 < 16; ++e4)
+                st_shared_v4(srow + 16 * e4, __float_as_uint(ov[4 * e4]),
+                             __float_as_uint(ov[4 * e4 + 1]), __float_as_uint(ov[4 * e4 + 2]),
+                             __float_as_uint(ov[4 * e4 + 3]));
+              fence_proxy_async_smem();
+              bulk_store_s2g(prm.o + grow * kD, srow, kD * 4);
+            }
             bulk_commit();
-            if (prm.Dn != nullptr) prm.Dn[seq_row0 + tok] = den;
+            if (prm.Dn != nullptr) prm.Dn[grow] = den;
           }
         }
         bulk_wait_read_all();  // this thread's staged rows have been read by the copy engine
@@ -625,7 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           }
         } else {
           if (f < kNF) {
-            const int c = f / kD + 1, a = f % kD;
+            int a, c;
+            feat_dim_chan(f, a, c);
             float4* dst = reinterpret_cast<float4*>(prm.S_out + (static_cast<int64_t>(bh) * 384 +
                                                                  6 * a + c) * 64);
 #pragma unroll
@@ -790,6 +755,7 @@ cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st) {
   p.nchunks = nchunks;
   p.S0 = a.S0;
   p.z0 = a.z0;
+  p.normalize = 1;
   if (nseg > 1) {
     // State-only pass: the sum of each segment but the last -> W[bh][p].  The
     // main pass then starts segment p from S0 plus the sums of segments < p.
