@@ -145,8 +145,9 @@ int sanatan_chunk_fwd(const void* q, const void* k, const void* v, int in_dtype,
 }
 
 size_t sanatan_chunk_bwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype) {
-  (void)B; (void)H; (void)T; (void)d; (void)dv; (void)in_dtype;
-  return 0;
+  if (B < 0 || H < 0 || T < 0 || d != 64 || dv != 64) return 0;
+  if (in_dtype != SANATAN_BF16) return 0;
+  return chunk_bwd_tc_workspace_bytes(B, H, T);
 }
 
 int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
@@ -188,7 +189,9 @@ int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
   a.dphi = dphi;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
-  return from_cuda(chunk_bwd_simt_launch(a, static_cast<cudaStream_t>(stream)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (in_dtype == SANATAN_BF16) return from_cuda(chunk_bwd_tc_launch(a, st));
+  return from_cuda(chunk_bwd_simt_launch(a, st));
 }
 
 int sanatan_set_profile_events(void* start, void* stop) {
@@ -201,7 +204,9 @@ int sanatan_set_profile_events(void* start, void* stop) {
 int sanatan_device_status(void* stream) {
   if (int s = check_arch()) return s;
   const int h = tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
-  if (h < 0) return SANATAN_ERR_CUDA;
+  const int hb = bwd_tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
+  if (h < 0 || hb < 0) return SANATAN_ERR_CUDA;
+  if (hb) return SANATAN_ERR_TIMEOUT;
   return h ? SANATAN_ERR_TIMEOUT : SANATAN_OK;
 }
 

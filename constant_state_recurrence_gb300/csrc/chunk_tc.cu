@@ -727,61 +727,97 @@ size_t chunk_fwd_tc_workspace_bytes(int B, int H, int T) {
   return static_cast<size_t>(B) * H * nseg * kSCRows * kSCCols * sizeof(float);
 }
 
-cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st) {
-  const int nchunks = (a.T + kC - 1) / kC;
-  const int nseg = tc_segments(a.B, a.H, a.T);
-  const int bhn = a.B * a.H;
-  float* W = static_cast<float*>(a.workspace);
-  {
-    cudaError_t e = cudaFuncSetAttribute(sanatan_tc_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(sanatan_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e != cudaSuccess) return e;
-  }
+namespace {
+
+cudaError_t tc_set_smem() {
+  cudaError_t e = cudaFuncSetAttribute(sanatan_tc_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(sanatan_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemBytes);
+}
+
+TcParams tc_params(const TcJob& job) {
   TcParams p{};
-  p.q = static_cast<const __nv_bfloat16*>(a.q);
-  p.k = static_cast<const __nv_bfloat16*>(a.k);
-  p.v = static_cast<const __nv_bfloat16*>(a.v);
-  p.gamma = a.gamma;
-  p.omega = a.omega;
-  p.phi = a.phi;
-  p.H = a.H;
-  p.T = a.T;
-  p.pos0 = a.pos0;
-  p.eps = a.eps;
-  p.nseg = nseg;
-  p.nchunks = nchunks;
-  p.S0 = a.S0;
-  p.z0 = a.z0;
-  p.normalize = 1;
-  if (nseg > 1) {
-    // State-only pass: the sum of each segment but the last -> W[bh][p].  The
-    // main pass then starts segment p from S0 plus the sums of segments < p.
-    TcParams d = p;
-    d.seg_grid = nseg - 1;
-    d.delta_out = W;
-    d.deltas = nullptr;
-    d.S0 = nullptr;
-    d.z0 = nullptr;
-    d.o = nullptr;
-    sanatan_tc_kernel<true><<<bhn * (nseg - 1), kThreads, kSmemBytes, st>>>(d);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+  p.q = static_cast<const __nv_bfloat16*>(job.q);
+  p.k = static_cast<const __nv_bfloat16*>(job.k);
+  p.v = static_cast<const __nv_bfloat16*>(job.v);
+  p.gamma = job.gamma;
+  p.omega = job.omega;
+  p.phi = job.phi;
+  p.H = job.H;
+  p.T = job.T;
+  p.pos0 = job.pos0;
+  p.eps = job.eps;
+  p.nseg = tc_segments(job.B, job.H, job.T);
+  p.nchunks = (job.T + kC - 1) / kC;
+  p.reverse = job.reverse;
+  p.normalize = job.normalize;
+  p.out_bf16 = job.out_bf16;
+  p.extra = job.extra;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t tc_state_pass(const TcJob& job, cudaStream_t st) {
+  cudaError_t e = tc_set_smem();
+  if (e != cudaSuccess) return e;
+  TcParams d = tc_params(job);
+  if (d.nseg <= 1) return cudaSuccess;
+  // The sum of each segment but the last -> deltas[bh][p].  A main pass then
+  // starts segment p from S0 plus the sums of segments < p.
+  d.seg_grid = d.nseg - 1;
+  d.delta_out = job.deltas;
+  sanatan_tc_kernel<true><<<job.B * job.H * (d.nseg - 1), kThreads, kSmemBytes, st>>>(d);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_attention(const TcJob& job, cudaStream_t st) {
+  cudaError_t e = tc_set_smem();
+  if (e != cudaSuccess) return e;
+  TcParams p = tc_params(job);
+  if (p.nseg > 1 && !job.deltas_ready) {
+    if ((e = tc_state_pass(job, st)) != cudaSuccess) return e;
   }
-  p.seg_grid = nseg;
-  p.deltas = nseg > 1 ? W : nullptr;
-  p.o = a.o;
-  p.Dn = a.D;
-  p.S_out = a.S_out;
-  p.z_out = a.z_out;
+  p.seg_grid = p.nseg;
+  p.deltas = p.nseg > 1 ? job.deltas : nullptr;
+  p.S0 = job.S0;
+  p.z0 = job.z0;
+  p.o = static_cast<float*>(job.o);
+  p.Dn = job.Dn;
+  p.S_out = job.S_out;
+  p.z_out = job.z_out;
   const ProfileEvents& pe = profile_events();
-  if (pe.start != nullptr) cudaEventRecord(pe.start, st);
-  sanatan_tc_kernel<false><<<bhn * nseg, kThreads, kSmemBytes, st>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (pe.stop != nullptr) cudaEventRecord(pe.stop, st);
+  const bool rec = job.record_events && pe.start != nullptr;
+  if (rec) cudaEventRecord(pe.start, st);
+  sanatan_tc_kernel<false><<<job.B * job.H * p.nseg, kThreads, kSmemBytes, st>>>(p);
+  e = cudaGetLastError();
+  if (rec) cudaEventRecord(pe.stop, st);
   return e;
+}
+
+cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st) {
+  TcJob job;
+  job.q = a.q;
+  job.k = a.k;
+  job.v = a.v;
+  job.gamma = a.gamma;
+  job.omega = a.omega;
+  job.phi = a.phi;
+  job.B = a.B;
+  job.H = a.H;
+  job.T = a.T;
+  job.pos0 = a.pos0;
+  job.eps = a.eps;
+  job.S0 = a.S0;
+  job.z0 = a.z0;
+  job.o = a.o;
+  job.Dn = a.D;
+  job.S_out = a.S_out;
+  job.z_out = a.z_out;
+  job.deltas = static_cast<float*>(a.workspace);
+  return tc_attention(job, st);
 }
 
 int tc_read_and_clear_error(cudaStream_t st) {

@@ -74,4 +74,41 @@ int tc_segments(int B, int H, int T);
 size_t chunk_fwd_tc_workspace_bytes(int B, int H, int T);
 cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st);
 int tc_read_and_clear_error(cudaStream_t st);
+
+// One causal (or, reversed, anti-causal) attention on the tensor-core kernel,
+// bf16 q, k, v of shape [B, H, T, 64].  `extra` replaces the ones column of
+// [V | 1] (the denominator) by a per-token value; `deltas` is the workspace of
+// per-segment state sums, B * H * tc_segments * 321 * 80 floats.
+struct TcJob {
+  const void* q = nullptr;
+  const void* k = nullptr;
+  const void* v = nullptr;
+  const float* extra = nullptr;
+  const float* gamma = nullptr;
+  const float* omega = nullptr;
+  const float* phi = nullptr;
+  int B = 0, H = 0, T = 0;
+  int64_t pos0 = 0;
+  float eps = 0.f;
+  const float* S0 = nullptr;
+  const float* z0 = nullptr;
+  void* o = nullptr;        // f32 or (out_bf16) bf16 [B, H, T, 64]
+  float* Dn = nullptr;
+  float* S_out = nullptr;
+  float* z_out = nullptr;
+  int reverse = 0;          // row u is processed at position T-1-u
+  int normalize = 1;        // 0: write the numerator only
+  int out_bf16 = 0;
+  float* deltas = nullptr;
+  int deltas_ready = 0;     // the state-only pass has already filled `deltas`
+  int record_events = 1;    // bracket the main launch with the profile events
+};
+// State-only pass: the sums of every segment but the last into job.deltas.
+cudaError_t tc_state_pass(const TcJob& job, cudaStream_t st);
+// The attention itself (running the state-only pass first unless deltas_ready).
+cudaError_t tc_attention(const TcJob& job, cudaStream_t st);
+
+size_t chunk_bwd_tc_workspace_bytes(int B, int H, int T);
+cudaError_t chunk_bwd_tc_launch(const ChunkBwdArgs& a, cudaStream_t st);
+int bwd_tc_read_and_clear_error(cudaStream_t st);
 }  // namespace sanatan

@@ -55,6 +55,24 @@ def test_bf16_multi_chunk():
     _compare(gr, ref, 1e-2)
 
 
+@pytest.mark.parametrize("T", [1, 127, 600, 1500])
+def test_bf16_with_state_eps_offset_segments(T):
+    """bf16 operands with an initial state, eps and a position offset; B*H = 3
+    splits T >= 256 into several segments (the per-segment sums of both time
+    directions are exercised)."""
+    x = W.make(W.TRAIN, B=1, H=3, T=T, with_grad_out=True)
+    x["phi"] = W.rates(3, 64, "geometric")
+    rng = np.random.default_rng(T + 1)
+    S0, z0 = O.final_state(rng.standard_normal((1, 3, 40, 64)), rng.standard_normal((1, 3, 40, 64)),
+                           f64(x["gamma"]), f64(x["omega"]), f64(x["phi"]), pos0=60)
+    S0 = torch.tensor(S0, dtype=torch.float32)
+    z0 = torch.tensor(z0, dtype=torch.float32)
+    gr = _run(x, x["dO"], pos0=100, eps=0.3, S0=S0, z0=z0)
+    ref = O.attn_backward(**ref_args(x), dO=f64(x["dO"]), pos0=100, eps=0.3, S0=f64(S0),
+                          z0=f64(z0))
+    _compare(gr, ref, 1e-2)
+
+
 def test_bf16_grad_dtype_f32_upstream():
     x = W.make(W.TRAIN, B=1, H=2, T=129, with_grad_out=True)
     gr = _run(x, x["dO"].float())
