@@ -12,9 +12,9 @@
 // Feature layout.  Channel 0 of every dimension is the constant 1, so its 64
 // features are the same for every token: they contribute exactly 64 to every
 // score and 64 * sum(v) to every numerator.  The tensor cores therefore see
-// only the 320 non-constant features, ordered channel-major
-// (f = (c-1)*64 + a for c = 1..5 = cos, sin, r, r cos, r sin); the constant
-// channel is added back in the epilogues.  The running sum of v and the token
+// only the 320 non-constant features (c = 1..5 = cos, sin, r, r cos, r sin),
+// ordered by groups of eight dimensions, f = 40 (a / 8) + 8 (c - 1) + a % 8;
+// the constant channel is added back in the epilogues.  The running sum of v and the token
 // count live in an extra state row (row 320) produced by a ones feature of
 // PhiK, so they accumulate in f32 on the tensor core with the rest of the
 // state.
