@@ -654,9 +654,14 @@ cudaError_t chunk_bwd_tc_launch(const ChunkBwdArgs& a, cudaStream_t st) {
     if ((e = tc_state_pass(rs, st)) != cudaSuccess) return e;
   }
   {
-    cudaError_t ee = cudaFuncSetAttribute(fsa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          kSmemBytes);
-    if (ee != cudaSuccess) return ee;
+    static bool done[64];
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (!(dev >= 0 && dev < 64 && done[dev])) {
+      e = cudaFuncSetAttribute(fsa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) done[dev] = true;
+    }
   }
   FsaParams p{};
   p.gamma = f.gamma; p.omega = f.omega; p.phi = f.phi;

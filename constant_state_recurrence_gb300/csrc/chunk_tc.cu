@@ -729,12 +729,20 @@ size_t chunk_fwd_tc_workspace_bytes(int B, int H, int T) {
 
 namespace {
 
+// The shared-memory opt-in is a per-device attribute of the kernel: set it once.
 cudaError_t tc_set_smem() {
-  cudaError_t e = cudaFuncSetAttribute(sanatan_tc_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static bool done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(sanatan_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemBytes);
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(sanatan_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(sanatan_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
 }
 
 TcParams tc_params(const TcJob& job) {
