@@ -19,14 +19,16 @@
 // PhiK, so they accumulate in f32 on the tensor core with the rest of the
 // state.
 //
-// Roles (512 threads, four warpgroups): warps 0-7 featurise q, k and stage v
-// into shared memory (168 registers each after setmaxnreg); warps 8-11 drain
-// TMEM (mask + split the scores into bf16 hi/lo parts, snapshot the state to
-// bf16 for the next chunk, normalise and store the outputs; 144 registers);
-// one thread of warp 12 issues every tcgen05.mma (warps 12-15 keep 32
-// registers).  All hand-offs are mbarriers with bounded waits.  The next
-// chunk's q, k, v are bulk-prefetched into L2 while the current one runs, and
-// output rows leave through bulk asynchronous copies.
+// Roles (768 threads, six warpgroups): warps 0-7 featurise q into Phi(Q) and
+// warps 8-15 k into Phi(K) (80 registers each, the launch allocation); warps
+// 16-19 drain TMEM (mask + split the scores into bf16 hi/lo parts, snapshot
+// the state to bf16 for the next chunk, normalise and store the outputs; 128
+// registers after setmaxnreg); one thread of warp 20 issues every
+// tcgen05.mma and warps 21-22 copy v rows into shared memory with cp.async
+// (that warpgroup keeps 32 registers).  All hand-offs are mbarriers with
+// bounded waits.  The next chunk's q, k, v are bulk-prefetched into L2 while
+// the current one runs; each output tile is staged in shared memory and
+// written with coalesced stores.
 //
 // Shared-memory operands use the canonical no-swizzle layout (8 x 16-byte
 // core matrices); TMEM holds P (128 cols), O_ext (80) and the f32 state
@@ -60,39 +62,45 @@ constexpr int kOffV = kOffS + 40 * kLBO_SV;
 constexpr int kOffMisc = kOffV + 16 * kLBO_SV + 128;
 
 enum Bar {
-  kFeatFull = 0, kPFull, kPTilde, kQFree, kStateDone, kPVDone, kSnapReady, kOFree, kDrain,
-  kNumBars
+  kFeatQ = 0, kFeatK, kFeatV, kPFull, kPTilde, kQFree, kStateDone, kPVDone, kSnapReady, kOFree,
+  kDrain, kNumBars
 };
 
 struct Misc {
   float4 dimc[64];   // per dim: gamma*sqrt2*cos(omega+pi/4), gamma*sqrt2*sin(omega+pi/4),
                      //          cos(8 phi), sin(8 phi)
+  float phi[64];     // rotation rates
   float vs[68];      // state row 320 before the current chunk: sum v (64), count
   float a0[68];      // constant-channel part of S0: sum_a S0[6a] (64), sum_a z0[6a]
   uint64_t bar[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
 };
-// Output staging for the bulk row stores: rows of 256 B at a 272-B pitch (the
-// extra 16 B spread consecutive rows over the banks).  It lives in the bf16
-// state snapshot buffer, which is free between the chunk's Phi(Q)[S|z]
-// product and the next snapshot.
+// Output staging: rows at a 272-B (f32) or 144-B (bf16) pitch, so that the
+// row-per-thread writes spread over the banks.  It lives in the bf16 state
+// snapshot buffer, which is free between the chunk's Phi(Q)[S|z] product and
+// the next snapshot.
 constexpr int kStagePitch = 272;
+constexpr int kStagePitchH = 144;
 static_assert(kC * kStagePitch <= 40 * kLBO_SV, "output staging must fit the snapshot buffer");
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kSmemBytes <= 232448, "shared memory layout exceeds 227 KB");
 
-constexpr int kThreads = 512;
-// Register split: 256 x 168 + 128 x 144 + 128 x 32 = 65,536 = 512 x 128, the
-// registers the block is launched with.
-constexpr uint32_t kRegFeat = 168;
-constexpr uint32_t kRegEpi = 144;
+constexpr int kThreads = 768;
+// Register split: the block is launched with 768 x 80 registers; the four
+// featuriser warpgroups keep 80, the MMA / value-loader warpgroup drops to 32
+// and the epilogue warpgroup takes the difference.
+constexpr uint32_t kRegLaunch = 80;
+constexpr uint32_t kRegEpi = 128;
 constexpr uint32_t kRegMma = 32;
-static_assert(256 * kRegFeat + 128 * kRegEpi + 128 * kRegMma <= kThreads * 128,
+static_assert(512 * kRegLaunch + 128 * kRegEpi + 128 * kRegMma <= kThreads * kRegLaunch,
               "setmaxnreg split must fit the launch allocation");
-constexpr int kFeatWarps = 8;
-constexpr int kEpiWarp0 = 8;
-constexpr int kMmaWarp = 12;
+constexpr int kQWarps = 8;     // warps 0-7: query features
+constexpr int kKWarp0 = 8;     // warps 8-15: key features
+constexpr int kEpiWarp0 = 16;  // warps 16-19: TMEM epilogue
+constexpr int kMmaWarp = 20;   // warp 20: MMA issue (one thread)
+constexpr int kVWarp0 = 21;    // warps 21-22: value loads
+constexpr int kVWarps = 2;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
 
 struct TcParams {
@@ -183,7 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
   }
   if (tid == 0) {
     for (int b = 0; b < kNumBars; ++b) {
-      const uint32_t cnt = (b == kFeatFull) ? kFeatWarps
+      // In the state-only pass both featuriser groups produce keys.
+      const uint32_t cnt = (b == kFeatQ) ? kQWarps
+                           : (b == kFeatK) ? (kStateOnly ? 16u : 8u)
+                           : (b == kFeatV) ? static_cast<uint32_t>(kVWarps)
                            : (b == kPTilde || b == kSnapReady || b == kOFree) ? 4u : 1u;
       mbar_init(&m.bar[b], cnt);
     }
@@ -198,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     sincosf(phase_mod_2pi(8, prm.phi[h * kD + tid]), &s8, &c8);
     // In reverse mode consecutive processing positions step back by one row.
     m.dimc[tid] = make_float4(g * cw, g * sw, c8, prm.reverse ? -s8 : s8);
+    m.phi[tid] = prm.phi[h * kD + tid];
   }
   if (tid >= 64 && tid < 64 + 68) {
     const int e = tid - 64;
@@ -222,142 +234,80 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
   tc_fence_after();
   const uint32_t tmem = m.tmem_base;
 
-  if (warp < kFeatWarps) {
-    // ------------------------------------------------------------ featuriser
-    setmaxnreg_inc<kRegFeat>();
+  if (warp < kEpiWarp0) {
+    // ------------------------------------------------------------ featurisers
+    // Warps 0-7 write Phi(Q), warps 8-15 Phi(K) (in the state-only pass both
+    // groups write Phi(K), two tokens each).  Lane (r, dimension group ag)
+    // owns tokens tq + 8 i of the chunk.  The block keeps its launch registers.
+    const bool kgrp = kStateOnly || warp >= kKWarp0;
+    const int fw = warp & 7;
     const int r = lane & 7;
-    const int ag = (lane >> 3) + 4 * (warp & 1);      // dimension group (8 dims)
-    const int tq = 32 * (warp >> 1) + r;              // first of this thread's 4 tokens
+    const int ag = (lane >> 3) + 4 * (fw & 1);
+    constexpr int kNI = kStateOnly ? 2 : 4;  // tokens per thread
+    const int tq = 32 * (fw >> 1) + r + ((kStateOnly && warp < kKWarp0) ? 16 : 0);
     const float4* dimc = &m.dimc[8 * ag];
-    float phi_r[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) phi_r[j] = prm.phi[h * kD + 8 * ag + j];
-    // Raw q / k of chunk `chunk` for this thread's four tokens (zero past the end).
-    auto load_raw = [&](const __nv_bfloat16* src, int chunk, uint4 (&dst)[4]) {
+    const float* phi_s = &m.phi[8 * ag];
+    const __nv_bfloat16* src = kgrp ? prm.k : prm.q;
+    const uint32_t sdst = kgrp ? sK : sQ;
+    const int pitch = kgrp ? kXK : kXQ;
+    // Raw rows of chunk `chunk` for this thread's tokens (zero past the end).
+    // They are loaded right after a hand-off and consumed after the next wait:
+    // an mbarrier arrive has release semantics and would stall on loads still
+    // in flight.
+    uint4 raw[kNI];
+    auto load_raw = [&](int chunk) {
       const int tok0 = chunk * kC;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < kNI; ++i) {
         const int t = tq + 8 * i;
-        dst[i] = (chunk < c_end && tok0 + t < prm.T)
+        raw[i] = (chunk < c_end && tok0 + t < prm.T)
                      ? ldg_nc_v4(src + (seq_row0 + orow(prm, tok0 + t)) * kD + 8 * ag)
                      : make_uint4(0u, 0u, 0u, 0u);
       }
     };
-    // q and k are loaded one chunk ahead: the loads of chunk c+1 are issued as
-    // soon as those of chunk c are consumed, so their latency hides behind the
-    // rest of chunk c and the hand-offs with the tensor core.
-    uint4 rq[4], rk[4];
-    if constexpr (!kStateOnly) load_raw(prm.q, c_begin, rq);
-    load_raw(prm.k, c_begin, rk);
+    load_raw(c_begin);
     for (int ci = 0; ci < nloc; ++ci) {
       const int chunk = c_begin + ci;
       const int tok0 = chunk * kC;
       if (tid == 0 && ci + 2 < nloc) prefetch_chunk<kStateOnly>(prm, seq_row0, chunk + 2);
-      float cb0[8], sb0[8];
+      float cb[8], sb[8];
       {
         const int64_t tabs = prm.pos0 + orow(prm, tok0 + tq);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) __sincosf(phase_mod_2pi(tabs, phi_r[j]), &sb0[j], &cb0[j]);
+        for (int j = 0; j < 8; ++j) __sincosf(phase_mod_2pi(tabs, phi_s[j]), &sb[j], &cb[j]);
       }
-      uint4 rv[4];
-      if constexpr (!kStateOnly) {
-        uint32_t qf[4][5][4];
-        float cb[8], sb[8];
+      // The buffer is free once the previous chunk's MMAs have read it.
+      if (ci > 0) wait_bar(m, kgrp ? kStateDone : kQFree, (ci - 1) & 1);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) { cb[j] = cb0[j]; sb[j] = sb0[j]; }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (tok0 + tq + 8 * i < prm.T) {
-            features8(rq[i], dimc, cb, sb, qf[i]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 5; ++c)
-#pragma unroll
-              for (int p = 0; p < 4; ++p) qf[i][c][p] = 0u;
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 kc = dimc[j];
-            const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
-            sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
-            cb[j] = nc;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int t = tq + 8 * i;
-          rv[i] = (tok0 + t < prm.T) ? ldg_nc_v4(prm.v + (seq_row0 + orow(prm, tok0 + t)) * kD + 8 * ag)
-                                     : make_uint4(0u, 0u, 0u, 0u);
-        }
-        load_raw(prm.q, chunk + 1, rq);
-        if (ci > 0) wait_bar(m, kQFree, (ci - 1) & 1);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int t = tq + 8 * i;
-          const uint32_t base = sQ + (t >> 3) * kXQ + (t & 7) * 16;
-#pragma unroll
-          for (int c = 0; c < 5; ++c)
-            st_shared_v4(base + feat_group(ag, c + 1) * 128, qf[i][c][0], qf[i][c][1],
-                         qf[i][c][2], qf[i][c][3]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int t = tq + 8 * i;
-          rv[i] = (tok0 + t < prm.T) ? ldg_nc_v4(prm.v + (seq_row0 + orow(prm, tok0 + t)) * kD + 8 * ag)
-                                     : make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      // keys
-      if (ci > 0) wait_bar(m, kStateDone, (ci - 1) & 1);
-      {
-        float cb[8], sb[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) { cb[j] = cb0[j]; sb[j] = sb0[j]; }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int t = tq + 8 * i;
-          const bool valid = tok0 + t < prm.T;
-          uint32_t kf[5][4];
-          if (valid) {
-            features8(rk[i], dimc, cb, sb, kf);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 5; ++c)
-#pragma unroll
-              for (int p = 0; p < 4; ++p) kf[c][p] = 0u;
-          }
-          const uint32_t base = sK + (t >> 3) * kXK + (t & 7) * 16;
-#pragma unroll
-          for (int c = 0; c < 5; ++c)
-            st_shared_v4(base + feat_group(ag, c + 1) * 128, kf[c][0], kf[c][1], kf[c][2], kf[c][3]);
-          if (ag == 0) st_shared_v4(base + 40 * 128, valid ? 0x3F80u : 0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 kc = dimc[j];
-            const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
-            sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
-            cb[j] = nc;
-          }
-        }
-      }
-      load_raw(prm.k, chunk + 1, rk);
-      // values: 8 columns (dimension group ag) of each of the 4 tokens
-      if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < kNI; ++i) {
         const int t = tq + 8 * i;
-        st_shared_v4(sV + (t >> 3) * kLBO_SV + ag * 128 + (t & 7) * 16, rv[i].x, rv[i].y,
-                     rv[i].z, rv[i].w);
-        if (prm.extra != nullptr && ag == 0) {
-          const float x = (tok0 + t < prm.T) ? prm.extra[seq_row0 + orow(prm, tok0 + t)] : 0.f;
-          st_shared_v4(sV + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16,
-                       __bfloat16_as_ushort(__float2bfloat16_rn(x)), 0u, 0u, 0u);
+        const bool valid = tok0 + t < prm.T;
+        uint32_t f[5][4];
+        if (valid) {
+          features8(raw[i], dimc, cb, sb, f);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 5; ++c)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) f[c][p] = 0u;
+        }
+        const uint32_t base = sdst + (t >> 3) * pitch + (t & 7) * 16;
+#pragma unroll
+        for (int c = 0; c < 5; ++c)
+          st_shared_v4(base + feat_group(ag, c + 1) * 128, f[c][0], f[c][1], f[c][2], f[c][3]);
+        if (kgrp && ag == 0) st_shared_v4(base + 40 * 128, valid ? 0x3F80u : 0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 kc = dimc[j];
+          const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
+          sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
+          cb[j] = nc;
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&m.bar[kFeatFull]);
+      if (lane == 0) mbar_arrive(&m.bar[kgrp ? kFeatK : kFeatQ]);
+      load_raw(chunk + 1);
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ TMEM epilogue
@@ -464,10 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         if (lane == 0) mbar_arrive(&m.bar[kPTilde]);
 
         // E3: outputs of this chunk (state row 320 in m.vs is still the pre-chunk one).
-        // Each row is normalised in registers, staged in the free snapshot buffer
-        // and written to global memory by one 256-byte bulk copy.
+        // Each row is normalised in registers and staged in the free snapshot
+        // buffer; the four warps then copy the staged tile out with coalesced
+        // 16-byte stores (each warp instruction writes whole rows).
         wait_bar(m, kPVDone, ci & 1);
         tc_fence_after();
+        const int nrow = min(kC, prm.T - tok0);
         {
           float ov[80];
 #pragma unroll
@@ -478,14 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
             for (int i = 0; i < 16; ++i) ov[16 * blk + i] = x[i];
           }
           tmem_ld_wait();
-          const int64_t tok = tok0 + row;
-          if (tok < prm.T) {
+          if (row < nrow) {
             const float den = ov[64] + 64.0f * m.vs[64] + m.a0[64];
             const float inv = prm.normalize ? 1.0f / (den + prm.eps) : 1.0f;
             const float4* vs4 = reinterpret_cast<const float4*>(m.vs);
             const float4* a04 = reinterpret_cast<const float4*>(m.a0);
-            const uint32_t srow = sS + row * kStagePitch;
-            const int64_t grow = seq_row0 + orow(prm, static_cast<int>(tok));
 #pragma unroll
             for (int e4 = 0; e4 < 16; ++e4) {
               const float4 w = vs4[e4];
@@ -496,31 +445,42 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
               ov[4 * e4 + 3] = (fmaf(64.0f, w.w, ov[4 * e4 + 3]) + c.w) * inv;
             }
             if (prm.out_bf16) {
+              const uint32_t srow = sS + row * kStagePitchH;
 #pragma unroll
               for (int e8 = 0; e8 < 8; ++e8)
                 st_shared_v4(srow + 16 * e8, pack_bf16x2(ov[8 * e8], ov[8 * e8 + 1]),
                              pack_bf16x2(ov[8 * e8 + 2], ov[8 * e8 + 3]),
                              pack_bf16x2(ov[8 * e8 + 4], ov[8 * e8 + 5]),
                              pack_bf16x2(ov[8 * e8 + 6], ov[8 * e8 + 7]));
-              fence_proxy_async_smem();
-              bulk_store_s2g(reinterpret_cast<__nv_bfloat16*>(prm.o) + grow * kD, srow, kD * 2);
             } else {
+              const uint32_t srow = sS + row * kStagePitch;
 #pragma unroll
               for (int e4 = 0; e4 < 16; ++e4)
                 st_shared_v4(srow + 16 * e4, __float_as_uint(ov[4 * e4]),
                              __float_as_uint(ov[4 * e4 + 1]), __float_as_uint(ov[4 * e4 + 2]),
                              __float_as_uint(ov[4 * e4 + 3]));
-              fence_proxy_async_smem();
-              bulk_store_s2g(prm.o + grow * kD, srow, kD * 4);
             }
-            bulk_commit();
-            if (prm.Dn != nullptr) prm.Dn[grow] = den;
+            if (prm.Dn != nullptr) prm.Dn[seq_row0 + orow(prm, tok0 + row)] = den;
           }
         }
-        bulk_wait_read_all();  // this thread's staged rows have been read by the copy engine
         tc_fence_before();
-        epi_sync();  // all staged rows read, every thread done with m.vs and O
+        epi_sync();  // every row staged, every thread done with m.vs and O
         if (lane == 0) mbar_arrive(&m.bar[kOFree]);
+        {
+          // 16-byte pieces: piece p is column piece p % per_row of staged row p / per_row.
+          const int et = tid - 32 * kEpiWarp0;
+          const int lg = prm.out_bf16 ? 3 : 4;  // log2 of pieces per row
+          const int pitch = prm.out_bf16 ? kStagePitchH : kStagePitch;
+          unsigned char* obase = reinterpret_cast<unsigned char*>(prm.o);
+          const int64_t row_bytes = int64_t{16} << lg;
+          for (int pc = et; pc < (nrow << lg); pc += 128) {
+            const int rr = pc >> lg, cc = pc & ((1 << lg) - 1);
+            const uint4 val = *reinterpret_cast<const uint4*>(smem + kOffS + rr * pitch + 16 * cc);
+            *reinterpret_cast<uint4*>(obase + (seq_row0 + orow(prm, tok0 + rr)) * row_bytes +
+                                      16 * cc) = val;
+          }
+        }
+        epi_sync();  // staged tile read out before the snapshot overwrites it
 
         // E2: snapshot of the state after this chunk, for the next chunk.
         wait_bar(m, kStateDone, ci & 1);
@@ -623,6 +583,36 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
   } else {
     setmaxnreg_dec<kRegMma>();
   }
+  if (warp >= kVWarp0 && warp < kVWarp0 + kVWarps) {
+    // ------------------------------------------------------------ value loads
+    // v rows go straight to [V | 1] in shared memory through 16-byte cp.async
+    // copies (the ones column is constant; the optional extra column replaces
+    // it per token).
+    const int vt = tid - 32 * kVWarp0;
+    for (int ci = 0; ci < nloc; ++ci) {
+      const int tok0 = (c_begin + ci) * kC;
+      const int nrow = min(kC, prm.T - tok0);
+      if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
+      for (int pc = vt; pc < kC * 8; pc += 32 * kVWarps) {
+        const int t = pc >> 3, ng = pc & 7;
+        const bool valid = t < nrow;
+        const __nv_bfloat16* gsrc =
+            prm.v + (seq_row0 + orow(prm, tok0 + (valid ? t : 0))) * kD + 8 * ng;
+        cp_async_16(sV + (t >> 3) * kLBO_SV + ng * 128 + (t & 7) * 16, gsrc, valid ? 16u : 0u);
+      }
+      if (prm.extra != nullptr) {
+        for (int t = vt; t < kC; t += 32 * kVWarps) {
+          const float x = t < nrow ? prm.extra[seq_row0 + orow(prm, tok0 + t)] : 0.f;
+          st_shared_v4(sV + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16,
+                       __bfloat16_as_ushort(__float2bfloat16_rn(x)), 0u, 0u, 0u);
+        }
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.bar[kFeatV]);
+    }
+  }
   if (warp == kMmaWarp && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idQK = idesc_bf16_f32(128, 128, false, false);
@@ -644,7 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       // this warpgroup's registers).
       uint64_t dQl = dQ, dKbl = dKb, dKal = dKa, dSl = dS, dVl = dV;
       asm volatile("" : "+l"(dQl), "+l"(dKbl), "+l"(dKal), "+l"(dSl), "+l"(dVl));
-      wait_bar(m, kFeatFull, ci & 1);
+      if constexpr (!kStateOnly) wait_bar(m, kFeatQ, ci & 1);
+      wait_bar(m, kFeatK, ci & 1);
       tc_fence_after();
       if constexpr (!kStateOnly) {
 #pragma unroll
@@ -663,6 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         wait_bar(m, kSnapReady, 0);  // initial state is in TMEM
         tc_fence_after();
       }
+      wait_bar(m, kFeatV, ci & 1);
+      tc_fence_after();
       asm volatile("" : "+l"(dKal), "+l"(dVl));
 #pragma unroll
       for (int s = 0; s < 8; ++s)
@@ -689,7 +682,6 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     wait_bar(m, kDrain, 0);
   }
 
-  if (warp >= kEpiWarp0 && warp < kMmaWarp) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {

@@ -124,6 +124,18 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (no registers held while in
+// flight); the destination is zero-filled past `src_bytes` (0 or 16).
+__device__ __forceinline__ void cp_async_16(uint32_t sdst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sdst), "l"(gsrc),
+               "r"(src_bytes)
+               : "memory");
+}
+// Wait until all of this thread's cp.async copies have landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // ------------------------------------------------------------ fences
 // Thread writes to shared memory -> visible to the async proxy (tensor core).
 __device__ __forceinline__ void fence_proxy_async_smem() {
