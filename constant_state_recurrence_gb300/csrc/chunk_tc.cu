@@ -60,16 +60,25 @@ constexpr int kOffV = kOffS + 40 * kLBO_SV;
 // The MMAs read up to 128 B past S'bf16 and V (ignored padding columns); the
 // pad keeps those reads inside this layout and away from the mbarriers.
 constexpr int kOffMisc = kOffV + 16 * kLBO_SV + 128;
+// The state-only pass needs no Phi(Q) and no snapshot: it double-buffers
+// Phi(K) and V instead, so that the keys of chunk c + 1 are featurised while
+// the tensor core accumulates chunk c.
+constexpr int kSoK1 = 16 * kXK;
+constexpr int kSoV0 = 2 * 16 * kXK;
+constexpr int kSoV1 = kSoV0 + 16 * kLBO_SV;
+static_assert(kSoV1 + 16 * kLBO_SV + 128 <= kOffMisc, "state-only buffers must fit");
 
 enum Bar {
   kFeatQ = 0, kFeatK, kFeatV, kPFull, kPTilde, kQFree, kStateDone, kPVDone, kSnapReady, kOFree,
-  kDrain, kNumBars
+  kDrain,
+  // second buffer of Phi(K) / V in the state-only pass
+  kFeatK1, kFeatV1, kStateDone1,
+  kNumBars
 };
 
 struct Misc {
   float4 dimc[64];   // per dim: gamma*sqrt2*cos(omega+pi/4), gamma*sqrt2*sin(omega+pi/4),
                      //          cos(8 phi), sin(8 phi)
-  float phi[64];     // rotation rates
   float vs[68];      // state row 320 before the current chunk: sum v (64), count
   float a0[68];      // constant-channel part of S0: sum_a S0[6a] (64), sum_a z0[6a]
   uint64_t bar[kNumBars];
@@ -193,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     for (int b = 0; b < kNumBars; ++b) {
       // In the state-only pass both featuriser groups produce keys.
       const uint32_t cnt = (b == kFeatQ) ? kQWarps
-                           : (b == kFeatK) ? (kStateOnly ? 16u : 8u)
-                           : (b == kFeatV) ? static_cast<uint32_t>(kVWarps)
+                           : (b == kFeatK || b == kFeatK1) ? (kStateOnly ? 16u : 8u)
+                           : (b == kFeatV || b == kFeatV1) ? static_cast<uint32_t>(kVWarps)
                            : (b == kPTilde || b == kSnapReady || b == kOFree) ? 4u : 1u;
       mbar_init(&m.bar[b], cnt);
     }
@@ -209,7 +218,6 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     sincosf(phase_mod_2pi(8, prm.phi[h * kD + tid]), &s8, &c8);
     // In reverse mode consecutive processing positions step back by one row.
     m.dimc[tid] = make_float4(g * cw, g * sw, c8, prm.reverse ? -s8 : s8);
-    m.phi[tid] = prm.phi[h * kD + tid];
   }
   if (tid >= 64 && tid < 64 + 68) {
     const int e = tid - 64;
@@ -226,7 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
   // Constant part of [V | 1 | 0]: column 64 is one, 65..71 zero.
   if (tid < 16 * 8) {
     const int kg = tid >> 3, row = tid & 7;
-    st_shared_v4(sV + kg * kLBO_SV + 8 * 128 + row * 16, 0x3F80u, 0u, 0u, 0u);
+    if constexpr (kStateOnly) {
+      st_shared_v4(smem_u32(smem + kSoV0) + kg * kLBO_SV + 8 * 128 + row * 16, 0x3F80u, 0u, 0u, 0u);
+      st_shared_v4(smem_u32(smem + kSoV1) + kg * kLBO_SV + 8 * 128 + row * 16, 0x3F80u, 0u, 0u, 0u);
+    } else {
+      st_shared_v4(sV + kg * kLBO_SV + 8 * 128 + row * 16, 0x3F80u, 0u, 0u, 0u);
+    }
   }
   if (tid < 8) st_shared_v4(sV + 16 * kLBO_SV + 16 * tid, 0u, 0u, 0u, 0u);  // over-read pad
   tc_fence_before();
@@ -246,9 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     constexpr int kNI = kStateOnly ? 2 : 4;  // tokens per thread
     const int tq = 32 * (fw >> 1) + r + ((kStateOnly && warp < kKWarp0) ? 16 : 0);
     const float4* dimc = &m.dimc[8 * ag];
-    const float* phi_s = &m.phi[8 * ag];
+    const float* phi_g = prm.phi + h * kD + 8 * ag;
     const __nv_bfloat16* src = kgrp ? prm.k : prm.q;
-    const uint32_t sdst = kgrp ? sK : sQ;
+    const uint32_t sdst0 = kgrp ? sK : sQ;
     const int pitch = kgrp ? kXK : kXQ;
     // Raw rows of chunk `chunk` for this thread's tokens (zero past the end).
     // They are loaded right after a hand-off and consumed after the next wait:
@@ -274,10 +287,16 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       {
         const int64_t tabs = prm.pos0 + orow(prm, tok0 + tq);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) __sincosf(phase_mod_2pi(tabs, phi_s[j]), &sb[j], &cb[j]);
+        for (int j = 0; j < 8; ++j) __sincosf(phase_mod_2pi(tabs, __ldg(phi_g + j)), &sb[j], &cb[j]);
       }
-      // The buffer is free once the previous chunk's MMAs have read it.
-      if (ci > 0) wait_bar(m, kgrp ? kStateDone : kQFree, (ci - 1) & 1);
+      // The buffer is free once the MMAs of its previous chunk have read it.
+      uint32_t sdst = sdst0;
+      if constexpr (kStateOnly) {
+        sdst = smem_u32(smem) + (ci & 1) * kSoK1;
+        if (ci > 1) wait_bar(m, (ci & 1) ? kStateDone1 : kStateDone, ((ci >> 1) - 1) & 1);
+      } else {
+        if (ci > 0) wait_bar(m, kgrp ? kStateDone : kQFree, (ci - 1) & 1);
+      }
 #pragma unroll
       for (int i = 0; i < kNI; ++i) {
         const int t = tq + 8 * i;
@@ -306,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&m.bar[kgrp ? kFeatK : kFeatQ]);
+      if (lane == 0)
+        mbar_arrive(&m.bar[kStateOnly ? ((ci & 1) ? kFeatK1 : kFeatK) : (kgrp ? kFeatK : kFeatQ)]);
       load_raw(chunk + 1);
     }
   } else if (warp < kMmaWarp) {
@@ -592,25 +612,31 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     for (int ci = 0; ci < nloc; ++ci) {
       const int tok0 = (c_begin + ci) * kC;
       const int nrow = min(kC, prm.T - tok0);
-      if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
+      uint32_t vdst = sV;
+      if constexpr (kStateOnly) {
+        vdst = smem_u32(smem + ((ci & 1) ? kSoV1 : kSoV0));
+        if (ci > 1) wait_bar(m, (ci & 1) ? kStateDone1 : kStateDone, ((ci >> 1) - 1) & 1);
+      } else {
+        if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
+      }
       for (int pc = vt; pc < kC * 8; pc += 32 * kVWarps) {
         const int t = pc >> 3, ng = pc & 7;
         const bool valid = t < nrow;
         const __nv_bfloat16* gsrc =
             prm.v + (seq_row0 + orow(prm, tok0 + (valid ? t : 0))) * kD + 8 * ng;
-        cp_async_16(sV + (t >> 3) * kLBO_SV + ng * 128 + (t & 7) * 16, gsrc, valid ? 16u : 0u);
+        cp_async_16(vdst + (t >> 3) * kLBO_SV + ng * 128 + (t & 7) * 16, gsrc, valid ? 16u : 0u);
       }
       if (prm.extra != nullptr) {
         for (int t = vt; t < kC; t += 32 * kVWarps) {
           const float x = t < nrow ? prm.extra[seq_row0 + orow(prm, tok0 + t)] : 0.f;
-          st_shared_v4(sV + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16,
+          st_shared_v4(vdst + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16,
                        __bfloat16_as_ushort(__float2bfloat16_rn(x)), 0u, 0u, 0u);
         }
       }
       cp_async_wait_all();
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&m.bar[kFeatV]);
+      if (lane == 0) mbar_arrive(&m.bar[(kStateOnly && (ci & 1)) ? kFeatV1 : kFeatV]);
     }
   }
   if (warp == kMmaWarp && lane == 0) {
@@ -633,9 +659,18 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       // next to its MMAs instead of hoisted (80 live descriptors would not fit
       // this warpgroup's registers).
       uint64_t dQl = dQ, dKbl = dKb, dKal = dKa, dSl = dS, dVl = dV;
+      if constexpr (kStateOnly) {
+        // double-buffered Phi(K) and V: chunk ci uses buffer ci & 1
+        dKal = smem_desc(smem_u32(smem) + (ci & 1) * kSoK1, kXK, 128);
+        dVl = smem_desc(smem_u32(smem + ((ci & 1) ? kSoV1 : kSoV0)), kLBO_SV, 128);
+      }
       asm volatile("" : "+l"(dQl), "+l"(dKbl), "+l"(dKal), "+l"(dSl), "+l"(dVl));
-      if constexpr (!kStateOnly) wait_bar(m, kFeatQ, ci & 1);
-      wait_bar(m, kFeatK, ci & 1);
+      if constexpr (kStateOnly) {
+        wait_bar(m, (ci & 1) ? kFeatK1 : kFeatK, (ci >> 1) & 1);
+      } else {
+        wait_bar(m, kFeatQ, ci & 1);
+        wait_bar(m, kFeatK, ci & 1);
+      }
       tc_fence_after();
       if constexpr (!kStateOnly) {
 #pragma unroll
@@ -654,7 +689,10 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         wait_bar(m, kSnapReady, 0);  // initial state is in TMEM
         tc_fence_after();
       }
-      wait_bar(m, kFeatV, ci & 1);
+      if constexpr (kStateOnly)
+        wait_bar(m, (ci & 1) ? kFeatV1 : kFeatV, (ci >> 1) & 1);
+      else
+        wait_bar(m, kFeatV, ci & 1);
       tc_fence_after();
       asm volatile("" : "+l"(dKal), "+l"(dVl));
 #pragma unroll
@@ -663,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         for (int mt = 0; mt < 3; ++mt)
           mma_ss(tmem + kTS + mt * kN, dKal + (2048 / 16) * mt + (2 * kXK / 16) * s,
                  dVl + (2 * kLBO_SV / 16) * s, idST, true);
-      mma_commit(&m.bar[kStateDone]);
+      mma_commit(&m.bar[(kStateOnly && (ci & 1)) ? kStateDone1 : kStateDone]);
       if constexpr (!kStateOnly) {
         wait_bar(m, kPTilde, ci & 1);
         tc_fence_after();
