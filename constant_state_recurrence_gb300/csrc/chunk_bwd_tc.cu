@@ -23,6 +23,8 @@
 // out_qq holds dPhi of 16 dimensions; the featuriser warps drain it from TMEM
 // and apply the chain rule through the feature map of `ue` (q for dq, k for
 // dk), accumulating dgamma, domega, dphi.
+#include <cuda_fp16.h>
+
 #include "sanatan_internal.h"
 #include "sanatan_math.cuh"
 #include "tc_common.cuh"
@@ -48,7 +50,12 @@ constexpr int kOffF = 0;                        // Phi(uk): 16 token groups x kX
 constexpr int kOffS = kOffF + 16 * kXK;         // state snapshot bf16: 40 x kLBO_SV
 constexpr int kOffQ = kOffS + 40 * kLBO_SV;     // Q'
 constexpr int kOffV = kOffQ + 16 * kXA;         // K' = [vk | ek | 0] (+ over-read pad)
-constexpr int kOffMisc = kOffV + 16 * kLBO_SV + 128;
+// Rotation factors cos(t phi_a), sin(t phi_a) of the chunk's tokens as f16
+// pairs, written while staging and read by the chain rule (rows padded to 272 B
+// so that row-per-lane reads spread over the banks).
+constexpr int kRotPitch = 272;
+constexpr int kOffR = kOffV + 16 * kLBO_SV + 128;
+constexpr int kOffMisc = kOffR + kC * kRotPitch;
 
 enum Bar {
   kFeatFull = 0, kSFull, kSTilde, kOutFull, kOutFree, kStateDone, kSnapReady, kDrain, kNumBars
@@ -108,6 +115,12 @@ __device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
 }
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void feat_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 __device__ __forceinline__ int frow(const FsaParams& p, int u) {
   return p.reverse ? p.T - 1 - u : u;
@@ -169,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
   const uint32_t sS = smem_u32(smem + kOffS);
   const uint32_t sQ = smem_u32(smem + kOffQ);
   const uint32_t sV = smem_u32(smem + kOffV);
+  const uint32_t sR = smem_u32(smem + kOffR);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -239,20 +253,28 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
     const int crow = 32 * lq + lane;   // token row of the chunk
     const float gam = prm.gamma[h];
 
-    for (int ci = 0; ci < nloc; ++ci) {
-      const int chunk = c_begin + ci;
+    // Raw uk, query and key rows of one chunk for this thread's four tokens.
+    // They are loaded right after the chunk's staging hand-off (an arrive with
+    // release semantics would wait for loads still in flight) and consumed when
+    // the next chunk is staged.
+    uint4 ru[4], rq[4], rk[4];
+    auto load_stage = [&](int chunk) {
       const int tok0 = chunk * kC;
-      // --- stage Phi(uk), Q', K' of the chunk
-      uint4 ru[4], rq[4], rk[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int t = tq + 8 * i;
-        const bool valid = tok0 + t < prm.T;
-        const int64_t off = (seq_row0 + frow(prm, tok0 + t)) * kD + 8 * ag;
+        const bool valid = chunk < c_end && tok0 + t < prm.T;
+        const int64_t off = (seq_row0 + frow(prm, valid ? tok0 + t : 0)) * kD + 8 * ag;
         ru[i] = valid ? ldg_nc_v4(prm.uk + off) : make_uint4(0u, 0u, 0u, 0u);
         rq[i] = valid ? ldg_nc_v4(prm.vq + off) : make_uint4(0u, 0u, 0u, 0u);
         rk[i] = valid ? ldg_nc_v4(prm.vk + off) : make_uint4(0u, 0u, 0u, 0u);
       }
+    };
+    load_stage(c_begin);
+    for (int ci = 0; ci < nloc; ++ci) {
+      const int chunk = c_begin + ci;
+      const int tok0 = chunk * kC;
+      // --- stage Phi(uk), Q', K' of the chunk
       float cb[8], sb[8];
       {
         const int64_t tabs = prm.pos0 + frow(prm, tok0 + tq);
@@ -260,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
         for (int j = 0; j < 8; ++j) __sincosf(phase_mod_2pi(tabs, phi_r[j]), &sb[j], &cb[j]);
       }
       if (ci > 0) wait_bar(m, kStateDone, (ci - 1) & 1);
+      feat_sync();  // every chain-rule read of the previous chunk's rotation table is done
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int t = tq + 8 * i;
@@ -281,8 +304,14 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
                      rq[i].w);
         st_shared_v4(sV + (t >> 3) * kLBO_SV + ag * 128 + (t & 7) * 16, rk[i].x, rk[i].y,
                      rk[i].z, rk[i].w);
+        // rotation factors of token t, dimensions 8 ag .. 8 ag + 7
+        const uint32_t rb = sR + t * kRotPitch + ag * 32;
+        st_shared_v4(rb, pack_half2(cb[0], sb[0]), pack_half2(cb[1], sb[1]),
+                     pack_half2(cb[2], sb[2]), pack_half2(cb[3], sb[3]));
+        st_shared_v4(rb + 16, pack_half2(cb[4], sb[4]), pack_half2(cb[5], sb[5]),
+                     pack_half2(cb[6], sb[6]), pack_half2(cb[7], sb[7]));
         if (ag == 0) {
-          const int64_t grow = seq_row0 + frow(prm, tok0 + t);
+          const int64_t grow = seq_row0 + frow(prm, valid ? tok0 + t : 0);
           if (prm.eq != nullptr) {
             const float x = valid ? prm.eq[grow] : 0.f;
             st_shared_v4(sQ + (t >> 3) * kXA + 8 * 128 + (t & 7) * 16,
@@ -305,17 +334,22 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&m.bar[kFeatFull]);
+      load_stage(chunk + 1);
+      feat_sync();  // the rotation table of this chunk is complete
 
       // --- chain rule for the four quarters of dPhi of this chunk
       const int u = tok0 + crow;
       const bool rvalid = u < prm.T;
       const int64_t grow = seq_row0 + frow(prm, rvalid ? u : 0);
       const int64_t tpos = prm.pos0 + frow(prm, rvalid ? u : 0);
+      // raw u of this row, one group of 8 dimensions ahead of its use
+      uint4 raw_next = rvalid ? ldg_nc_v4(prm.ue + grow * kD + 8 * half) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
       for (int qq = 0; qq < 4; ++qq) {
         const int dg = 2 * qq + half;
-        // raw u of this row's 8 dimensions (its latency hides behind the wait)
-        const uint4 raw = rvalid ? ldg_nc_v4(prm.ue + grow * kD + 8 * dg) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 raw = raw_next;
+        if (qq < 3)
+          raw_next = rvalid ? ldg_nc_v4(prm.ue + grow * kD + 8 * (dg + 2)) : make_uint4(0u, 0u, 0u, 0u);
         wait_bar(m, kOutFull, (4 * ci + qq) & 1);
         tc_fence_after();
         float dphi5[5][8];
@@ -325,7 +359,16 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&m.bar[kOutFree]);
+        if (lane == 0) mbar_arrive_relaxed(&m.bar[kOutFree]);  // the quarter is in registers
+        // rotation factors of this row for the 8 dimensions of group dg
+        uint32_t rot[8];
+        {
+          const uint32_t rb = sR + crow * kRotPitch + dg * 32;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(rot[0]), "=r"(rot[1]), "=r"(rot[2]), "=r"(rot[3]) : "r"(rb));
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(rot[4]), "=r"(rot[5]), "=r"(rot[6]), "=r"(rot[7]) : "r"(rb + 16));
+        }
         // chain rule through the feature map of ue for the 8 dimensions of group dg
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
         float red[16];
@@ -344,8 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
           const float gx = cx - sx;
           const float gpx = -sx - cx;
           const float rr = tanh_fast(gam * gx);
-          float sp, cp;
-          __sincosf(phase_mod_2pi(tpos, pc.z), &sp, &cp);
+          const float2 rcs = __half22float2(*reinterpret_cast<const __half2*>(&rot[j]));
+          const float cp = rcs.x, sp = rcs.y;
           const float cr = ct * cp - st * sp;
           const float sr = st * cp + ct * sp;
           const float d1 = dphi5[0][j], d2 = dphi5[1][j], d3 = dphi5[2][j];
