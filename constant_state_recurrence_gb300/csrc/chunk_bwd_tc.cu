@@ -72,15 +72,19 @@ struct Misc {
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kSmemBytes <= 232448, "shared memory layout exceeds 227 KB");
 
-constexpr int kThreads = 512;
-constexpr uint32_t kRegFeat = 168;
-constexpr uint32_t kRegEpi = 144;
+// 768 threads: warps 0-15 stage the chunk and apply the chain rule (the
+// launch allocation of 80 registers), warps 16-19 drain TMEM (128 registers
+// after setmaxnreg), one thread of warp 20 issues the MMAs (its warpgroup
+// keeps 32).
+constexpr int kThreads = 768;
+constexpr uint32_t kRegLaunch = 80;
+constexpr uint32_t kRegEpi = 128;
 constexpr uint32_t kRegMma = 32;
-static_assert(256 * kRegFeat + 128 * kRegEpi + 128 * kRegMma <= kThreads * 128,
+static_assert(512 * kRegLaunch + 128 * kRegEpi + 128 * kRegMma <= kThreads * kRegLaunch,
               "setmaxnreg split must fit the launch allocation");
-constexpr int kFeatWarps = 8;
-constexpr int kEpiWarp0 = 8;
-constexpr int kMmaWarp = 12;
+constexpr int kFeatWarps = 16;
+constexpr int kEpiWarp0 = 16;
+constexpr int kMmaWarp = 20;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct FsaParams {
@@ -115,7 +119,31 @@ __device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
 }
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void feat_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+__device__ __forceinline__ void feat_sync() { asm volatile("bar.sync 2, 512;" ::: "memory"); }
+
+// L2 prefetch of one chunk's rows of uk, ue, the query and key rows and the
+// extra columns (sizes rounded down to whole 16-byte pieces).
+__device__ __forceinline__ void prefetch_chunk_rows(const FsaParams& prm, int64_t seq_row0, int chunk) {
+  const int tok0 = chunk * kC;
+  const int n = min(kC, prm.T - tok0);
+  if (n <= 0) return;
+  const int64_t row = seq_row0 + (prm.reverse ? prm.T - tok0 - n : tok0);
+  const uint32_t bytes = static_cast<uint32_t>(n) * kD * 2;
+  prefetch_l2_bulk(prm.uk + row * kD, bytes);
+  prefetch_l2_bulk(prm.ue + row * kD, bytes);
+  prefetch_l2_bulk(prm.vq + row * kD, bytes);
+  prefetch_l2_bulk(prm.vk + row * kD, bytes);
+  const uint32_t xb = (static_cast<uint32_t>(n) * 4) & ~15u;
+  const float* x = prm.eq != nullptr ? prm.eq : prm.ek;
+  if (x != nullptr && xb > 0 && ((reinterpret_cast<uintptr_t>(x + row) & 15u) == 0))
+    prefetch_l2_bulk(x + row, xb);
+}
+
+__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -126,54 +154,45 @@ __device__ __forceinline__ int frow(const FsaParams& p, int u) {
   return p.reverse ? p.T - 1 - u : u;
 }
 
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(taddr));
 #pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Reduce 16 per-lane values over the 32 lanes of a warp (reduce-scatter by
-// halving): afterwards lanes 2i and 2i+1 hold the total of value index
-// slot(i), with slot taken from lane bits 4..1.
-__device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
+// Reduce 8 per-lane values over the 32 lanes of a warp: afterwards the four
+// lanes 4i..4i+3 hold the total of value index slot8(i), with slot taken from
+// lane bits 4..2.
+__device__ __forceinline__ float warp_reduce8(float (&v)[8], int lane) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 4; ++i) {
     const bool up = lane & 16;
-    const float send = up ? v[i] : v[i + 8];
-    const float keep = up ? v[i + 8] : v[i];
+    const float send = up ? v[i] : v[i + 4];
+    const float keep = up ? v[i + 4] : v[i];
     v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const bool up = lane & 8;
-    const float send = up ? v[i] : v[i + 4];
-    const float keep = up ? v[i + 4] : v[i];
-    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
-#pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const bool up = lane & 4;
+    const bool up = lane & 8;
     const float send = up ? v[i] : v[i + 2];
     const float keep = up ? v[i + 2] : v[i];
-    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
   }
   {
-    const bool up = lane & 2;
+    const bool up = lane & 4;
     const float send = up ? v[0] : v[1];
     const float keep = up ? v[1] : v[0];
-    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
   }
-  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+  float t = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 2);
+  return t + __shfl_xor_sync(0xffffffffu, t, 1);
 }
-// Value index that lane `lane` holds after warp_reduce16.
-__device__ __forceinline__ int reduce16_slot(int lane) {
-  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+__device__ __forceinline__ int reduce8_slot(int lane) {
+  return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
 }
-
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -239,52 +258,62 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
 
   if (warp < kFeatWarps) {
     // ------------------------------------------------- featuriser + chain rule
-    setmaxnreg_inc<kRegFeat>();
+    // Staging role: lane (r, dimension group ag) of warp w owns tokens
+    // tq + 8 i (i = 0, 1) of the chunk.
+    const int fw = warp & 7;
     const int r = lane & 7;
-    const int ag = (lane >> 3) + 4 * (warp & 1);
-    const int tq = 32 * (warp >> 1) + r;
+    const int ag = (lane >> 3) + 4 * (fw & 1);
+    const int tq = 32 * (fw >> 1) + r + 16 * (warp >> 3);
     const float4* dimc = &m.dimc[8 * ag];
-    float phi_r[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) phi_r[j] = prm.phi[h * kD + 8 * ag + j];
-    // chain-rule role: TMEM lane quarter and which dimension group of a quarter
+    // chain-rule role: TMEM lane quarter lq, and four dimensions (4 sub) of
+    // each quarter's sixteen
     const int lq = warp & 3;
-    const int half = warp >> 2;
+    const int sub = warp >> 2;
     const int crow = 32 * lq + lane;   // token row of the chunk
     const float gam = prm.gamma[h];
 
-    // Raw uk, query and key rows of one chunk for this thread's four tokens.
+    // Raw uk, query and key rows of one chunk for this thread's two tokens.
     // They are loaded right after the chunk's staging hand-off (an arrive with
     // release semantics would wait for loads still in flight) and consumed when
     // the next chunk is staged.
-    uint4 ru[4], rq[4], rk[4];
+    uint4 ru[2], rq[2], rk[2];
+    float xq[2], xk[2];  // extra columns (read by the ag == 0 lanes)
     auto load_stage = [&](int chunk) {
       const int tok0 = chunk * kC;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 2; ++i) {
         const int t = tq + 8 * i;
         const bool valid = chunk < c_end && tok0 + t < prm.T;
-        const int64_t off = (seq_row0 + frow(prm, valid ? tok0 + t : 0)) * kD + 8 * ag;
+        const int64_t row = seq_row0 + frow(prm, valid ? tok0 + t : 0);
+        const int64_t off = row * kD + 8 * ag;
         ru[i] = valid ? ldg_nc_v4(prm.uk + off) : make_uint4(0u, 0u, 0u, 0u);
         rq[i] = valid ? ldg_nc_v4(prm.vq + off) : make_uint4(0u, 0u, 0u, 0u);
         rk[i] = valid ? ldg_nc_v4(prm.vk + off) : make_uint4(0u, 0u, 0u, 0u);
+        xq[i] = (valid && ag == 0 && prm.eq != nullptr) ? __ldg(prm.eq + row) : 0.f;
+        xk[i] = (valid && ag == 0 && prm.ek != nullptr) ? __ldg(prm.ek + row) : 0.f;
       }
     };
+    if (tid == 0) {
+      if (nloc > 0) prefetch_chunk_rows(prm, seq_row0, c_begin);
+      if (nloc > 1) prefetch_chunk_rows(prm, seq_row0, c_begin + 1);
+    }
     load_stage(c_begin);
     for (int ci = 0; ci < nloc; ++ci) {
       const int chunk = c_begin + ci;
       const int tok0 = chunk * kC;
+      if (tid == 0 && ci + 2 < nloc) prefetch_chunk_rows(prm, seq_row0, chunk + 2);
       // --- stage Phi(uk), Q', K' of the chunk
       float cb[8], sb[8];
       {
         const int64_t tabs = prm.pos0 + frow(prm, tok0 + tq);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) __sincosf(phase_mod_2pi(tabs, phi_r[j]), &sb[j], &cb[j]);
+        for (int j = 0; j < 8; ++j)
+          __sincosf(phase_mod_2pi(tabs, m.pc[8 * ag + j].z), &sb[j], &cb[j]);
       }
       if (ci > 0) wait_bar(m, kStateDone, (ci - 1) & 1);
       feat_sync();  // every chain-rule read of the previous chunk's rotation table is done
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 2; ++i) {
         const int t = tq + 8 * i;
         const bool valid = tok0 + t < prm.T;
         uint32_t kf[5][4];
@@ -311,24 +340,21 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
         st_shared_v4(rb + 16, pack_half2(cb[4], sb[4]), pack_half2(cb[5], sb[5]),
                      pack_half2(cb[6], sb[6]), pack_half2(cb[7], sb[7]));
         if (ag == 0) {
-          const int64_t grow = seq_row0 + frow(prm, valid ? tok0 + t : 0);
-          if (prm.eq != nullptr) {
-            const float x = valid ? prm.eq[grow] : 0.f;
+          if (prm.eq != nullptr)
             st_shared_v4(sQ + (t >> 3) * kXA + 8 * 128 + (t & 7) * 16,
-                         __bfloat16_as_ushort(__float2bfloat16_rn(x)), 0u, 0u, 0u);
-          }
-          if (prm.ek != nullptr) {
-            const float x = valid ? prm.ek[grow] : 0.f;
+                         __bfloat16_as_ushort(__float2bfloat16_rn(xq[i])), 0u, 0u, 0u);
+          if (prm.ek != nullptr)
             st_shared_v4(sV + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16,
-                         __bfloat16_as_ushort(__float2bfloat16_rn(x)), 0u, 0u, 0u);
-          }
+                         __bfloat16_as_ushort(__float2bfloat16_rn(xk[i])), 0u, 0u, 0u);
         }
+        if (i == 0) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 kc = dimc[j];
-          const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
-          sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
-          cb[j] = nc;
+          for (int j = 0; j < 8; ++j) {
+            const float4 kc = dimc[j];
+            const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
+            sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
+            cb[j] = nc;
+          }
         }
       }
       fence_proxy_async_smem();
@@ -342,46 +368,44 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
       const bool rvalid = u < prm.T;
       const int64_t grow = seq_row0 + frow(prm, rvalid ? u : 0);
       const int64_t tpos = prm.pos0 + frow(prm, rvalid ? u : 0);
-      // raw u of this row, one group of 8 dimensions ahead of its use
-      uint4 raw_next = rvalid ? ldg_nc_v4(prm.ue + grow * kD + 8 * half) : make_uint4(0u, 0u, 0u, 0u);
+      const float tposf = static_cast<float>(tpos);
+      // dimensions a0 .. a0 + 3 of quarter qq: a0(qq) = 16 qq + 8 (sub / 2) + 4 (sub % 2)
+      const int a_sub = 8 * (sub >> 1) + 4 * (sub & 1);
+      // raw u of this row, one quarter ahead of its use
+      uint2 raw_next = rvalid ? ldg_nc_v2(prm.ue + grow * kD + a_sub) : make_uint2(0u, 0u);
 #pragma unroll 1
       for (int qq = 0; qq < 4; ++qq) {
-        const int dg = 2 * qq + half;
-        const uint4 raw = raw_next;
+        const int a0 = 16 * qq + a_sub;
+        const uint2 raw = raw_next;
         if (qq < 3)
-          raw_next = rvalid ? ldg_nc_v4(prm.ue + grow * kD + 8 * (dg + 2)) : make_uint4(0u, 0u, 0u, 0u);
+          raw_next = rvalid ? ldg_nc_v2(prm.ue + grow * kD + a0 + 16) : make_uint2(0u, 0u);
         wait_bar(m, kOutFull, (4 * ci + qq) & 1);
         tc_fence_after();
-        float dphi5[5][8];
-        const uint32_t ta = tmem + (static_cast<uint32_t>(32 * lq) << 16) + kTQ + 40 * half;
+        float dphi5[5][4];
+        const uint32_t ta = tmem + (static_cast<uint32_t>(32 * lq) << 16) + kTQ + 40 * (sub >> 1) +
+                            4 * (sub & 1);
 #pragma unroll
-        for (int c = 0; c < 5; ++c) tmem_ld8(ta + 8 * c, dphi5[c]);
+        for (int c = 0; c < 5; ++c) tmem_ld4(ta + 8 * c, dphi5[c]);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(&m.bar[kOutFree]);  // the quarter is in registers
-        // rotation factors of this row for the 8 dimensions of group dg
-        uint32_t rot[8];
-        {
-          const uint32_t rb = sR + crow * kRotPitch + dg * 32;
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(rot[0]), "=r"(rot[1]), "=r"(rot[2]), "=r"(rot[3]) : "r"(rb));
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(rot[4]), "=r"(rot[5]), "=r"(rot[6]), "=r"(rot[7]) : "r"(rb + 16));
-        }
-        // chain rule through the feature map of ue for the 8 dimensions of group dg
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        float red[16];
-        uint32_t outp[4];
+        // rotation factors of this row for dimensions a0 .. a0 + 3
+        uint32_t rot[4];
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(rot[0]), "=r"(rot[1]), "=r"(rot[2]), "=r"(rot[3])
+                     : "r"(sR + crow * kRotPitch + a0 * 4));
+        const uint32_t w[2] = {raw.x, raw.y};
+        float red[8];
+        uint32_t outp[2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int a = 8 * dg + j;
+        for (int j = 0; j < 4; ++j) {
           const float uu = __uint_as_float((j & 1) ? (w[j >> 1] & 0xffff0000u) : (w[j >> 1] << 16));
           const float den = 1.0f + fabsf(uu);
           const float th = kPi * __fdividef(uu, den);
           float st, ct;
           __sincosf(th, &st, &ct);
-          const float4 pc = m.pc[a];
+          const float4 pc = m.pc[a0 + j];
           const float cx = ct * pc.x - st * pc.y;   // cos(theta + omega)
           const float sx = st * pc.x + ct * pc.y;   // sin(theta + omega)
           const float gx = cx - sx;
@@ -399,22 +423,20 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
           const float dth_rot = ds * cr - dc * sr;
           const float dpre = dr * (1.0f - rr * rr);
           const float dtheta = fmaf(dpre * gam, gpx, dth_rot);
-          const float du = rvalid ? dtheta * kPi / (den * den) : 0.f;
+          const float du = rvalid ? __fdividef(dtheta * kPi, den * den) : 0.f;
           if (j & 1)
             outp[j >> 1] |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(du))) << 16;
           else
             outp[j >> 1] = __bfloat16_as_ushort(__float2bfloat16_rn(du));
-          red[j] = rvalid ? dpre * gam * gpx : 0.f;                       // domega
-          red[8 + j] = rvalid ? dth_rot * static_cast<float>(tpos) : 0.f;  // dphi
+          red[j] = rvalid ? dpre * gam * gpx : 0.f;   // domega
+          red[4 + j] = rvalid ? dth_rot * tposf : 0.f; // dphi
           acc_gamma += rvalid ? dpre * gx : 0.f;
         }
-        if (rvalid)
-          *reinterpret_cast<uint4*>(prm.du + grow * kD + 8 * dg) =
-              make_uint4(outp[0], outp[1], outp[2], outp[3]);
-        const float tot = warp_reduce16(red, lane);
-        if ((lane & 1) == 0) {
-          const int slot = reduce16_slot(lane);
-          atomicAdd(&m.gacc[(slot < 8 ? 0 : 64) + 8 * dg + (slot & 7)], tot);
+        if (rvalid) *reinterpret_cast<uint2*>(prm.du + grow * kD + a0) = make_uint2(outp[0], outp[1]);
+        const float tot = warp_reduce8(red, lane);
+        if ((lane & 3) == 0) {
+          const int slot = reduce8_slot(lane);
+          atomicAdd(&m.gacc[(slot < 4 ? 0 : 64) + a0 + (slot & 3)], tot);
         }
       }
     }
