@@ -125,6 +125,8 @@ struct TcParams {
   int nseg;         // segments per sequence
   int seg_grid;     // CTAs per sequence in this launch
   int nchunks;      // chunks per sequence
+  int bhn;          // sequences (B * H); CTA b handles segment b / bhn of sequence b % bhn
+  int pdl;          // launched as a programmatic dependent of the state-only pass
   const float* deltas;   // per-segment state sums [B*H][nseg][321][80] (slots 0..nseg-2) or null
   const float* S0;       // full initial state (export of constant rows) or null
   const float* z0;
@@ -181,8 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int bh = blockIdx.x / prm.seg_grid;
-  const int seg = blockIdx.x % prm.seg_grid;
+  // Segment-major CTA order: the first segments' CTAs are scheduled first (in
+  // a dependent launch they need nothing from the state-only pass).
+  const int seg = blockIdx.x / prm.bhn;
+  const int bh = blockIdx.x % prm.bhn;
   const int h = bh % prm.H;
   const int c_begin = static_cast<int>(static_cast<int64_t>(seg) * prm.nchunks / prm.nseg);
   const int c_end = static_cast<int>(static_cast<int64_t>(seg + 1) * prm.nchunks / prm.nseg);
@@ -190,6 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
   const int64_t seq_row0 = static_cast<int64_t>(bh) * prm.T;  // first token row of the sequence
   const bool last_seg = (seg == prm.nseg - 1);
 
+  // The main pass may be launched (and start its first segments) while this
+  // state-only pass runs; it waits for its completion before reading the sums.
+  if constexpr (kStateOnly) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     if (nloc > 0) prefetch_chunk<kStateOnly>(prm, seq_row0, c_begin);
     if (nloc > 1) prefetch_chunk<kStateOnly>(prm, seq_row0, c_begin + 1);
@@ -337,6 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
     // Initial state -> TMEM tiles (and the bf16 snapshot for the first chunk):
     // the caller's state (S0, z0) plus the sums of all earlier segments.
+    if (!kStateOnly && prm.pdl && seg > 0)
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the state-only pass is complete
     {
       for (int mt = 0; mt < 3; ++mt) {
         const int f = mt * 128 + row;
@@ -788,6 +797,7 @@ TcParams tc_params(const TcJob& job) {
   p.pos0 = job.pos0;
   p.eps = job.eps;
   p.nseg = tc_segments(job.B, job.H, job.T);
+  p.bhn = job.B * job.H;
   p.nchunks = (job.T + kC - 1) / kC;
   p.reverse = job.reverse;
   p.normalize = job.normalize;
@@ -815,7 +825,8 @@ cudaError_t tc_attention(const TcJob& job, cudaStream_t st) {
   cudaError_t e = tc_set_smem();
   if (e != cudaSuccess) return e;
   TcParams p = tc_params(job);
-  if (p.nseg > 1 && !job.deltas_ready) {
+  const bool state_pass = p.nseg > 1 && !job.deltas_ready;
+  if (state_pass) {
     if ((e = tc_state_pass(job, st)) != cudaSuccess) return e;
   }
   p.seg_grid = p.nseg;
@@ -829,8 +840,26 @@ cudaError_t tc_attention(const TcJob& job, cudaStream_t st) {
   const ProfileEvents& pe = profile_events();
   const bool rec = job.record_events && pe.start != nullptr;
   if (rec) cudaEventRecord(pe.start, st);
-  sanatan_tc_kernel<false><<<job.B * job.H * p.nseg, kThreads, kSmemBytes, st>>>(p);
-  e = cudaGetLastError();
+  const unsigned grid = static_cast<unsigned>(job.B * job.H * p.nseg);
+  if (state_pass && !rec) {
+    // Programmatic dependent launch: the main pass starts as soon as SMs free
+    // up; only CTAs of segments > 0 wait for the state-only pass.
+    p.pdl = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, sanatan_tc_kernel<false>, p);
+  } else {
+    sanatan_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p);
+    e = cudaGetLastError();
+  }
   if (rec) cudaEventRecord(pe.stop, st);
   return e;
 }
