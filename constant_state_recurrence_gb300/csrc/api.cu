@@ -124,6 +124,22 @@ int sanatan_chunk_fwd(const void* q, const void* k, const void* v, int in_dtype,
                       int T, int d, int dv, int64_t pos0, float eps, const float* S0,
                       const float* z0, float* o, float* D, float* S_out, float* z_out,
                       void* workspace, size_t workspace_bytes, void* stream) {
+  return sanatan::chunk_fwd_checked(q, k, v, in_dtype, gamma, omega, phi, B, H, T, d, dv, pos0,
+                                    eps, S0, z0, o, D, S_out, z_out, workspace, workspace_bytes,
+                                    stream, false);
+}
+
+}  // extern "C"
+
+namespace sanatan {
+// Argument checks and dispatch of sanatan_chunk_fwd.  With `fewer_segments`
+// a workspace smaller than sanatan_chunk_fwd_workspace_size is accepted and
+// the tensor-core path splits sequences into as many segments as it holds.
+int chunk_fwd_checked(const void* q, const void* k, const void* v, int in_dtype,
+                      const float* gamma, const float* omega, const float* phi, int B, int H,
+                      int T, int d, int dv, int64_t pos0, float eps, const float* S0,
+                      const float* z0, float* o, float* D, float* S_out, float* z_out,
+                      void* workspace, size_t workspace_bytes, void* stream, bool fewer_segments) {
   if (!ok_dtype(in_dtype)) return SANATAN_ERR_INVALID;
   if (int s = check_sizes(B, H, T, d, dv)) return s;
   if ((S0 == nullptr) != (z0 == nullptr)) return SANATAN_ERR_INVALID;
@@ -134,7 +150,8 @@ int sanatan_chunk_fwd(const void* q, const void* k, const void* v, int in_dtype,
   if (static_cast<int64_t>(B) * H == 0) return SANATAN_OK;
   if (T > 0 && (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(o))) return SANATAN_ERR_INVALID;
   if (int s = check_params(gamma, omega, phi)) return s;
-  if (workspace_bytes < sanatan_chunk_fwd_workspace_size(B, H, T, d, dv, in_dtype))
+  if (!fewer_segments &&
+      workspace_bytes < sanatan_chunk_fwd_workspace_size(B, H, T, d, dv, in_dtype))
     return SANATAN_ERR_INVALID;
   if (int s = check_arch()) return s;
   ChunkFwdArgs a{q, k, v, in_dtype, gamma, omega, phi, B, H, T, d, dv, pos0, eps,
@@ -143,6 +160,9 @@ int sanatan_chunk_fwd(const void* q, const void* k, const void* v, int in_dtype,
   if (in_dtype == SANATAN_BF16) return from_cuda(chunk_fwd_tc_launch(a, st));
   return from_cuda(chunk_fwd_simt_launch(a, st));
 }
+}  // namespace sanatan
+
+extern "C" {
 
 size_t sanatan_chunk_bwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype) {
   if (B < 0 || H < 0 || T < 0 || d != 64 || dv != 64) return 0;

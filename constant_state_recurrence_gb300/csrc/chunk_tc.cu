@@ -756,9 +756,31 @@ int tc_segments(int B, int H, int T) {
   const int64_t bhn = static_cast<int64_t>(B) * H;
   const int nchunks = (T + kC - 1) / kC;
   if (bhn <= 0 || nchunks <= 1) return 1;
-  const int64_t per = sm_count() / bhn;
-  if (per <= 1) return 1;
+  const int64_t sms = sm_count();
+  const int64_t per = sms / bhn;
+  if (per <= 1) {
+    if (bhn >= sms) return 1;
+    // With about one CTA per sequence some SMs would idle.  More segments run
+    // as several waves of one-CTA-per-SM work: pick the count that minimises
+    // waves x chunks per segment, charging one chunk for the state-only pass
+    // that any split needs.
+    int best = 1;
+    int64_t best_cost = (bhn + sms - 1) / sms * nchunks;
+    for (int sg = 2; sg <= 8 && sg <= nchunks; ++sg) {
+      const int64_t waves = (bhn * sg + sms - 1) / sms;
+      const int64_t cost = waves * ((nchunks + sg - 1) / sg) + 1;
+      if (cost < best_cost) { best_cost = cost; best = sg; }
+    }
+    return best;
+  }
   return static_cast<int>(per < nchunks ? per : nchunks);
+}
+
+int tc_segments_fit(int B, int H, int T, size_t bytes) {
+  const size_t slot = static_cast<size_t>(B) * H * kSCRows * kSCCols * sizeof(float);
+  int sg = tc_segments(B, H, T);
+  while (sg > 1 && static_cast<size_t>(sg) * slot > bytes) --sg;
+  return sg;
 }
 
 size_t chunk_fwd_tc_workspace_bytes(int B, int H, int T) {
@@ -796,7 +818,7 @@ TcParams tc_params(const TcJob& job) {
   p.T = job.T;
   p.pos0 = job.pos0;
   p.eps = job.eps;
-  p.nseg = tc_segments(job.B, job.H, job.T);
+  p.nseg = job.nseg > 0 ? job.nseg : tc_segments(job.B, job.H, job.T);
   p.bhn = job.B * job.H;
   p.nchunks = (job.T + kC - 1) / kC;
   p.reverse = job.reverse;
@@ -884,6 +906,7 @@ cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st) {
   job.S_out = a.S_out;
   job.z_out = a.z_out;
   job.deltas = static_cast<float*>(a.workspace);
+  job.nseg = tc_segments_fit(a.B, a.H, a.T, a.workspace_bytes);
   return tc_attention(job, st);
 }
 

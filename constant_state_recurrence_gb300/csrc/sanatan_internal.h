@@ -102,6 +102,7 @@ struct TcJob {
   float* deltas = nullptr;
   int deltas_ready = 0;     // the state-only pass has already filled `deltas`
   int record_events = 1;    // bracket the main launch with the profile events
+  int nseg = 0;             // segments per sequence (0: tc_segments)
 };
 // State-only pass: the sums of every segment but the last into job.deltas.
 cudaError_t tc_state_pass(const TcJob& job, cudaStream_t st);
@@ -109,6 +110,13 @@ cudaError_t tc_state_pass(const TcJob& job, cudaStream_t st);
 cudaError_t tc_attention(const TcJob& job, cudaStream_t st);
 
 size_t chunk_bwd_tc_workspace_bytes(int B, int H, int T);
+// Segments that a workspace of `bytes` holds (at most tc_segments; 1 needs none).
+int tc_segments_fit(int B, int H, int T, size_t bytes);
+int chunk_fwd_checked(const void* q, const void* k, const void* v, int in_dtype,
+                      const float* gamma, const float* omega, const float* phi, int B, int H,
+                      int T, int d, int dv, int64_t pos0, float eps, const float* S0,
+                      const float* z0, float* o, float* D, float* S_out, float* z_out,
+                      void* workspace, size_t workspace_bytes, void* stream, bool fewer_segments);
 cudaError_t chunk_bwd_tc_launch(const ChunkBwdArgs& a, cudaStream_t st);
 int bwd_tc_read_and_clear_error(cudaStream_t st);
 }  // namespace sanatan
