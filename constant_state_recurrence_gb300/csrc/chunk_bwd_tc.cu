@@ -624,25 +624,48 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
   }
 }
 
-// dN = dO / (D + eps) (bf16) and dD = -(dO . o) / (D + eps) (f32), one warp per row.
+// dN = dO / (D + eps) (bf16) and dD = -(dO . o) / (D + eps) (f32).  Eight
+// lanes per row, eight elements per lane (16- and 32-byte accesses).
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&g)[8]) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    g[2 * i] = __uint_as_float(u[i] << 16);
+    g[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&g)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
+  g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+}
+
 template <typename Tg>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const Tg* __restrict__ dO,
                                                        const float* __restrict__ o,
                                                        const float* __restrict__ Dn, float eps,
                                                        int64_t rows, __nv_bfloat16* __restrict__ dN,
                                                        float* __restrict__ dD) {
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const float inv = 1.0f / (Dn[row] + eps);
-  const float g0 = load_as_float(dO + row * 64 + 2 * lane);
-  const float g1 = load_as_float(dO + row * 64 + 2 * lane + 1);
-  const float2 ov = reinterpret_cast<const float2*>(o + row * 64)[lane];
-  float dot = g0 * ov.x + g1 * ov.y;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 32 + (threadIdx.x >> 3);
+  const int part = threadIdx.x & 7;  // elements 8 part .. 8 part + 7 of the row
+  const bool ok = row < rows;
+  const int64_t r = ok ? row : 0;
+  float g[8], ov[8];
+  load8(dO + r * 64 + 8 * part, g);
+  load8(o + r * 64 + 8 * part, ov);
+  const float inv = 1.0f / (Dn[r] + eps);
+  float dot = 0.f;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-  reinterpret_cast<uint32_t*>(dN + row * 64)[lane] = pack_bf16x2(g0 * inv, g1 * inv);
-  if (lane == 0) dD[row] = -dot * inv;
+  for (int i = 0; i < 8; ++i) dot = fmaf(g[i], ov[i], dot);
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  if (!ok) return;
+  *reinterpret_cast<uint4*>(dN + r * 64 + 8 * part) =
+      make_uint4(pack_bf16x2(g[0] * inv, g[1] * inv), pack_bf16x2(g[2] * inv, g[3] * inv),
+                 pack_bf16x2(g[4] * inv, g[5] * inv), pack_bf16x2(g[6] * inv, g[7] * inv));
+  if (part == 0) dD[r] = -dot * inv;
 }
 
 }  // namespace
@@ -692,7 +715,7 @@ cudaError_t chunk_bwd_tc_launch(const ChunkBwdArgs& a, cudaStream_t st) {
   float* rdeltas = reinterpret_cast<float*>(ws + dn_bytes + dd_bytes + delta_bytes);
 
   {
-    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+    const unsigned blocks = static_cast<unsigned>((rows + 31) / 32);
     if (a.grad_dtype == SANATAN_F32)
       bwd_prep_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(a.dO), a.o, a.Dn,
                                                      f.eps, rows, dN, dD);

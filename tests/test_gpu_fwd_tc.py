@@ -116,3 +116,12 @@ def test_long_prefill_full_size_sampled():
     x = W.make(W.LONG, device="cpu")
     rows = [0, 5, 127, 128, 4095, 4096, 16383, 20000, 32766, 32767]
     _sampled_rows_check(x, rows, [(0, 0), (0, 6), (0, 11)])
+
+
+def test_training_shape_forward_full_size_sampled():
+    """B=8, H=12, T=4096 (96 sequences: the multi-wave segment split, three
+    segments per sequence, 288 CTAs), rows and final state of sampled heads."""
+    assert S.chunk_fwd_plan(8, 12, 4096)[0] >= 2
+    x = W.make(W.TRAIN, device="cpu")
+    rows = [0, 127, 128, 1364, 1365, 1366, 2730, 2731, 4095]
+    _sampled_rows_check(x, rows, [(0, 0), (7, 11), (4, 3)])

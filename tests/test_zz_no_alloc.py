@@ -35,7 +35,9 @@ def _noalloc_raw(g, o, D, Sx, zx):
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-@pytest.mark.parametrize("shape", [(4, 12, 2048), (1, 3, 700)])
+# (8, 12, 4096): the preferred split (three segments for 96 sequences) needs
+# more scratch than the array holds, so the entry point uses fewer segments.
+@pytest.mark.parametrize("shape", [(4, 12, 2048), (1, 3, 700), (8, 12, 4096)])
 def test_noalloc_matches_workspace_entry_twice(shape):
     dev = torch.device("cuda:0")
     B, H, T = shape
