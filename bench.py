@@ -62,6 +62,10 @@ FLUSH_BYTES = 256 << 20
 # Both arms report this metric on the layer-forward workload (B=4 H=12 T=2048).
 METRIC = "SANATAN p=1 prefill tokens/s"
 
+# Data shard of this process: under torchrun every rank processes its own
+# sequences (same gamma, omega, phi), set in main().
+SHARD = 0
+
 
 def peaks():
     try:
@@ -201,7 +205,7 @@ def timed_steps(step, steps, flush, stream, profile=None, per_step_inputs=False)
 
 def prefill_case(w, dev, flush, steps, warmup, stream):
     from constant_state_recurrence_gb300 import sanatan as S
-    x = W.make(w, device=dev)
+    x = W.make(w, device=dev, shard=SHARD)
     g = {n: x[n] for n in ("q", "k", "v", "gamma", "omega", "phi")}
     B, H, T = x["B"], x["H"], x["T"]
     o = torch.empty(B, H, T, 64, dtype=torch.float32, device=dev)
@@ -262,7 +266,7 @@ def decode_case(batch, dev, flush, steps, warmup, stream):
     from constant_state_recurrence_gb300 import sanatan as S
     w = W.DECODE
     G = 144
-    x = W.make(w, device=dev, B=batch)
+    x = W.make(w, device=dev, B=batch, shard=SHARD)
     _, _, Sx, zx = S.sanatan_chunk_fwd(x["q"], x["k"], x["v"], x["gamma"], x["omega"], x["phi"],
                                        want_D=False, want_state=True)
     del x["q"], x["k"], x["v"]
@@ -290,7 +294,7 @@ def train_case(dev, flush, steps, warmup, stream):
     """Training step of the B=8, H=12, T=4096 workload: the chunked forward
     (keeping o and D) then the backward to dq, dk, dv, dgamma, domega, dphi."""
     from constant_state_recurrence_gb300 import sanatan as S
-    x = W.make(W.TRAIN, device=dev, with_grad_out=True)
+    x = W.make(W.TRAIN, device=dev, with_grad_out=True, shard=SHARD)
     g = {n: x[n] for n in ("q", "k", "v", "gamma", "omega", "phi", "dO")}
     B, H, T = x["B"], x["H"], x["T"]
     o = torch.empty(B, H, T, 64, dtype=torch.float32, device=dev)
@@ -336,31 +340,20 @@ def oracle_prefill_sample(batch=4, T=2048):
 
 
 def dist_setup(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if torch.cuda.is_available():
-            torch.cuda.set_device(local)
-        dist.init_process_group(backend)
-    return world, rank, local
+    from constant_state_recurrence_gb300 import replicas
+    r = replicas.setup(use_cuda=torch.cuda.is_available() and args.impl != "reference")
+    return r.world, r.rank, r.local
 
 
 def barrier(world):
+    from constant_state_recurrence_gb300 import replicas
     if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+        replicas.barrier(replicas.Replica(world, 0, 0))
 
 
 def max_over_ranks(x, world, dev):
-    if world == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from constant_state_recurrence_gb300 import replicas
+    return replicas.max_over_ranks(x, replicas.Replica(world, 0, 0), dev)
 
 
 def run_reference(args, world, rank):
@@ -405,6 +398,8 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)
+    global SHARD
+    SHARD = rank
     if args.impl == "reference":
         run_reference(args, world, rank)
         return

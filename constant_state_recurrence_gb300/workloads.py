@@ -64,6 +64,11 @@ ALL = (TINY, LAYER, LONG, DECODE, TRAIN)
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
+def shard_seed(seed: int, shard: int) -> int:
+    """Seed of the data of replica ``shard`` (shard 0 keeps the workload's)."""
+    return int(seed) + 1_000_003 * int(shard)
+
+
 def generator(seed: int, device="cpu") -> torch.Generator:
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
@@ -96,17 +101,20 @@ def normal(shape, gen: torch.Generator, dtype: str, device=None) -> torch.Tensor
     return x if device is None else x.to(device)
 
 
-def make(w: Workload, device="cpu", B=None, H=None, T=None, with_grad_out=False):
+def make(w: Workload, device="cpu", B=None, H=None, T=None, with_grad_out=False, shard=0):
     """Inputs of workload ``w`` (optionally with B/H/T overridden for a
     reduced-size case that keeps the same distributions).  Random numbers are
     drawn on ``device`` (a CUDA generator for device tensors, so that large
     cases need no host copy); the returned dict holds q, k, v (and dO), gamma,
-    omega, phi, and the sizes."""
+    omega, phi, and the sizes.  ``shard`` > 0 draws another batch of q, k, v
+    (a data-parallel replica's own sequences) with the same gamma, omega, phi."""
     B = w.B if B is None else B
     H = w.H if H is None else H
     T = w.T if T is None else T
     gen = generator(w.seed, device)
     gamma, omega, phi = params(H, w.d, w.phi_kind, gen, w.gamma0, device)
+    if shard:
+        gen = generator(shard_seed(w.seed, shard), device)
     out = dict(B=B, H=H, T=T, d=w.d, dv=w.dv, dtype=w.dtype,
                gamma=gamma, omega=omega, phi=phi)
     out["q"] = normal((B, H, T, w.d), gen, w.dtype)
