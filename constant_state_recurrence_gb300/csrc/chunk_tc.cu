@@ -22,10 +22,10 @@
 // Roles (768 threads, six warpgroups): warps 0-7 featurise q into Phi(Q) and
 // warps 8-15 k into Phi(K) (80 registers each, the launch allocation); warps
 // 16-19 drain TMEM (mask + split the scores into bf16 hi/lo parts, snapshot
-// the state to bf16 for the next chunk, normalise and store the outputs; 128
+// the state to bf16 for the next chunk, normalise and store the outputs; 120
 // registers after setmaxnreg); one thread of warp 20 issues every
 // tcgen05.mma and warps 21-22 copy v rows into shared memory with cp.async
-// (that warpgroup keeps 32 registers).  All hand-offs are mbarriers with
+// (that warpgroup keeps 40 registers).  All hand-offs are mbarriers with
 // bounded waits.  The next chunk's q, k, v are bulk-prefetched into L2 while
 // the current one runs; each output tile is staged in shared memory and
 // written with coalesced stores.
@@ -97,11 +97,11 @@ static_assert(kSmemBytes <= 232448, "shared memory layout exceeds 227 KB");
 
 constexpr int kThreads = 768;
 // Register split: the block is launched with 768 x 80 registers; the four
-// featuriser warpgroups keep 80, the MMA / value-loader warpgroup drops to 32
+// featuriser warpgroups keep 80, the MMA / value-loader warpgroup drops to 40
 // and the epilogue warpgroup takes the difference.
 constexpr uint32_t kRegLaunch = 80;
-constexpr uint32_t kRegEpi = 128;
-constexpr uint32_t kRegMma = 32;
+constexpr uint32_t kRegEpi = 120;
+constexpr uint32_t kRegMma = 40;
 static_assert(512 * kRegLaunch + 128 * kRegEpi + 128 * kRegMma <= kThreads * kRegLaunch,
               "setmaxnreg split must fit the launch allocation");
 constexpr int kQWarps = 8;     // warps 0-7: query features
