@@ -148,6 +148,35 @@ def attn_quadratic(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None
     return o, D
 
 
+def attn_power(q, k, v, gamma, omega, phi, p, pos0=0, eps=0.0):
+    """Power-sharpened causal attention (Notes §2.6, eq. (8)), the parallel
+    quadratic form used for training at p > 1:
+
+        a_tj = (s_tj / 4d)^p / (sum_{l<=t} (s_tl / 4d)^p + eps),   o_t = sum_{j<=t} a_tj v_j
+
+    with s_tj = Phi(q_t).Phi(k_j) and d the key dimension.  p is a positive
+    integer; at p = 1 this is attn_quadratic with eps scaled by 4d.
+    Returns o [B,H,T,dv] and D [B,H,T] = sum_{l<=t} (s_tl / 4d)^p (without eps)."""
+    p = int(p)
+    if p < 1:
+        raise ValueError("p must be a positive integer")
+    pq = featurize(q, gamma, omega, phi, pos0)
+    pk = featurize(k, gamma, omega, phi, pos0)
+    v = _heads(v)
+    B, H, T, F = pq.shape
+    d = F // N_CHANNELS
+    mask = np.tril(np.ones((T, T)))
+    o = np.zeros((B, H, T, v.shape[-1]))
+    D = np.zeros((B, H, T))
+    for b in range(B):
+        for h in range(H):
+            w = (pair_kernel(pq[b, h], pk[b, h]) / (4.0 * d)) ** p * mask
+            den = w.sum(axis=1)
+            o[b, h] = (w @ v[b, h]) / (den + eps)[:, None]
+            D[b, h] = den
+    return o, D
+
+
 def attn_recurrent(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None):
     """Constant-state recurrent form (Notes §2.7, eq. (9)):
 

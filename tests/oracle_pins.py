@@ -312,6 +312,57 @@ def check_memory_accounting():
         assert round(O.kv_cache_bytes(int(n), 12, 768) / 1e6, 1) == mb, (n, mb)
 
 
+# --------------------------------------------------------------------------
+# eq. (8) at p > 1: power-sharpened attention (Notes §2.6)
+# --------------------------------------------------------------------------
+
+def _tensor_power_features(phi, p):
+    """Phi^{(x)p}: the p-fold outer product of each feature vector, flattened."""
+    out = phi
+    for _ in range(p - 1):
+        out = np.einsum("...i,...j->...ij", out, phi).reshape(phi.shape[:-1] + (-1,))
+    return out
+
+
+def check_power_matches_tensor_power_features():
+    """The notes' identity (Phi(q).Phi(k))^p = <Phi(q)^(x)p, Phi(k)^(x)p>: build the
+    (6d)^p tensor-power features explicitly and run plain linear attention on them."""
+    for p, d in ((2, 2), (4, 1), (3, 1)):
+        c = _small_case(40 + p, B=1, H=2, T=7, d=d, dv=3)
+        o, D = O.attn_power(**c, p=p, eps=0.25)
+        pq = O.featurize(c["q"], c["gamma"], c["omega"], c["phi"])
+        pk = O.featurize(c["k"], c["gamma"], c["omega"], c["phi"])
+        Fq = _tensor_power_features(pq, p) / (4.0 * d) ** p
+        Fk = _tensor_power_features(pk, p)
+        T = c["q"].shape[2]
+        for h in range(2):
+            o_ref = np.zeros((T, 3))
+            for t in range(T):
+                w = np.array([Fq[0, h, t] @ Fk[0, h, j] for j in range(t + 1)])
+                o_ref[t] = (w[:, None] * c["v"][0, h, :t + 1]).sum(0) / (w.sum() + 0.25)
+                assert abs(D[0, h, t] - w.sum()) <= 1e-12 * max(1.0, w.sum())
+            assert np.allclose(o[0, h], o_ref, rtol=1e-11, atol=1e-12)
+
+
+def check_power_one_is_linear_attention():
+    """At p = 1 eq. (8) is the linear attention with the raw-score eps scaled by 4d."""
+    c = _small_case(50, B=2, H=2, T=11, d=3, dv=2)
+    o1, D1 = O.attn_power(**c, p=1, eps=0.3)
+    o2, D2 = O.attn_quadratic(**c, eps=0.3 * 4 * 3)
+    assert np.allclose(o1, o2, rtol=1e-12, atol=1e-13)
+    assert np.allclose(D1 * (4 * 3), D2, rtol=1e-12, atol=1e-12)
+
+
+def check_power_single_token_and_constant_values():
+    c = _small_case(51, B=1, H=2, T=1, d=3, dv=2)
+    o, _ = O.attn_power(**c, p=2)
+    assert np.allclose(o, c["v"], rtol=0, atol=1e-14)
+    c = _small_case(52, B=1, H=2, T=9, d=3, dv=3)
+    c["v"] = np.broadcast_to(np.array([1.5, -0.25, 4.0]), c["v"].shape).copy()
+    o, _ = O.attn_power(**c, p=4)
+    assert np.allclose(o, c["v"], rtol=1e-13, atol=1e-13)
+
+
 ALL_CHECKS = [
     check_squash_closed_forms,
     check_soft_root_closed_forms,
@@ -327,4 +378,7 @@ ALL_CHECKS = [
     check_rows_and_decode,
     check_backward_finite_differences,
     check_memory_accounting,
+    check_power_matches_tensor_power_features,
+    check_power_one_is_linear_attention,
+    check_power_single_token_and_constant_values,
 ]

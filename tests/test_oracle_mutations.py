@@ -12,7 +12,7 @@ import oracle_pins as P
 
 _orig = {n: getattr(O, n) for n in ("squash", "soft_root", "rotate", "features_from_angles",
                                      "attn_quadratic", "attn_recurrent", "attn_backward",
-                                     "_feature_vjp", "state_bytes", "featurize")}
+                                     "_feature_vjp", "state_bytes", "featurize", "attn_power")}
 
 
 def m_squash_no_abs(u):
@@ -151,6 +151,28 @@ def m_state_bytes_no_z(layers, heads, d, dv, bytes_per_float=4):
     return layers * heads * (6 * d * dv) * bytes_per_float
 
 
+def _power_mutant(kind):
+    def f(q, k, v, gamma, omega, phi, p, pos0=0, eps=0.0):
+        if kind == "exponent":
+            return _orig["attn_power"](q, k, v, gamma, omega, phi, int(p) + 1, pos0, eps)
+        # kind == "no_scale": (s)^p instead of (s / 4d)^p
+        pq = O.featurize(q, gamma, omega, phi, pos0)
+        pk = O.featurize(k, gamma, omega, phi, pos0)
+        v = np.asarray(v, dtype=np.float64)
+        B, H, T, _ = pq.shape
+        mask = np.tril(np.ones((T, T)))
+        o = np.zeros((B, H, T, v.shape[-1]))
+        D = np.zeros((B, H, T))
+        for b in range(B):
+            for h in range(H):
+                w = O.pair_kernel(pq[b, h], pk[b, h]) ** int(p) * mask
+                den = w.sum(1)
+                o[b, h] = (w @ v[b, h]) / (den + eps)[:, None]
+                D[b, h] = den
+        return o, D
+    return f
+
+
 MUTANTS = {
     "squash_no_abs": ("squash", m_squash_no_abs),
     "squash_square": ("squash", m_squash_square),
@@ -170,6 +192,8 @@ MUTANTS = {
     "vjp_squash_derivative": ("_feature_vjp", _vjp_mutant("squash_deriv")),
     "backward_flipped_upstream": ("attn_backward", m_backward_sign_error),
     "state_bytes_without_z": ("state_bytes", m_state_bytes_no_z),
+    "power_exponent_off_by_one": ("attn_power", _power_mutant("exponent")),
+    "power_without_4d_scale": ("attn_power", _power_mutant("no_scale")),
 }
 
 
