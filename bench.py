@@ -61,6 +61,7 @@ FLUSH_BYTES = 256 << 20
 
 # Both arms report this metric on the layer-forward workload (B=4 H=12 T=2048).
 METRIC = "SANATAN p=1 prefill tokens/s"
+POWER_P = 2          # power of the sharpened-attention leg (the pre-training stage's p)
 
 # Data shard of this process: under torchrun every rank processes its own
 # sequences (same gamma, omega, phi), set in main().
@@ -318,6 +319,35 @@ def train_case(dev, flush, steps, warmup, stream):
     return dict(step=step, B=B, H=H, T=T, fwd_launches=fwd_launches)
 
 
+def power_case(p, dev, flush, steps, warmup, stream):
+    """Power-sharpened attention (eq. (8) at integer p) over the layer-forward
+    workload: feature preparation plus the quadratic tensor-core kernel."""
+    from constant_state_recurrence_gb300 import sanatan as S
+    x = W.make(W.LAYER, device=dev, shard=SHARD)
+    g = {n: x[n] for n in ("q", "k", "v", "gamma", "omega", "phi")}
+    B, H, T = x["B"], x["H"], x["T"]
+    o = torch.empty(B, H, T, 64, dtype=torch.float32, device=dev)
+    D = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    ws = torch.empty(S.power_fwd_workspace_size(B, H, T), dtype=torch.uint8, device=dev)
+
+    def step(_i):
+        S.sanatan_power_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], p, out=o,
+                            D_out=D, workspace=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step(0)
+    torch.cuda.synchronize()
+    S.device_status()
+    return dict(step=step, B=B, H=H, T=T, p=p)
+
+
+def power_flops(B, H, T, F=384, dv=64):
+    """Algorithmic flops of the causal quadratic form: every pair j <= t takes
+    one F-long score and one dv-long weighted sum."""
+    return B * H * (T * (T + 1) // 2) * (2 * F + 2 * dv)
+
+
 def oracle_prefill_sample(batch=4, T=2048):
     """The float64 oracle's recurrent form on B x 12 heads x T tokens of the
     layer-forward workload; returns (tokens/s, seconds, threads)."""
@@ -393,7 +423,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["layer", "long", "decode", "train"], default=None,
+    ap.add_argument("--only", choices=["layer", "long", "decode", "train", "power"], default=None,
                     help="run one workload only (profiling); the JSON line keeps its keys")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -422,6 +452,8 @@ def main():
     dec64 = decode_case(64, dev, flush, d64_steps, warm, stream) if want("decode") else None
     tr_steps = max(3, steps // 10)
     train = train_case(dev, flush, tr_steps, warm, stream) if want("train") else None
+    pw_steps = max(4, steps // 5)
+    power = power_case(POWER_P, dev, flush, pw_steps, warm, stream) if want("power") else None
 
     gpu_idx = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -447,6 +479,9 @@ def main():
         tr_whole, tr_kern = [nan], [nan]
         if train:
             tr_whole, tr_kern = timed_steps(train["step"], tr_steps, flush, stream, profile=True)
+        pw_whole, pw_kern = [nan], [nan]
+        if power:
+            pw_whole, pw_kern = timed_steps(power["step"], pw_steps, flush, stream, profile=True)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
     barrier(world)
@@ -534,6 +569,18 @@ def main():
                             / (statistics.mean(tr_whole) * 1e-3) / 1e12 / pk["bf16"],
             "flops_per_token_head": FWD_FLOPS_PER_TOKEN_HEAD + BWD_FLOPS_PER_TOKEN_HEAD,
             "note": "forward + backward per step; bwd_kernel_ms times the backward's dominant kernel"},
+        "power": {
+            "workload": W.LAYER.name, "p": POWER_P, "steps": pw_steps,
+            "tokens_per_s": 4 * 2048 / (statistics.mean(pw_whole) * 1e-3),
+            "ms_per_step": statistics.mean(pw_whole),
+            "kernel_ms": statistics.mean(pw_kern),
+            "flops_per_step": power_flops(4, 12, 2048),
+            "tc_frac_kernel": power_flops(4, 12, 2048) / (statistics.mean(pw_kern) * 1e-3)
+                              / 1e12 / pk["bf16"],
+            "tc_frac_step": power_flops(4, 12, 2048) / (statistics.mean(pw_whole) * 1e-3)
+                            / 1e12 / pk["bf16"],
+            "note": "causal quadratic power attention; flops = pairs j<=t x (2*384 + 2*64); "
+                    "step = feature preparation + attention kernel (kernel_ms)"},
         "timed_region_wall_s": t_wall,
     }
     clocks = clk.summary()

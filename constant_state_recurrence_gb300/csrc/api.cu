@@ -9,6 +9,7 @@ namespace {
 using namespace sanatan;
 
 constexpr int kAbiVersion = 1;
+constexpr int kMaxPower = 8;   // largest p of sanatan_power_fwd
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
@@ -214,6 +215,45 @@ int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
   return from_cuda(chunk_bwd_simt_launch(a, st));
 }
 
+size_t sanatan_power_fwd_workspace_size(int B, int H, int T, int d, int dv) {
+  if (B < 0 || H < 0 || T < 0 || d != 64 || dv != 64) return 0;
+  return pow_fwd_tc_workspace_bytes(B, H, T);
+}
+
+int sanatan_power_fwd(const void* q, const void* k, const void* v, const float* gamma,
+                      const float* omega, const float* phi, int B, int H, int T, int d, int dv,
+                      int64_t pos0, int p, float eps, float* o, float* D, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (int s = check_sizes(B, H, T, d, dv)) return s;
+  if (p < 1) return SANATAN_ERR_INVALID;
+  if (p > kMaxPower) return SANATAN_ERR_UNSUPPORTED;
+  if (!ok_nullable(D)) return SANATAN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * H == 0 || T == 0) return SANATAN_OK;
+  if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(o) || !ok_ptr(workspace))
+    return SANATAN_ERR_INVALID;
+  if (int s = check_params(gamma, omega, phi)) return s;
+  if (workspace_bytes < pow_fwd_tc_workspace_bytes(B, H, T)) return SANATAN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * H * ((T + 127) / 128) > 0x7fffffffLL) return SANATAN_ERR_UNSUPPORTED;
+  if (int s = check_arch()) return s;
+  PowFwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.gamma = gamma;
+  a.omega = omega;
+  a.phi = phi;
+  a.B = B;
+  a.H = H;
+  a.T = T;
+  a.pos0 = pos0;
+  a.p = p;
+  a.eps = eps;
+  a.o = o;
+  a.D = D;
+  a.workspace = workspace;
+  return from_cuda(pow_fwd_tc_launch(a, static_cast<cudaStream_t>(stream)));
+}
+
 int sanatan_set_profile_events(void* start, void* stop) {
   if ((start == nullptr) != (stop == nullptr)) return SANATAN_ERR_INVALID;
   profile_events().start = static_cast<cudaEvent_t>(start);
@@ -225,8 +265,9 @@ int sanatan_device_status(void* stream) {
   if (int s = check_arch()) return s;
   const int h = tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
   const int hb = bwd_tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
-  if (h < 0 || hb < 0) return SANATAN_ERR_CUDA;
-  if (hb) return SANATAN_ERR_TIMEOUT;
+  const int hp = pow_tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
+  if (h < 0 || hb < 0 || hp < 0) return SANATAN_ERR_CUDA;
+  if (hb || hp) return SANATAN_ERR_TIMEOUT;
   return h ? SANATAN_ERR_TIMEOUT : SANATAN_OK;
 }
 

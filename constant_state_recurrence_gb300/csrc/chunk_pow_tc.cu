@@ -1,0 +1,515 @@
+// Power-sharpened causal attention on the tensor cores (bf16 operands, f32
+// accumulation): eq. (8) of "SANATAN: Root-Parity Gated Angular Attention with
+// an Exact Constant-State Recurrent Form" (reading notes §2.6) at a positive
+// integer power p,
+//   a_tj = (s_tj / 4d)^p / (sum_{l<=t} (s_tl / 4d)^p + eps),  o_t = sum_{j<=t} a_tj v_j,
+// with s_tj = Phi(q_t).Phi(k_j).  For p > 1 there is no small state (the
+// notes: the tensor-power features grow as (6d)^p), so this is the parallel
+// quadratic form the paper trains with.
+//
+// Two kernels.  The preparation kernel featurises q and k once (the bf16
+// feature map of the recurrent path) and writes Phi(Q), Phi(K) and V chunk by
+// chunk in the shared-memory operand layouts, so the attention kernel fetches
+// each 128-token chunk with plain bulk copies.  The attention kernel runs one
+// CTA per (sequence, query chunk): Phi(Q) stays in shared memory; for every
+// key chunk j up to the diagonal, P = Phi(Q) Phi(K_j)^T (M = N = 128, K = 320)
+// lands in one of two TMEM buffers, the epilogue raises (P + 64) / 4d to the
+// power p (64 is the constant channel's exact contribution), masks the
+// diagonal chunk, adds the row sums to the denominator in registers and
+// splits the weights into bf16 hi + lo halves in place, and O += P~ V_j
+// (`.ts`, N = 64) accumulates in TMEM.  Heavy (late) query chunks are
+// scheduled first.
+#include "sanatan_internal.h"
+#include "sanatan_math.cuh"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace sanatan {
+
+__device__ int g_pow_tc_error;  // set when a bounded wait gives up
+
+namespace {
+
+using namespace tc;
+using namespace tcc;
+
+// Chunk layouts in the workspace and in shared memory (canonical no-swizzle
+// core matrices of 8 rows x 16 bytes):
+//   Phi: token group tg (8 tokens) at tg * kXQ, feature group fg (8 features)
+//        at fg * 128, token row r at r * 16   (80 KB per chunk)
+//   V:   token group tg at tg * 1024, column group ng (8 columns) at ng * 128,
+//        token row r at r * 16                 (16 KB per chunk)
+constexpr uint32_t kPhiBytes = 16 * kXQ;   // 81920
+constexpr uint32_t kVBytes = 16 * 1024;    // 16384
+constexpr uint32_t kChunkBytes = 2 * kPhiBytes + kVBytes;
+
+// Shared memory: two Phi(K) and two V buffers (chunk j uses buffer j & 1).
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + 2 * kPhiBytes;
+constexpr int kOffMisc = kOffV + 2 * kVBytes;
+
+// TMEM columns: two score buffers, the output accumulator, and Phi(Q) as the
+// A operand of the score products (320 bf16 features = 160 columns; column
+// 4 fg + p holds dimensions 2p, 2p + 1 of feature group fg).
+constexpr uint32_t kTP0 = 0;      // score buffers at 0 and 128
+constexpr uint32_t kTO = 256;     // output accumulator (64 columns)
+constexpr uint32_t kTQ = 320;     // Phi(Q)
+constexpr uint32_t kTmemCols = 512;
+
+enum Bar {
+  kQReady = 0, kKFull0, kKFull1, kKFree0, kKFree1, kVFull0, kVFull1, kPFull0, kPFull1,
+  kPTilde0, kPTilde1, kPVDone0, kPVDone1, kODone, kNumBars
+};
+
+struct Misc {
+  uint64_t bar[kNumBars];
+  uint32_t tmem_base;
+  int abort_flag;
+  float rowsum[2][128];   // partial denominators of the two column halves
+};
+constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
+static_assert(kSmemBytes <= 232448, "shared memory layout exceeds 227 KB");
+
+// warps 0-7 epilogue (warp w: TMEM lanes 32 (w % 4) .. +31, key columns
+// 64 (w / 4) .. +63), warp 8 MMA issue, warp 9 bulk loads
+constexpr int kEpiWarps = 8;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kThreads = 32 * (kLoadWarp + 1);
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct PowParams {
+  const unsigned char* ws;   // per (sequence, chunk): Phi(Q) | Phi(K) | V
+  int H, T, nchunks, bhn;
+  float eps;
+  float* o;                  // [B, H, T, 64] f32
+  float* Dn;                 // [B, H, T] f32 or null
+};
+
+struct PrepParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const float* gamma;
+  const float* omega;
+  const float* phi;
+  int H, T, nchunks;
+  int64_t pos0;
+  unsigned char* ws;
+};
+
+// Byte offset of (token t, feature group fg) in a Phi chunk.
+__host__ __device__ constexpr uint32_t phi_offset(int t, int fg) {
+  return (t >> 3) * kXQ + fg * 128 + (t & 7) * 16;
+}
+
+__device__ __forceinline__ const unsigned char* chunk_base(const unsigned char* ws, int64_t bh,
+                                                           int nchunks, int c) {
+  return ws + (bh * nchunks + c) * static_cast<int64_t>(kChunkBytes);
+}
+
+// ---------------------------------------------------------------------------
+// Preparation: one CTA of 256 threads per (sequence, chunk).  Lane (r, dimension
+// group ag) of warp w owns tokens tq + 8 i (i < 4), tq = 32 (w / 2) + r.
+__global__ void __launch_bounds__(256) pow_prep_kernel(PrepParams prm) {
+  __shared__ float4 dimc[64];
+  const int bh = blockIdx.x / prm.nchunks;
+  const int chunk = blockIdx.x % prm.nchunks;
+  const int h = bh % prm.H;
+  const int tid = threadIdx.x;
+  if (tid < kD) {
+    const float g = prm.gamma[h] * 1.41421356237309515f;
+    float sw, cw;
+    sincosf(prm.omega[h * kD + tid] + 0.785398163397448310f, &sw, &cw);
+    float s8, c8;
+    sincosf(phase_mod_2pi(8, prm.phi[h * kD + tid]), &s8, &c8);
+    dimc[tid] = make_float4(g * cw, g * sw, c8, s8);
+  }
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  const int r = lane & 7;
+  const int ag = (lane >> 3) + 4 * (warp & 1);
+  const int tq = 32 * (warp >> 1) + r;
+  const int tok0 = chunk * kC;
+  const int64_t seq_row0 = static_cast<int64_t>(bh) * prm.T;
+  unsigned char* base = prm.ws + (static_cast<int64_t>(bh) * prm.nchunks + chunk) * kChunkBytes;
+  // every load of the thread first (q, k, v of its four tokens), then the math
+  uint4 raw[3][4];
+#pragma unroll
+  for (int w = 0; w < 3; ++w) {
+    const __nv_bfloat16* src = w == 0 ? prm.q : (w == 1 ? prm.k : prm.v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = tq + 8 * i;
+      raw[w][i] = (tok0 + t < prm.T) ? ldg_nc_v4(src + (seq_row0 + tok0 + t) * kD + 8 * ag)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  // V: 8 columns (group ag) of each of the thread's 4 tokens (zero past the end)
+  unsigned char* vdst = base + 2 * kPhiBytes;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = tq + 8 * i;
+    *reinterpret_cast<uint4*>(vdst + (t >> 3) * 1024 + ag * 128 + (t & 7) * 16) = raw[2][i];
+  }
+  const float4* dc = &dimc[8 * ag];
+  float cb0[8], sb0[8];
+  {
+    const int64_t tabs = prm.pos0 + tok0 + tq;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      __sincosf(phase_mod_2pi(tabs, prm.phi[h * kD + 8 * ag + j]), &sb0[j], &cb0[j]);
+  }
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    unsigned char* dst = base + which * kPhiBytes;
+    float cb[8], sb[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) { cb[j] = cb0[j]; sb[j] = sb0[j]; }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = tq + 8 * i;
+      uint32_t f[5][4];
+      if (tok0 + t < prm.T) {
+        features8(raw[which][i], dc, cb, sb, f);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 5; ++c)
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) f[c][pp] = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < 5; ++c)
+        *reinterpret_cast<uint4*>(dst + phi_offset(t, feat_group(ag, c + 1))) =
+            make_uint4(f[c][0], f[c][1], f[c][2], f[c][3]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 kc = dc[j];
+        const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
+        sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
+        cb[j] = nc;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
+  if (*reinterpret_cast<volatile int*>(&m.abort_flag)) return false;
+  if (mbar_wait_bounded(&m.bar[b], parity, kWaitNs)) return true;
+  m.abort_flag = 1;
+  atomicOr(&g_pow_tc_error, 1);
+  return false;
+}
+
+template <int P>
+__device__ __forceinline__ float pow_int(float x) {
+  if constexpr (P == 1) {
+    return x;
+  } else {
+    const float h = pow_int<P / 2>(x);
+    return (P & 1) ? h * h * x : h * h;
+  }
+}
+
+// Named barrier of the eight epilogue warps.
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+template <int P>
+__global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
+  const uint32_t sK = smem_u32(smem + kOffK);
+  const uint32_t sV = smem_u32(smem + kOffV);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  // query chunk qi of sequence bh; the late (heavier) chunks first
+  const int qi = prm.nchunks - 1 - static_cast<int>(blockIdx.x) / prm.bhn;
+  const int bh = static_cast<int>(blockIdx.x) % prm.bhn;
+  const int nk = qi + 1;
+
+  if (warp == kMmaWarp) {
+    tmem_alloc(&m.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int b = 0; b < kNumBars; ++b) {
+      const bool epi = b == kQReady || b == kPTilde0 || b == kPTilde1;
+      mbar_init(&m.bar[b], epi ? static_cast<uint32_t>(kEpiWarps) : 1u);
+    }
+    m.abort_flag = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------- bulk loads
+    if (lane == 0) {
+      for (int j = 0; j < nk; ++j) {
+        const unsigned char* cj = chunk_base(prm.ws, bh, prm.nchunks, j);
+        const int b = j & 1;
+        // Phi(K_j) into buffer b once the scores of chunk j - 2 have read it
+        if (j >= 2) wait_bar(m, b ? kKFree1 : kKFree0, ((j >> 1) - 1) & 1);
+        mbar_arrive_expect_tx(&m.bar[b ? kKFull1 : kKFull0], kPhiBytes);
+        for (uint32_t off = 0; off < kPhiBytes; off += 16384)
+          bulk_load_g2s(sK + b * kPhiBytes + off, cj + kPhiBytes + off, 16384,
+                        &m.bar[b ? kKFull1 : kKFull0]);
+        // V_j into buffer b once P~ V of chunk j - 2 is done
+        if (j >= 2) wait_bar(m, b ? kPVDone1 : kPVDone0, ((j >> 1) - 1) & 1);
+        mbar_arrive_expect_tx(&m.bar[b ? kVFull1 : kVFull0], kVBytes);
+        bulk_load_g2s(sV + b * kVBytes, cj + 2 * kPhiBytes, kVBytes, &m.bar[b ? kVFull1 : kVFull0]);
+      }
+      // No copy may still be writing shared memory when the CTA exits, even
+      // after an abandoned wait: wait (bounded) for the last phases.
+      for (int j = (nk >= 2 ? nk - 2 : 0); j < nk; ++j) {
+        const int b = j & 1;
+        mbar_wait_bounded(&m.bar[b ? kKFull1 : kKFull0], (j >> 1) & 1, kWaitNs);
+        mbar_wait_bounded(&m.bar[b ? kVFull1 : kVFull0], (j >> 1) & 1, kWaitNs);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idQK = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(128, 64, false, true);
+      wait_bar(m, kQReady, 0);
+      auto issue_qk = [&](int j) {
+        const int b = j & 1;
+        // score buffer b is free once P~ V of chunk j - 2 is done
+        if (j >= 2) wait_bar(m, b ? kPVDone1 : kPVDone0, ((j >> 1) - 1) & 1);
+        uint64_t dk = smem_desc(sK + b * kPhiBytes, 128, kXQ);  // Phi(K_j), K-major B
+        asm volatile("" : "+l"(dk));
+        wait_bar(m, b ? kKFull1 : kKFull0, (j >> 1) & 1);
+        tc_fence_after();
+#pragma unroll
+        for (int st = 0; st < 20; ++st)
+          mma_ts(tmem + kTP0 + 128 * b, tmem + kTQ + 8 * st, dk + 16 * st, idQK, st > 0);
+        mma_commit(&m.bar[b ? kKFree1 : kKFree0]);
+        mma_commit(&m.bar[b ? kPFull1 : kPFull0]);
+      };
+      issue_qk(0);
+      for (int j = 0; j < nk; ++j) {
+        if (j + 1 < nk) issue_qk(j + 1);
+        const int b = j & 1;
+        wait_bar(m, b ? kPTilde1 : kPTilde0, (j >> 1) & 1);
+        wait_bar(m, b ? kVFull1 : kVFull0, (j >> 1) & 1);
+        tc_fence_after();
+        uint64_t dv = smem_desc(sV + b * kVBytes, 1024, 128);  // V_j, MN-major B
+        asm volatile("" : "+l"(dv));
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const uint32_t hi = tmem + kTP0 + 128 * b + 32 * (st >> 1) + 8 * (st & 1);
+          mma_ts(tmem + kTO, hi, dv + (2 * 1024 / 16) * st, idPV, (j | st) != 0);
+          mma_ts(tmem + kTO, hi + 16, dv + (2 * 1024 / 16) * st, idPV, true);
+        }
+        mma_commit(&m.bar[b ? kPVDone1 : kPVDone0]);
+      }
+      mma_commit(&m.bar[kODone]);
+      // nothing may be in flight when TMEM is released
+      mbar_wait_bounded(&m.bar[kODone], 0, kWaitNs);
+    }
+  } else {
+    // ------------------------------------------------- epilogue (warps 0-7)
+    const int qd = warp & 3;
+    const int ch = warp >> 2;
+    const int row = 32 * qd + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
+    {
+      // Phi(Q) of this row, feature groups 20 ch .. 20 ch + 19, into TMEM
+      const unsigned char* src = chunk_base(prm.ws, bh, prm.nchunks, qi) + phi_offset(row, 20 * ch);
+      uint4 w[20];
+#pragma unroll
+      for (int g = 0; g < 20; ++g) w[g] = ldg_nc_v4(src + g * 128);
+#pragma unroll
+      for (int s4 = 0; s4 < 5; ++s4) {
+        uint32_t r[16];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          r[4 * g] = w[4 * s4 + g].x;
+          r[4 * g + 1] = w[4 * s4 + g].y;
+          r[4 * g + 2] = w[4 * s4 + g].z;
+          r[4 * g + 3] = w[4 * s4 + g].w;
+        }
+        tmem_st16(tmem + lane_off + kTQ + 80 * ch + 16 * s4, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.bar[kQReady]);
+    }
+    constexpr float kInv4d = 1.0f / (4.0f * kD);
+    constexpr float kConst = 64.0f * kInv4d;   // the constant channel's share of s / 4d
+    float rowsum = 0.f;
+    for (int j = 0; j < nk; ++j) {
+      const int b = j & 1;
+      wait_bar(m, b ? kPFull1 : kPFull0, (j >> 1) & 1);
+      tc_fence_after();
+      const bool diag = (j == qi);
+      const uint32_t col0 = tmem + lane_off + kTP0 + 128 * b + 64 * ch;
+      float pv[64];
+      if (!(diag && 2 * ch > qd)) {
+        tmem_ld16(col0, *reinterpret_cast<float(*)[16]>(&pv[0]));
+        tmem_ld16(col0 + 16, *reinterpret_cast<float(*)[16]>(&pv[16]));
+        tmem_ld16(col0 + 32, *reinterpret_cast<float(*)[16]>(&pv[32]));
+        tmem_ld16(col0 + 48, *reinterpret_cast<float(*)[16]>(&pv[48]));
+        tmem_ld_wait();
+      }
+#pragma unroll
+      for (int bi = 0; bi < 2; ++bi) {
+        const int blk = 2 * ch + bi;
+        uint32_t hi[16], lo[16];
+        if (diag && blk > qd) {  // every key of this block is after every row of this warp
+#pragma unroll
+          for (int i = 0; i < 16; ++i) { hi[i] = 0u; lo[i] = 0u; }
+        } else {
+          const int lim = (diag && blk == qd) ? lane : 31;  // last key of the block to keep
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float x0 = pow_int<P>(fmaf(pv[32 * bi + 2 * i], kInv4d, kConst));
+            float x1 = pow_int<P>(fmaf(pv[32 * bi + 2 * i + 1], kInv4d, kConst));
+            if (2 * i > lim) x0 = 0.f;
+            if (2 * i + 1 > lim) x1 = 0.f;
+            rowsum += x0 + x1;
+            const uint32_t hpk = pack_bf16x2(x0, x1);
+            hi[i] = hpk;
+            lo[i] = pack_bf16x2(x0 - __uint_as_float(hpk << 16), x1 - __uint_as_float(hpk & 0xffff0000u));
+          }
+        }
+        // in place: hi over keys 32 blk .. +15 of the block's own columns, lo after it
+        tmem_st16(col0 + 32 * bi, hi);
+        tmem_st16(col0 + 32 * bi + 16, lo);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.bar[b ? kPTilde1 : kPTilde0]);
+    }
+    m.rowsum[ch][row] = rowsum;
+    wait_bar(m, kODone, 0);
+    tc_fence_after();
+    float ov[32];
+    tmem_ld16(tmem + lane_off + kTO + 32 * ch, *reinterpret_cast<float(*)[16]>(&ov[0]));
+    tmem_ld16(tmem + lane_off + kTO + 32 * ch + 16, *reinterpret_cast<float(*)[16]>(&ov[16]));
+    tmem_ld_wait();
+    epi_sync();
+    const float den = m.rowsum[0][row] + m.rowsum[1][row];
+    const int t = qi * kC + row;
+    if (t < prm.T) {
+      const int64_t grow = static_cast<int64_t>(bh) * prm.T + t;
+      const float inv = 1.0f / (den + prm.eps);
+      float4* dst = reinterpret_cast<float4*>(prm.o + grow * kD + 32 * ch);
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4)
+        dst[e4] = make_float4(ov[4 * e4] * inv, ov[4 * e4 + 1] * inv, ov[4 * e4 + 2] * inv,
+                              ov[4 * e4 + 3] * inv);
+      if (prm.Dn != nullptr && ch == 0) prm.Dn[grow] = den;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t pow_fwd_tc_workspace_bytes(int B, int H, int T) {
+  const int64_t nchunks = (static_cast<int64_t>(T) + kC - 1) / kC;
+  return static_cast<size_t>(B) * H * nchunks * kChunkBytes;
+}
+
+namespace {
+constexpr int kMaxP = 8;
+using AttnKernel = void (*)(PowParams);
+AttnKernel attn_kernel_for(int p) {
+  switch (p) {
+    case 1: return pow_attn_kernel<1>;
+    case 2: return pow_attn_kernel<2>;
+    case 3: return pow_attn_kernel<3>;
+    case 4: return pow_attn_kernel<4>;
+    case 5: return pow_attn_kernel<5>;
+    case 6: return pow_attn_kernel<6>;
+    case 7: return pow_attn_kernel<7>;
+    default: return pow_attn_kernel<8>;
+  }
+}
+
+cudaError_t pow_set_smem() {
+  static bool done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  for (int p = 1; p <= kMaxP && e == cudaSuccess; ++p)
+    e = cudaFuncSetAttribute(attn_kernel_for(p), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+}  // namespace
+
+cudaError_t pow_fwd_tc_launch(const PowFwdArgs& a, cudaStream_t st) {
+  const int bhn = a.B * a.H;
+  const int nchunks = (a.T + kC - 1) / kC;
+  if (bhn == 0 || nchunks == 0) return cudaSuccess;
+  cudaError_t e = pow_set_smem();
+  if (e != cudaSuccess) return e;
+  PrepParams pp{};
+  pp.q = static_cast<const __nv_bfloat16*>(a.q);
+  pp.k = static_cast<const __nv_bfloat16*>(a.k);
+  pp.v = static_cast<const __nv_bfloat16*>(a.v);
+  pp.gamma = a.gamma;
+  pp.omega = a.omega;
+  pp.phi = a.phi;
+  pp.H = a.H;
+  pp.T = a.T;
+  pp.nchunks = nchunks;
+  pp.pos0 = a.pos0;
+  pp.ws = static_cast<unsigned char*>(a.workspace);
+  const unsigned grid = static_cast<unsigned>(bhn) * static_cast<unsigned>(nchunks);
+  pow_prep_kernel<<<grid, 256, 0, st>>>(pp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  PowParams p{};
+  p.ws = pp.ws;
+  p.H = a.H;
+  p.T = a.T;
+  p.nchunks = nchunks;
+  p.bhn = bhn;
+  p.eps = a.eps;
+  p.o = a.o;
+  p.Dn = a.D;
+  const ProfileEvents& pe = profile_events();
+  const bool rec = pe.start != nullptr;
+  if (rec) cudaEventRecord(pe.start, st);
+  if (a.p < 1 || a.p > kMaxP) return cudaErrorInvalidValue;
+  attn_kernel_for(a.p)<<<grid, kThreads, kSmemBytes, st>>>(p);
+  e = cudaGetLastError();
+  if (rec) cudaEventRecord(pe.stop, st);
+  return e;
+}
+
+int pow_tc_read_and_clear_error(cudaStream_t st) {
+  int h = 0;
+  if (cudaMemcpyFromSymbolAsync(&h, g_pow_tc_error, sizeof(int), 0, cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return -1;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_pow_tc_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                                st) != cudaSuccess)
+      return -1;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+  }
+  return h;
+}
+
+}  // namespace sanatan

@@ -119,4 +119,24 @@ int chunk_fwd_checked(const void* q, const void* k, const void* v, int in_dtype,
                       void* workspace, size_t workspace_bytes, void* stream, bool fewer_segments);
 cudaError_t chunk_bwd_tc_launch(const ChunkBwdArgs& a, cudaStream_t st);
 int bwd_tc_read_and_clear_error(cudaStream_t st);
+
+// Power-sharpened causal attention (bf16 q, k, v [B, H, T, 64], integer p).
+struct PowFwdArgs {
+  const void* q = nullptr;
+  const void* k = nullptr;
+  const void* v = nullptr;
+  const float* gamma = nullptr;
+  const float* omega = nullptr;
+  const float* phi = nullptr;
+  int B = 0, H = 0, T = 0;
+  int64_t pos0 = 0;
+  int p = 1;
+  float eps = 0.f;
+  float* o = nullptr;
+  float* D = nullptr;
+  void* workspace = nullptr;   // pow_fwd_tc_workspace_bytes
+};
+size_t pow_fwd_tc_workspace_bytes(int B, int H, int T);
+cudaError_t pow_fwd_tc_launch(const PowFwdArgs& a, cudaStream_t st);
+int pow_tc_read_and_clear_error(cudaStream_t st);
 }  // namespace sanatan

@@ -38,6 +38,27 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
       : "memory");
 }
 
+// Arrive and add `bytes` to the transaction count the current phase waits for
+// (the bulk copies that follow complete it).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+// Bulk asynchronous copy global -> shared of `bytes` (both addresses 16-byte
+// aligned, bytes a multiple of 16); completion is counted on `bar`.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t sdst, const void* gsrc, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          sdst),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Arrive without release semantics: the thread does not wait for its earlier
 // global loads and stores.  Only for hand-offs that order nothing but work the
 // thread has already waited for (e.g. TMEM loads after tcgen05.wait::ld).

@@ -43,6 +43,10 @@ _SIGS = {
                                    _c_int, _c_int, _c_int, _c_i64, _c_f, _c_p, _c_p, _c_p, _c_p,
                                    _c_p, _c_int, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_sz,
                                    _c_p]),
+    "sanatan_power_fwd_workspace_size": (_c_sz, [_c_int] * 5),
+    "sanatan_power_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int,
+                                   _c_int, _c_int, _c_i64, _c_int, _c_f, _c_p, _c_p, _c_p, _c_sz,
+                                   _c_p]),
     "sanatan_device_status": (_c_int, [_c_p]),
     "sanatan_set_profile_events": (_c_int, [_c_p, _c_p]),
     "sanatan_decode_step": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int,
@@ -228,6 +232,41 @@ def sanatan_chunk_fwd_noalloc(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=No
                                          _stream(dev))
     _check("sanatan_chunk_fwd_noalloc", st)
     return o, D, S, z
+
+
+def power_fwd_workspace_size(B, H, T, d=64, dv=64):
+    return int(lib().sanatan_power_fwd_workspace_size(B, H, T, d, dv))
+
+
+def sanatan_power_fwd(q, k, v, gamma, omega, phi, p, pos0=0, eps=0.0, want_D=True, out=None,
+                      D_out=None, workspace=None):
+    """Power-sharpened causal attention at integer power p (bf16 q, k, v).
+
+    Returns (o [B,H,T,dv] f32, D [B,H,T] f32 or None)."""
+    _need(q, "q", (torch.bfloat16,))
+    B, H, T, d = q.shape
+    _need(k, "k", (torch.bfloat16,), (B, H, T, d))
+    dv = v.shape[-1]
+    _need(v, "v", (torch.bfloat16,), (B, H, T, dv))
+    for n, t in (("gamma", gamma), ("omega", omega), ("phi", phi)):
+        _need(t, n, (torch.float32,))
+    dev = q.device
+    o = out if out is not None else torch.empty(B, H, T, dv, dtype=torch.float32, device=dev)
+    _need(o, "o", (torch.float32,), (B, H, T, dv))
+    D = D_out
+    if D is None and want_D:
+        D = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    if D is not None:
+        _need(D, "D", (torch.float32,), (B, H, T))
+    ws_size = power_fwd_workspace_size(B, H, T, d, dv)
+    if workspace is None and ws_size > 0:
+        workspace = torch.empty(ws_size, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().sanatan_power_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(omega), _ptr(phi),
+                                 B, H, T, d, dv, int(pos0), int(p), float(eps), _ptr(o), _ptr(D),
+                                 _ptr(workspace), ws_bytes, _stream(dev))
+    _check("sanatan_power_fwd", st)
+    return o, D
 
 
 def chunk_bwd_workspace_size(B, H, T, d=64, dv=64, dtype=torch.bfloat16):

@@ -169,9 +169,35 @@ SANATAN_API int sanatan_chunk_bwd(const void* q, const void* k, const void* v, i
                       void* stream);
 
 /*
+ * sanatan_power_fwd -- power-sharpened causal attention, eq. (8) (Notes §2.6),
+ * at a positive integer power p, in the parallel (quadratic) form the paper
+ * trains with; for p > 1 it has no constant-size state:
+ *     a_tj = (s_tj / 4d)^p / (sum_{l<=t} (s_tl / 4d)^p + eps),
+ *     o_t  = sum_{j<=t} a_tj v_j,      s_tj = Phi(q_t) . Phi(k_j).
+ * At p = 1 it equals sanatan_chunk_fwd with eps multiplied by 4d.
+ *   q, k    [B, H, T, d]  bf16;  v [B, H, T, dv] bf16
+ *   p       1 <= p <= 8 (SANATAN_ERR_INVALID below 1, SANATAN_ERR_UNSUPPORTED above 8)
+ *   o       [B, H, T, dv] f32 output
+ *   D       [B, H, T] f32 output or NULL: sum_{l<=t} (s_tl / 4d)^p, without eps
+ *   workspace / workspace_bytes: device scratch of at least
+ *           sanatan_power_fwd_workspace_size(...) bytes (about 1.4 KB per
+ *           token, rounded up to whole 128-token chunks): the bf16 features
+ *           Phi(q), Phi(k) and v laid out for the tensor cores; its contents on
+ *           entry do not matter.
+ * Scores, the power and the denominator are float32; features and values
+ * enter the tensor cores as bf16, the weights (s/4d)^p as a bf16 pair (hi +
+ * lo).  T = 0 or B * H = 0 does nothing.
+ */
+SANATAN_API size_t sanatan_power_fwd_workspace_size(int B, int H, int T, int d, int dv);
+SANATAN_API int sanatan_power_fwd(const void* q, const void* k, const void* v, const float* gamma,
+                                  const float* omega, const float* phi, int B, int H, int T, int d,
+                                  int dv, int64_t pos0, int p, float eps, float* o, float* D,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * sanatan_set_profile_events -- instrumentation for benchmarks.  When both
- * are non-NULL, the calling thread's subsequent sanatan_chunk_fwd and
- * sanatan_chunk_bwd calls record `start` (a cudaEvent_t) on their stream just
+ * are non-NULL, the calling thread's subsequent sanatan_chunk_fwd,
+ * sanatan_chunk_bwd and sanatan_power_fwd calls record `start` (a cudaEvent_t) on their stream just
  * before their dominant kernel launch and `stop` just after it, so the caller
  * can time that kernel alone.  Pass NULL, NULL to turn it off.  Thread-local;
  * the events stay owned by the caller.

@@ -77,6 +77,30 @@ def test_argument_errors_before_any_launch(lib):
                                    64, 0.0, None, None) == 1
     assert lib.sanatan_decode_step(None, P(16), P(16), P(16), P(16), P(16), P(16), P(16), P(16),
                                    4, 4, 64, 64, 0.0, P(16), None) == 1
+    # power attention: p below 1, p above the largest supported, misaligned D
+    assert lib.sanatan_power_fwd(None, None, None, None, None, None, 1, 1, 4, 64, 64, 0, 0, 0.0,
+                                 None, None, None, 0, None) == 1
+    assert lib.sanatan_power_fwd(None, None, None, None, None, None, 1, 1, 4, 64, 64, 0, 9, 0.0,
+                                 None, None, None, 0, None) == 2
+    assert lib.sanatan_power_fwd(P(16), P(16), P(16), P(16), P(16), P(16), 1, 1, 4, 64, 64, 0, 2,
+                                 0.0, P(16), P(8), P(16), 1 << 20, None) == 1
+    # empty problems are no-ops; a short workspace is rejected
+    assert lib.sanatan_power_fwd(None, None, None, None, None, None, 1, 1, 0, 64, 64, 0, 2, 0.0,
+                                 None, None, None, 0, None) == 0
+    need = lib.sanatan_power_fwd_workspace_size(1, 1, 4, 64, 64)
+    assert lib.sanatan_power_fwd(P(16), P(16), P(16), P(16), P(16), P(16), 1, 1, 4, 64, 64, 0, 2,
+                                 0.0, P(16), None, P(16), need - 16, None) == 1
+
+
+def test_power_workspace_size(lib):
+    # bf16 Phi(q), Phi(k) (320 non-constant features each) and v per token,
+    # whole 128-token chunks
+    per_chunk = 128 * (2 * 320 + 64) * 2
+    assert lib.sanatan_power_fwd_workspace_size(1, 1, 1, 64, 64) == per_chunk
+    assert lib.sanatan_power_fwd_workspace_size(4, 12, 2048, 64, 64) == 48 * 16 * per_chunk
+    assert lib.sanatan_power_fwd_workspace_size(2, 3, 129, 64, 64) == 6 * 2 * per_chunk
+    assert lib.sanatan_power_fwd_workspace_size(1, 1, 0, 64, 64) == 0
+    assert lib.sanatan_power_fwd_workspace_size(1, 1, 4, 32, 64) == 0
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
