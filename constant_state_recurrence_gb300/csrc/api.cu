@@ -233,7 +233,7 @@ int sanatan_power_fwd(const void* q, const void* k, const void* v, const float* 
     return SANATAN_ERR_INVALID;
   if (int s = check_params(gamma, omega, phi)) return s;
   if (workspace_bytes < pow_fwd_tc_workspace_bytes(B, H, T)) return SANATAN_ERR_INVALID;
-  if (static_cast<int64_t>(B) * H * ((T + 127) / 128) > 0x7fffffffLL) return SANATAN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * H * ((T + 127) / 128) > 0x3fffffffLL) return SANATAN_ERR_UNSUPPORTED;
   if (int s = check_arch()) return s;
   PowFwdArgs a;
   a.q = q;

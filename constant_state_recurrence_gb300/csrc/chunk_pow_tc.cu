@@ -37,10 +37,14 @@ using namespace tcc;
 // core matrices of 8 rows x 16 bytes):
 //   Phi: token group tg (8 tokens) at tg * kXQ, feature group fg (8 features)
 //        at fg * 128, token row r at r * 16   (80 KB per chunk)
-//   V:   token group tg at tg * 1024, column group ng (8 columns) at ng * 128,
-//        token row r at r * 16                 (16 KB per chunk)
+//   V:   [V | 1 | 0] (80 columns: the ones column makes the tensor core sum
+//        the weights, i.e. the denominator, next to the outputs): token group
+//        tg at tg * 1280, column group ng (8 columns) at ng * 128, token row r
+//        at r * 16                             (20 KB per chunk)
 constexpr uint32_t kPhiBytes = 16 * kXQ;   // 81920
-constexpr uint32_t kVBytes = 16 * 1024;    // 16384
+constexpr uint32_t kVGroup = 10 * 128;     // bytes per 8-token group of [V | 1 | 0]
+constexpr uint32_t kVBytes = 16 * kVGroup; // 20480
+constexpr int kNV = 80;                    // N of the value product
 constexpr uint32_t kChunkBytes = 2 * kPhiBytes + kVBytes;
 
 // Shared memory: two Phi(K) and two V buffers (chunk j uses buffer j & 1).
@@ -52,8 +56,8 @@ constexpr int kOffMisc = kOffV + 2 * kVBytes;
 // A operand of the score products (320 bf16 features = 160 columns; column
 // 4 fg + p holds dimensions 2p, 2p + 1 of feature group fg).
 constexpr uint32_t kTP0 = 0;      // score buffers at 0 and 128
-constexpr uint32_t kTO = 256;     // output accumulator (64 columns)
-constexpr uint32_t kTQ = 320;     // Phi(Q)
+constexpr uint32_t kTO = 256;     // output accumulator [O | denominator | 0] (80 columns)
+constexpr uint32_t kTQ = 352;     // Phi(Q)
 constexpr uint32_t kTmemCols = 512;
 
 enum Bar {
@@ -65,17 +69,17 @@ struct Misc {
   uint64_t bar[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
-  float rowsum[2][128];   // partial denominators of the two column halves
 };
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kSmemBytes <= 232448, "shared memory layout exceeds 227 KB");
 
 // warps 0-7 epilogue (warp w: TMEM lanes 32 (w % 4) .. +31, key columns
-// 64 (w / 4) .. +63), warp 8 MMA issue, warp 9 bulk loads
+// 64 (w / 4) .. +63), warp 8 MMA issue, warp 9 Phi(K) loads, warp 10 V loads
 constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
-constexpr int kThreads = 32 * (kLoadWarp + 1);
+constexpr int kVLoadWarp = 10;
+constexpr int kThreads = 32 * (kVLoadWarp + 1);
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct PowParams {
@@ -109,12 +113,15 @@ __device__ __forceinline__ const unsigned char* chunk_base(const unsigned char* 
 }
 
 // ---------------------------------------------------------------------------
-// Preparation: one CTA of 256 threads per (sequence, chunk).  Lane (r, dimension
-// group ag) of warp w owns tokens tq + 8 i (i < 4), tq = 32 (w / 2) + r.
+// Preparation: one CTA of 256 threads per half chunk (64 tokens).  Lane
+// (r, dimension group ag) of warp w owns the chunk's tokens tq + 8 i (i < 2),
+// tq = 64 half + 16 (w / 2) + r.
+constexpr int kPrepTok = 2;
 __global__ void __launch_bounds__(256) pow_prep_kernel(PrepParams prm) {
   __shared__ float4 dimc[64];
-  const int bh = blockIdx.x / prm.nchunks;
-  const int chunk = blockIdx.x % prm.nchunks;
+  const int half = blockIdx.x & 1;
+  const int bh = (blockIdx.x >> 1) / prm.nchunks;
+  const int chunk = (blockIdx.x >> 1) % prm.nchunks;
   const int h = bh % prm.H;
   const int tid = threadIdx.x;
   if (tid < kD) {
@@ -129,28 +136,33 @@ __global__ void __launch_bounds__(256) pow_prep_kernel(PrepParams prm) {
   const int warp = tid >> 5, lane = tid & 31;
   const int r = lane & 7;
   const int ag = (lane >> 3) + 4 * (warp & 1);
-  const int tq = 32 * (warp >> 1) + r;
+  const int tq = 64 * half + 16 * (warp >> 1) + r;
   const int tok0 = chunk * kC;
   const int64_t seq_row0 = static_cast<int64_t>(bh) * prm.T;
   unsigned char* base = prm.ws + (static_cast<int64_t>(bh) * prm.nchunks + chunk) * kChunkBytes;
-  // every load of the thread first (q, k, v of its four tokens), then the math
-  uint4 raw[3][4];
+  // every load of the thread first (q, k, v of its tokens), then the math
+  uint4 raw[3][kPrepTok];
 #pragma unroll
   for (int w = 0; w < 3; ++w) {
     const __nv_bfloat16* src = w == 0 ? prm.q : (w == 1 ? prm.k : prm.v);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kPrepTok; ++i) {
       const int t = tq + 8 * i;
       raw[w][i] = (tok0 + t < prm.T) ? ldg_nc_v4(src + (seq_row0 + tok0 + t) * kD + 8 * ag)
                                      : make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  // V: 8 columns (group ag) of each of the thread's 4 tokens (zero past the end)
+  // V: 8 columns (group ag) of each of the thread's tokens (zero past the end)
   unsigned char* vdst = base + 2 * kPhiBytes;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < kPrepTok; ++i) {
     const int t = tq + 8 * i;
-    *reinterpret_cast<uint4*>(vdst + (t >> 3) * 1024 + ag * 128 + (t & 7) * 16) = raw[2][i];
+    unsigned char* vrow = vdst + (t >> 3) * kVGroup + (t & 7) * 16;
+    *reinterpret_cast<uint4*>(vrow + ag * 128) = raw[2][i];
+    if (ag == 0) {  // the ones column (bf16 1.0) and its zero padding
+      *reinterpret_cast<uint4*>(vrow + 8 * 128) = make_uint4(0x3F80u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(vrow + 9 * 128) = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   const float4* dc = &dimc[8 * ag];
   float cb0[8], sb0[8];
@@ -167,7 +179,7 @@ __global__ void __launch_bounds__(256) pow_prep_kernel(PrepParams prm) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) { cb[j] = cb0[j]; sb[j] = sb0[j]; }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kPrepTok; ++i) {
       const int t = tq + 8 * i;
       uint32_t f[5][4];
       if (tok0 + t < prm.T) {
@@ -211,9 +223,27 @@ __device__ __forceinline__ float pow_int(float x) {
   }
 }
 
-// Named barrier of the eight epilogue warps.
-__device__ __forceinline__ void epi_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+// The weights ((s / 4d)^p) of 32 keys of one row from their scores,
+// split into bf16 pairs hi (the truncated value) + lo (the rounded rest), keys
+// 2i and 2i + 1 in word i.  MASK: keys after `lim` get weight 0.
+template <int P, bool MASK>
+__device__ __forceinline__ void weights32(const float* pv, int lim, uint32_t (&hi)[16],
+                                          uint32_t (&lo)[16]) {
+  constexpr float kInv4d = 1.0f / (4.0f * kD);
+  constexpr float kConst = 64.0f * kInv4d;   // the constant channel's share of s / 4d
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float x0 = pow_int<P>(fmaf(pv[2 * i], kInv4d, kConst));
+    float x1 = pow_int<P>(fmaf(pv[2 * i + 1], kInv4d, kConst));
+    if (MASK) {
+      if (2 * i > lim) x0 = 0.f;
+      if (2 * i + 1 > lim) x1 = 0.f;
+    }
+    const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+    hi[i] = __byte_perm(b0, b1, 0x7632);
+    lo[i] = pack_bf16x2(x0 - __uint_as_float(b0 & 0xffff0000u),
+                        x1 - __uint_as_float(b1 & 0xffff0000u));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -228,7 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
   const int lane = tid & 31;
   // query chunk qi of sequence bh; the late (heavier) chunks first
   const int qi = prm.nchunks - 1 - static_cast<int>(blockIdx.x) / prm.bhn;
-  const int bh = static_cast<int>(blockIdx.x) % prm.bhn;
+  // sequences in reverse order: the preparation kernel wrote the last ones
+  // most recently, so they are the likeliest to still be in L2
+  const int bh = prm.bhn - 1 - static_cast<int>(blockIdx.x) % prm.bhn;
   const int nk = qi + 1;
 
   if (warp == kMmaWarp) {
@@ -249,35 +281,47 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
   const uint32_t tmem = m.tmem_base;
 
   if (warp == kLoadWarp) {
-    // ------------------------------------------------- bulk loads
+    // ------------------------------------------------- Phi(K) loads
     if (lane == 0) {
       for (int j = 0; j < nk; ++j) {
         const unsigned char* cj = chunk_base(prm.ws, bh, prm.nchunks, j);
         const int b = j & 1;
+        // chunk j + 2 into L2 ahead of its shared-memory load
+        if (j + 2 < nk) {
+          const unsigned char* cn = chunk_base(prm.ws, bh, prm.nchunks, j + 2);
+          prefetch_l2_bulk(cn + kPhiBytes, kPhiBytes + kVBytes);
+        }
         // Phi(K_j) into buffer b once the scores of chunk j - 2 have read it
         if (j >= 2) wait_bar(m, b ? kKFree1 : kKFree0, ((j >> 1) - 1) & 1);
         mbar_arrive_expect_tx(&m.bar[b ? kKFull1 : kKFull0], kPhiBytes);
         for (uint32_t off = 0; off < kPhiBytes; off += 16384)
           bulk_load_g2s(sK + b * kPhiBytes + off, cj + kPhiBytes + off, 16384,
                         &m.bar[b ? kKFull1 : kKFull0]);
+      }
+      // No copy may still be writing shared memory when the CTA exits, even
+      // after an abandoned wait: wait (bounded) for the last phases.
+      for (int j = (nk >= 2 ? nk - 2 : 0); j < nk; ++j)
+        mbar_wait_bounded(&m.bar[(j & 1) ? kKFull1 : kKFull0], (j >> 1) & 1, kWaitNs);
+    }
+  } else if (warp == kVLoadWarp) {
+    // ------------------------------------------------- V loads
+    if (lane == 0) {
+      for (int j = 0; j < nk; ++j) {
+        const unsigned char* cj = chunk_base(prm.ws, bh, prm.nchunks, j);
+        const int b = j & 1;
         // V_j into buffer b once P~ V of chunk j - 2 is done
         if (j >= 2) wait_bar(m, b ? kPVDone1 : kPVDone0, ((j >> 1) - 1) & 1);
         mbar_arrive_expect_tx(&m.bar[b ? kVFull1 : kVFull0], kVBytes);
         bulk_load_g2s(sV + b * kVBytes, cj + 2 * kPhiBytes, kVBytes, &m.bar[b ? kVFull1 : kVFull0]);
       }
-      // No copy may still be writing shared memory when the CTA exits, even
-      // after an abandoned wait: wait (bounded) for the last phases.
-      for (int j = (nk >= 2 ? nk - 2 : 0); j < nk; ++j) {
-        const int b = j & 1;
-        mbar_wait_bounded(&m.bar[b ? kKFull1 : kKFull0], (j >> 1) & 1, kWaitNs);
-        mbar_wait_bounded(&m.bar[b ? kVFull1 : kVFull0], (j >> 1) & 1, kWaitNs);
-      }
+      for (int j = (nk >= 2 ? nk - 2 : 0); j < nk; ++j)
+        mbar_wait_bounded(&m.bar[(j & 1) ? kVFull1 : kVFull0], (j >> 1) & 1, kWaitNs);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------- MMA issue
     if (lane == 0) {
       constexpr uint32_t idQK = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idPV = idesc_bf16_f32(128, 64, false, true);
+      constexpr uint32_t idPV = idesc_bf16_f32(128, kNV, false, true);
       wait_bar(m, kQReady, 0);
       auto issue_qk = [&](int j) {
         const int b = j & 1;
@@ -300,13 +344,13 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
         wait_bar(m, b ? kPTilde1 : kPTilde0, (j >> 1) & 1);
         wait_bar(m, b ? kVFull1 : kVFull0, (j >> 1) & 1);
         tc_fence_after();
-        uint64_t dv = smem_desc(sV + b * kVBytes, 1024, 128);  // V_j, MN-major B
+        uint64_t dv = smem_desc(sV + b * kVBytes, kVGroup, 128);  // [V_j | 1 | 0], MN-major B
         asm volatile("" : "+l"(dv));
 #pragma unroll
         for (int st = 0; st < 8; ++st) {
           const uint32_t hi = tmem + kTP0 + 128 * b + 32 * (st >> 1) + 8 * (st & 1);
-          mma_ts(tmem + kTO, hi, dv + (2 * 1024 / 16) * st, idPV, (j | st) != 0);
-          mma_ts(tmem + kTO, hi + 16, dv + (2 * 1024 / 16) * st, idPV, true);
+          mma_ts(tmem + kTO, hi, dv + (2 * kVGroup / 16) * st, idPV, (j | st) != 0);
+          mma_ts(tmem + kTO, hi + 16, dv + (2 * kVGroup / 16) * st, idPV, true);
         }
         mma_commit(&m.bar[b ? kPVDone1 : kPVDone0]);
       }
@@ -343,9 +387,6 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&m.bar[kQReady]);
     }
-    constexpr float kInv4d = 1.0f / (4.0f * kD);
-    constexpr float kConst = 64.0f * kInv4d;   // the constant channel's share of s / 4d
-    float rowsum = 0.f;
     for (int j = 0; j < nk; ++j) {
       const int b = j & 1;
       wait_bar(m, b ? kPFull1 : kPFull0, (j >> 1) & 1);
@@ -364,22 +405,15 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
       for (int bi = 0; bi < 2; ++bi) {
         const int blk = 2 * ch + bi;
         uint32_t hi[16], lo[16];
-        if (diag && blk > qd) {  // every key of this block is after every row of this warp
+        if (!diag) {
+          weights32<P, false>(pv + 32 * bi, 31, hi, lo);
+        } else if (blk == qd) {  // keys up to the row's own
+          weights32<P, true>(pv + 32 * bi, lane, hi, lo);
+        } else if (blk < qd) {
+          weights32<P, false>(pv + 32 * bi, 31, hi, lo);
+        } else {  // every key of this block is after every row of this warp
 #pragma unroll
           for (int i = 0; i < 16; ++i) { hi[i] = 0u; lo[i] = 0u; }
-        } else {
-          const int lim = (diag && blk == qd) ? lane : 31;  // last key of the block to keep
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x0 = pow_int<P>(fmaf(pv[32 * bi + 2 * i], kInv4d, kConst));
-            float x1 = pow_int<P>(fmaf(pv[32 * bi + 2 * i + 1], kInv4d, kConst));
-            if (2 * i > lim) x0 = 0.f;
-            if (2 * i + 1 > lim) x1 = 0.f;
-            rowsum += x0 + x1;
-            const uint32_t hpk = pack_bf16x2(x0, x1);
-            hi[i] = hpk;
-            lo[i] = pack_bf16x2(x0 - __uint_as_float(hpk << 16), x1 - __uint_as_float(hpk & 0xffff0000u));
-          }
         }
         // in place: hi over keys 32 blk .. +15 of the block's own columns, lo after it
         tmem_st16(col0 + 32 * bi, hi);
@@ -390,15 +424,14 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&m.bar[b ? kPTilde1 : kPTilde0]);
     }
-    m.rowsum[ch][row] = rowsum;
     wait_bar(m, kODone, 0);
     tc_fence_after();
-    float ov[32];
+    float ov[32], dn[16];
     tmem_ld16(tmem + lane_off + kTO + 32 * ch, *reinterpret_cast<float(*)[16]>(&ov[0]));
     tmem_ld16(tmem + lane_off + kTO + 32 * ch + 16, *reinterpret_cast<float(*)[16]>(&ov[16]));
+    tmem_ld16(tmem + lane_off + kTO + 64, dn);   // the denominator column
     tmem_ld_wait();
-    epi_sync();
-    const float den = m.rowsum[0][row] + m.rowsum[1][row];
+    const float den = dn[0];
     const int t = qi * kC + row;
     if (t < prm.T) {
       const int64_t grow = static_cast<int64_t>(bh) * prm.T + t;
@@ -475,7 +508,7 @@ cudaError_t pow_fwd_tc_launch(const PowFwdArgs& a, cudaStream_t st) {
   pp.pos0 = a.pos0;
   pp.ws = static_cast<unsigned char*>(a.workspace);
   const unsigned grid = static_cast<unsigned>(bhn) * static_cast<unsigned>(nchunks);
-  pow_prep_kernel<<<grid, 256, 0, st>>>(pp);
+  pow_prep_kernel<<<2 * grid, 256, 0, st>>>(pp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   PowParams p{};
   p.ws = pp.ws;

@@ -93,9 +93,9 @@ def test_argument_errors_before_any_launch(lib):
 
 
 def test_power_workspace_size(lib):
-    # bf16 Phi(q), Phi(k) (320 non-constant features each) and v per token,
+    # bf16 Phi(q), Phi(k) (320 non-constant features each) and [v | 1 | 0] per token,
     # whole 128-token chunks
-    per_chunk = 128 * (2 * 320 + 64) * 2
+    per_chunk = 128 * (2 * 320 + 80) * 2
     assert lib.sanatan_power_fwd_workspace_size(1, 1, 1, 64, 64) == per_chunk
     assert lib.sanatan_power_fwd_workspace_size(4, 12, 2048, 64, 64) == 48 * 16 * per_chunk
     assert lib.sanatan_power_fwd_workspace_size(2, 3, 129, 64, 64) == 6 * 2 * per_chunk
