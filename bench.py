@@ -46,6 +46,8 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "sanatan_tc_kernel": os.path.join(ROOT, "constant_state_recurrence_gb300", "csrc", "chunk_tc.cu"),
+    "pow_attn_kernel": os.path.join(ROOT, "constant_state_recurrence_gb300", "csrc",
+                                    "chunk_pow_tc.cu"),
 }
 
 # Algorithmic work per token-head (d = dv = 64, F = 6d = 384, C = 64), the
@@ -579,6 +581,7 @@ def main():
                               / 1e12 / pk["bf16"],
             "tc_frac_step": power_flops(4, 12, 2048) / (statistics.mean(pw_whole) * 1e-3)
                             / 1e12 / pk["bf16"],
+            "traffic": traffic_for("pow_attn_kernel", W.LAYER.name),
             "note": "causal quadratic power attention; flops = pairs j<=t x (2*384 + 2*64); "
                     "step = feature preparation + attention kernel (kernel_ms)"},
         "timed_region_wall_s": t_wall,
