@@ -9,7 +9,8 @@ feature map, intra-chunk scores, value products, state carry, segment scan,
 normalisation, stores).  `value` is prefill tokens/s (B*T per step, all heads),
 timed with CUDA events on the launching stream, L2 flushed (256 MiB write)
 before every timed step.  The same line also carries the long-prefill,
-decode and training measurements (each timed the same way), the roofline of
+decode, training and power-sharpened attention (p = 2) measurements (each
+timed the same way), the roofline of
 the dominant kernel, an end-to-end figure through the C ABI with pinned host
 buffers, the float64 oracle timed on the host cores, and the SM clocks
 sampled during the timed region.
