@@ -352,6 +352,49 @@ def attn_backward(q, k, v, gamma, omega, phi, dO, pos0=0, eps=0.0, S0=None, z0=N
                 dphi=dph_q + dph_k)
 
 
+def attn_power_backward(q, k, v, gamma, omega, phi, dO, p, pos0=0, eps=0.0):
+    """Gradients of sum(o * dO) for ``attn_power`` (Notes §2.6, eq. (8)); the
+    pages give no gradient, so this is the chain rule.  With
+    w_tj = [j <= t] (s_tj / 4d)^p, D_t = sum_j w_tj, Dh_t = D_t + eps and
+    o_t = sum_j w_tj v_j / Dh_t:
+        dN_t = dO_t / Dh_t,          dD_t = -(dO_t . o_t) / Dh_t,
+        dw_tj = [j <= t] (dN_t . v_j + dD_t),
+        ds_tj = dw_tj p (s_tj / 4d)^(p-1) / 4d,
+        dv_j = sum_t w_tj dN_t,
+        dPhi(q_t) = sum_j ds_tj Phi(k_j),    dPhi(k_j) = sum_t ds_tj Phi(q_t),
+    then through the feature map.  Returns the dict of ``attn_backward``."""
+    p = int(p)
+    if p < 1:
+        raise ValueError("p must be a positive integer")
+    pq = featurize(q, gamma, omega, phi, pos0)
+    pk = featurize(k, gamma, omega, phi, pos0)
+    v = _heads(v)
+    dO = _heads(dO)
+    B, H, T, F = pq.shape
+    c4d = 4.0 * (F // N_CHANNELS)
+    mask = np.tril(np.ones((T, T)))
+    dpq = np.zeros_like(pq)
+    dpk = np.zeros_like(pk)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            x = pair_kernel(pq[b, h], pk[b, h]) / c4d
+            w = x ** p * mask
+            dh = w.sum(axis=1) + eps
+            o = (w @ v[b, h]) / dh[:, None]
+            dN = dO[b, h] / dh[:, None]
+            dD = -(dO[b, h] * o).sum(axis=1) / dh
+            dw = (dN @ v[b, h].T + dD[:, None]) * mask
+            ds = dw * p * x ** (p - 1) / c4d
+            dv[b, h] = w.T @ dN
+            dpq[b, h] = ds @ pk[b, h]
+            dpk[b, h] = ds.T @ pq[b, h]
+    dq, dg_q, dom_q, dph_q = _feature_vjp(_feature_parts(q, gamma, omega, phi, pos0), dpq)
+    dk, dg_k, dom_k, dph_k = _feature_vjp(_feature_parts(k, gamma, omega, phi, pos0), dpk)
+    return dict(dq=dq, dk=dk, dv=dv, dgamma=dg_q + dg_k, domega=dom_q + dom_k,
+                dphi=dph_q + dph_k)
+
+
 # ---------------------------------------------------------------------------
 # Memory accounting: Notes §4.5 [paper §4.4]
 # ---------------------------------------------------------------------------

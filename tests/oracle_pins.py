@@ -363,6 +363,48 @@ def check_power_single_token_and_constant_values():
     assert np.allclose(o, c["v"], rtol=1e-13, atol=1e-13)
 
 
+def _power_loss(c, dO, p, pos0, eps):
+    o, _ = O.attn_power(c["q"], c["k"], c["v"], c["gamma"], c["omega"], c["phi"], p=p,
+                        pos0=pos0, eps=eps)
+    return float((o * dO).sum())
+
+
+def check_power_backward_finite_differences():
+    """Every gradient of eq. (8) at p = 2 and 3 against central differences of
+    the forward."""
+    c = _small_case(60, B=1, H=2, T=6, d=2, dv=2, phi_scale=0.8)
+    g = _rng(61)
+    dO = g.standard_normal(c["v"].shape)
+    for p, pos0, eps in ((2, 3, 0.0), (3, 0, 0.05)):
+        grads = O.attn_power_backward(c["q"], c["k"], c["v"], c["gamma"], c["omega"], c["phi"],
+                                      dO, p=p, pos0=pos0, eps=eps)
+        h = 1e-6
+        for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("gamma", "dgamma"),
+                            ("omega", "domega"), ("phi", "dphi")):
+            x = c[name]
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                old = x[idx]
+                x[idx] = old + h
+                lp = _power_loss(c, dO, p, pos0, eps)
+                x[idx] = old - h
+                lm = _power_loss(c, dO, p, pos0, eps)
+                x[idx] = old
+                num[idx] = (lp - lm) / (2 * h)
+            err = np.abs(num - grads[gname]).max() / max(1e-3, np.abs(num).max())
+            assert err < 1e-6, (p, name, err)
+
+
+def check_power_one_backward_is_linear_backward():
+    """At p = 1 the gradients are those of the p = 1 attention with eps x 4d."""
+    c = _small_case(62, B=2, H=2, T=9, d=3, dv=2)
+    dO = _rng(63).standard_normal(c["v"].shape)
+    g1 = O.attn_power_backward(**c, dO=dO, p=1, pos0=4, eps=0.2)
+    g2 = O.attn_backward(**c, dO=dO, pos0=4, eps=0.2 * 4 * 3)
+    for n in ("dq", "dk", "dv", "dgamma", "domega", "dphi"):
+        assert np.allclose(g1[n], g2[n], rtol=1e-10, atol=1e-12), n
+
+
 ALL_CHECKS = [
     check_squash_closed_forms,
     check_soft_root_closed_forms,
@@ -381,4 +423,6 @@ ALL_CHECKS = [
     check_power_matches_tensor_power_features,
     check_power_one_is_linear_attention,
     check_power_single_token_and_constant_values,
+    check_power_backward_finite_differences,
+    check_power_one_backward_is_linear_backward,
 ]

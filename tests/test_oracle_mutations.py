@@ -12,7 +12,8 @@ import oracle_pins as P
 
 _orig = {n: getattr(O, n) for n in ("squash", "soft_root", "rotate", "features_from_angles",
                                      "attn_quadratic", "attn_recurrent", "attn_backward",
-                                     "_feature_vjp", "state_bytes", "featurize", "attn_power")}
+                                     "_feature_vjp", "state_bytes", "featurize", "attn_power",
+                                     "attn_power_backward")}
 
 
 def m_squash_no_abs(u):
@@ -173,6 +174,22 @@ def _power_mutant(kind):
     return f
 
 
+def _power_bwd_mutant(kind):
+    # the gradient of the powered weight taken as if p were 1 (the factor
+    # p x^(p-1) dropped), or the value gradient taken with the raw scores
+    def f(q, k, v, gamma, omega, phi, dO, p, pos0=0, eps=0.0):
+        g = _orig["attn_power_backward"](q, k, v, gamma, omega, phi, dO, p, pos0, eps)
+        if kind == "no_chain_factor":
+            g1 = _orig["attn_power_backward"](q, k, v, gamma, omega, phi, dO, 1, pos0, eps)
+            for n in ("dq", "dk", "dgamma", "domega", "dphi"):
+                g[n] = g1[n]
+        else:  # "dv_unpowered"
+            g1 = _orig["attn_power_backward"](q, k, v, gamma, omega, phi, dO, 1, pos0, eps)
+            g["dv"] = g1["dv"]
+        return g
+    return f
+
+
 MUTANTS = {
     "squash_no_abs": ("squash", m_squash_no_abs),
     "squash_square": ("squash", m_squash_square),
@@ -194,6 +211,8 @@ MUTANTS = {
     "state_bytes_without_z": ("state_bytes", m_state_bytes_no_z),
     "power_exponent_off_by_one": ("attn_power", _power_mutant("exponent")),
     "power_without_4d_scale": ("attn_power", _power_mutant("no_scale")),
+    "power_backward_no_chain_factor": ("attn_power_backward", _power_bwd_mutant("no_chain_factor")),
+    "power_backward_dv_unpowered": ("attn_power_backward", _power_bwd_mutant("dv_unpowered")),
 }
 
 
