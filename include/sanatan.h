@@ -186,7 +186,11 @@ SANATAN_API int sanatan_chunk_bwd(const void* q, const void* k, const void* v, i
  *           entry do not matter.
  * Scores, the power and the denominator are float32; features and values
  * enter the tensor cores as bf16, the weights (s/4d)^p as a bf16 pair (hi +
- * lo).  T = 0 or B * H = 0 does nothing.
+ * lo), and the tensor core sums the same weights for the denominator.
+ * T = 0 or B * H = 0 does nothing.  Errors: SANATAN_ERR_INVALID for a null
+ * or misaligned pointer (D may be NULL) or a workspace smaller than the size
+ * above; SANATAN_ERR_UNSUPPORTED for d or dv other than 64 or more than 2^30
+ * (sequence, 128-token chunk) pairs.
  */
 SANATAN_API size_t sanatan_power_fwd_workspace_size(int B, int H, int T, int d, int dv);
 SANATAN_API int sanatan_power_fwd(const void* q, const void* k, const void* v, const float* gamma,

@@ -1,4 +1,6 @@
-"""Float64 CPU oracle for SANATAN p=1 root-parity gated angular attention.
+"""Float64 CPU oracle for SANATAN root-parity gated angular attention: the
+feature map, the p = 1 causal attention in its quadratic and recurrent forms,
+the power-sharpened attention of eq. (8) at integer p, and their gradients.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
