@@ -8,17 +8,18 @@
 // quadratic form the paper trains with.
 //
 // Two kernels.  The preparation kernel featurises q and k once (the bf16
-// feature map of the recurrent path) and writes Phi(Q), Phi(K) and V chunk by
-// chunk in the shared-memory operand layouts, so the attention kernel fetches
-// each 128-token chunk with plain bulk copies.  The attention kernel runs one
-// CTA per (sequence, query chunk): Phi(Q) stays in shared memory; for every
-// key chunk j up to the diagonal, P = Phi(Q) Phi(K_j)^T (M = N = 128, K = 320)
-// lands in one of two TMEM buffers, the epilogue raises (P + 64) / 4d to the
-// power p (64 is the constant channel's exact contribution), masks the
-// diagonal chunk, adds the row sums to the denominator in registers and
-// splits the weights into bf16 hi + lo halves in place, and O += P~ V_j
-// (`.ts`, N = 64) accumulates in TMEM.  Heavy (late) query chunks are
-// scheduled first.
+// feature map of the recurrent path) and writes Phi(Q), Phi(K) and [V | 1 | 0]
+// chunk by chunk in the operand layouts, so the attention kernel fetches each
+// 128-token chunk with plain bulk copies.  The attention kernel runs one CTA
+// per (sequence, query chunk): Phi(Q) is copied once into TMEM and is the A
+// operand of every score product; for every key chunk j up to the diagonal,
+// P = Phi(Q) Phi(K_j)^T (M = N = 128, K = 320) lands in one of two TMEM
+// buffers, the epilogue raises (P + 64) / 4d to the power p (64 is the
+// constant channel's exact contribution), masks the diagonal chunk and
+// splits the weights into bf16 hi + lo halves in place, and
+// O += P~ [V_j | 1 | 0] (`.ts`, N = 80) accumulates the outputs and, in the
+// ones column, the denominator.  Heavy (late) query chunks are scheduled
+// first.
 #include "sanatan_internal.h"
 #include "sanatan_math.cuh"
 #include "tc_common.cuh"
