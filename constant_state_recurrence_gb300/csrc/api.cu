@@ -271,6 +271,13 @@ int sanatan_device_status(void* stream) {
   return h ? SANATAN_ERR_TIMEOUT : SANATAN_OK;
 }
 
+int sanatan_selftest_wait_timeout(uint64_t timeout_ns, int arrive, void* stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 1000000000ull) return SANATAN_ERR_INVALID;
+  if (arrive != 0 && arrive != 1) return SANATAN_ERR_INVALID;
+  if (int s = check_arch()) return s;
+  return from_cuda(tc_timeout_probe_launch(timeout_ns, arrive, static_cast<cudaStream_t>(stream)));
+}
+
 int sanatan_decode_step(float* S, float* z, const float* q, const float* k, const float* v,
                         const float* gamma, const float* omega, const float* phi,
                         const int64_t* pos, int N, int G, int d, int dv, float eps, float* o,

@@ -607,8 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
                  vb + (2 * kLBO_SV / 16) * s, idST, true);
       mma_commit(&m.bar[kStateDone]);
     }
+    // Wait (bounded) for the drain even after an abandoned wait.
     mma_commit(&m.bar[kDrain]);
-    wait_bar(m, kDrain, 0);
+    mbar_wait_bounded(&m.bar[kDrain], 0, kWaitNs);
   }
 
   tc_fence_before();
@@ -690,7 +691,10 @@ size_t chunk_bwd_tc_workspace_bytes(int B, int H, int T) {
   const size_t rows = static_cast<size_t>(B) * H * T;
   const size_t dn = (rows * 64 * 2 + 255) / 256 * 256;
   const size_t dd = (rows * 4 + 255) / 256 * 256;
-  const size_t deltas = static_cast<size_t>(B) * H * tc_segments(B, H, T) * kSCRows * kSCCols * 4;
+  const int nseg = tc_segments(B, H, T);
+  // One segment reads and writes no per-segment sums.
+  const size_t deltas =
+      nseg > 1 ? static_cast<size_t>(B) * H * nseg * kSCRows * kSCCols * 4 : 0;
   return dn + dd + 2 * deltas;
 }
 

@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
   if (warp == kLoadWarp) {
     // ------------------------------------------------- Phi(K) loads
     if (lane == 0) {
+      int issued = 0;
       for (int j = 0; j < nk; ++j) {
         const unsigned char* cj = chunk_base(prm.ws, bh, prm.nchunks, j);
         const int b = j & 1;
@@ -292,30 +293,34 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
           const unsigned char* cn = chunk_base(prm.ws, bh, prm.nchunks, j + 2);
           prefetch_l2_bulk(cn + kPhiBytes, kPhiBytes + kVBytes);
         }
-        // Phi(K_j) into buffer b once the scores of chunk j - 2 have read it
-        if (j >= 2) wait_bar(m, b ? kKFree1 : kKFree0, ((j >> 1) - 1) & 1);
+        // Phi(K_j) into buffer b once the scores of chunk j - 2 have read it;
+        // after an abandoned wait nothing more is issued
+        if (j >= 2 && !wait_bar(m, b ? kKFree1 : kKFree0, ((j >> 1) - 1) & 1)) break;
         mbar_arrive_expect_tx(&m.bar[b ? kKFull1 : kKFull0], kPhiBytes);
         for (uint32_t off = 0; off < kPhiBytes; off += 16384)
           bulk_load_g2s(sK + b * kPhiBytes + off, cj + kPhiBytes + off, 16384,
                         &m.bar[b ? kKFull1 : kKFull0]);
+        issued = j + 1;
       }
       // No copy may still be writing shared memory when the CTA exits, even
-      // after an abandoned wait: wait (bounded) for the last phases.
-      for (int j = (nk >= 2 ? nk - 2 : 0); j < nk; ++j)
+      // after an abandoned wait: wait (bounded) for the last issued phases.
+      for (int j = (issued >= 2 ? issued - 2 : 0); j < issued; ++j)
         mbar_wait_bounded(&m.bar[(j & 1) ? kKFull1 : kKFull0], (j >> 1) & 1, kWaitNs);
     }
   } else if (warp == kVLoadWarp) {
     // ------------------------------------------------- V loads
     if (lane == 0) {
+      int issued = 0;
       for (int j = 0; j < nk; ++j) {
         const unsigned char* cj = chunk_base(prm.ws, bh, prm.nchunks, j);
         const int b = j & 1;
         // V_j into buffer b once P~ V of chunk j - 2 is done
-        if (j >= 2) wait_bar(m, b ? kPVDone1 : kPVDone0, ((j >> 1) - 1) & 1);
+        if (j >= 2 && !wait_bar(m, b ? kPVDone1 : kPVDone0, ((j >> 1) - 1) & 1)) break;
         mbar_arrive_expect_tx(&m.bar[b ? kVFull1 : kVFull0], kVBytes);
         bulk_load_g2s(sV + b * kVBytes, cj + 2 * kPhiBytes, kVBytes, &m.bar[b ? kVFull1 : kVFull0]);
+        issued = j + 1;
       }
-      for (int j = (nk >= 2 ? nk - 2 : 0); j < nk; ++j)
+      for (int j = (issued >= 2 ? issued - 2 : 0); j < issued; ++j)
         mbar_wait_bounded(&m.bar[(j & 1) ? kVFull1 : kVFull0], (j >> 1) & 1, kWaitNs);
     }
   } else if (warp == kMmaWarp) {
@@ -323,27 +328,30 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
     if (lane == 0) {
       constexpr uint32_t idQK = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16_f32(128, kNV, false, true);
-      wait_bar(m, kQReady, 0);
+      // After an abandoned wait no further MMA is issued (the drain below
+      // still waits for the ones already issued).
+      bool live = wait_bar(m, kQReady, 0);
       auto issue_qk = [&](int j) {
         const int b = j & 1;
         // score buffer b is free once P~ V of chunk j - 2 is done
-        if (j >= 2) wait_bar(m, b ? kPVDone1 : kPVDone0, ((j >> 1) - 1) & 1);
+        if (j >= 2 && !wait_bar(m, b ? kPVDone1 : kPVDone0, ((j >> 1) - 1) & 1)) return false;
         uint64_t dk = smem_desc(sK + b * kPhiBytes, 128, kXQ);  // Phi(K_j), K-major B
         asm volatile("" : "+l"(dk));
-        wait_bar(m, b ? kKFull1 : kKFull0, (j >> 1) & 1);
+        if (!wait_bar(m, b ? kKFull1 : kKFull0, (j >> 1) & 1)) return false;
         tc_fence_after();
 #pragma unroll
         for (int st = 0; st < 20; ++st)
           mma_ts(tmem + kTP0 + 128 * b, tmem + kTQ + 8 * st, dk + 16 * st, idQK, st > 0);
         mma_commit(&m.bar[b ? kKFree1 : kKFree0]);
         mma_commit(&m.bar[b ? kPFull1 : kPFull0]);
+        return true;
       };
-      issue_qk(0);
-      for (int j = 0; j < nk; ++j) {
-        if (j + 1 < nk) issue_qk(j + 1);
+      live = live && issue_qk(0);
+      for (int j = 0; j < nk && live; ++j) {
+        if (j + 1 < nk && !issue_qk(j + 1)) break;
         const int b = j & 1;
-        wait_bar(m, b ? kPTilde1 : kPTilde0, (j >> 1) & 1);
-        wait_bar(m, b ? kVFull1 : kVFull0, (j >> 1) & 1);
+        if (!wait_bar(m, b ? kPTilde1 : kPTilde0, (j >> 1) & 1)) break;
+        if (!wait_bar(m, b ? kVFull1 : kVFull0, (j >> 1) & 1)) break;
         tc_fence_after();
         uint64_t dv = smem_desc(sV + b * kVBytes, kVGroup, 128);  // [V_j | 1 | 0], MN-major B
         asm volatile("" : "+l"(dv));
@@ -390,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
     }
     for (int j = 0; j < nk; ++j) {
       const int b = j & 1;
-      wait_bar(m, b ? kPFull1 : kPFull0, (j >> 1) & 1);
+      if (!wait_bar(m, b ? kPFull1 : kPFull0, (j >> 1) & 1)) break;
       tc_fence_after();
       const bool diag = (j == qi);
       const uint32_t col0 = tmem + lane_off + kTP0 + 128 * b + 64 * ch;

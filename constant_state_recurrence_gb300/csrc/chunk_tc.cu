@@ -724,9 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       }
       mma_commit(&m.bar[kPVDone]);
     }
-    // Nothing may still be in flight when TMEM is released.
+    // Nothing may still be in flight when TMEM is released: wait (bounded) for
+    // the drain even after an abandoned wait, when wait_bar returns at once.
     mma_commit(&m.bar[kDrain]);
-    wait_bar(m, kDrain, 0);
+    mbar_wait_bounded(&m.bar[kDrain], 0, kWaitNs);
   }
 
   tc_fence_before();
@@ -785,6 +786,7 @@ int tc_segments_fit(int B, int H, int T, size_t bytes) {
 
 size_t chunk_fwd_tc_workspace_bytes(int B, int H, int T) {
   const int nseg = tc_segments(B, H, T);
+  if (nseg <= 1) return 0;  // one segment reads and writes no per-segment sums
   return static_cast<size_t>(B) * H * nseg * kSCRows * kSCCols * sizeof(float);
 }
 
@@ -908,6 +910,27 @@ cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st) {
   job.deltas = static_cast<float*>(a.workspace);
   job.nseg = tc_segments_fit(a.B, a.H, a.T, a.workspace_bytes);
   return tc_attention(job, st);
+}
+
+namespace {
+// Failure-detection probe: one thread waits, with the kernels' bounded wait,
+// on an mbarrier that nothing arrives at (unless `arrive`), and records a
+// timeout in the same error word as the tensor-core kernels.
+__global__ void timeout_probe_kernel(uint64_t timeout_ns, int arrive) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 1 && arrive) mbar_arrive(&bar);
+  if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0, timeout_ns)) atomicOr(&g_tc_error, 1);
+}
+}  // namespace
+
+cudaError_t tc_timeout_probe_launch(uint64_t timeout_ns, int arrive, cudaStream_t st) {
+  timeout_probe_kernel<<<1, 32, 0, st>>>(timeout_ns, arrive);
+  return cudaGetLastError();
 }
 
 int tc_read_and_clear_error(cudaStream_t st) {

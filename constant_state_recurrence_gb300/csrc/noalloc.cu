@@ -8,11 +8,12 @@
 namespace sanatan {
 namespace {
 
-// The scratch of the segment split (per-segment state sums and the scanned
-// initial states of each segment).  16 MiB holds 163 (sequence, segment)
-// slots of 321 x 80 floats: on one GB300 (152 SMs, at most one segment per SM
-// when sequences are few) that covers every problem with B*H <= 163.  Every
-// GPU that loads the library keeps this array until the process exits.
+// The scratch of the segment split (per-segment state sums of every segment
+// but the last, 321 x 80 floats per (sequence, segment)).  16 MiB holds 163
+// such slots.  A problem whose preferred split needs more is run with as many
+// segments as the array holds; one segment needs no scratch at all, so every
+// problem size runs.  Every GPU that loads the library keeps this array until
+// the process exits.
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -58,12 +59,13 @@ extern "C" int sanatan_chunk_fwd_noalloc(const void* q, const void* k, const voi
   if (B < 0 || H < 0 || T < 0 || d < 0 || dv < 0) return SANATAN_ERR_INVALID;
   if (d != 64 || dv != 64) return SANATAN_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(B) * H > (1LL << 31) - 1) return SANATAN_ERR_UNSUPPORTED;
-  // One slot of per-segment sums per sequence must fit (B * H <= 163); more
-  // segments are used where the array holds them.
-  const size_t slot = static_cast<size_t>(B) * H * 321 * 80 * sizeof(float);
-  if (slot > kNoAllocScratchBytes) return SANATAN_ERR_UNSUPPORTED;  // beyond the fixed scratch
+  // The split is chosen to fit the array (tc_segments_fit); the check below
+  // only guards that contract.
+  const int nseg = tc_segments_fit(B, H, T, kNoAllocScratchBytes);
+  const size_t need = nseg > 1 ? static_cast<size_t>(B) * H * nseg * 321 * 80 * sizeof(float) : 0;
+  if (need > kNoAllocScratchBytes) return SANATAN_ERR_UNSUPPORTED;  // beyond the fixed scratch
   void* scratch = nullptr;
-  if (static_cast<int64_t>(B) * H > 0) {
+  if (need > 0) {
     if (scratch_address(&scratch) != cudaSuccess) return SANATAN_ERR_CUDA;
     if (!aligned16(scratch)) return SANATAN_ERR_CUDA;
   }

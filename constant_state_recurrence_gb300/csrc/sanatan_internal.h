@@ -74,6 +74,9 @@ int tc_segments(int B, int H, int T);
 size_t chunk_fwd_tc_workspace_bytes(int B, int H, int T);
 cudaError_t chunk_fwd_tc_launch(const ChunkFwdArgs& a, cudaStream_t st);
 int tc_read_and_clear_error(cudaStream_t st);
+// One CTA whose bounded wait on an mbarrier nobody arrives at (unless
+// `arrive`) gives up after timeout_ns and records a timeout.
+cudaError_t tc_timeout_probe_launch(uint64_t timeout_ns, int arrive, cudaStream_t st);
 
 // One causal (or, reversed, anti-causal) attention on the tensor-core kernel,
 // bf16 q, k, v of shape [B, H, T, 64].  `extra` replaces the ones column of

@@ -49,6 +49,7 @@ _SIGS = {
                                    _c_p]),
     "sanatan_device_status": (_c_int, [_c_p]),
     "sanatan_set_profile_events": (_c_int, [_c_p, _c_p]),
+    "sanatan_selftest_wait_timeout": (_c_int, [ctypes.c_uint64, _c_int, _c_p]),
     "sanatan_decode_step": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int,
                                      _c_int, _c_int, _c_int, _c_f, _c_p, _c_p]),
 }
@@ -119,6 +120,14 @@ def device_status(device=None):
     up a bounded device-side wait since the last check."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     _check("sanatan_device_status", lib().sanatan_device_status(_stream(dev)))
+
+
+def selftest_wait_timeout(timeout_ns=1_000_000, arrive=False, device=None):
+    """Enqueue the library's failure-detection probe: a bounded wait on an
+    mbarrier nobody arrives at (or, with arrive=True, one that completes)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _check("sanatan_selftest_wait_timeout",
+           lib().sanatan_selftest_wait_timeout(int(timeout_ns), int(bool(arrive)), _stream(dev)))
 
 
 def set_profile_events(start=None, stop=None):

@@ -129,10 +129,14 @@ SANATAN_API int sanatan_chunk_fwd(const void* q, const void* k, const void* v, i
  *   SANATAN_BF16 and without the workspace pair.
  *   Scratch: a fixed array inside the library, 16 MiB per device
  *   (sanatan_chunk_fwd_noalloc_max_scratch_bytes()), held by every GPU that
- *   loads the library until the process exits.  Problems whose workspace
- *   (sanatan_chunk_fwd_workspace_size) would exceed it return
- *   SANATAN_ERR_UNSUPPORTED; on one GB300 these are the problems with more
- *   than 163 sequences (B * H > 163).
+ *   loads the library until the process exits.  It holds the per-segment
+ *   state sums of the long-sequence split: a problem whose preferred split
+ *   (sanatan_chunk_fwd_workspace_size) needs more than 16 MiB runs with as
+ *   many segments per sequence as the array holds (one segment needs no
+ *   scratch), so every problem size sanatan_chunk_fwd accepts runs here too,
+ *   with the same results up to rounding; only the split, and so the speed,
+ *   can differ.  SANATAN_ERR_UNSUPPORTED is returned only if a split would
+ *   ever need more than the array (it cannot with this build's split rule).
  *   The first call on a device looks up the array's device address (no
  *   allocation); make that first call before any stream capture.
  *   Calls share the array: two calls whose kernels overlap on the GPU (other
@@ -216,6 +220,19 @@ SANATAN_API int sanatan_set_profile_events(void* start, void* stop);
  * them skip their remaining waits and return, with undefined outputs.
  */
 SANATAN_API int sanatan_device_status(void* stream);
+
+/*
+ * sanatan_selftest_wait_timeout -- failure-detection self-test (the paper has
+ * no counterpart).  Enqueues one small kernel whose thread waits, with the
+ * same bounded mbarrier wait the tensor-core kernels use, on a barrier that
+ * nothing arrives at (arrive = 0) or that another thread completes (arrive =
+ * 1).  After timeout_ns (1e3 <= timeout_ns <= 1e9, SANATAN_ERR_INVALID
+ * otherwise) the wait gives up and records a timeout in the library's device
+ * error word, so the next sanatan_device_status returns SANATAN_ERR_TIMEOUT;
+ * with arrive = 1 nothing is recorded.  The probe touches no caller memory and
+ * leaves the CUDA context usable.
+ */
+SANATAN_API int sanatan_selftest_wait_timeout(uint64_t timeout_ns, int arrive, void* stream);
 
 /*
  * sanatan_decode_step -- one token of the constant-state recurrence of eq. (9)

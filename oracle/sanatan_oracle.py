@@ -211,7 +211,7 @@ def final_state(k, v, gamma, omega, phi, pos0=0, S0=None, z0=None):
     """S_T = S0 + sum_t Phi(k_t) v_t^T and z_T = z0 + sum_t Phi(k_t)
     (Notes §2.7: the definition of the state as a sum, written directly)."""
     pk = featurize(k, gamma, omega, phi, pos0)
-    S = np.einsum("bhtf,bhte->bhfe", pk, _heads(v))
+    S = np.matmul(np.swapaxes(pk, -1, -2), _heads(v))   # sum_t Phi(k_t) v_t^T per head
     z = pk.sum(axis=2)
     if S0 is not None:
         S = S + _heads(S0)

@@ -109,3 +109,9 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(sanatan, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError):
         sanatan.lib()
+
+
+def test_selftest_probe_rejects_bad_limits_before_any_launch(lib):
+    assert lib.sanatan_selftest_wait_timeout(10, 0, None) == 1             # below 1 us
+    assert lib.sanatan_selftest_wait_timeout(2 * 10**9, 0, None) == 1      # above 1 s
+    assert lib.sanatan_selftest_wait_timeout(10**6, 2, None) == 1          # bad flag

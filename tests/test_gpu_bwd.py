@@ -92,16 +92,33 @@ def test_autograd_function_matches_oracle():
         assert rel_fro(f64(leaves[n].grad), ref["d" + n]) <= 1e-2, n
 
 
-def test_training_workload_full_size_sampled():
-    """B=8, H=12, T=4096 (bf16 q, k, v, dO): dq, dk, dv of sampled (batch, head)
-    sequences against the oracle on that sequence alone (the gradient of one
-    sequence depends on nothing else)."""
+def test_training_workload_full_size_all_sequences():
+    """B=8, H=12, T=4096 (bf16 q, k, v, dO; three segments per sequence):
+    dq, dk, dv of all 96 sequences and the parameter gradients dgamma,
+    domega, dphi (sums over the batch and over q and k) against the oracle's
+    backward run one (batch, head) at a time (the gradient of one sequence
+    depends on nothing else; the parameter gradients are the sums of the
+    per-sequence ones)."""
     x = W.make(W.TRAIN, device="cpu", with_grad_out=True)
     gr = _run(x, x["dO"])
     ra = ref_args(x)
-    for b, h in ((0, 0), (5, 7)):
-        sl = {n: ra[n][b:b + 1, h:h + 1] for n in ("q", "k", "v")}
-        ref = O.attn_backward(**sl, gamma=ra["gamma"][h:h + 1], omega=ra["omega"][h:h + 1],
-                              phi=ra["phi"][h:h + 1], dO=f64(x["dO"])[b:b + 1, h:h + 1])
-        for n in ("dq", "dk", "dv"):
-            assert rel_fro(f64(gr[n])[b, h], ref[n][0, 0]) <= 1e-2, (b, h, n)
+    dO = f64(x["dO"])
+    B, H = x["B"], x["H"]
+    ref = {n: np.zeros(ra[n[1:]].shape) for n in ("dq", "dk", "dv")}
+    pref = {n: np.zeros(ra[n[1:]].shape) for n in ("dgamma", "domega", "dphi")}
+    for b in range(B):
+        for h in range(H):
+            sl = {n: ra[n][b:b + 1, h:h + 1] for n in ("q", "k", "v")}
+            r = O.attn_backward(**sl, gamma=ra["gamma"][h:h + 1], omega=ra["omega"][h:h + 1],
+                                phi=ra["phi"][h:h + 1], dO=dO[b:b + 1, h:h + 1])
+            for n in ("dq", "dk", "dv"):
+                ref[n][b, h] = r[n][0, 0]
+            for n in ("dgamma", "domega", "dphi"):
+                pref[n][h] += r[n][0]
+    for n in ("dq", "dk", "dv"):
+        g = f64(gr[n])
+        assert rel_fro(g, ref[n]) <= 1e-2, n
+        worst = max(rel_fro(g[b, h], ref[n][b, h]) for b in range(B) for h in range(H))
+        assert worst <= 1e-2, (n, worst)
+    for n in ("dgamma", "domega", "dphi"):
+        assert rel_fro(f64(gr[n]), pref[n]) <= 1e-2, n

@@ -58,20 +58,26 @@ def test_noalloc_matches_workspace_entry_twice(shape):
         assert ((zx - z_ref).norm() / z_ref.norm()).item() <= TOL_BF16
 
 
-def test_noalloc_rejects_problems_beyond_its_scratch():
+@pytest.mark.parametrize("shape", [(200, 1, 8), (64, 12, 4096)])
+def test_noalloc_runs_problems_whose_split_needs_no_scratch(shape):
+    """Problems with more sequences than the array has per-segment slots (more
+    than 163 here) run with one segment per sequence, which needs no scratch:
+    200 single-chunk sequences, and the batched-decode prefill (64 x 12
+    sequences of 4096 tokens)."""
     cap = S.lib().sanatan_chunk_fwd_noalloc_max_scratch_bytes()
     assert cap == 16 << 20
     dev = torch.device("cuda:0")
-    B, H, T = 200, 1, 8  # 200 sequences: more scratch slots than the 163 the array holds
-    assert S.chunk_fwd_workspace_size(B, H, T) > cap
-    q = torch.zeros(B, H, T, 64, dtype=torch.bfloat16, device=dev)
-    prm = [torch.ones(H, device=dev), torch.zeros(H, 64, device=dev), torch.zeros(H, 64, device=dev)]
-    with pytest.raises(S.SanatanError) as err:
-        S.sanatan_chunk_fwd_noalloc(q, q, q, *prm)
-    assert err.value.status == 2
-    # the largest accepted case still runs
-    B = 163
-    q = torch.zeros(B, H, T, 64, dtype=torch.bfloat16, device=dev)
-    o, _, _, _ = S.sanatan_chunk_fwd_noalloc(q, q, q, *prm)
-    S.device_status()
-    assert torch.allclose(o, torch.zeros_like(o))
+    B, H, T = shape
+    assert S.chunk_fwd_plan(B, H, T)[0] == 1
+    assert S.chunk_fwd_workspace_size(B, H, T) == 0
+    x = W.make(W.LAYER, device=dev, B=B, H=H, T=T)
+    g = {n: x[n] for n in ("q", "k", "v", "gamma", "omega", "phi")}
+    for _ in range(2):
+        o_ref, D_ref, S_ref, z_ref = _ref(g)
+        o, D, Sx, zx = S.sanatan_chunk_fwd_noalloc(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
+                                                   g["phi"], want_state=True)
+        S.device_status()
+        assert (o - o_ref).abs().max().item() <= TOL_BF16
+        assert ((Sx - S_ref).norm() / S_ref.norm()).item() <= TOL_BF16
+        assert ((zx - z_ref).norm() / z_ref.norm()).item() <= TOL_BF16
+        del o, D, Sx, zx, o_ref, D_ref, S_ref, z_ref
