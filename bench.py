@@ -345,6 +345,32 @@ def power_case(p, dev, flush, steps, warmup, stream):
     return dict(step=step, B=B, H=H, T=T, p=p)
 
 
+def power_train_case(p, dev, flush, steps, warmup, stream):
+    """Power-sharpened attention training step on the layer workload: the
+    forward (keeping o and D) then the backward."""
+    from constant_state_recurrence_gb300 import sanatan as S
+    x = W.make(W.LAYER, device=dev, with_grad_out=True, shard=SHARD)
+    g = {n: x[n] for n in ("q", "k", "v", "gamma", "omega", "phi", "dO")}
+    B, H, T = x["B"], x["H"], x["T"]
+    o = torch.empty(B, H, T, 64, dtype=torch.float32, device=dev)
+    D = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    ws = torch.empty(S.power_fwd_workspace_size(B, H, T), dtype=torch.uint8, device=dev)
+    bws = torch.empty(S.power_bwd_workspace_size(B, H, T), dtype=torch.uint8, device=dev)
+
+    def step(_i):
+        S.sanatan_power_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], p, out=o,
+                            D_out=D, workspace=ws)
+        S.sanatan_power_bwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], p, o, D,
+                            g["dO"], workspace=bws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step(0)
+    torch.cuda.synchronize()
+    S.device_status()
+    return dict(step=step, B=B, H=H, T=T, p=p)
+
+
 def power_flops(B, H, T, F=384, dv=64):
     """Algorithmic flops of the causal quadratic form: every pair j <= t takes
     one F-long score and one dv-long weighted sum."""
@@ -457,6 +483,7 @@ def main():
     train = train_case(dev, flush, tr_steps, warm, stream) if want("train") else None
     pw_steps = max(4, steps // 5)
     power = power_case(POWER_P, dev, flush, pw_steps, warm, stream) if want("power") else None
+    ptrain = power_train_case(POWER_P, dev, flush, pw_steps, warm, stream) if want("power") else None
 
     gpu_idx = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -483,8 +510,10 @@ def main():
         if train:
             tr_whole, tr_kern = timed_steps(train["step"], tr_steps, flush, stream, profile=True)
         pw_whole, pw_kern = [nan], [nan]
+        pt_whole, pt_kern = [nan], [nan]
         if power:
             pw_whole, pw_kern = timed_steps(power["step"], pw_steps, flush, stream, profile=True)
+            pt_whole, pt_kern = timed_steps(ptrain["step"], pw_steps, flush, stream, profile=True)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
     barrier(world)
@@ -585,6 +614,12 @@ def main():
             "traffic": traffic_for("pow_attn_kernel", W.LAYER.name),
             "note": "causal quadratic power attention; flops = pairs j<=t x (2*384 + 2*64); "
                     "step = feature preparation + attention kernel (kernel_ms)"},
+        "power_train": {
+            "workload": W.LAYER.name, "p": POWER_P, "steps": pw_steps,
+            "tokens_per_s": 4 * 2048 / (statistics.mean(pt_whole) * 1e-3),
+            "ms_per_step": statistics.mean(pt_whole),
+            "bwd_key_pass_ms": statistics.mean(pt_kern),
+            "note": "forward + backward of the power-sharpened attention per step"},
         "timed_region_wall_s": t_wall,
     }
     clocks = clk.summary()

@@ -254,6 +254,62 @@ int sanatan_power_fwd(const void* q, const void* k, const void* v, const float* 
   return from_cuda(pow_fwd_tc_launch(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t sanatan_power_bwd_workspace_size(int B, int H, int T, int d, int dv) {
+  if (B < 0 || H < 0 || T < 0 || d != 64 || dv != 64) return 0;
+  return pow_bwd_tc_workspace_bytes(B, H, T);
+}
+
+int sanatan_power_bwd(const void* q, const void* k, const void* v, const float* gamma,
+                      const float* omega, const float* phi, int B, int H, int T, int d, int dv,
+                      int64_t pos0, int p, float eps, const float* o, const float* D,
+                      const void* dO, int grad_dtype, void* dq, void* dk, void* dv_out,
+                      float* dgamma, float* domega, float* dphi, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (int s = check_sizes(B, H, T, d, dv)) return s;
+  if (p < 1 || !ok_dtype(grad_dtype)) return SANATAN_ERR_INVALID;
+  if (p > kMaxPower) return SANATAN_ERR_UNSUPPORTED;
+  if (H > 0 && (!ok_ptr(dgamma) || !ok_ptr(domega) || !ok_nullable(dphi)))
+    return SANATAN_ERR_INVALID;
+  if (H > 0) {
+    if (int s = check_params(gamma, omega, phi)) return s;
+  }
+  if (static_cast<int64_t>(B) * H > 0 && T > 0) {
+    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(o) || !ok_ptr(D) || !ok_ptr(dO) ||
+        !ok_ptr(dq) || !ok_ptr(dk) || !ok_ptr(dv_out) || !ok_ptr(workspace))
+      return SANATAN_ERR_INVALID;
+    if (workspace_bytes < pow_bwd_tc_workspace_bytes(B, H, T)) return SANATAN_ERR_INVALID;
+    if (static_cast<int64_t>(B) * H * ((T + 127) / 128) > 0x3fffffffLL)
+      return SANATAN_ERR_UNSUPPORTED;
+  }
+  if (H == 0) return SANATAN_OK;
+  if (int s = check_arch()) return s;
+  PowBwdArgs a;
+  a.f.q = q;
+  a.f.k = k;
+  a.f.v = v;
+  a.f.gamma = gamma;
+  a.f.omega = omega;
+  a.f.phi = phi;
+  a.f.B = B;
+  a.f.H = H;
+  a.f.T = T;
+  a.f.pos0 = pos0;
+  a.f.p = p;
+  a.f.eps = eps;
+  a.f.workspace = workspace;
+  a.o = o;
+  a.D = D;
+  a.dO = dO;
+  a.grad_dtype = grad_dtype;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv_out;
+  a.dgamma = dgamma;
+  a.domega = domega;
+  a.dphi = dphi;
+  return from_cuda(pow_bwd_tc_launch(a, static_cast<cudaStream_t>(stream)));
+}
+
 int sanatan_set_profile_events(void* start, void* stop) {
   if ((start == nullptr) != (stop == nullptr)) return SANATAN_ERR_INVALID;
   profile_events().start = static_cast<cudaEvent_t>(start);
@@ -266,8 +322,9 @@ int sanatan_device_status(void* stream) {
   const int h = tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
   const int hb = bwd_tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
   const int hp = pow_tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
-  if (h < 0 || hb < 0 || hp < 0) return SANATAN_ERR_CUDA;
-  if (hb || hp) return SANATAN_ERR_TIMEOUT;
+  const int hpb = pow_bwd_tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
+  if (h < 0 || hb < 0 || hp < 0 || hpb < 0) return SANATAN_ERR_CUDA;
+  if (hb || hp || hpb) return SANATAN_ERR_TIMEOUT;
   return h ? SANATAN_ERR_TIMEOUT : SANATAN_OK;
 }
 

@@ -1,0 +1,779 @@
+// Gradients of the power-sharpened causal attention (eq. (8) of "SANATAN:
+// Root-Parity Gated Angular Attention with an Exact Constant-State Recurrent
+// Form", reading notes §2.6) on the tensor cores.  The pages give no
+// gradient; with x_tj = s_tj / 4d, w_tj = [j <= t] x_tj^p, D_t = sum_j w_tj,
+// Dh_t = D_t + eps and o_t = sum_j w_tj v_j / Dh_t, the chain rule gives
+//   dN_t = dO_t / Dh_t,   dD_t = -(dO_t . o_t) / Dh_t,
+//   ds_tj = [j <= t] (dN_t . v_j + dD_t) p x_tj^(p-1) / 4d,
+//   dv_j = sum_t w_tj dN_t,
+//   dPhi(q_t) = sum_j ds_tj Phi(k_j),   dPhi(k_j) = sum_t ds_tj Phi(q_t),
+// and then the feature map's own chain rule (eqs. (2)-(4), (6)) to dq, dk and
+// the per-head dgamma, domega, dphi.
+//
+// Launches: the forward's preparation kernel (Phi(Q), Phi(K), [V | 1 | 0]
+// per chunk), a small kernel for dN (bf16, operand layout) and dD, then two
+// tensor-core passes, each one CTA per (sequence, chunk, feature half):
+//   query pass: per query chunk i, for key chunks j <= i: S = Phi(Q_i) Phi(K_j)^T,
+//     dW = dN_i V_j^T, the epilogue forms dS in TMEM, and
+//     dPhi(Q_i)[half] += dS Phi(K_j)[half];
+//   key pass: per key chunk j, for query chunks i >= j: S^T, dW^T likewise,
+//     dPhi(K_j)[half] += dS^T Phi(Q_i)[half] and (half 0) dv_j += W^T dN_i.
+// Each accumulator of 320 features is split into two halves of 160 (whole
+// dimensions: all five channels of 32 dimensions) so that scores, their
+// gradients and the feature gradient fit the 512 TMEM columns.  After its
+// last tile each CTA applies the feature map's chain rule to its half and
+// writes du, and adds its share of dgamma, domega, dphi with atomics.
+#include "pow_common.cuh"
+#include "sanatan_internal.h"
+#include "sanatan_math.cuh"
+#include "tc_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace sanatan {
+
+__device__ int g_pow_bwd_error;  // set when a bounded wait gives up
+
+namespace {
+
+using namespace tc;
+using namespace tcc;
+using namespace powc;
+
+constexpr uint32_t kDNBytes = 16 * 1024;   // dN of one chunk: [tg * 1024 + ng * 128 + r * 16]
+constexpr uint32_t kDDBytes = kC * 4;      // dD of one chunk (f32)
+
+// TMEM columns (both passes).
+constexpr uint32_t kTS = 0;       // scores (weights in place, key pass)
+constexpr uint32_t kTDW = 128;    // score gradients (dS in place)
+constexpr uint32_t kTF = 256;     // feature-gradient half (160 columns)
+constexpr uint32_t kTV = 416;     // dv (key pass, 64 columns)
+constexpr uint32_t kTmemCols = 512;
+
+enum Bar { kResFull = 0, kStrFull, kSDone, kDSReady, kTileDone, kNumBars };
+
+constexpr int kEpiWarps = 8;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kThreads = 32 * (kLoadWarp + 1);
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct Misc {
+  uint64_t bar[kNumBars];
+  uint32_t tmem_base;
+  int abort_flag;
+  float red_omega[32];   // this CTA's share of domega, dphi (its 32 dimensions) and dgamma
+  float red_phi[32];
+  float red_gamma;
+};
+
+struct BwdParams {
+  const unsigned char* ws;    // per (sequence, chunk): Phi(Q) | Phi(K) | [V | 1 | 0]
+  const unsigned char* dn;    // per (sequence, chunk): dN, kDNBytes
+  const float* dd;            // per (sequence, chunk): dD, 128 floats
+  const __nv_bfloat16* u;     // raw q (query pass) or k (key pass) [B, H, T, 64]
+  const float* gamma;
+  const float* omega;
+  const float* phi;
+  int H, T, nchunks, bhn;
+  int64_t pos0;
+  __nv_bfloat16* du;          // dq or dk
+  __nv_bfloat16* dv;          // key pass only
+  float* dgamma;
+  float* domega;
+  float* dphi;                // may be null
+};
+
+struct DPrepParams {
+  const void* dO;
+  int grad_bf16;
+  const float* o;
+  const float* D;
+  float eps;
+  int T, nchunks;
+  int64_t ntok;               // bhn * nchunks * 128
+  unsigned char* dn;
+  float* dd;
+};
+
+__device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
+  if (*reinterpret_cast<volatile int*>(&m.abort_flag)) return false;
+  if (mbar_wait_bounded(&m.bar[b], parity, kWaitNs)) return true;
+  m.abort_flag = 1;
+  atomicOr(&g_pow_bwd_error, 1);
+  return false;
+}
+
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// dN = dO / Dh (bf16, the operand layout of a chunk) and dD = -(dO . o) / Dh,
+// zero for the padding rows of the last chunk.  Eight threads per token, eight
+// columns each.
+__global__ void __launch_bounds__(256) pow_dprep_kernel(DPrepParams prm) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t tok = g >> 3;          // (sequence, chunk, row), row fastest
+  const int ng = static_cast<int>(g & 7);
+  const bool in_range = tok < prm.ntok;
+  const int row = static_cast<int>(tok % kC);
+  const int64_t sc = tok / kC;         // sequence * nchunks + chunk
+  const int chunk = static_cast<int>(sc % prm.nchunks);
+  const int64_t bh = sc / prm.nchunks;
+  const int t = chunk * kC + row;
+  const bool valid = in_range && t < prm.T;
+  float dov[8], ov[8];
+  float dh = 1.0f;
+  if (valid) {
+    const int64_t grow = bh * prm.T + t;
+    if (prm.grad_bf16) {
+      const uint4 w = ldg_nc_v4(static_cast<const __nv_bfloat16*>(prm.dO) + grow * kD + 8 * ng);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        dov[2 * i] = __uint_as_float(ww[i] << 16);
+        dov[2 * i + 1] = __uint_as_float(ww[i] & 0xffff0000u);
+      }
+    } else {
+      const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(prm.dO) +
+                                                        grow * kD + 8 * ng);
+      const float4 a = p[0], b = p[1];
+      dov[0] = a.x; dov[1] = a.y; dov[2] = a.z; dov[3] = a.w;
+      dov[4] = b.x; dov[5] = b.y; dov[6] = b.z; dov[7] = b.w;
+    }
+    const float4* po = reinterpret_cast<const float4*>(prm.o + grow * kD + 8 * ng);
+    const float4 a = po[0], b = po[1];
+    ov[0] = a.x; ov[1] = a.y; ov[2] = a.z; ov[3] = a.w;
+    ov[4] = b.x; ov[5] = b.y; ov[6] = b.z; ov[7] = b.w;
+    dh = prm.D[grow] + prm.eps;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { dov[i] = 0.f; ov[i] = 0.f; }
+  }
+  const float inv = 1.0f / dh;
+  float dot = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) dot = fmaf(dov[i], ov[i], dot);
+  dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+  dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+  dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+  if (!in_range) return;
+  uint4 packed;
+  packed.x = pack_bf16x2(dov[0] * inv, dov[1] * inv);
+  packed.y = pack_bf16x2(dov[2] * inv, dov[3] * inv);
+  packed.z = pack_bf16x2(dov[4] * inv, dov[5] * inv);
+  packed.w = pack_bf16x2(dov[6] * inv, dov[7] * inv);
+  unsigned char* dst = prm.dn + sc * static_cast<int64_t>(kDNBytes) + (row >> 3) * 1024 + ng * 128 +
+                       (row & 7) * 16;
+  *reinterpret_cast<uint4*>(dst) = packed;
+  if (ng == 0) prm.dd[sc * kC + row] = valid ? -dot * inv : 0.f;
+}
+
+// ---------------------------------------------------------------------------
+// The feature map's chain rule for one token and the 16 dimensions
+// 32 fh + 16 ch .. + 15 (two groups of eight), reading the feature gradients of
+// this CTA's half from TMEM: inside the half, dimension group ag' (0..3) holds
+// channels c = 1..5 in columns 40 ag' + 8 (c - 1) + e for dimension 8 ag' + e.
+//   dc = d1 + r d4, ds = d2 + r d5, dr = d3 + c d4 + s d5,
+//   dth_rot = -s dc + c ds, dpre = dr (1 - r^2),
+//   dtheta = dth_rot + dpre gamma g'(theta + omega), du = dtheta pi / (1 + |u|)^2,
+//   dgamma += dpre g, domega += dpre gamma g', dphi += dth_rot t,
+// with g(x) = cos x - sin x, g'(x) = -sin x - cos x.  Sums over the tokens of
+// the CTA go to shared memory (warp shuffles first); du is written as bf16.
+__device__ __forceinline__ void chain_rule16(uint32_t trow, int fh, int ch, int h, int64_t tpos,
+                                             bool valid, const __nv_bfloat16* urow,
+                                             const BwdParams& prm, __nv_bfloat16* durow,
+                                             Misc& m, int lane) {
+  const float gam = prm.gamma[h];
+  float du[16];
+  float dgam = 0.f;
+  uint4 raw[2];
+  raw[0] = valid ? ldg_nc_v4(urow + 32 * fh + 16 * ch) : make_uint4(0u, 0u, 0u, 0u);
+  raw[1] = valid ? ldg_nc_v4(urow + 32 * fh + 16 * ch + 8) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int gi = 0; gi < 2; ++gi) {
+    const int agl = 2 * ch + gi;   // dimension group inside the half
+    float dphi_ch[48];
+    tmem_ld16(trow + 40 * agl, *reinterpret_cast<float(*)[16]>(&dphi_ch[0]));
+    tmem_ld16(trow + 40 * agl + 16, *reinterpret_cast<float(*)[16]>(&dphi_ch[16]));
+    tmem_ld16(trow + 40 * agl + 32, *reinterpret_cast<float(*)[16]>(&dphi_ch[32]));
+    tmem_ld_wait();
+    const uint32_t w[4] = {raw[gi].x, raw[gi].y, raw[gi].z, raw[gi].w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int a = 32 * fh + 8 * agl + e;   // dimension
+      const float u = __uint_as_float((e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16));
+      const float inv = 1.0f / (1.0f + fabsf(u));
+      const float th = kPi * u * inv;
+      float sx, cx;
+      sincosf(th + prm.omega[h * kD + a], &sx, &cx);
+      const float g = cx - sx;
+      const float gp = -sx - cx;
+      const float r = tanhf(gam * g);
+      float sr, cr;
+      sincosf(th + phase_mod_2pi(tpos, prm.phi[h * kD + a]), &sr, &cr);
+      const float d1 = dphi_ch[e], d2 = dphi_ch[8 + e], d3 = dphi_ch[16 + e];
+      const float d4 = dphi_ch[24 + e], d5 = dphi_ch[32 + e];
+      const float dc = fmaf(r, d4, d1);
+      const float ds = fmaf(r, d5, d2);
+      const float dr = fmaf(sr, d5, fmaf(cr, d4, d3));
+      const float dthr = fmaf(cr, ds, -sr * dc);
+      const float dpre = valid ? dr * (1.0f - r * r) : 0.f;
+      const float dtheta = fmaf(dpre * gam, gp, dthr);
+      du[8 * gi + e] = dtheta * kPi * inv * inv;
+      dgam = fmaf(dpre, g, dgam);
+      float om = dpre * gam * gp;
+      float ph = valid ? dthr * static_cast<float>(tpos) : 0.f;
+#pragma unroll
+      for (int sh = 16; sh > 0; sh >>= 1) {
+        om += __shfl_xor_sync(0xffffffffu, om, sh);
+        ph += __shfl_xor_sync(0xffffffffu, ph, sh);
+      }
+      if (lane == 0) {
+        atomicAdd(&m.red_omega[a - 32 * fh], om);
+        atomicAdd(&m.red_phi[a - 32 * fh], ph);
+      }
+    }
+  }
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) dgam += __shfl_xor_sync(0xffffffffu, dgam, sh);
+  if (lane == 0) atomicAdd(&m.red_gamma, dgam);
+  if (valid) {
+    uint4 o0, o1;
+    o0.x = pack_bf16x2(du[0], du[1]);   o0.y = pack_bf16x2(du[2], du[3]);
+    o0.z = pack_bf16x2(du[4], du[5]);   o0.w = pack_bf16x2(du[6], du[7]);
+    o1.x = pack_bf16x2(du[8], du[9]);   o1.y = pack_bf16x2(du[10], du[11]);
+    o1.z = pack_bf16x2(du[12], du[13]); o1.w = pack_bf16x2(du[14], du[15]);
+    uint4* dst = reinterpret_cast<uint4*>(durow + 32 * fh + 16 * ch);
+    dst[0] = o0;
+    dst[1] = o1;
+  }
+}
+
+// Adds the CTA's shares of dgamma, domega, dphi to the outputs (after every
+// epilogue thread has contributed).
+__device__ __forceinline__ void flush_param_grads(const Misc& m, const BwdParams& prm, int h,
+                                                  int fh, int tid) {
+  if (tid < 32) {
+    atomicAdd(&prm.domega[h * kD + 32 * fh + tid], m.red_omega[tid]);
+    if (prm.dphi != nullptr) atomicAdd(&prm.dphi[h * kD + 32 * fh + tid], m.red_phi[tid]);
+  }
+  if (tid == 0) atomicAdd(&prm.dgamma[h], m.red_gamma);
+}
+
+// Score-gradient (and weight) pairs of 32 keys: ds = (dw + dd) p x^(p-1) / 4d
+// with x = (s + 64) / 4d; elements with keep(i) false get 0.  Written as bf16
+// hi (truncated) + lo (rounded rest) pairs, element 2i and 2i + 1 in word i.
+template <int P, typename Keep>
+__device__ __forceinline__ void grads32(const float* sv, const float* dwv, const float* dd,
+                                        Keep keep, uint32_t (&dhi)[16], uint32_t (&dlo)[16],
+                                        uint32_t (&whi)[16], uint32_t (&wlo)[16]) {
+  constexpr float kInv4d = 1.0f / (4.0f * kD);
+  constexpr float kConst = 64.0f * kInv4d;
+  constexpr float kScale = static_cast<float>(P) * kInv4d;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float g2[2], w2[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int k = 2 * i + e;
+      const float x = fmaf(sv[k], kInv4d, kConst);
+      const float xp1 = pow_int<P - 1>(x);
+      const bool kp = keep(k);
+      g2[e] = kp ? (dwv[k] + dd[k]) * kScale * xp1 : 0.f;
+      w2[e] = kp ? xp1 * x : 0.f;
+    }
+    const uint32_t b0 = __float_as_uint(g2[0]), b1 = __float_as_uint(g2[1]);
+    dhi[i] = __byte_perm(b0, b1, 0x7632);
+    dlo[i] = pack_bf16x2(g2[0] - __uint_as_float(b0 & 0xffff0000u),
+                         g2[1] - __uint_as_float(b1 & 0xffff0000u));
+    const uint32_t c0 = __float_as_uint(w2[0]), c1 = __float_as_uint(w2[1]);
+    whi[i] = __byte_perm(c0, c1, 0x7632);
+    wlo[i] = pack_bf16x2(w2[0] - __uint_as_float(c0 & 0xffff0000u),
+                         w2[1] - __uint_as_float(c1 & 0xffff0000u));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Query pass.  Shared memory: Phi(Q_i) and dN_i resident, Phi(K_j) and
+// [V_j | 1 | 0] streamed (single buffer).
+constexpr int kQOffQ = 0;
+constexpr int kQOffDN = kQOffQ + kPhiBytes;
+constexpr int kQOffK = kQOffDN + kDNBytes;
+constexpr int kQOffV = kQOffK + kPhiBytes;
+constexpr int kQOffMisc = kQOffV + kVBytes;
+constexpr int kQSmem = kQOffMisc + static_cast<int>(sizeof(Misc));
+static_assert(kQSmem <= 232448, "query pass: shared memory exceeds 227 KB");
+
+template <int P>
+__global__ void __launch_bounds__(kThreads, 1) pow_bwd_q_kernel(BwdParams prm) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  Misc& m = *reinterpret_cast<Misc*>(smem + kQOffMisc);
+  const uint32_t sQ = smem_u32(smem + kQOffQ), sDN = smem_u32(smem + kQOffDN);
+  const uint32_t sK = smem_u32(smem + kQOffK), sV = smem_u32(smem + kQOffV);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int fh = static_cast<int>(blockIdx.x) & 1;
+  const int rest = static_cast<int>(blockIdx.x) >> 1;
+  const int qi = prm.nchunks - 1 - rest / prm.bhn;   // heavy (late) query chunks first
+  const int bh = rest % prm.bhn;
+  const int h = bh % prm.H;
+  const int ntiles = qi + 1;
+
+  if (warp == kMmaWarp) {
+    tmem_alloc(&m.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int b = 0; b < kNumBars; ++b)
+      mbar_init(&m.bar[b], b == kDSReady ? static_cast<uint32_t>(kEpiWarps) : 1u);
+    m.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (tid < 32) { m.red_omega[tid] = 0.f; m.red_phi[tid] = 0.f; }
+  if (tid == 0) m.red_gamma = 0.f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) {
+      const unsigned char* cq = chunk_base(prm.ws, bh, prm.nchunks, qi);
+      const unsigned char* dq = prm.dn + (static_cast<int64_t>(bh) * prm.nchunks + qi) * kDNBytes;
+      mbar_arrive_expect_tx(&m.bar[kResFull], kPhiBytes + kDNBytes);
+      for (uint32_t off = 0; off < kPhiBytes; off += 16384)
+        bulk_load_g2s(sQ + off, cq + off, 16384, &m.bar[kResFull]);
+      bulk_load_g2s(sDN, dq, kDNBytes, &m.bar[kResFull]);
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        // the previous tile has read K, V; after an abandoned wait nothing more is issued
+        if (j > 0 && !wait_bar(m, kTileDone, (j - 1) & 1)) break;
+        const unsigned char* cj = chunk_base(prm.ws, bh, prm.nchunks, j);
+        mbar_arrive_expect_tx(&m.bar[kStrFull], kPhiBytes + kVBytes);
+        for (uint32_t off = 0; off < kPhiBytes; off += 16384)
+          bulk_load_g2s(sK + off, cj + kPhiBytes + off, 16384, &m.bar[kStrFull]);
+        bulk_load_g2s(sV, cj + 2 * kPhiBytes, kVBytes, &m.bar[kStrFull]);
+        issued = j + 1;
+      }
+      // no copy may still be writing shared memory when the CTA exits
+      mbar_wait_bounded(&m.bar[kResFull], 0, kWaitNs);
+      if (issued > 0) mbar_wait_bounded(&m.bar[kStrFull], (issued - 1) & 1, kWaitNs);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idF = idesc_bf16_f32(128, 160, false, true);
+      wait_bar(m, kResFull, 0);
+      for (int j = 0; j < ntiles; ++j) {
+        wait_bar(m, kStrFull, j & 1);   // also implies the previous tile's MMAs are done
+        tc_fence_after();
+        uint64_t dQ = smem_desc(sQ, 128, kXQ);          // Phi(Q_i), K-major A
+        uint64_t dK = smem_desc(sK, 128, kXQ);          // Phi(K_j), K-major B (N = keys)
+        uint64_t dN = smem_desc(sDN, 128, 1024);        // dN_i, K-major A
+        uint64_t dV = smem_desc(sV, 128, kVGroup);      // V_j, K-major B (N = keys)
+        asm volatile("" : "+l"(dQ), "+l"(dK), "+l"(dN), "+l"(dV));
+#pragma unroll
+        for (int st = 0; st < 20; ++st)
+          mma_ss(tmem + kTS, dQ + 16 * st, dK + 16 * st, idS, st > 0);
+#pragma unroll
+        for (int st = 0; st < 4; ++st)
+          mma_ss(tmem + kTDW, dN + 16 * st, dV + 16 * st, idS, st > 0);
+        mma_commit(&m.bar[kSDone]);
+        wait_bar(m, kDSReady, j & 1);
+        tc_fence_after();
+        uint64_t dKf = smem_desc(sK + 20 * 128 * fh, kXQ, 128);   // Phi(K_j) half, MN-major B
+        asm volatile("" : "+l"(dKf));
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const uint32_t hi = tmem + kTDW + 32 * (st >> 1) + 8 * (st & 1);
+          mma_ts(tmem + kTF, hi, dKf + (2 * kXQ / 16) * st, idF, (j | st) != 0);
+          mma_ts(tmem + kTF, hi + 16, dKf + (2 * kXQ / 16) * st, idF, true);
+        }
+        mma_commit(&m.bar[kTileDone]);
+      }
+      mbar_wait_bounded(&m.bar[kTileDone], (ntiles - 1) & 1, kWaitNs);
+    }
+  } else {
+    // epilogue: warp (qd, ch) owns query rows 32 qd .. + 31 and keys 64 ch .. + 63
+    const int qd = warp & 3, ch = warp >> 2;
+    const int row = 32 * qd + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
+    const float ddrow = prm.dd[(static_cast<int64_t>(bh) * prm.nchunks + qi) * kC + row];
+    float ddv[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) ddv[k] = ddrow;
+    for (int j = 0; j < ntiles; ++j) {
+      wait_bar(m, kSDone, j & 1);
+      tc_fence_after();
+      const bool diag = (j == qi);
+#pragma unroll 1
+      for (int bi = 0; bi < 2; ++bi) {
+        const int blk = 2 * ch + bi;
+        const uint32_t cs = tmem + lane_off + kTS + 32 * blk;
+        const uint32_t cd = tmem + lane_off + kTDW + 32 * blk;
+        uint32_t dhi[16], dlo[16], whi[16], wlo[16];
+        if (diag && blk > qd) {   // every key of the block is after every row of the warp
+#pragma unroll
+          for (int i = 0; i < 16; ++i) { dhi[i] = 0u; dlo[i] = 0u; }
+        } else {
+          float sv[32], dwv[32];
+          tmem_ld16(cs, *reinterpret_cast<float(*)[16]>(&sv[0]));
+          tmem_ld16(cs + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
+          tmem_ld16(cd, *reinterpret_cast<float(*)[16]>(&dwv[0]));
+          tmem_ld16(cd + 16, *reinterpret_cast<float(*)[16]>(&dwv[16]));
+          tmem_ld_wait();
+          const int lim = (diag && blk == qd) ? lane : 31;   // keys up to the row's own
+          grads32<P>(sv, dwv, ddv, [lim](int k) { return k <= lim; }, dhi, dlo, whi, wlo);
+        }
+        tmem_st16(cd, dhi);
+        tmem_st16(cd + 16, dlo);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.bar[kDSReady]);
+    }
+    wait_bar(m, kTileDone, (ntiles - 1) & 1);
+    tc_fence_after();
+    const int t = qi * kC + row;
+    const bool valid = t < prm.T;
+    const int64_t grow = static_cast<int64_t>(bh) * prm.T + (valid ? t : 0);
+    chain_rule16(tmem + lane_off + kTF, fh, ch, h, prm.pos0 + t, valid, prm.u + grow * kD, prm,
+                 prm.du + grow * kD, m, lane);
+    epi_sync();
+    flush_param_grads(m, prm, h, fh, tid);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Key pass.  Shared memory: Phi(K_j) and [V_j | 1 | 0] resident, Phi(Q_i), dN_i
+// and dD_i streamed (single buffer).
+constexpr int kKOffK = 0;
+constexpr int kKOffV = kKOffK + kPhiBytes;
+constexpr int kKOffQ = kKOffV + kVBytes;
+constexpr int kKOffDN = kKOffQ + kPhiBytes;
+constexpr int kKOffDD = kKOffDN + kDNBytes;
+constexpr int kKOffMisc = kKOffDD + kDDBytes;
+constexpr int kKSmem = kKOffMisc + static_cast<int>(sizeof(Misc));
+static_assert(kKSmem <= 232448, "key pass: shared memory exceeds 227 KB");
+
+template <int P>
+__global__ void __launch_bounds__(kThreads, 1) pow_bwd_k_kernel(BwdParams prm) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  Misc& m = *reinterpret_cast<Misc*>(smem + kKOffMisc);
+  const float* sdd = reinterpret_cast<const float*>(smem + kKOffDD);
+  const uint32_t sK = smem_u32(smem + kKOffK), sV = smem_u32(smem + kKOffV);
+  const uint32_t sQ = smem_u32(smem + kKOffQ), sDN = smem_u32(smem + kKOffDN);
+  const uint32_t sDD = smem_u32(smem + kKOffDD);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int fh = static_cast<int>(blockIdx.x) & 1;
+  const int rest = static_cast<int>(blockIdx.x) >> 1;
+  const int kj = rest / prm.bhn;   // early key chunks (the most query chunks) first
+  const int bh = rest % prm.bhn;
+  const int h = bh % prm.H;
+  const int ntiles = prm.nchunks - kj;
+  const bool with_dv = (fh == 0);
+
+  if (warp == kMmaWarp) {
+    tmem_alloc(&m.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int b = 0; b < kNumBars; ++b)
+      mbar_init(&m.bar[b], b == kDSReady ? static_cast<uint32_t>(kEpiWarps) : 1u);
+    m.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (tid < 32) { m.red_omega[tid] = 0.f; m.red_phi[tid] = 0.f; }
+  if (tid == 0) m.red_gamma = 0.f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) {
+      const unsigned char* ck = chunk_base(prm.ws, bh, prm.nchunks, kj);
+      mbar_arrive_expect_tx(&m.bar[kResFull], kPhiBytes + kVBytes);
+      for (uint32_t off = 0; off < kPhiBytes; off += 16384)
+        bulk_load_g2s(sK + off, ck + kPhiBytes + off, 16384, &m.bar[kResFull]);
+      bulk_load_g2s(sV, ck + 2 * kPhiBytes, kVBytes, &m.bar[kResFull]);
+      int issued = 0;
+      for (int n = 0; n < ntiles; ++n) {
+        const int qi = kj + n;
+        // the previous tile has read Q, dN, dD; after an abandoned wait nothing more is issued
+        if (n > 0 && !wait_bar(m, kTileDone, (n - 1) & 1)) break;
+        const unsigned char* cq = chunk_base(prm.ws, bh, prm.nchunks, qi);
+        const int64_t sc = static_cast<int64_t>(bh) * prm.nchunks + qi;
+        mbar_arrive_expect_tx(&m.bar[kStrFull], kPhiBytes + kDNBytes + kDDBytes);
+        for (uint32_t off = 0; off < kPhiBytes; off += 16384)
+          bulk_load_g2s(sQ + off, cq + off, 16384, &m.bar[kStrFull]);
+        bulk_load_g2s(sDN, prm.dn + sc * kDNBytes, kDNBytes, &m.bar[kStrFull]);
+        bulk_load_g2s(sDD, prm.dd + sc * kC, kDDBytes, &m.bar[kStrFull]);
+        issued = n + 1;
+      }
+      mbar_wait_bounded(&m.bar[kResFull], 0, kWaitNs);
+      if (issued > 0) mbar_wait_bounded(&m.bar[kStrFull], (issued - 1) & 1, kWaitNs);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idF = idesc_bf16_f32(128, 160, false, true);
+      constexpr uint32_t idV = idesc_bf16_f32(128, 64, false, true);
+      wait_bar(m, kResFull, 0);
+      for (int n = 0; n < ntiles; ++n) {
+        wait_bar(m, kStrFull, n & 1);
+        tc_fence_after();
+        uint64_t dK = smem_desc(sK, 128, kXQ);          // Phi(K_j), K-major A (M = keys)
+        uint64_t dQ = smem_desc(sQ, 128, kXQ);          // Phi(Q_i), K-major B (N = queries)
+        uint64_t dV = smem_desc(sV, 128, kVGroup);      // V_j, K-major A
+        uint64_t dN = smem_desc(sDN, 128, 1024);        // dN_i, K-major B (N = queries)
+        asm volatile("" : "+l"(dK), "+l"(dQ), "+l"(dV), "+l"(dN));
+#pragma unroll
+        for (int st = 0; st < 20; ++st)
+          mma_ss(tmem + kTS, dK + 16 * st, dQ + 16 * st, idS, st > 0);
+#pragma unroll
+        for (int st = 0; st < 4; ++st)
+          mma_ss(tmem + kTDW, dV + 16 * st, dN + 16 * st, idS, st > 0);
+        mma_commit(&m.bar[kSDone]);
+        wait_bar(m, kDSReady, n & 1);
+        tc_fence_after();
+        uint64_t dQf = smem_desc(sQ + 20 * 128 * fh, kXQ, 128);   // Phi(Q_i) half, MN-major B
+        uint64_t dNv = smem_desc(sDN, 1024, 128);                 // dN_i, MN-major B
+        asm volatile("" : "+l"(dQf), "+l"(dNv));
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const uint32_t hi = tmem + kTDW + 32 * (st >> 1) + 8 * (st & 1);
+          mma_ts(tmem + kTF, hi, dQf + (2 * kXQ / 16) * st, idF, (n | st) != 0);
+          mma_ts(tmem + kTF, hi + 16, dQf + (2 * kXQ / 16) * st, idF, true);
+        }
+        if (with_dv) {
+#pragma unroll
+          for (int st = 0; st < 8; ++st) {
+            const uint32_t hi = tmem + kTS + 32 * (st >> 1) + 8 * (st & 1);
+            mma_ts(tmem + kTV, hi, dNv + (2 * 1024 / 16) * st, idV, (n | st) != 0);
+            mma_ts(tmem + kTV, hi + 16, dNv + (2 * 1024 / 16) * st, idV, true);
+          }
+        }
+        mma_commit(&m.bar[kTileDone]);
+      }
+      mbar_wait_bounded(&m.bar[kTileDone], (ntiles - 1) & 1, kWaitNs);
+    }
+  } else {
+    // epilogue: warp (qd, ch) owns key rows 32 qd .. + 31 and queries 64 ch .. + 63
+    const int qd = warp & 3, ch = warp >> 2;
+    const int row = 32 * qd + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
+    for (int n = 0; n < ntiles; ++n) {
+      wait_bar(m, kStrFull, n & 1);   // dD_i in shared memory (the bulk copy's own barrier)
+      wait_bar(m, kSDone, n & 1);
+      tc_fence_after();
+      const bool diag = (n == 0);   // query chunk == key chunk
+#pragma unroll 1
+      for (int bi = 0; bi < 2; ++bi) {
+        const int blk = 2 * ch + bi;
+        const uint32_t cs = tmem + lane_off + kTS + 32 * blk;
+        const uint32_t cd = tmem + lane_off + kTDW + 32 * blk;
+        uint32_t dhi[16], dlo[16], whi[16], wlo[16];
+        if (diag && blk < qd) {   // every query of the block is before every key of the warp
+#pragma unroll
+          for (int i = 0; i < 16; ++i) { dhi[i] = 0u; dlo[i] = 0u; whi[i] = 0u; wlo[i] = 0u; }
+        } else {
+          float sv[32], dwv[32];
+          tmem_ld16(cs, *reinterpret_cast<float(*)[16]>(&sv[0]));
+          tmem_ld16(cs + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
+          tmem_ld16(cd, *reinterpret_cast<float(*)[16]>(&dwv[0]));
+          tmem_ld16(cd + 16, *reinterpret_cast<float(*)[16]>(&dwv[16]));
+          tmem_ld_wait();
+          const int first = (diag && blk == qd) ? lane : 0;   // queries from the key's own
+          grads32<P>(sv, dwv, sdd + 32 * blk, [first](int k) { return k >= first; }, dhi, dlo,
+                     whi, wlo);
+        }
+        tmem_st16(cs, whi);
+        tmem_st16(cs + 16, wlo);
+        tmem_st16(cd, dhi);
+        tmem_st16(cd + 16, dlo);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.bar[kDSReady]);
+    }
+    wait_bar(m, kTileDone, (ntiles - 1) & 1);
+    tc_fence_after();
+    const int t = kj * kC + row;
+    const bool valid = t < prm.T;
+    const int64_t grow = static_cast<int64_t>(bh) * prm.T + (valid ? t : 0);
+    if (with_dv) {
+      float dvv[32];
+      tmem_ld16(tmem + lane_off + kTV + 32 * ch, *reinterpret_cast<float(*)[16]>(&dvv[0]));
+      tmem_ld16(tmem + lane_off + kTV + 32 * ch + 16, *reinterpret_cast<float(*)[16]>(&dvv[16]));
+      tmem_ld_wait();
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(prm.dv + grow * kD + 32 * ch);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          dst[q4] = make_uint4(pack_bf16x2(dvv[8 * q4], dvv[8 * q4 + 1]),
+                               pack_bf16x2(dvv[8 * q4 + 2], dvv[8 * q4 + 3]),
+                               pack_bf16x2(dvv[8 * q4 + 4], dvv[8 * q4 + 5]),
+                               pack_bf16x2(dvv[8 * q4 + 6], dvv[8 * q4 + 7]));
+      }
+    }
+    chain_rule16(tmem + lane_off + kTF, fh, ch, h, prm.pos0 + t, valid, prm.u + grow * kD, prm,
+                 prm.du + grow * kD, m, lane);
+    epi_sync();
+    flush_param_grads(m, prm, h, fh, tid);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t pow_bwd_tc_workspace_bytes(int B, int H, int T) {
+  const int64_t nchunks = (static_cast<int64_t>(T) + kC - 1) / kC;
+  return static_cast<size_t>(B) * H * nchunks * (kChunkBytes + kDNBytes + kDDBytes);
+}
+
+namespace {
+constexpr int kMaxP = 8;
+using BwdKernel = void (*)(BwdParams);
+
+BwdKernel q_kernel_for(int p) {
+  switch (p) {
+    case 1: return pow_bwd_q_kernel<1>;
+    case 2: return pow_bwd_q_kernel<2>;
+    case 3: return pow_bwd_q_kernel<3>;
+    case 4: return pow_bwd_q_kernel<4>;
+    case 5: return pow_bwd_q_kernel<5>;
+    case 6: return pow_bwd_q_kernel<6>;
+    case 7: return pow_bwd_q_kernel<7>;
+    default: return pow_bwd_q_kernel<8>;
+  }
+}
+
+BwdKernel k_kernel_for(int p) {
+  switch (p) {
+    case 1: return pow_bwd_k_kernel<1>;
+    case 2: return pow_bwd_k_kernel<2>;
+    case 3: return pow_bwd_k_kernel<3>;
+    case 4: return pow_bwd_k_kernel<4>;
+    case 5: return pow_bwd_k_kernel<5>;
+    case 6: return pow_bwd_k_kernel<6>;
+    case 7: return pow_bwd_k_kernel<7>;
+    default: return pow_bwd_k_kernel<8>;
+  }
+}
+
+cudaError_t bwd_set_smem() {
+  static bool done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  for (int p = 1; p <= kMaxP && e == cudaSuccess; ++p) {
+    e = cudaFuncSetAttribute(q_kernel_for(p), cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_kernel_for(p), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kKSmem);
+  }
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+}  // namespace
+
+cudaError_t pow_bwd_tc_launch(const PowBwdArgs& a, cudaStream_t st) {
+  const PowFwdArgs& f = a.f;
+  const int bhn = f.B * f.H;
+  const int nchunks = (f.T + kC - 1) / kC;
+  cudaError_t e;
+  // the parameter gradients are sums: start from zero
+  if (f.H > 0) {
+    if ((e = cudaMemsetAsync(a.dgamma, 0, sizeof(float) * f.H, st)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.domega, 0, sizeof(float) * f.H * kD, st)) != cudaSuccess) return e;
+    if (a.dphi != nullptr &&
+        (e = cudaMemsetAsync(a.dphi, 0, sizeof(float) * f.H * kD, st)) != cudaSuccess)
+      return e;
+  }
+  if (bhn == 0 || nchunks == 0) return cudaSuccess;
+  if (f.p < 1 || f.p > kMaxP) return cudaErrorInvalidValue;
+  if ((e = bwd_set_smem()) != cudaSuccess) return e;
+  unsigned char* ws = static_cast<unsigned char*>(f.workspace);
+  const int64_t nsc = static_cast<int64_t>(bhn) * nchunks;
+  unsigned char* dn = ws + nsc * kChunkBytes;
+  float* dd = reinterpret_cast<float*>(dn + nsc * kDNBytes);
+  if ((e = pow_prep_launch(f, st)) != cudaSuccess) return e;
+  DPrepParams dp{};
+  dp.dO = a.dO;
+  dp.grad_bf16 = a.grad_dtype == SANATAN_BF16;
+  dp.o = a.o;
+  dp.D = a.D;
+  dp.eps = f.eps;
+  dp.T = f.T;
+  dp.nchunks = nchunks;
+  dp.ntok = nsc * kC;
+  dp.dn = dn;
+  dp.dd = dd;
+  const int64_t threads = dp.ntok * 8;
+  pow_dprep_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(dp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  BwdParams bp{};
+  bp.ws = ws;
+  bp.dn = dn;
+  bp.dd = dd;
+  bp.gamma = f.gamma;
+  bp.omega = f.omega;
+  bp.phi = f.phi;
+  bp.H = f.H;
+  bp.T = f.T;
+  bp.nchunks = nchunks;
+  bp.bhn = bhn;
+  bp.pos0 = f.pos0;
+  bp.dgamma = a.dgamma;
+  bp.domega = a.domega;
+  bp.dphi = a.dphi;
+  const unsigned grid = static_cast<unsigned>(2 * nsc);
+  bp.u = static_cast<const __nv_bfloat16*>(f.q);
+  bp.du = static_cast<__nv_bfloat16*>(a.dq);
+  bp.dv = nullptr;
+  q_kernel_for(f.p)<<<grid, kThreads, kQSmem, st>>>(bp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bp.u = static_cast<const __nv_bfloat16*>(f.k);
+  bp.du = static_cast<__nv_bfloat16*>(a.dk);
+  bp.dv = static_cast<__nv_bfloat16*>(a.dv);
+  const ProfileEvents& pe = profile_events();
+  const bool rec = pe.start != nullptr;
+  if (rec) cudaEventRecord(pe.start, st);
+  k_kernel_for(f.p)<<<grid, kThreads, kKSmem, st>>>(bp);
+  e = cudaGetLastError();
+  if (rec) cudaEventRecord(pe.stop, st);
+  return e;
+}
+
+int pow_bwd_tc_read_and_clear_error(cudaStream_t st) {
+  int h = 0;
+  if (cudaMemcpyFromSymbolAsync(&h, g_pow_bwd_error, sizeof(int), 0, cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return -1;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_pow_bwd_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                                st) != cudaSuccess)
+      return -1;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+  }
+  return h;
+}
+
+}  // namespace sanatan

@@ -24,6 +24,7 @@
 #include "sanatan_math.cuh"
 #include "tc_common.cuh"
 #include "tc_ptx.cuh"
+#include "pow_common.cuh"
 
 namespace sanatan {
 
@@ -33,20 +34,7 @@ namespace {
 
 using namespace tc;
 using namespace tcc;
-
-// Chunk layouts in the workspace and in shared memory (canonical no-swizzle
-// core matrices of 8 rows x 16 bytes):
-//   Phi: token group tg (8 tokens) at tg * kXQ, feature group fg (8 features)
-//        at fg * 128, token row r at r * 16   (80 KB per chunk)
-//   V:   [V | 1 | 0] (80 columns: the ones column makes the tensor core sum
-//        the weights, i.e. the denominator, next to the outputs): token group
-//        tg at tg * 1280, column group ng (8 columns) at ng * 128, token row r
-//        at r * 16                             (20 KB per chunk)
-constexpr uint32_t kPhiBytes = 16 * kXQ;   // 81920
-constexpr uint32_t kVGroup = 10 * 128;     // bytes per 8-token group of [V | 1 | 0]
-constexpr uint32_t kVBytes = 16 * kVGroup; // 20480
-constexpr int kNV = 80;                    // N of the value product
-constexpr uint32_t kChunkBytes = 2 * kPhiBytes + kVBytes;
+using namespace powc;
 
 // Shared memory: two Phi(K) and two V buffers (chunk j uses buffer j & 1).
 constexpr int kOffK = 0;
@@ -102,16 +90,6 @@ struct PrepParams {
   int64_t pos0;
   unsigned char* ws;
 };
-
-// Byte offset of (token t, feature group fg) in a Phi chunk.
-__host__ __device__ constexpr uint32_t phi_offset(int t, int fg) {
-  return (t >> 3) * kXQ + fg * 128 + (t & 7) * 16;
-}
-
-__device__ __forceinline__ const unsigned char* chunk_base(const unsigned char* ws, int64_t bh,
-                                                           int nchunks, int c) {
-  return ws + (bh * nchunks + c) * static_cast<int64_t>(kChunkBytes);
-}
 
 // ---------------------------------------------------------------------------
 // Preparation: one CTA of 256 threads per half chunk (64 tokens).  Lane
@@ -212,16 +190,6 @@ __device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
   m.abort_flag = 1;
   atomicOr(&g_pow_tc_error, 1);
   return false;
-}
-
-template <int P>
-__device__ __forceinline__ float pow_int(float x) {
-  if constexpr (P == 1) {
-    return x;
-  } else {
-    const float h = pow_int<P / 2>(x);
-    return (P & 1) ? h * h * x : h * h;
-  }
 }
 
 // The weights ((s / 4d)^p) of 32 keys of one row from their scores,
@@ -497,6 +465,27 @@ cudaError_t pow_set_smem() {
   return e;
 }
 }  // namespace
+
+cudaError_t pow_prep_launch(const PowFwdArgs& a, cudaStream_t st) {
+  const int bhn = a.B * a.H;
+  const int nchunks = (a.T + kC - 1) / kC;
+  if (bhn == 0 || nchunks == 0) return cudaSuccess;
+  PrepParams pp{};
+  pp.q = static_cast<const __nv_bfloat16*>(a.q);
+  pp.k = static_cast<const __nv_bfloat16*>(a.k);
+  pp.v = static_cast<const __nv_bfloat16*>(a.v);
+  pp.gamma = a.gamma;
+  pp.omega = a.omega;
+  pp.phi = a.phi;
+  pp.H = a.H;
+  pp.T = a.T;
+  pp.nchunks = nchunks;
+  pp.pos0 = a.pos0;
+  pp.ws = static_cast<unsigned char*>(a.workspace);
+  const unsigned grid = static_cast<unsigned>(bhn) * static_cast<unsigned>(nchunks);
+  pow_prep_kernel<<<2 * grid, 256, 0, st>>>(pp);
+  return cudaGetLastError();
+}
 
 cudaError_t pow_fwd_tc_launch(const PowFwdArgs& a, cudaStream_t st) {
   const int bhn = a.B * a.H;

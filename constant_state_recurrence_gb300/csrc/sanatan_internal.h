@@ -141,5 +141,25 @@ struct PowFwdArgs {
 };
 size_t pow_fwd_tc_workspace_bytes(int B, int H, int T);
 cudaError_t pow_fwd_tc_launch(const PowFwdArgs& a, cudaStream_t st);
+// The preparation kernel alone (features and [V | 1 | 0] into a.workspace).
+cudaError_t pow_prep_launch(const PowFwdArgs& a, cudaStream_t st);
+
+// Gradients of the power-sharpened attention.
+struct PowBwdArgs {
+  PowFwdArgs f;               // q, k, v, params, sizes, p, eps; f.workspace = the whole workspace
+  const float* o = nullptr;   // [B, H, T, 64] f32, the forward's output
+  const float* D = nullptr;   // [B, H, T] f32, the forward's denominator (without eps)
+  const void* dO = nullptr;   // [B, H, T, 64], grad_dtype
+  int grad_dtype = 0;
+  void* dq = nullptr;         // bf16 [B, H, T, 64]
+  void* dk = nullptr;
+  void* dv = nullptr;
+  float* dgamma = nullptr;    // [H], overwritten
+  float* domega = nullptr;    // [H, 64], overwritten
+  float* dphi = nullptr;      // [H, 64], overwritten (may be null)
+};
+size_t pow_bwd_tc_workspace_bytes(int B, int H, int T);
+cudaError_t pow_bwd_tc_launch(const PowBwdArgs& a, cudaStream_t st);
+int pow_bwd_tc_read_and_clear_error(cudaStream_t st);
 int pow_tc_read_and_clear_error(cudaStream_t st);
 }  // namespace sanatan

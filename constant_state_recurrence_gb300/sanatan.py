@@ -47,6 +47,10 @@ _SIGS = {
     "sanatan_power_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int,
                                    _c_int, _c_int, _c_i64, _c_int, _c_f, _c_p, _c_p, _c_p, _c_sz,
                                    _c_p]),
+    "sanatan_power_bwd_workspace_size": (_c_sz, [_c_int] * 5),
+    "sanatan_power_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int,
+                                   _c_int, _c_int, _c_i64, _c_int, _c_f, _c_p, _c_p, _c_p, _c_int,
+                                   _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "sanatan_device_status": (_c_int, [_c_p]),
     "sanatan_set_profile_events": (_c_int, [_c_p, _c_p]),
     "sanatan_selftest_wait_timeout": (_c_int, [ctypes.c_uint64, _c_int, _c_p]),
@@ -276,6 +280,42 @@ def sanatan_power_fwd(q, k, v, gamma, omega, phi, p, pos0=0, eps=0.0, want_D=Tru
                                  _ptr(workspace), ws_bytes, _stream(dev))
     _check("sanatan_power_fwd", st)
     return o, D
+
+
+def power_bwd_workspace_size(B, H, T, d=64, dv=64):
+    return int(lib().sanatan_power_bwd_workspace_size(B, H, T, d, dv))
+
+
+def sanatan_power_bwd(q, k, v, gamma, omega, phi, p, o, D, dO, pos0=0, eps=0.0, want_dphi=True,
+                      workspace=None):
+    """Gradients of sum(o * dO) for sanatan_power_fwd (bf16 q, k, v).
+
+    Returns a dict with dq, dk, dv (bf16), dgamma, domega and dphi (f32; dphi
+    None unless want_dphi)."""
+    _need(q, "q", (torch.bfloat16,))
+    B, H, T, d = q.shape
+    _need(k, "k", (torch.bfloat16,), (B, H, T, d))
+    dv_ = v.shape[-1]
+    _need(v, "v", (torch.bfloat16,), (B, H, T, dv_))
+    _need(o, "o", (torch.float32,), (B, H, T, dv_))
+    _need(D, "D", (torch.float32,), (B, H, T))
+    _need(dO, "dO", (torch.float32, torch.bfloat16), (B, H, T, dv_))
+    dev = q.device
+    dq, dk, dvo = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dgamma = torch.empty(H, dtype=torch.float32, device=dev)
+    domega = torch.empty(H, d, dtype=torch.float32, device=dev)
+    dphi = torch.empty(H, d, dtype=torch.float32, device=dev) if want_dphi else None
+    ws_size = power_bwd_workspace_size(B, H, T, d, dv_)
+    if workspace is None and ws_size > 0:
+        workspace = torch.empty(ws_size, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().sanatan_power_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(omega), _ptr(phi),
+                                 B, H, T, d, dv_, int(pos0), int(p), float(eps), _ptr(o), _ptr(D),
+                                 _ptr(dO), _DT[dO.dtype], _ptr(dq), _ptr(dk), _ptr(dvo),
+                                 _ptr(dgamma), _ptr(domega), _ptr(dphi), _ptr(workspace),
+                                 ws_bytes, _stream(dev))
+    _check("sanatan_power_bwd", st)
+    return dict(dq=dq, dk=dk, dv=dvo, dgamma=dgamma, domega=domega, dphi=dphi)
 
 
 def chunk_bwd_workspace_size(B, H, T, d=64, dv=64, dtype=torch.bfloat16):

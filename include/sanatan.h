@@ -203,6 +203,27 @@ SANATAN_API int sanatan_power_fwd(const void* q, const void* k, const void* v, c
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sanatan_power_bwd -- gradients of sum(o * dO) for sanatan_power_fwd (the
+ * chain rule through eq. (8) and the feature map; the pages give no backward).
+ *   q, k, v, gamma, omega, phi, sizes, pos0, p, eps: as for the forward
+ *   o [B, H, T, dv] f32 and D [B, H, T] f32: the forward's outputs
+ *   dO [B, H, T, dv] in grad_dtype (SANATAN_F32 or SANATAN_BF16)
+ *   dq, dk [B, H, T, d] bf16 outputs; dv_out [B, H, T, dv] bf16 output
+ *   dgamma [H] f32, domega [H, d] f32 outputs (overwritten, summed over the
+ *   batch and both q and k); dphi [H, d] f32 output or NULL
+ *   workspace: at least sanatan_power_bwd_workspace_size(...) bytes.
+ * Errors as for sanatan_power_fwd; grad_dtype outside the enum is INVALID.
+ */
+SANATAN_API size_t sanatan_power_bwd_workspace_size(int B, int H, int T, int d, int dv);
+SANATAN_API int sanatan_power_bwd(const void* q, const void* k, const void* v, const float* gamma,
+                                  const float* omega, const float* phi, int B, int H, int T, int d,
+                                  int dv, int64_t pos0, int p, float eps, const float* o,
+                                  const float* D, const void* dO, int grad_dtype, void* dq,
+                                  void* dk, void* dv_out, float* dgamma, float* domega,
+                                  float* dphi, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/*
  * sanatan_set_profile_events -- instrumentation for benchmarks.  When both
  * are non-NULL, the calling thread's subsequent sanatan_chunk_fwd,
  * sanatan_chunk_bwd and sanatan_power_fwd calls record `start` (a cudaEvent_t) on their stream just
