@@ -76,6 +76,7 @@ struct BwdParams {
   const float* phi;
   int H, T, nchunks, bhn;
   int64_t pos0;
+  int64_t pos_mid;            // pos0 + (T - 1) / 2: the reference position of the phi gradient
   __nv_bfloat16* du;          // dq or dk
   __nv_bfloat16* dv;          // key pass only
   float* dgamma;
@@ -177,8 +178,14 @@ __global__ void __launch_bounds__(256) pow_dprep_kernel(DPrepParams prm) {
 //   dc = d1 + r d4, ds = d2 + r d5, dr = d3 + c d4 + s d5,
 //   dth_rot = -s dc + c ds, dpre = dr (1 - r^2),
 //   dtheta = dth_rot + dpre gamma g'(theta + omega), du = dtheta pi / (1 + |u|)^2,
-//   dgamma += dpre g, domega += dpre gamma g', dphi += dth_rot t,
-// with g(x) = cos x - sin x, g'(x) = -sin x - cos x.  Sums over the tokens of
+//   dgamma += dpre g, domega += dpre gamma g', dphi += dth_rot (t - t_mid),
+// with g(x) = cos x - sin x, g'(x) = -sin x - cos x.  The outputs do not
+// change when every position of a sequence moves by the same amount (each
+// score depends on positions only through t - j), so for every dimension the
+// phase gradients dth_rot of all q and k tokens of a sequence sum to zero and
+// sum_t dth_rot t = sum_t dth_rot (t - t_mid) exactly; the second form, with
+// t_mid the middle position, keeps a large position offset from amplifying
+// the rounding of the individual terms.  Sums over the tokens of
 // the CTA go to shared memory (warp shuffles first); du is written as bf16.
 __device__ __forceinline__ void chain_rule16(uint32_t trow, int fh, int ch, int h, int64_t tpos,
                                              bool valid, const __nv_bfloat16* urow,
@@ -223,7 +230,7 @@ __device__ __forceinline__ void chain_rule16(uint32_t trow, int fh, int ch, int 
       du[8 * gi + e] = dtheta * kPi * inv * inv;
       dgam = fmaf(dpre, g, dgam);
       float om = dpre * gam * gp;
-      float ph = valid ? dthr * static_cast<float>(tpos) : 0.f;
+      float ph = valid ? dthr * static_cast<float>(tpos - prm.pos_mid) : 0.f;
 #pragma unroll
       for (int sh = 16; sh > 0; sh >>= 1) {
         om += __shfl_xor_sync(0xffffffffu, om, sh);
@@ -739,6 +746,7 @@ cudaError_t pow_bwd_tc_launch(const PowBwdArgs& a, cudaStream_t st) {
   bp.nchunks = nchunks;
   bp.bhn = bhn;
   bp.pos0 = f.pos0;
+  bp.pos_mid = f.pos0 + (f.T - 1) / 2;
   bp.dgamma = a.dgamma;
   bp.domega = a.domega;
   bp.dphi = a.dphi;

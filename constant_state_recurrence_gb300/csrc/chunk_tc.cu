@@ -111,6 +111,10 @@ constexpr int kMmaWarp = 20;   // warp 20: MMA issue (one thread)
 constexpr int kVWarp0 = 21;    // warps 21-22: value loads
 constexpr int kVWarps = 2;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
+#ifndef SANATAN_SINPOLY
+#define SANATAN_SINPOLY 0
+#endif
+constexpr bool kSinPoly = SANATAN_SINPOLY != 0;  // sine/cosine of the angle on the FMA pipe
 
 struct TcParams {
   const __nv_bfloat16* q;
@@ -290,6 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       const int chunk = c_begin + ci;
       const int tok0 = chunk * kC;
       if (tid == 0 && ci + 2 < nloc) prefetch_chunk<kStateOnly>(prm, seq_row0, chunk + 2);
+      // rotation factors cos, sin(t phi) of the thread's first token (exact
+      // product, reduction mod 2 pi), then rotated by 8 phi per token
       float cb[8], sb[8];
       {
         const int64_t tabs = prm.pos0 + orow(prm, tok0 + tq);
@@ -309,26 +315,15 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         const int t = tq + 8 * i;
         const bool valid = tok0 + t < prm.T;
         uint32_t f[5][4];
-        if (valid) {
-          features8(raw[i], dimc, cb, sb, f);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 5; ++c)
-#pragma unroll
-            for (int p = 0; p < 4; ++p) f[c][p] = 0u;
-        }
+        // (raw is zero past the end, so the math stays finite; the rotation
+        // advances for every token)
+        features8_rot<kSinPoly>(raw[i], dimc, cb, sb, f);
         const uint32_t base = sdst + (t >> 3) * pitch + (t & 7) * 16;
 #pragma unroll
         for (int c = 0; c < 5; ++c)
-          st_shared_v4(base + feat_group(ag, c + 1) * 128, f[c][0], f[c][1], f[c][2], f[c][3]);
-        if (kgrp && ag == 0) st_shared_v4(base + 40 * 128, valid ? 0x3F80u : 0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 kc = dimc[j];
-          const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
-          sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
-          cb[j] = nc;
-        }
+          st_shared_v4_nc(base + feat_group(ag, c + 1) * 128, valid ? f[c][0] : 0u,
+                          valid ? f[c][1] : 0u, valid ? f[c][2] : 0u, valid ? f[c][3] : 0u);
+        if (kgrp && ag == 0) st_shared_v4_nc(base + 40 * 128, valid ? 0x3F80u : 0u, 0u, 0u, 0u);
       }
       fence_proxy_async_smem();
       __syncwarp();

@@ -119,6 +119,14 @@ def _need(t, name, dtypes=None, shape=None):
     return t
 
 
+def _need_params(gamma, omega, phi, H, d):
+    """gamma [H], omega [H, d], phi [H, d] float32 on the device (the kernels
+    read H rows of each)."""
+    _need(gamma, "gamma", (torch.float32,), (H,))
+    _need(omega, "omega", (torch.float32,), (H, d))
+    _need(phi, "phi", (torch.float32,), (H, d))
+
+
 def device_status(device=None):
     """Synchronise the current stream and raise if a kernel of the library gave
     up a bounded device-side wait since the last check."""
@@ -157,8 +165,7 @@ def sanatan_featurize(u, gamma, omega, phi, pos0=0, out_dtype=None, out=None):
     if out is None:
         out = torch.empty(B, H, T, 6 * d, dtype=odt, device=u.device)
     _need(out, "out", (torch.float32, torch.bfloat16), (B, H, T, 6 * d))
-    for n, t in (("gamma", gamma), ("omega", omega), ("phi", phi)):
-        _need(t, n, (torch.float32,))
+    _need_params(gamma, omega, phi, H, d)
     st = lib().sanatan_featurize(_ptr(u), _DT[u.dtype], _ptr(gamma), _ptr(omega), _ptr(phi),
                                  B, H, T, d, int(pos0), _ptr(out), _DT[out.dtype],
                                  _stream(u.device))
@@ -191,8 +198,7 @@ def sanatan_chunk_fwd(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=N
     _need(v, "v", (q.dtype,))
     dv = v.shape[-1]
     _need(v, "v", (q.dtype,), (B, H, T, dv))
-    for n, t in (("gamma", gamma), ("omega", omega), ("phi", phi)):
-        _need(t, n, (torch.float32,))
+    _need_params(gamma, omega, phi, H, d)
     dev = q.device
     F = 6 * d
     o = out if out is not None else torch.empty(B, H, T, dv, dtype=torch.float32, device=dev)
@@ -231,6 +237,7 @@ def sanatan_chunk_fwd_noalloc(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=No
     _need(k, "k", (torch.bfloat16,), (B, H, T, d))
     dv = v.shape[-1]
     _need(v, "v", (torch.bfloat16,), (B, H, T, dv))
+    _need_params(gamma, omega, phi, H, d)
     dev = q.device
     F = 6 * d
     o = torch.empty(B, H, T, dv, dtype=torch.float32, device=dev)
@@ -261,8 +268,7 @@ def sanatan_power_fwd(q, k, v, gamma, omega, phi, p, pos0=0, eps=0.0, want_D=Tru
     _need(k, "k", (torch.bfloat16,), (B, H, T, d))
     dv = v.shape[-1]
     _need(v, "v", (torch.bfloat16,), (B, H, T, dv))
-    for n, t in (("gamma", gamma), ("omega", omega), ("phi", phi)):
-        _need(t, n, (torch.float32,))
+    _need_params(gamma, omega, phi, H, d)
     dev = q.device
     o = out if out is not None else torch.empty(B, H, T, dv, dtype=torch.float32, device=dev)
     _need(o, "o", (torch.float32,), (B, H, T, dv))
@@ -300,6 +306,7 @@ def sanatan_power_bwd(q, k, v, gamma, omega, phi, p, o, D, dO, pos0=0, eps=0.0, 
     _need(o, "o", (torch.float32,), (B, H, T, dv_))
     _need(D, "D", (torch.float32,), (B, H, T))
     _need(dO, "dO", (torch.float32, torch.bfloat16), (B, H, T, dv_))
+    _need_params(gamma, omega, phi, H, d)
     dev = q.device
     dq, dk, dvo = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dgamma = torch.empty(H, dtype=torch.float32, device=dev)
@@ -333,6 +340,7 @@ def sanatan_chunk_bwd(q, k, v, gamma, omega, phi, o, D, dO, pos0=0, eps=0.0, S0=
     _need(o, "o", (torch.float32,), (B, H, T, dv))
     _need(D, "D", (torch.float32,), (B, H, T))
     _need(dO, "dO", (torch.float32, torch.bfloat16), (B, H, T, dv))
+    _need_params(gamma, omega, phi, H, d)
     dev = q.device
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)

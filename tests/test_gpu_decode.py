@@ -165,11 +165,12 @@ def test_decode_workload_B64_sampled_slots():
         pos = torch.full((N,), 4096 + i, dtype=torch.int64, device=dev())
         S.sanatan_decode_step(Sd, zd, q[i], k[i], v[i], x["gamma"], x["omega"], x["phi"], pos,
                               out=od[i])
-    oc, _, _, _ = S.sanatan_chunk_fwd(_stack_tokens(q), _stack_tokens(k), _stack_tokens(v),
-                                      x["gamma"], x["omega"], x["phi"], pos0=4096,
-                                      S0=S0.unsqueeze(0), z0=z0.unsqueeze(0), want_D=False)
+    # the same tokens as 64 sequences x 144 heads (slot n = 144 b + h uses head h's parameters)
+    seqs = lambda t: _stack_tokens(t).reshape(B, G, steps, 64)  # noqa: E731
+    oc, _, _, _ = S.sanatan_chunk_fwd(seqs(q), seqs(k), seqs(v), x["gamma"], x["omega"], x["phi"],
+                                      pos0=4096, S0=Sx, z0=zx, want_D=False)
     torch.cuda.synchronize()
-    assert (oc[0] - od.permute(1, 0, 2)).abs().max().item() <= 1e-4
+    assert (oc.reshape(N, steps, 64) - od.permute(1, 0, 2)).abs().max().item() <= 1e-4
 
     sl = torch.tensor(slots, device=dev())
     b_idx, h_idx = [n // G for n in slots], [n % G for n in slots]
