@@ -57,9 +57,10 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + 16 * kXQ;
 constexpr int kOffS = kOffK + 16 * kXK;
 constexpr int kOffV = kOffS + 40 * kLBO_SV;
-// The MMAs read up to 128 B past S'bf16 and V (ignored padding columns); the
-// pad keeps those reads inside this layout and away from the mbarriers.
-constexpr int kOffMisc = kOffV + 16 * kLBO_SV + 128;
+// The MMAs read up to 128 B past S'bf16 and V (the ignored padding columns
+// 72..79 of their N = 80): past V they read the start of Misc, the
+// featuriser constants, never written while MMAs run.
+constexpr int kOffMisc = kOffV + 16 * kLBO_SV;
 // The state-only pass needs no Phi(Q) and no snapshot: it double-buffers
 // Phi(K) and V instead, so that the keys of chunk c + 1 are featurised while
 // the tensor core accumulates chunk c.
@@ -70,7 +71,7 @@ static_assert(kSoV1 + 16 * kLBO_SV + 128 <= kOffMisc, "state-only buffers must f
 
 enum Bar {
   kFeatQ = 0, kFeatK, kFeatV, kPFull, kPTilde, kQFree, kStateDone, kPVDone, kSnapReady, kOFree,
-  kDrain,
+  kDrain, kInitDone,
   // second buffer of Phi(K) / V in the state-only pass
   kFeatK1, kFeatV1, kStateDone1,
   kNumBars
@@ -78,20 +79,14 @@ enum Bar {
 
 struct Misc {
   float4 dimc[64];   // per dim: gamma*sqrt2*cos(omega+pi/4), gamma*sqrt2*sin(omega+pi/4),
-                     //          cos(8 phi), sin(8 phi)
-  float vs[68];      // state row 320 before the current chunk: sum v (64), count
+                     //          cos(8 phi), sin(8 phi)  (first: the MMAs' over-read lands here)
+  float vs[2][68];   // state row 320 before chunk ci, in vs[ci & 1]: sum v (64), count
   float a0[68];      // constant-channel part of S0: sum_a S0[6a] (64), sum_a z0[6a]
   uint64_t bar[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
 };
-// Output staging: rows at a 272-B (f32) or 144-B (bf16) pitch, so that the
-// row-per-thread writes spread over the banks.  It lives in the bf16 state
-// snapshot buffer, which is free between the chunk's Phi(Q)[S|z] product and
-// the next snapshot.
-constexpr int kStagePitch = 272;
-constexpr int kStagePitchH = 144;
-static_assert(kC * kStagePitch <= 40 * kLBO_SV, "output staging must fit the snapshot buffer");
+static_assert(sizeof(float4) * 8 <= sizeof(Misc::dimc), "the over-read must stay in dimc");
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kSmemBytes <= 232448, "shared memory layout exceeds 227 KB");
 
@@ -160,6 +155,18 @@ __device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
 }
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Warps 8-23 (key featurisers, epilogue, MMA and value loaders).
+__device__ __forceinline__ void upper_sync() { asm volatile("bar.sync 2, 512;" ::: "memory"); }
+
+// Initial state of a later segment, gathered by warps 8-23 before the roles
+// start: the sums of the earlier segments (the compact slot layout, 68 x 321
+// floats) are added up with 16-byte loads into a shared-memory copy of one
+// slot.  It lives in the Phi(K) buffer and the start of the snapshot buffer;
+// the query featurisers, which write only Phi(Q), proceed meanwhile.
+constexpr int kOffInit = kOffK;
+constexpr int kSlotUsed4 = kSCUsedCols * kSCRows / 4;     // float4 per slot actually used
+constexpr int kSlot4 = kSCRows * kSCCols / 4;             // float4 stride between slots
+static_assert(kOffInit + kSlotUsed4 * 16 <= kOffV, "initial-state copy must fit before V");
 
 // L2 prefetch of one chunk's rows of q (unless state-only), k and v.
 template <bool kStateOnly>
@@ -215,7 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       const uint32_t cnt = (b == kFeatQ) ? kQWarps
                            : (b == kFeatK || b == kFeatK1) ? (kStateOnly ? 16u : 8u)
                            : (b == kFeatV || b == kFeatV1) ? static_cast<uint32_t>(kVWarps)
-                           : (b == kPTilde || b == kSnapReady || b == kOFree) ? 4u : 1u;
+                           : (b == kPTilde || b == kSnapReady || b == kOFree || b == kInitDone)
+                               ? 4u
+                               : 1u;
       mbar_init(&m.bar[b], cnt);
     }
     m.abort_flag = 0;
@@ -257,6 +266,26 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = m.tmem_base;
+
+  // A later segment starts from the sums of the earlier ones (written by the
+  // state-only pass): warps 8-23 add them up into shared memory.
+  const bool init_copy = !kStateOnly && prm.deltas != nullptr && seg > 0;
+  if (init_copy && warp >= kKWarp0) {
+    if (prm.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");  // the state-only pass is complete
+    const float4* d0 = reinterpret_cast<const float4*>(
+        prm.deltas + static_cast<int64_t>(bh) * prm.nseg * kSCRows * kSCCols);
+    float4* dst = reinterpret_cast<float4*>(smem + kOffInit);
+#pragma unroll 4
+    for (int i = tid - 32 * kKWarp0; i < kSlotUsed4; i += 512) {
+      float4 acc = d0[i];
+      for (int sp = 1; sp < seg; ++sp) {
+        const float4 x = d0[static_cast<int64_t>(sp) * kSlot4 + i];
+        acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+      }
+      dst[i] = acc;
+    }
+    upper_sync();
+  }
 
   if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ featurisers
@@ -309,6 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         if (ci > 1) wait_bar(m, (ci & 1) ? kStateDone1 : kStateDone, ((ci >> 1) - 1) & 1);
       } else {
         if (ci > 0) wait_bar(m, kgrp ? kStateDone : kQFree, (ci - 1) & 1);
+        // the initial-state copy in the Phi(K) buffer has been read
+        if (ci == 0 && kgrp && init_copy) wait_bar(m, kInitDone, 0);
       }
 #pragma unroll
       for (int i = 0; i < kNI; ++i) {
@@ -339,9 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
     // Initial state -> TMEM tiles (and the bf16 snapshot for the first chunk):
     // the caller's state (S0, z0) plus the sums of all earlier segments.
-    if (!kStateOnly && prm.pdl && seg > 0)
-      asm volatile("griddepcontrol.wait;" ::: "memory");  // the state-only pass is complete
     {
+      const float* init_sum = reinterpret_cast<const float*>(smem + kOffInit);
       for (int mt = 0; mt < 3; ++mt) {
         const int f = mt * 128 + row;
         if (mt == 2 && qd == 3) continue;  // rows 352..383 are never used
@@ -360,13 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           }
           val[64] = prm.z0[rowi];
         }
-        if (!kStateOnly && f < kSCRows && prm.deltas != nullptr) {
-          const float* d0 = prm.deltas + static_cast<int64_t>(bh) * prm.nseg * kSCRows * kSCCols;
-          for (int sp = 0; sp < seg; ++sp) {
-            const float* ds = d0 + static_cast<int64_t>(sp) * kSCRows * kSCCols;
+        if (init_copy && f < kSCRows) {
 #pragma unroll
-            for (int e = 0; e < 65; ++e) val[e] += ds[sc_index(f, e)];
-          }
+          for (int e = 0; e < 65; ++e) val[e] += init_sum[sc_index(f, e)];
         }
 #pragma unroll
         for (int blk = 0; blk < 5; ++blk) {
@@ -376,21 +402,42 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           tmem_st16(tmem + lane_off + kTS + mt * kN + 16 * blk, rr);
         }
         if constexpr (!kStateOnly) {
-          if (f < kNF) {
-            const uint32_t base = sS + (f >> 3) * kLBO_SV + (f & 7) * 16;
+          if (f == kNF) {
 #pragma unroll
-            for (int ng = 0; ng < kNG; ++ng)
-              st_shared_v4(base + ng * 128, pack_bf16x2(val[8 * ng], val[8 * ng + 1]),
-                           pack_bf16x2(val[8 * ng + 2], val[8 * ng + 3]),
-                           pack_bf16x2(val[8 * ng + 4], val[8 * ng + 5]),
-                           pack_bf16x2(val[8 * ng + 6], val[8 * ng + 7]));
-          } else if (f == kNF) {
-#pragma unroll
-            for (int e = 0; e < 65; ++e) m.vs[e] = val[e];
+            for (int e = 0; e < 65; ++e) m.vs[0][e] = val[e];
           }
         }
       }
       tmem_st_wait();
+      if constexpr (!kStateOnly) {
+        // The bf16 snapshot for the first chunk, from TMEM: its buffer overlaps
+        // the initial-state copy, which every epilogue thread has read by now.
+        tc_fence_before();
+        epi_sync();
+        tc_fence_after();
+        if (lane == 0 && init_copy) mbar_arrive(&m.bar[kInitDone]);
+        for (int mt = 0; mt < 3; ++mt) {
+          const int f = mt * 128 + row;
+          if (f >= kNF) continue;
+          float val[72];
+#pragma unroll
+          for (int blk = 0; blk < 5; ++blk) {
+            float x[16];
+            tmem_ld16(tmem + lane_off + kTS + mt * kN + 16 * blk, x);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (16 * blk + i < 72) val[16 * blk + i] = x[i];
+          }
+          tmem_ld_wait();
+          const uint32_t base = sS + (f >> 3) * kLBO_SV + (f & 7) * 16;
+#pragma unroll
+          for (int ng = 0; ng < kNG; ++ng)
+            st_shared_v4(base + ng * 128, pack_bf16x2(val[8 * ng], val[8 * ng + 1]),
+                         pack_bf16x2(val[8 * ng + 2], val[8 * ng + 3]),
+                         pack_bf16x2(val[8 * ng + 4], val[8 * ng + 5]),
+                         pack_bf16x2(val[8 * ng + 6], val[8 * ng + 7]));
+        }
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       epi_sync();
@@ -437,79 +484,14 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&m.bar[kPTilde]);
 
-        // E3: outputs of this chunk (state row 320 in m.vs is still the pre-chunk one).
-        // Each row is normalised in registers and staged in the free snapshot
-        // buffer; the four warps then copy the staged tile out with coalesced
-        // 16-byte stores (each warp instruction writes whole rows).
-        wait_bar(m, kPVDone, ci & 1);
-        tc_fence_after();
-        const int nrow = min(kC, prm.T - tok0);
-        {
-          float ov[80];
-#pragma unroll
-          for (int blk = 0; blk < 5; ++blk) {
-            float x[16];
-            tmem_ld16(tmem + lane_off + kTO + 16 * blk, x);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) ov[16 * blk + i] = x[i];
-          }
-          tmem_ld_wait();
-          if (row < nrow) {
-            const float den = ov[64] + 64.0f * m.vs[64] + m.a0[64];
-            const float inv = prm.normalize ? 1.0f / (den + prm.eps) : 1.0f;
-            const float4* vs4 = reinterpret_cast<const float4*>(m.vs);
-            const float4* a04 = reinterpret_cast<const float4*>(m.a0);
-#pragma unroll
-            for (int e4 = 0; e4 < 16; ++e4) {
-              const float4 w = vs4[e4];
-              const float4 c = a04[e4];
-              ov[4 * e4 + 0] = (fmaf(64.0f, w.x, ov[4 * e4 + 0]) + c.x) * inv;
-              ov[4 * e4 + 1] = (fmaf(64.0f, w.y, ov[4 * e4 + 1]) + c.y) * inv;
-              ov[4 * e4 + 2] = (fmaf(64.0f, w.z, ov[4 * e4 + 2]) + c.z) * inv;
-              ov[4 * e4 + 3] = (fmaf(64.0f, w.w, ov[4 * e4 + 3]) + c.w) * inv;
-            }
-            if (prm.out_bf16) {
-              const uint32_t srow = sS + row * kStagePitchH;
-#pragma unroll
-              for (int e8 = 0; e8 < 8; ++e8)
-                st_shared_v4(srow + 16 * e8, pack_bf16x2(ov[8 * e8], ov[8 * e8 + 1]),
-                             pack_bf16x2(ov[8 * e8 + 2], ov[8 * e8 + 3]),
-                             pack_bf16x2(ov[8 * e8 + 4], ov[8 * e8 + 5]),
-                             pack_bf16x2(ov[8 * e8 + 6], ov[8 * e8 + 7]));
-            } else {
-              const uint32_t srow = sS + row * kStagePitch;
-#pragma unroll
-              for (int e4 = 0; e4 < 16; ++e4)
-                st_shared_v4(srow + 16 * e4, __float_as_uint(ov[4 * e4]),
-                             __float_as_uint(ov[4 * e4 + 1]), __float_as_uint(ov[4 * e4 + 2]),
-                             __float_as_uint(ov[4 * e4 + 3]));
-            }
-            if (prm.Dn != nullptr) prm.Dn[seq_row0 + orow(prm, tok0 + row)] = den;
-          }
-        }
-        tc_fence_before();
-        epi_sync();  // every row staged, every thread done with m.vs and O
-        if (lane == 0) mbar_arrive(&m.bar[kOFree]);
-        {
-          // 16-byte pieces: piece p is column piece p % per_row of staged row p / per_row.
-          const int et = tid - 32 * kEpiWarp0;
-          const int lg = prm.out_bf16 ? 3 : 4;  // log2 of pieces per row
-          const int pitch = prm.out_bf16 ? kStagePitchH : kStagePitch;
-          unsigned char* obase = reinterpret_cast<unsigned char*>(prm.o);
-          const int64_t row_bytes = int64_t{16} << lg;
-          for (int pc = et; pc < (nrow << lg); pc += 128) {
-            const int rr = pc >> lg, cc = pc & ((1 << lg) - 1);
-            const uint4 val = *reinterpret_cast<const uint4*>(smem + kOffS + rr * pitch + 16 * cc);
-            *reinterpret_cast<uint4*>(obase + (seq_row0 + orow(prm, tok0 + rr)) * row_bytes +
-                                      16 * cc) = val;
-          }
-        }
-        epi_sync();  // staged tile read out before the snapshot overwrites it
-
-        // E2: snapshot of the state after this chunk, for the next chunk.
+        // E2: snapshot of the state after this chunk, for the next chunk's
+        // Phi(Q)[S|z] (StateDone also covers this chunk's Phi(Q)[S|z], the
+        // snapshot buffer's last reader).  It comes before the outputs so that
+        // the next chunk's tensor-core work does not wait for their stores.
         wait_bar(m, kStateDone, ci & 1);
         tc_fence_after();
         if (ci + 1 < nloc) {
+          epi_sync();  // every thread's outputs of the previous chunk have read vs[(ci + 1) & 1]
           for (int mt = 0; mt < 3; ++mt) {
             if (mt == 2 && qd >= 3) continue;
             const int f = mt * 128 + row;
@@ -533,13 +515,67 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
                              pack_bf16x2(val[8 * ng + 6], val[8 * ng + 7]));
             } else if (f == kNF) {
 #pragma unroll
-              for (int e = 0; e < 65; ++e) m.vs[e] = val[e];
+              for (int e = 0; e < 65; ++e) m.vs[(ci + 1) & 1][e] = val[e];
             }
           }
           fence_proxy_async_smem();
           tc_fence_before();
           epi_sync();
           if (lane == 0) mbar_arrive(&m.bar[kSnapReady]);
+        }
+
+        // E3: outputs of this chunk (vs[ci & 1] holds state row 320 before it).
+        // Each warp hands the accumulator back as soon as its rows are in
+        // registers; each thread then normalises its row and stores it.
+        wait_bar(m, kPVDone, ci & 1);
+        tc_fence_after();
+        const int nrow = min(kC, prm.T - tok0);
+        {
+          float ov[80];
+#pragma unroll
+          for (int blk = 0; blk < 5; ++blk) {
+            float x[16];
+            tmem_ld16(tmem + lane_off + kTO + 16 * blk, x);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[16 * blk + i] = x[i];
+          }
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&m.bar[kOFree]);
+          if (row < nrow) {
+            const float* vsc = m.vs[ci & 1];
+            const float den = ov[64] + 64.0f * vsc[64] + m.a0[64];
+            const float inv = prm.normalize ? 1.0f / (den + prm.eps) : 1.0f;
+            const float4* vs4 = reinterpret_cast<const float4*>(vsc);
+            const float4* a04 = reinterpret_cast<const float4*>(m.a0);
+#pragma unroll
+            for (int e4 = 0; e4 < 16; ++e4) {
+              const float4 w = vs4[e4];
+              const float4 c = a04[e4];
+              ov[4 * e4 + 0] = (fmaf(64.0f, w.x, ov[4 * e4 + 0]) + c.x) * inv;
+              ov[4 * e4 + 1] = (fmaf(64.0f, w.y, ov[4 * e4 + 1]) + c.y) * inv;
+              ov[4 * e4 + 2] = (fmaf(64.0f, w.z, ov[4 * e4 + 2]) + c.z) * inv;
+              ov[4 * e4 + 3] = (fmaf(64.0f, w.w, ov[4 * e4 + 3]) + c.w) * inv;
+            }
+            const int64_t grow = seq_row0 + orow(prm, tok0 + row);
+            if (prm.out_bf16) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(
+                               static_cast<void*>(prm.o)) + grow * kD);
+#pragma unroll
+              for (int e8 = 0; e8 < 8; ++e8)
+                dst[e8] = make_uint4(pack_bf16x2(ov[8 * e8], ov[8 * e8 + 1]),
+                                     pack_bf16x2(ov[8 * e8 + 2], ov[8 * e8 + 3]),
+                                     pack_bf16x2(ov[8 * e8 + 4], ov[8 * e8 + 5]),
+                                     pack_bf16x2(ov[8 * e8 + 6], ov[8 * e8 + 7]));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(prm.o + grow * kD);
+#pragma unroll
+              for (int e4 = 0; e4 < 16; ++e4)
+                dst[e4] = make_float4(ov[4 * e4], ov[4 * e4 + 1], ov[4 * e4 + 2], ov[4 * e4 + 3]);
+            }
+            if (prm.Dn != nullptr) prm.Dn[grow] = den;
+          }
         }
       }
     } else {
@@ -583,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
             prm.z_out[static_cast<int64_t>(bh) * 384 + 6 * a + c] = val[64];
           } else if (f == kNF) {
 #pragma unroll
-            for (int e = 0; e < 65; ++e) m.vs[e] = val[e];
+            for (int e = 0; e < 65; ++e) m.vs[nloc & 1][e] = val[e];
           }
         }
       }
@@ -596,10 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           const int64_t rowi = static_cast<int64_t>(bh) * 384 + 6 * a;
           if (e < 64) {
             const float base = prm.S0 ? prm.S0[rowi * 64 + e] : 0.f;
-            prm.S_out[rowi * 64 + e] = base + m.vs[e];
+            prm.S_out[rowi * 64 + e] = base + m.vs[nloc & 1][e];
           } else {
             const float base = prm.z0 ? prm.z0[rowi] : 0.f;
-            prm.z_out[rowi] = base + m.vs[64];
+            prm.z_out[rowi] = base + m.vs[nloc & 1][64];
           }
         }
       }
