@@ -261,7 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       st_shared_v4(sV + kg * kLBO_SV + 8 * 128 + row * 16, 0x3F80u, 0u, 0u, 0u);
     }
   }
-  if (tid < 8) st_shared_v4(sV + 16 * kLBO_SV + 16 * tid, 0u, 0u, 0u, 0u);  // over-read pad
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -485,10 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         if (lane == 0) mbar_arrive(&m.bar[kPTilde]);
 
         // E2: snapshot of the state after this chunk, for the next chunk's
-        // Phi(Q)[S|z] (StateDone also covers this chunk's Phi(Q)[S|z], the
-        // snapshot buffer's last reader).  It comes before the outputs so that
-        // the next chunk's tensor-core work does not wait for their stores.
-        wait_bar(m, kStateDone, ci & 1);
+        // Phi(Q)[S|z] (QFree: this chunk's Phi(Q)[S|z], the snapshot buffer's
+        // last reader, and the state update before it are complete).  It comes
+        // before the outputs so that the next chunk's tensor-core work does not
+        // wait for their stores.
+        wait_bar(m, kQFree, ci & 1);
         tc_fence_after();
         if (ci + 1 < nloc) {
           epi_sync();  // every thread's outputs of the previous chunk have read vs[(ci + 1) & 1]
@@ -712,23 +712,17 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         wait_bar(m, kFeatK, ci & 1);
       }
       tc_fence_after();
+      // Order: scores, state update (the key buffer is free after it), then
+      // Phi(Q)[S|z] from the previous chunk's snapshot, then P~[V|1].
       if constexpr (!kStateOnly) {
 #pragma unroll
         for (int s = 0; s < 20; ++s)
           mma_ss(tmem + kTP, dQl + 16 * s, dKbl + 16 * s, idQK, s > 0);
         mma_commit(&m.bar[kPFull]);
-        wait_bar(m, kSnapReady, ci & 1);  // bf16 state snapshot of the previous chunk
-        wait_bar(m, kOFree, ci & 1);      // previous outputs drained from TMEM
-        tc_fence_after();
-        asm volatile("" : "+l"(dQl), "+l"(dSl));
-#pragma unroll
-        for (int s = 0; s < 20; ++s)
-          mma_ss(tmem + kTO, dQl + 16 * s, dSl + (2 * kLBO_SV / 16) * s, idIN, s > 0);
-        mma_commit(&m.bar[kQFree]);
-      } else if (ci == 0) {
-        wait_bar(m, kSnapReady, 0);  // initial state is in TMEM
-        tc_fence_after();
       }
+      // the state may change once the previous snapshot has been taken (at
+      // ci = 0: once the initial state is in TMEM)
+      if (!kStateOnly || ci == 0) wait_bar(m, kSnapReady, ci & 1);
       if constexpr (kStateOnly)
         wait_bar(m, (ci & 1) ? kFeatV1 : kFeatV, (ci >> 1) & 1);
       else
@@ -743,6 +737,13 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
                  dVl + (2 * kLBO_SV / 16) * s, idST, true);
       mma_commit(&m.bar[(kStateOnly && (ci & 1)) ? kStateDone1 : kStateDone]);
       if constexpr (!kStateOnly) {
+        wait_bar(m, kOFree, ci & 1);      // previous outputs drained from TMEM
+        tc_fence_after();
+        asm volatile("" : "+l"(dQl), "+l"(dSl));
+#pragma unroll
+        for (int s = 0; s < 20; ++s)
+          mma_ss(tmem + kTO, dQl + 16 * s, dSl + (2 * kLBO_SV / 16) * s, idIN, s > 0);
+        mma_commit(&m.bar[kQFree]);
         wait_bar(m, kPTilde, ci & 1);
         tc_fence_after();
         asm volatile("" : "+l"(dVl));

@@ -227,6 +227,77 @@ def sanatan_chunk_fwd(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=N
     return o, D, S, z
 
 
+class HostForward:
+    """sanatan_chunk_fwd over pinned HOST tensors q, k, v (bf16 [B, H, T, d])
+    into a pinned host o (f32 [B, H, T, dv]), pipelined over slices of the
+    batch: the host-to-device copy of slice i + 1, the attention of slice i
+    and the device-to-host copy of slice i - 1 run on three CUDA streams at
+    once (one cudaMemcpyAsync per tensor slice).  Device staging (two slices
+    of q, k, v and o, and the workspace) is allocated once, here, with torch;
+    each call then allocates nothing.  The calling stream waits for the last
+    copy, so `o` is complete once that stream is synchronised."""
+
+    def __init__(self, B, H, T, d=64, dv=64, slices=4, device=None):
+        if B % slices:
+            raise ValueError("B must be a multiple of slices")
+        self.dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.B, self.H, self.T, self.d, self.dv, self.n = B, H, T, d, dv, slices
+        b = B // slices
+        mk = lambda dt, last: [torch.empty(b, H, T, last, dtype=dt, device=self.dev)  # noqa: E731
+                               for _ in range(2)]
+        self.q, self.k, self.v = mk(torch.bfloat16, d), mk(torch.bfloat16, d), mk(torch.bfloat16, dv)
+        self.o = mk(torch.float32, dv)
+        ws = chunk_fwd_workspace_size(b, H, T, d, dv)
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.dev)
+        self.s_in = torch.cuda.Stream(self.dev)
+        self.s_run = torch.cuda.Stream(self.dev)
+        self.s_out = torch.cuda.Stream(self.dev)
+        self.loaded = [torch.cuda.Event() for _ in range(2)]
+        self.done = [torch.cuda.Event() for _ in range(2)]
+        self.freed_in = [torch.cuda.Event() for _ in range(2)]
+        self.freed_out = [torch.cuda.Event() for _ in range(2)]
+
+    def __call__(self, qh, kh, vh, gamma, omega, phi, oh, pos0=0, eps=0.0):
+        for t, n in ((qh, "q"), (kh, "k"), (vh, "v"), (oh, "o")):
+            if t.is_cuda or not t.is_pinned():
+                raise ValueError(f"{n} must be a pinned host tensor")
+        b = self.B // self.n
+        caller = torch.cuda.current_stream(self.dev)
+        for st in (self.s_in, self.s_run, self.s_out):
+            st.wait_stream(caller)
+        for i in range(self.n + 2):
+            j = i % 2
+            if i < self.n:                      # H2D of slice i into buffer j
+                with torch.cuda.stream(self.s_in):
+                    if i >= 2:
+                        self.s_in.wait_event(self.freed_in[j])
+                    sl = slice(i * b, (i + 1) * b)
+                    self.q[j].copy_(qh[sl], non_blocking=True)
+                    self.k[j].copy_(kh[sl], non_blocking=True)
+                    self.v[j].copy_(vh[sl], non_blocking=True)
+                    self.loaded[j].record(self.s_in)
+            if 1 <= i <= self.n:                # attention of slice i - 1
+                jj = (i - 1) % 2
+                with torch.cuda.stream(self.s_run):
+                    self.s_run.wait_event(self.loaded[jj])
+                    if i - 1 >= 2:
+                        self.s_run.wait_event(self.freed_out[jj])
+                    sanatan_chunk_fwd(self.q[jj], self.k[jj], self.v[jj], gamma, omega, phi,
+                                      pos0=pos0, eps=eps, want_D=False, out=self.o[jj],
+                                      workspace=self.ws)
+                    self.freed_in[jj].record(self.s_run)
+                    self.done[jj].record(self.s_run)
+            if i >= 2:                          # D2H of slice i - 2
+                jj = (i - 2) % 2
+                with torch.cuda.stream(self.s_out):
+                    self.s_out.wait_event(self.done[jj])
+                    sl = slice((i - 2) * b, (i - 1) * b)
+                    oh[sl].copy_(self.o[jj], non_blocking=True)
+                    self.freed_out[jj].record(self.s_out)
+        caller.wait_stream(self.s_out)
+        return oh
+
+
 def sanatan_chunk_fwd_noalloc(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None,
                               want_D=True, want_state=False):
     """sanatan_chunk_fwd for bf16 inputs without a workspace: the library uses

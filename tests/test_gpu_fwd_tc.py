@@ -125,3 +125,20 @@ def test_training_shape_forward_full_size_whole_tensor():
     assert S.chunk_fwd_plan(8, 12, 4096)[0] >= 2
     x = W.make(W.TRAIN, device="cpu")
     _whole_tensor_check(x)
+
+
+@pytest.mark.parametrize("slices", [1, 2, 4])
+def test_host_forward_pipeline(slices):
+    """HostForward: pinned host q, k, v in, host o out, pipelined over batch
+    slices on three streams; the outputs are those of the definition."""
+    x = W.make(W.LAYER, device="cpu", B=4, H=2, T=300)
+    hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
+    ho = torch.full((4, 2, 300, 64), float("nan")).pin_memory()
+    g = to_dev(x, ("gamma", "omega", "phi"))
+    hf = S.HostForward(4, 2, 300, slices=slices)
+    for _ in range(2):
+        hf(hq, hk, hv, g["gamma"], g["omega"], g["phi"], ho)
+        torch.cuda.current_stream().synchronize()
+        S.device_status()
+        o_ref, _ = O.attn_quadratic(**ref_args(x))
+        assert max_abs(f64(ho), o_ref) <= TOL_BF16
