@@ -1,6 +1,7 @@
 """Float64 CPU oracle for SANATAN root-parity gated angular attention: the
 feature map, the p = 1 causal attention in its quadratic and recurrent forms,
-the power-sharpened attention of eq. (8) at integer p, and their gradients.
+the power-sharpened attention of eq. (8) at integer p, and their gradients,
+and the four- and three-channel ablation kernels.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
@@ -395,6 +396,96 @@ def attn_power_backward(q, k, v, gamma, omega, phi, dO, p, pos0=0, eps=0.0):
     dk, dg_k, dom_k, dph_k = _feature_vjp(_feature_parts(k, gamma, omega, phi, pos0), dpk)
     return dict(dq=dq, dk=dk, dv=dv, dgamma=dg_q + dg_k, domega=dom_q + dom_k,
                 dphi=dph_q + dph_k)
+
+
+# ---------------------------------------------------------------------------
+# Ablation kernels: the four-channel map (Notes §2.5, "四通道为什么是另一种核")
+# and the three-channel map of the root-ablation (Notes §4.4, the remark on the
+# three-channel comparison), both used in the power-sharpened parallel form
+# ---------------------------------------------------------------------------
+
+
+def features4_from_angles(theta_rot, r):
+    """Four-channel block per dimension (Notes §2.5): [1, r, r cos th_rot,
+    r sin th_rot] -- the six-channel block without the separate cos, sin --
+    concatenated so that channel c of dimension a sits at 4a + c."""
+    c = np.cos(theta_rot)
+    s = np.sin(theta_rot)
+    one = np.ones_like(c)
+    blk = np.stack([one, r, r * c, r * s], axis=-1)
+    return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * 4,))
+
+
+def features3_from_angles(theta_rot):
+    """Three-channel block per dimension (Notes §4.4): [1, cos th_rot,
+    sin th_rot] (no root channel), channel c of dimension a at 3a + c."""
+    c = np.cos(theta_rot)
+    s = np.sin(theta_rot)
+    blk = np.stack([np.ones_like(c), c, s], axis=-1)
+    return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * 3,))
+
+
+def featurize_ablation(u, gamma, omega, phi, channels, pos0=0):
+    """The four- or three-channel features of a [B, H, T, d] tensor, through
+    the same squash, soft root (un-rotated angle) and rotation as ``featurize``."""
+    u = np.asarray(u, dtype=np.float64)
+    B, H, T, d = u.shape
+    g = np.asarray(gamma, dtype=np.float64).reshape(1, H, 1, 1)
+    om = np.asarray(omega, dtype=np.float64).reshape(1, H, 1, d)
+    ph = np.asarray(phi, dtype=np.float64).reshape(1, H, 1, d)
+    t = positions(T, pos0).astype(np.float64).reshape(1, 1, T, 1)
+    theta = squash(u)
+    th_rot = rotate(theta, t, ph)
+    if channels == 4:
+        return features4_from_angles(th_rot, soft_root(theta, g, om))
+    if channels == 3:
+        return features3_from_angles(th_rot)
+    raise ValueError("channels must be 4 or 3")
+
+
+def ablation_scale(channels, d, shift=0.0):
+    """The score scale c of the ablation weights: the largest score the map
+    can give, 3d for the four-channel kernel (each dimension at most
+    1 + 1 * 2) and 2d + shift for the three-channel one (d + sum cos <= 2d,
+    the printed ablation divides s3 + d by 3d).  It cancels at eps = 0."""
+    return 3.0 * d if channels == 4 else 2.0 * d + shift
+
+
+def attn_ablation(q, k, v, gamma, omega, phi, p, channels, shift=0.0, pos0=0, eps=0.0):
+    """Power-sharpened causal attention with an ablation kernel:
+
+        four channels (Notes §2.5): s_tj = Phi4(q_t).Phi4(k_j), which can be
+            negative; the total score is clipped, max(s, 0), before the power;
+        three channels (Notes §4.4): s_tj = Phi3(q_t).Phi3(k_j) = d + sum_a
+            cos(dtheta_a), in [0, 2d], plus ``shift`` (the printed ablation adds
+            d; the fair ablation the notes ask for has shift 0);
+
+        w_tj = [j <= t] (max(s_tj + shift, 0) / c)^p,   c = ablation_scale(...),
+        o_t = sum_j w_tj v_j / (sum_j w_tj + eps).
+
+    ``shift`` applies to the three-channel kernel only.  Returns o [B,H,T,dv]
+    and D [B,H,T] = sum_j w_tj (without eps)."""
+    p = int(p)
+    if p < 1:
+        raise ValueError("p must be a positive integer")
+    if channels == 4 and shift != 0.0:
+        raise ValueError("the four-channel kernel takes no shift")
+    pq = featurize_ablation(q, gamma, omega, phi, channels, pos0)
+    pk = featurize_ablation(k, gamma, omega, phi, channels, pos0)
+    v = _heads(v)
+    B, H, T, F = pq.shape
+    c = ablation_scale(channels, F // channels, shift)
+    mask = np.tril(np.ones((T, T)))
+    o = np.zeros((B, H, T, v.shape[-1]))
+    D = np.zeros((B, H, T))
+    for b in range(B):
+        for h in range(H):
+            s = pair_kernel(pq[b, h], pk[b, h]) + shift
+            w = (np.maximum(s, 0.0) / c) ** p * mask
+            den = w.sum(axis=1)
+            o[b, h] = (w @ v[b, h]) / (den + eps)[:, None]
+            D[b, h] = den
+    return o, D
 
 
 # ---------------------------------------------------------------------------

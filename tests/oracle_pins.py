@@ -426,3 +426,128 @@ ALL_CHECKS = [
     check_power_backward_finite_differences,
     check_power_one_backward_is_linear_backward,
 ]
+
+
+# --------------------------------------------------------------------------
+# Ablation kernels: four channels (Notes §2.5) and three channels (Notes §4.4)
+# --------------------------------------------------------------------------
+
+def _angles(c, u, pos0=0):
+    """Un-rotated and rotated angles and roots of one head, from the pages'
+    formulas typed directly (not through the oracle's feature functions)."""
+    th = math.pi * u / (1.0 + np.abs(u))
+    t = (np.arange(u.shape[-2]) + pos0)[:, None]
+    om, ph, g = c["omega"][0], c["phi"][0], c["gamma"][0]
+    r = np.tanh(g * (np.cos(th + om) - np.sin(th + om)))
+    return th + t * ph, r
+
+
+def check_four_channel_kernel_closed_form():
+    # Phi4(q).Phi4(k) = sum_a 1 + r_q r_k (1 + cos(dtheta_a)) (Notes §2.5)
+    c = _small_case(seed=11, T=7, d=5)
+    pq = O.featurize_ablation(c["q"], c["gamma"], c["omega"], c["phi"], 4)[0, 0]
+    pk = O.featurize_ablation(c["k"], c["gamma"], c["omega"], c["phi"], 4)[0, 0]
+    tq, rq = _angles(c, c["q"][0, 0])
+    tk, rk = _angles(c, c["k"][0, 0])
+    for i in range(7):
+        for j in range(7):
+            want = np.sum(1.0 + rq[i] * rk[j] * (1.0 + np.cos(tq[i] - tk[j])))
+            assert abs(pq[i] @ pk[j] - want) < 1e-12
+    assert pq.shape[-1] == 4 * 5
+
+
+def check_four_channel_hard_roots():
+    # matching hard roots give 2 + cos(dtheta) in [1, 3], mismatched -cos(dtheta)
+    # in [-1, 1] (Notes §2.5)
+    dth = np.linspace(-math.pi, math.pi, 101)
+    for rq, rk, want in ((1.0, 1.0, 2.0 + np.cos(dth)), (-1.0, -1.0, 2.0 + np.cos(dth)),
+                         (1.0, -1.0, -np.cos(dth)), (-1.0, 1.0, -np.cos(dth))):
+        fq = O.features4_from_angles(dth[:, None] * 0 + dth[:, None], np.full((101, 1), rq))
+        fk = O.features4_from_angles(np.zeros((101, 1)), np.full((101, 1), rk))
+        got = np.sum(fq * fk, axis=-1)
+        assert np.allclose(got, want, atol=1e-14)
+
+
+def check_four_channel_clip():
+    # A key whose total four-channel score is negative gets weight zero (the
+    # max(s, 0) before the power, Notes §2.5): query 1 = key 0 (matched roots,
+    # score 3d) and key 1 with the opposite root (score about -0.98 d), so
+    # o_1 = v_0 exactly.
+    d = 4
+    th = math.pi - 0.1
+    u = th / (math.pi - th)                      # squash(u) = th
+    q = np.array([[[[0.3] * d, [u] * d]]])
+    k = np.array([[[[u] * d, [-u] * d]]])
+    v = np.array([[[[1.0, 2.0], [-5.0, 7.0]]]])
+    gamma = np.array([100.0])
+    omega = np.full((1, d), math.pi / 4)
+    phi = np.zeros((1, d))
+    pq = O.featurize_ablation(q, gamma, omega, phi, 4)[0, 0]
+    pk = O.featurize_ablation(k, gamma, omega, phi, 4)[0, 0]
+    assert pq[1] @ pk[1] < -0.9 * d and abs(pq[1] @ pk[0] - 3 * d) < 1e-6
+    for p in (1, 2, 4):
+        o, D = O.attn_ablation(q, k, v, gamma, omega, phi, p, 4)
+        assert np.allclose(o[0, 0, 1], v[0, 0, 0], atol=1e-12), (p, o[0, 0, 1])
+        assert abs(D[0, 0, 1] - 1.0) < 1e-6     # (3d / 3d)^p from key 0 alone
+
+
+def check_three_channel_score_range_and_shift():
+    # s3 = d + sum_a cos(dtheta_a), in [0, 2d] (Notes §4.4, not the [-d, 3d] of
+    # the printed comment); the printed ablation adds d and divides by 3d
+    c = _small_case(seed=12, T=11, d=6)
+    pq = O.featurize_ablation(c["q"], c["gamma"], c["omega"], c["phi"], 3)[0, 0]
+    pk = O.featurize_ablation(c["k"], c["gamma"], c["omega"], c["phi"], 3)[0, 0]
+    tq, _ = _angles(c, c["q"][0, 0])
+    tk, _ = _angles(c, c["k"][0, 0])
+    s = pq @ pk.T
+    want = 6 + np.cos(tq[:, None, :] - tk[None, :, :]).sum(axis=-1)
+    assert np.allclose(s, want, atol=1e-12)
+    assert s.min() >= 0 and s.max() <= 12
+    o0, D0 = O.attn_ablation(**c, p=2, channels=3)
+    o1, D1 = O.attn_ablation(**c, p=2, channels=3, shift=6.0)
+    mask = np.tril(np.ones((11, 11)))
+    w = ((s + 6.0) / 18.0) ** 2 * mask
+    assert np.allclose(D1[0, 0], w.sum(1), atol=1e-12)
+    assert np.allclose(o1[0, 0], (w @ c["v"][0, 0]) / w.sum(1)[:, None], atol=1e-12)
+    assert not np.allclose(o0, o1, atol=1e-3)    # the shift changes the distribution
+
+
+def check_three_channel_p1_is_linear_attention():
+    # without shift and clip the three-channel p = 1 form is a linear attention
+    # over Phi3: the recurrence S += Phi3(k) v^T, z += Phi3(k) gives the same o
+    c = _small_case(seed=13, B=2, T=10, d=3)
+    o, D = O.attn_ablation(**c, p=1, channels=3, eps=0.7)
+    pq = O.featurize_ablation(c["q"], c["gamma"], c["omega"], c["phi"], 3)
+    pk = O.featurize_ablation(c["k"], c["gamma"], c["omega"], c["phi"], 3)
+    B, H, T, F = pq.shape
+    Sx = np.zeros((B, H, F, 2))
+    zx = np.zeros((B, H, F))
+    for t in range(T):
+        Sx += pk[:, :, t, :, None] * c["v"][:, :, t, None, :]
+        zx += pk[:, :, t]
+        num = np.einsum("bhf,bhfe->bhe", pq[:, :, t], Sx)
+        den = np.einsum("bhf,bhf->bh", pq[:, :, t], zx)
+        assert np.allclose(o[:, :, t], num / (den + 0.7 * 2 * 3)[..., None], atol=1e-12)
+        assert np.allclose(D[:, :, t] * 6, den, atol=1e-12)
+
+
+def check_ablation_single_token_and_constant_values():
+    for ch in (4, 3):
+        c = _small_case(seed=14, T=1)
+        o, _ = O.attn_ablation(**c, p=2, channels=ch)
+        assert np.allclose(o, c["v"], atol=1e-12)
+        c = _small_case(seed=15, T=8)
+        c["v"] = np.broadcast_to(np.array([0.5, -2.0]), c["v"].shape).copy()
+        o, _ = O.attn_ablation(**c, p=3, channels=ch)
+        # the four-channel scores of these inputs are positive, so no row is empty
+        assert np.allclose(o, c["v"], atol=1e-12)
+
+
+ALL_CHECKS += [
+    check_four_channel_kernel_closed_form,
+    check_four_channel_hard_roots,
+    check_four_channel_clip,
+    check_three_channel_score_range_and_shift,
+    check_three_channel_p1_is_linear_attention,
+    check_ablation_single_token_and_constant_values,
+]

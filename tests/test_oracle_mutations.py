@@ -13,7 +13,8 @@ import oracle_pins as P
 _orig = {n: getattr(O, n) for n in ("squash", "soft_root", "rotate", "features_from_angles",
                                      "attn_quadratic", "attn_recurrent", "attn_backward",
                                      "_feature_vjp", "state_bytes", "featurize", "attn_power",
-                                     "attn_power_backward")}
+                                     "attn_power_backward", "attn_ablation",
+                                     "features4_from_angles", "ablation_scale")}
 
 
 def m_squash_no_abs(u):
@@ -190,6 +191,39 @@ def _power_bwd_mutant(kind):
     return f
 
 
+def _ablation_mutant(kind):
+    orig = _orig["attn_ablation"]
+
+    def f(q, k, v, gamma, omega, phi, p, channels, shift=0.0, pos0=0, eps=0.0):
+        if kind == "no_clip" and channels == 4:
+            pq = O.featurize_ablation(q, gamma, omega, phi, 4, pos0)
+            pk = O.featurize_ablation(k, gamma, omega, phi, 4, pos0)
+            T = pq.shape[2]
+            mask = np.tril(np.ones((T, T)))
+            o = np.zeros(np.asarray(v).shape)
+            D = np.zeros(pq.shape[:3])
+            for b in range(pq.shape[0]):
+                for h in range(pq.shape[1]):
+                    w = ((pq[b, h] @ pk[b, h].T) / (3.0 * (pq.shape[-1] // 4))) ** p * mask
+                    D[b, h] = w.sum(1)
+                    o[b, h] = (w @ np.asarray(v)[b, h]) / (D[b, h] + eps)[:, None]
+            return o, D
+        if kind == "shift_ignored":
+            return orig(q, k, v, gamma, omega, phi, p, channels, 0.0, pos0, eps)
+        return orig(q, k, v, gamma, omega, phi, p, channels, shift, pos0, eps)
+    return f
+
+
+def m_features4_unrooted(theta_rot, r):
+    c, s = np.cos(theta_rot), np.sin(theta_rot)
+    blk = np.stack([np.ones_like(c), r, c, s], axis=-1)
+    return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * 4,))
+
+
+def m_ablation_scale_4d(channels, d, shift=0.0):
+    return 4.0 * d
+
+
 MUTANTS = {
     "squash_no_abs": ("squash", m_squash_no_abs),
     "squash_square": ("squash", m_squash_square),
@@ -213,6 +247,10 @@ MUTANTS = {
     "power_without_4d_scale": ("attn_power", _power_mutant("no_scale")),
     "power_backward_no_chain_factor": ("attn_power_backward", _power_bwd_mutant("no_chain_factor")),
     "power_backward_dv_unpowered": ("attn_power_backward", _power_bwd_mutant("dv_unpowered")),
+    "four_channel_without_clip": ("attn_ablation", _ablation_mutant("no_clip")),
+    "three_channel_shift_ignored": ("attn_ablation", _ablation_mutant("shift_ignored")),
+    "four_channel_angles_unrooted": ("features4_from_angles", m_features4_unrooted),
+    "ablation_scale_4d": ("ablation_scale", m_ablation_scale_4d),
 }
 
 
