@@ -254,6 +254,43 @@ int sanatan_power_fwd(const void* q, const void* k, const void* v, const float* 
   return from_cuda(pow_fwd_tc_launch(a, static_cast<cudaStream_t>(stream)));
 }
 
+int sanatan_ablation_fwd(const void* q, const void* k, const void* v, const float* gamma,
+                         const float* omega, const float* phi, int B, int H, int T, int d,
+                         int dv, int64_t pos0, int p, int channels, float shift, float eps,
+                         float* o, float* D, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  if (int s = check_sizes(B, H, T, d, dv)) return s;
+  if (channels != 3 && channels != 4) return SANATAN_ERR_INVALID;
+  if (!(shift >= 0.0f) || (channels == 4 && shift != 0.0f)) return SANATAN_ERR_INVALID;
+  if (p < 1) return SANATAN_ERR_INVALID;
+  if (p != 1 && p != 2 && p != 4) return SANATAN_ERR_UNSUPPORTED;
+  if (!ok_nullable(D)) return SANATAN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * H == 0 || T == 0) return SANATAN_OK;
+  if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(o) || !ok_ptr(workspace))
+    return SANATAN_ERR_INVALID;
+  if (int s = check_params(gamma, omega, phi)) return s;
+  if (workspace_bytes < pow_fwd_tc_workspace_bytes(B, H, T)) return SANATAN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * H * ((T + 127) / 128) > 0x3fffffffLL) return SANATAN_ERR_UNSUPPORTED;
+  if (int s = check_arch()) return s;
+  PowFwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.gamma = gamma;
+  a.omega = omega;
+  a.phi = phi;
+  a.B = B;
+  a.H = H;
+  a.T = T;
+  a.pos0 = pos0;
+  a.p = p;
+  a.eps = eps;
+  a.o = o;
+  a.D = D;
+  a.workspace = workspace;
+  return from_cuda(ablation_fwd_tc_launch(a, channels, shift, static_cast<cudaStream_t>(stream)));
+}
+
 size_t sanatan_power_bwd_workspace_size(int B, int H, int T, int d, int dv) {
   if (B < 0 || H < 0 || T < 0 || d != 64 || dv != 64) return 0;
   return pow_bwd_tc_workspace_bytes(B, H, T);

@@ -75,6 +75,8 @@ struct PowParams {
   const unsigned char* ws;   // per (sequence, chunk): Phi(Q) | Phi(K) | V
   int H, T, nchunks, bhn;
   float eps;
+  float inv_c;               // ablation maps: 1 / (score scale)
+  float cst;                 // ablation maps: (d + shift) / scale, the constant channel and shift
   float* o;                  // [B, H, T, 64] f32
   float* Dn;                 // [B, H, T] f32 or null
 };
@@ -95,7 +97,11 @@ struct PrepParams {
 // Preparation: one CTA of 256 threads per half chunk (64 tokens).  Lane
 // (r, dimension group ag) of warp w owns the chunk's tokens tq + 8 i (i < 2),
 // tq = 64 half + 16 (w / 2) + r.
+// CH = 6: the six-channel map; CH = 4 / 3: the ablation maps, whose CH - 1
+// non-constant channels fill feature groups (CH - 1) ag + c - 1 of the same
+// chunk layout (the rest of a chunk's feature groups is not read).
 constexpr int kPrepTok = 2;
+template <int CH>
 __global__ void __launch_bounds__(256) pow_prep_kernel(PrepParams prm) {
   __shared__ float4 dimc[64];
   const int half = blockIdx.x & 1;
@@ -160,25 +166,35 @@ __global__ void __launch_bounds__(256) pow_prep_kernel(PrepParams prm) {
 #pragma unroll
     for (int i = 0; i < kPrepTok; ++i) {
       const int t = tq + 8 * i;
-      uint32_t f[5][4];
-      if (tok0 + t < prm.T) {
-        features8(raw[which][i], dc, cb, sb, f);
-      } else {
+      const bool valid = tok0 + t < prm.T;
+      if constexpr (CH == 6) {
+        uint32_t f[5][4];
+        if (valid) {
+          features8(raw[which][i], dc, cb, sb, f);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 5; ++c)
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) f[c][pp] = 0u;
+        }
 #pragma unroll
         for (int c = 0; c < 5; ++c)
+          *reinterpret_cast<uint4*>(dst + phi_offset(t, feat_group(ag, c + 1))) =
+              make_uint4(f[c][0], f[c][1], f[c][2], f[c][3]);
 #pragma unroll
-          for (int pp = 0; pp < 4; ++pp) f[c][pp] = 0u;
-      }
+        for (int j = 0; j < 8; ++j) {
+          const float4 kc = dc[j];
+          const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
+          sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
+          cb[j] = nc;
+        }
+      } else {
+        uint32_t f[CH - 1][4];
+        features8_map<CH>(raw[which][i], dc, cb, sb, f);  // raw is zero past the end
 #pragma unroll
-      for (int c = 0; c < 5; ++c)
-        *reinterpret_cast<uint4*>(dst + phi_offset(t, feat_group(ag, c + 1))) =
-            make_uint4(f[c][0], f[c][1], f[c][2], f[c][3]);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 kc = dc[j];
-        const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
-        sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
-        cb[j] = nc;
+        for (int c = 0; c < CH - 1; ++c)
+          *reinterpret_cast<uint4*>(dst + phi_offset(t, (CH - 1) * ag + c)) =
+              valid ? make_uint4(f[c][0], f[c][1], f[c][2], f[c][3]) : make_uint4(0u, 0u, 0u, 0u);
       }
     }
   }
@@ -215,9 +231,43 @@ __device__ __forceinline__ void weights32(const float* pv, int lim, uint32_t (&h
   }
 }
 
+// The same for an ablation map: x = max(s + d + shift, 0) / c, with s the
+// non-constant part of the score (the clip matters for the four-channel map,
+// whose scores can be negative).
+template <int P, bool MASK>
+__device__ __forceinline__ void weights32_map(const float* pv, int lim, float inv_c, float cst,
+                                              uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float x0 = pow_int<P>(fmaxf(fmaf(pv[2 * i], inv_c, cst), 0.0f));
+    float x1 = pow_int<P>(fmaxf(fmaf(pv[2 * i + 1], inv_c, cst), 0.0f));
+    if (MASK) {
+      if (2 * i > lim) x0 = 0.f;
+      if (2 * i + 1 > lim) x1 = 0.f;
+    }
+    const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+    hi[i] = __byte_perm(b0, b1, 0x7632);
+    lo[i] = pack_bf16x2(x0 - __uint_as_float(b0 & 0xffff0000u),
+                        x1 - __uint_as_float(b1 & 0xffff0000u));
+  }
+}
+
+template <int P, int CH, bool MASK>
+__device__ __forceinline__ void weights_for(const float* pv, int lim, const PowParams& prm,
+                                            uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+  if constexpr (CH == 6)
+    weights32<P, MASK>(pv, lim, hi, lo);
+  else
+    weights32_map<P, MASK>(pv, lim, prm.inv_c, prm.cst, hi, lo);
+}
+
 // ---------------------------------------------------------------------------
-template <int P>
+// CH: channels per dimension of the feature map (6; 4 and 3 for the ablation
+// maps, whose 8 (CH - 1) feature groups shorten the score products).
+template <int P, int CH>
 __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
+  constexpr int kNFG = 8 * (CH - 1);   // non-constant feature groups
+  constexpr int kKSteps = kNFG / 2;    // K = 16 per score MMA
   extern __shared__ __align__(1024) unsigned char smem[];
   Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
   const uint32_t sK = smem_u32(smem + kOffK);
@@ -308,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
         if (!wait_bar(m, b ? kKFull1 : kKFull0, (j >> 1) & 1)) return false;
         tc_fence_after();
 #pragma unroll
-        for (int st = 0; st < 20; ++st)
+        for (int st = 0; st < kKSteps; ++st)
           mma_ts(tmem + kTP0 + 128 * b, tmem + kTQ + 8 * st, dk + 16 * st, idQK, st > 0);
         mma_commit(&m.bar[b ? kKFree1 : kKFree0]);
         mma_commit(&m.bar[b ? kPFull1 : kPFull0]);
@@ -343,12 +393,14 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
     {
       // Phi(Q) of this row, feature groups 20 ch .. 20 ch + 19, into TMEM
-      const unsigned char* src = chunk_base(prm.ws, bh, prm.nchunks, qi) + phi_offset(row, 20 * ch);
-      uint4 w[20];
+      constexpr int kHalf = kNFG / 2;   // feature groups per half
+      const unsigned char* src =
+          chunk_base(prm.ws, bh, prm.nchunks, qi) + phi_offset(row, kHalf * ch);
+      uint4 w[kHalf];
 #pragma unroll
-      for (int g = 0; g < 20; ++g) w[g] = ldg_nc_v4(src + g * 128);
+      for (int g = 0; g < kHalf; ++g) w[g] = ldg_nc_v4(src + g * 128);
 #pragma unroll
-      for (int s4 = 0; s4 < 5; ++s4) {
+      for (int s4 = 0; s4 < kHalf / 4; ++s4) {
         uint32_t r[16];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -357,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
           r[4 * g + 2] = w[4 * s4 + g].z;
           r[4 * g + 3] = w[4 * s4 + g].w;
         }
-        tmem_st16(tmem + lane_off + kTQ + 80 * ch + 16 * s4, r);
+        tmem_st16(tmem + lane_off + kTQ + 4 * kHalf * ch + 16 * s4, r);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -383,11 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
         const int blk = 2 * ch + bi;
         uint32_t hi[16], lo[16];
         if (!diag) {
-          weights32<P, false>(pv + 32 * bi, 31, hi, lo);
+          weights_for<P, CH, false>(pv + 32 * bi, 31, prm, hi, lo);
         } else if (blk == qd) {  // keys up to the row's own
-          weights32<P, true>(pv + 32 * bi, lane, hi, lo);
+          weights_for<P, CH, true>(pv + 32 * bi, lane, prm, hi, lo);
         } else if (blk < qd) {
-          weights32<P, false>(pv + 32 * bi, 31, hi, lo);
+          weights_for<P, CH, false>(pv + 32 * bi, 31, prm, hi, lo);
         } else {  // every key of this block is after every row of this warp
 #pragma unroll
           for (int i = 0; i < 16; ++i) { hi[i] = 0u; lo[i] = 0u; }
@@ -441,15 +493,29 @@ constexpr int kMaxP = 8;
 using AttnKernel = void (*)(PowParams);
 AttnKernel attn_kernel_for(int p) {
   switch (p) {
-    case 1: return pow_attn_kernel<1>;
-    case 2: return pow_attn_kernel<2>;
-    case 3: return pow_attn_kernel<3>;
-    case 4: return pow_attn_kernel<4>;
-    case 5: return pow_attn_kernel<5>;
-    case 6: return pow_attn_kernel<6>;
-    case 7: return pow_attn_kernel<7>;
-    default: return pow_attn_kernel<8>;
+    case 1: return pow_attn_kernel<1, 6>;
+    case 2: return pow_attn_kernel<2, 6>;
+    case 3: return pow_attn_kernel<3, 6>;
+    case 4: return pow_attn_kernel<4, 6>;
+    case 5: return pow_attn_kernel<5, 6>;
+    case 6: return pow_attn_kernel<6, 6>;
+    case 7: return pow_attn_kernel<7, 6>;
+    default: return pow_attn_kernel<8, 6>;
   }
+}
+
+// Ablation maps: p in {1, 2, 4} (nullptr otherwise).
+AttnKernel ablation_kernel_for(int p, int channels) {
+  if (channels == 4) {
+    if (p == 1) return pow_attn_kernel<1, 4>;
+    if (p == 2) return pow_attn_kernel<2, 4>;
+    if (p == 4) return pow_attn_kernel<4, 4>;
+  } else if (channels == 3) {
+    if (p == 1) return pow_attn_kernel<1, 3>;
+    if (p == 2) return pow_attn_kernel<2, 3>;
+    if (p == 4) return pow_attn_kernel<4, 3>;
+  }
+  return nullptr;
 }
 
 cudaError_t pow_set_smem() {
@@ -461,6 +527,10 @@ cudaError_t pow_set_smem() {
   for (int p = 1; p <= kMaxP && e == cudaSuccess; ++p)
     e = cudaFuncSetAttribute(attn_kernel_for(p), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
+  for (int ch = 3; ch <= 4 && e == cudaSuccess; ++ch)
+    for (int p = 1; p <= 4 && e == cudaSuccess; ++p)
+      if (AttnKernel kf = ablation_kernel_for(p, ch))
+        e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
@@ -483,7 +553,7 @@ cudaError_t pow_prep_launch(const PowFwdArgs& a, cudaStream_t st) {
   pp.pos0 = a.pos0;
   pp.ws = static_cast<unsigned char*>(a.workspace);
   const unsigned grid = static_cast<unsigned>(bhn) * static_cast<unsigned>(nchunks);
-  pow_prep_kernel<<<2 * grid, 256, 0, st>>>(pp);
+  pow_prep_kernel<6><<<2 * grid, 256, 0, st>>>(pp);
   return cudaGetLastError();
 }
 
@@ -506,7 +576,7 @@ cudaError_t pow_fwd_tc_launch(const PowFwdArgs& a, cudaStream_t st) {
   pp.pos0 = a.pos0;
   pp.ws = static_cast<unsigned char*>(a.workspace);
   const unsigned grid = static_cast<unsigned>(bhn) * static_cast<unsigned>(nchunks);
-  pow_prep_kernel<<<2 * grid, 256, 0, st>>>(pp);
+  pow_prep_kernel<6><<<2 * grid, 256, 0, st>>>(pp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   PowParams p{};
   p.ws = pp.ws;
@@ -522,6 +592,55 @@ cudaError_t pow_fwd_tc_launch(const PowFwdArgs& a, cudaStream_t st) {
   if (rec) cudaEventRecord(pe.start, st);
   if (a.p < 1 || a.p > kMaxP) return cudaErrorInvalidValue;
   attn_kernel_for(a.p)<<<grid, kThreads, kSmemBytes, st>>>(p);
+  e = cudaGetLastError();
+  if (rec) cudaEventRecord(pe.stop, st);
+  return e;
+}
+
+cudaError_t ablation_fwd_tc_launch(const PowFwdArgs& a, int channels, float shift,
+                                  cudaStream_t st) {
+  const int bhn = a.B * a.H;
+  const int nchunks = (a.T + kC - 1) / kC;
+  if (bhn == 0 || nchunks == 0) return cudaSuccess;
+  AttnKernel kf = ablation_kernel_for(a.p, channels);
+  if (kf == nullptr) return cudaErrorInvalidValue;
+  cudaError_t e = pow_set_smem();
+  if (e != cudaSuccess) return e;
+  PrepParams pp{};
+  pp.q = static_cast<const __nv_bfloat16*>(a.q);
+  pp.k = static_cast<const __nv_bfloat16*>(a.k);
+  pp.v = static_cast<const __nv_bfloat16*>(a.v);
+  pp.gamma = a.gamma;
+  pp.omega = a.omega;
+  pp.phi = a.phi;
+  pp.H = a.H;
+  pp.T = a.T;
+  pp.nchunks = nchunks;
+  pp.pos0 = a.pos0;
+  pp.ws = static_cast<unsigned char*>(a.workspace);
+  const unsigned grid = static_cast<unsigned>(bhn) * static_cast<unsigned>(nchunks);
+  if (channels == 4)
+    pow_prep_kernel<4><<<2 * grid, 256, 0, st>>>(pp);
+  else
+    pow_prep_kernel<3><<<2 * grid, 256, 0, st>>>(pp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  PowParams p{};
+  p.ws = pp.ws;
+  p.H = a.H;
+  p.T = a.T;
+  p.nchunks = nchunks;
+  p.bhn = bhn;
+  p.eps = a.eps;
+  // score scale: the map's largest score, 3d (four channels) or 2d + shift
+  const float c = channels == 4 ? 3.0f * kD : 2.0f * kD + shift;
+  p.inv_c = 1.0f / c;
+  p.cst = (static_cast<float>(kD) + shift) / c;
+  p.o = a.o;
+  p.Dn = a.D;
+  const ProfileEvents& pe = profile_events();
+  const bool rec = pe.start != nullptr;
+  if (rec) cudaEventRecord(pe.start, st);
+  kf<<<grid, kThreads, kSmemBytes, st>>>(p);
   e = cudaGetLastError();
   if (rec) cudaEventRecord(pe.stop, st);
   return e;

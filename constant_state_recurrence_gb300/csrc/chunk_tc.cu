@@ -71,7 +71,7 @@ static_assert(kSoV1 + 16 * kLBO_SV + 128 <= kOffMisc, "state-only buffers must f
 
 enum Bar {
   kFeatQ = 0, kFeatK, kFeatV, kPFull, kPTilde, kQFree, kStateDone, kPVDone, kSnapReady, kOFree,
-  kDrain, kInitDone,
+  kDrain, kInitDone, kStageFree,
   // second buffer of Phi(K) / V in the state-only pass
   kFeatK1, kFeatV1, kStateDone1,
   kNumBars
@@ -87,6 +87,12 @@ struct Misc {
   int abort_flag;
 };
 static_assert(sizeof(float4) * 8 <= sizeof(Misc::dimc), "the over-read must stay in dimc");
+// Output staging in the value buffer: 64 f32 rows at a 272-B pitch or 128 bf16
+// rows at 144 B (the pitches spread a warp's row-per-lane stores over the banks).
+constexpr uint32_t kStagePitch = 272;
+constexpr uint32_t kStagePitchH = 144;
+static_assert(64 * kStagePitch <= 16 * kLBO_SV && 128 * kStagePitchH <= 16 * kLBO_SV,
+              "output staging must fit the value buffer");
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kSmemBytes <= 232448, "shared memory layout exceeds 227 KB");
 
@@ -526,58 +532,88 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
 
         // E3: outputs of this chunk (vs[ci & 1] holds state row 320 before it).
         // Each warp hands the accumulator back as soon as its rows are in
-        // registers; each thread then normalises its row and stores it.
+        // registers; the rows are normalised, staged in the value buffer (free
+        // once this chunk's P~[V|1] is done) and written with bulk copies
+        // (64 f32 rows or 128 bf16 rows per copy: a contiguous range of the
+        // output), so the output stores leave the load/store pipe alone.
         wait_bar(m, kPVDone, ci & 1);
         tc_fence_after();
         const int nrow = min(kC, prm.T - tok0);
+        float ov[80];
+#pragma unroll
+        for (int blk = 0; blk < 5; ++blk) {
+          float x[16];
+          tmem_ld16(tmem + lane_off + kTO + 16 * blk, x);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ov[16 * blk + i] = x[i];
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&m.bar[kOFree]);
+        if (row < nrow) {
+          const float* vsc = m.vs[ci & 1];
+          const float den = ov[64] + 64.0f * vsc[64] + m.a0[64];
+          const float inv = prm.normalize ? 1.0f / (den + prm.eps) : 1.0f;
+          const float4* vs4 = reinterpret_cast<const float4*>(vsc);
+          const float4* a04 = reinterpret_cast<const float4*>(m.a0);
+#pragma unroll
+          for (int e4 = 0; e4 < 16; ++e4) {
+            const float4 w = vs4[e4];
+            const float4 c = a04[e4];
+            ov[4 * e4 + 0] = (fmaf(64.0f, w.x, ov[4 * e4 + 0]) + c.x) * inv;
+            ov[4 * e4 + 1] = (fmaf(64.0f, w.y, ov[4 * e4 + 1]) + c.y) * inv;
+            ov[4 * e4 + 2] = (fmaf(64.0f, w.z, ov[4 * e4 + 2]) + c.z) * inv;
+            ov[4 * e4 + 3] = (fmaf(64.0f, w.w, ov[4 * e4 + 3]) + c.w) * inv;
+          }
+          if (prm.Dn != nullptr) prm.Dn[seq_row0 + orow(prm, tok0 + row)] = den;
+        }
         {
-          float ov[80];
+          const int et = tid - 32 * kEpiWarp0;
+          const int rows_per_pass = prm.out_bf16 ? kC : kC / 2;
+          const uint32_t row_bytes = prm.out_bf16 ? 128u : 256u;
+          const uint32_t pitch = prm.out_bf16 ? kStagePitchH : kStagePitch;
+          for (int pass = 0; pass * rows_per_pass < kC; ++pass) {
+            const int u0 = pass * rows_per_pass;                    // first chunk row
+            const int n = max(0, min(rows_per_pass, nrow - u0));    // rows in this pass
+            if (n == 0) break;
+            const int lr = row - u0;
+            if (lr >= 0 && lr < n) {
+              const uint32_t srow = sV + static_cast<uint32_t>(lr) * pitch;
+              if (prm.out_bf16) {
 #pragma unroll
-          for (int blk = 0; blk < 5; ++blk) {
-            float x[16];
-            tmem_ld16(tmem + lane_off + kTO + 16 * blk, x);
+                for (int j = 0; j < 8; ++j)
+                  st_shared_v4(srow + 16 * j, pack_bf16x2(ov[8 * j], ov[8 * j + 1]),
+                               pack_bf16x2(ov[8 * j + 2], ov[8 * j + 3]),
+                               pack_bf16x2(ov[8 * j + 4], ov[8 * j + 5]),
+                               pack_bf16x2(ov[8 * j + 6], ov[8 * j + 7]));
+              } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) ov[16 * blk + i] = x[i];
-          }
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&m.bar[kOFree]);
-          if (row < nrow) {
-            const float* vsc = m.vs[ci & 1];
-            const float den = ov[64] + 64.0f * vsc[64] + m.a0[64];
-            const float inv = prm.normalize ? 1.0f / (den + prm.eps) : 1.0f;
-            const float4* vs4 = reinterpret_cast<const float4*>(vsc);
-            const float4* a04 = reinterpret_cast<const float4*>(m.a0);
-#pragma unroll
-            for (int e4 = 0; e4 < 16; ++e4) {
-              const float4 w = vs4[e4];
-              const float4 c = a04[e4];
-              ov[4 * e4 + 0] = (fmaf(64.0f, w.x, ov[4 * e4 + 0]) + c.x) * inv;
-              ov[4 * e4 + 1] = (fmaf(64.0f, w.y, ov[4 * e4 + 1]) + c.y) * inv;
-              ov[4 * e4 + 2] = (fmaf(64.0f, w.z, ov[4 * e4 + 2]) + c.z) * inv;
-              ov[4 * e4 + 3] = (fmaf(64.0f, w.w, ov[4 * e4 + 3]) + c.w) * inv;
+                for (int j = 0; j < 16; ++j)
+                  st_shared_v4(srow + 16 * j, __float_as_uint(ov[4 * j]),
+                               __float_as_uint(ov[4 * j + 1]), __float_as_uint(ov[4 * j + 2]),
+                               __float_as_uint(ov[4 * j + 3]));
+              }
             }
-            const int64_t grow = seq_row0 + orow(prm, tok0 + row);
-            if (prm.out_bf16) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(
-                               static_cast<void*>(prm.o)) + grow * kD);
-#pragma unroll
-              for (int e8 = 0; e8 < 8; ++e8)
-                dst[e8] = make_uint4(pack_bf16x2(ov[8 * e8], ov[8 * e8 + 1]),
-                                     pack_bf16x2(ov[8 * e8 + 2], ov[8 * e8 + 3]),
-                                     pack_bf16x2(ov[8 * e8 + 4], ov[8 * e8 + 5]),
-                                     pack_bf16x2(ov[8 * e8 + 6], ov[8 * e8 + 7]));
-            } else {
-              float4* dst = reinterpret_cast<float4*>(prm.o + grow * kD);
-#pragma unroll
-              for (int e4 = 0; e4 < 16; ++e4)
-                dst[e4] = make_float4(ov[4 * e4], ov[4 * e4 + 1], ov[4 * e4 + 2], ov[4 * e4 + 3]);
+            fence_proxy_async_smem();
+            epi_sync();
+            if (warp == kEpiWarp0) {
+              // one bulk copy per staged row, issued by the 32 lanes of one warp
+              unsigned char* obase = reinterpret_cast<unsigned char*>(prm.o);
+              for (int r2 = lane; r2 < n; r2 += 32)
+                bulk_store_s2g(obase + (seq_row0 + orow(prm, tok0 + u0 + r2)) *
+                                           static_cast<int64_t>(row_bytes),
+                               sV + static_cast<uint32_t>(r2) * pitch, row_bytes);
+              bulk_commit();
+              bulk_wait_read_all();   // this lane's staged rows have been read
             }
-            if (prm.Dn != nullptr) prm.Dn[grow] = den;
+            epi_sync();
           }
+          if (et == 0) mbar_arrive(&m.bar[kStageFree]);
         }
       }
+      // the last bulk output copies have landed
+      if (warp == kEpiWarp0) bulk_wait_all();
     } else {
       // One wait on the single-phase drain barrier: a wait on the last
       // state_done phase could alias an earlier phase of the same parity.
@@ -657,7 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         vdst = smem_u32(smem + ((ci & 1) ? kSoV1 : kSoV0));
         if (ci > 1) wait_bar(m, (ci & 1) ? kStateDone1 : kStateDone, ((ci >> 1) - 1) & 1);
       } else {
-        if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
+        // the buffer is free once the previous chunk's outputs staged in it
+        // have been copied out (which follows its P~[V|1])
+        if (ci > 0) wait_bar(m, kStageFree, (ci - 1) & 1);
       }
       for (int pc = vt; pc < kC * 8; pc += 32 * kVWarps) {
         const int t = pc >> 3, ng = pc & 7;
@@ -672,6 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
           st_shared_v4(vdst + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16,
                        __bfloat16_as_ushort(__float2bfloat16_rn(x)), 0u, 0u, 0u);
         }
+      } else if (!kStateOnly && ci > 0) {
+        // the ones column (and its zero padding), overwritten by the staging
+        for (int t = vt; t < kC; t += 32 * kVWarps)
+          st_shared_v4(vdst + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16, 0x3F80u, 0u, 0u, 0u);
       }
       cp_async_wait_all();
       fence_proxy_async_smem();

@@ -141,6 +141,10 @@ struct PowFwdArgs {
 };
 size_t pow_fwd_tc_workspace_bytes(int B, int H, int T);
 cudaError_t pow_fwd_tc_launch(const PowFwdArgs& a, cudaStream_t st);
+// The four- (channels = 4) or three-channel (channels = 3, with `shift`) map in
+// the same kernels; p in {1, 2, 4}.
+cudaError_t ablation_fwd_tc_launch(const PowFwdArgs& a, int channels, float shift,
+                                   cudaStream_t st);
 // The preparation kernel alone (features and [V | 1 | 0] into a.workspace).
 cudaError_t pow_prep_launch(const PowFwdArgs& a, cudaStream_t st);
 

@@ -145,6 +145,58 @@ __device__ __forceinline__ void features8_rot(uint4 raw, const float4* __restric
   }
 }
 
+// The non-constant channels of eight dimensions of one token for the
+// feature map with CH channels per dimension, packed as bf16 pairs
+// (out[c][j/2] holds dims j, j+1 of channel c), then the rotation of
+// (cb, sb) to the thread's next token:
+//   CH = 6: cos, sin, r, r cos, r sin  (the six-channel map, eq. (6))
+//   CH = 4: r, r cos, r sin            (the four-channel map)
+//   CH = 3: cos, sin                   (the three-channel map, no root)
+// with cos, sin of the rotated angle and r from the un-rotated one.
+template <int CH>
+__device__ __forceinline__ void features8_map(uint4 raw, const float4* __restrict__ dimc,
+                                              float (&cb)[8], float (&sb)[8],
+                                              uint32_t (&out)[CH - 1][4]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    float ch[CH - 1][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = 2 * p + h;
+      const float u = __uint_as_float((h == 0 ? (w[p] << 16) : (w[p] & 0xffff0000u)));
+      const float th = __fdividef(u, fmaf(fabsf(u), 0.318309886183790672f, 0.318309886183790672f));
+      float s, c;
+      __sincosf(th, &s, &c);
+      const float4 kc = dimc[j];
+      const float cr = fmaf(c, cb[j], -s * sb[j]);
+      const float sr = fmaf(s, cb[j], c * sb[j]);
+      if constexpr (CH == 3) {
+        ch[0][h] = cr;
+        ch[1][h] = sr;
+      } else {
+        const float r = tanh_fast(fmaf(kc.x, c, -kc.y * s));
+        if constexpr (CH == 6) {
+          ch[0][h] = cr;
+          ch[1][h] = sr;
+          ch[2][h] = r;
+          ch[3][h] = r * cr;
+          ch[4][h] = r * sr;
+        } else {
+          ch[0][h] = r;
+          ch[1][h] = r * cr;
+          ch[2][h] = r * sr;
+        }
+      }
+      const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
+      sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
+      cb[j] = nc;
+    }
+#pragma unroll
+    for (int c = 0; c < CH - 1; ++c) out[c][p] = pack_bf16x2(ch[c][0], ch[c][1]);
+  }
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

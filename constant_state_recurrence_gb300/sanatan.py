@@ -47,6 +47,9 @@ _SIGS = {
     "sanatan_power_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int,
                                    _c_int, _c_int, _c_i64, _c_int, _c_f, _c_p, _c_p, _c_p, _c_sz,
                                    _c_p]),
+    "sanatan_ablation_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int,
+                                      _c_int, _c_int, _c_i64, _c_int, _c_int, _c_f, _c_f, _c_p,
+                                      _c_p, _c_p, _c_sz, _c_p]),
     "sanatan_power_bwd_workspace_size": (_c_sz, [_c_int] * 5),
     "sanatan_power_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int,
                                    _c_int, _c_int, _c_i64, _c_int, _c_f, _c_p, _c_p, _c_p, _c_int,
@@ -394,6 +397,38 @@ def sanatan_power_bwd(q, k, v, gamma, omega, phi, p, o, D, dO, pos0=0, eps=0.0, 
                                  ws_bytes, _stream(dev))
     _check("sanatan_power_bwd", st)
     return dict(dq=dq, dk=dk, dv=dvo, dgamma=dgamma, domega=domega, dphi=dphi)
+
+
+def sanatan_ablation_fwd(q, k, v, gamma, omega, phi, p, channels, shift=0.0, pos0=0, eps=0.0,
+                         want_D=True, out=None, D_out=None, workspace=None):
+    """Power-sharpened causal attention with the four-channel (clipped) or the
+    three-channel (optionally shifted) ablation map; bf16 q, k, v, p in {1, 2, 4}.
+
+    Returns (o [B,H,T,dv] f32, D [B,H,T] f32 or None)."""
+    _need(q, "q", (torch.bfloat16,))
+    B, H, T, d = q.shape
+    _need(k, "k", (torch.bfloat16,), (B, H, T, d))
+    dv = v.shape[-1]
+    _need(v, "v", (torch.bfloat16,), (B, H, T, dv))
+    _need_params(gamma, omega, phi, H, d)
+    dev = q.device
+    o = out if out is not None else torch.empty(B, H, T, dv, dtype=torch.float32, device=dev)
+    _need(o, "o", (torch.float32,), (B, H, T, dv))
+    D = D_out
+    if D is None and want_D:
+        D = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    if D is not None:
+        _need(D, "D", (torch.float32,), (B, H, T))
+    ws_size = power_fwd_workspace_size(B, H, T, d, dv)
+    if workspace is None and ws_size > 0:
+        workspace = torch.empty(ws_size, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().sanatan_ablation_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(omega),
+                                    _ptr(phi), B, H, T, d, dv, int(pos0), int(p), int(channels),
+                                    float(shift), float(eps), _ptr(o), _ptr(D), _ptr(workspace),
+                                    ws_bytes, _stream(dev))
+    _check("sanatan_ablation_fwd", st)
+    return o, D
 
 
 def chunk_bwd_workspace_size(B, H, T, d=64, dv=64, dtype=torch.bfloat16):

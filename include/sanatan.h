@@ -203,6 +203,31 @@ SANATAN_API int sanatan_power_fwd(const void* q, const void* k, const void* v, c
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sanatan_ablation_fwd -- the power-sharpened causal attention of
+ * sanatan_power_fwd with one of the two ablation feature maps of the notes in
+ * place of the six-channel map (same squash, soft root from the un-rotated
+ * angle, and rotation):
+ *   channels = 4: Phi4_a = [1, r, r cos th_rot, r sin th_rot] (Notes §2.5).  The
+ *       per-dimension kernel 1 + r_q r_k (1 + cos dth) can be negative, and the
+ *       total score is clipped at zero before the power:
+ *       w_tj = (max(s_tj, 0) / 3d)^p.
+ *   channels = 3: Phi3_a = [1, cos th_rot, sin th_rot] (Notes §4.4), so
+ *       s_tj = d + sum_a cos dth_a in [0, 2d]; `shift` is added to every score
+ *       first (the printed ablation adds d; shift = 0 is the fair ablation the
+ *       notes ask for): w_tj = ((s_tj + shift) / (2d + shift))^p.
+ *   o_t = sum_{j<=t} w_tj v_j / (sum_{j<=t} w_tj + eps);  D_t = sum_{j<=t} w_tj.
+ *   p in {1, 2, 4}.  Other arguments, layouts, the workspace
+ *   (sanatan_power_fwd_workspace_size) and errors as for sanatan_power_fwd;
+ *   SANATAN_ERR_INVALID for channels other than 3 or 4, a negative shift or a
+ *   nonzero shift with channels = 4; SANATAN_ERR_UNSUPPORTED for another p.
+ */
+SANATAN_API int sanatan_ablation_fwd(const void* q, const void* k, const void* v,
+                                     const float* gamma, const float* omega, const float* phi,
+                                     int B, int H, int T, int d, int dv, int64_t pos0, int p,
+                                     int channels, float shift, float eps, float* o, float* D,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * sanatan_power_bwd -- gradients of sum(o * dO) for sanatan_power_fwd (the
  * chain rule through eq. (8) and the feature map; the pages give no backward).
  *   q, k, v, gamma, omega, phi, sizes, pos0, p, eps: as for the forward

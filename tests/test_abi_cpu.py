@@ -115,3 +115,14 @@ def test_selftest_probe_rejects_bad_limits_before_any_launch(lib):
     assert lib.sanatan_selftest_wait_timeout(10, 0, None) == 1             # below 1 us
     assert lib.sanatan_selftest_wait_timeout(2 * 10**9, 0, None) == 1      # above 1 s
     assert lib.sanatan_selftest_wait_timeout(10**6, 2, None) == 1          # bad flag
+
+
+def test_ablation_argument_errors_before_any_launch(lib):
+    P = ctypes.c_void_p
+    args = lambda p, ch, sh: (None, None, None, None, None, None, 1, 1, 8, 64, 64, 0, p, ch,  # noqa
+                              sh, 0.0, None, None, None, 0, None)
+    assert lib.sanatan_ablation_fwd(*args(2, 5, 0.0)) == 1      # channels
+    assert lib.sanatan_ablation_fwd(*args(2, 4, 1.0)) == 1      # shift with four channels
+    assert lib.sanatan_ablation_fwd(*args(2, 3, -1.0)) == 1     # negative shift
+    assert lib.sanatan_ablation_fwd(*args(3, 3, 0.0)) == 2      # unsupported power
+    del P
