@@ -93,6 +93,32 @@ int sanatan_featurize(const void* u, int u_dtype, const float* gamma, const floa
                                     out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
+int sanatan_rate_from_raw(const float* lambda_raw, int n, float scale, float* phi, void* stream) {
+  if (n < 0) return SANATAN_ERR_INVALID;
+  if (n == 0) return SANATAN_OK;
+  if (!ok_ptr(lambda_raw) || !ok_ptr(phi)) return SANATAN_ERR_INVALID;
+  if (int s = check_arch()) return s;
+  return from_cuda(rate_launch(lambda_raw, nullptr, n, scale, phi,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+int sanatan_rate_from_raw_bwd(const float* lambda_raw, const float* dphi, int n, float scale,
+                              float* dlambda_raw, void* stream) {
+  if (n < 0) return SANATAN_ERR_INVALID;
+  if (n == 0) return SANATAN_OK;
+  if (!ok_ptr(lambda_raw) || !ok_ptr(dphi) || !ok_ptr(dlambda_raw)) return SANATAN_ERR_INVALID;
+  if (int s = check_arch()) return s;
+  return from_cuda(rate_launch(lambda_raw, dphi, n, scale, dlambda_raw,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+float sanatan_eps_raw(float eps, int d, int convention) {
+  if (d <= 0) return -1.0f;
+  if (convention == 0) return (4.0f * static_cast<float>(d) + 1e-6f) * eps;
+  if (convention == 1) return (4.0f * static_cast<float>(d) * 1e-6f) * eps;
+  return -1.0f;
+}
+
 size_t sanatan_chunk_fwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype) {
   if (B < 0 || H < 0 || T < 0 || d != 64 || dv != 64) return 0;
   if (in_dtype != SANATAN_BF16) return 0;

@@ -33,6 +33,9 @@
 // Shared-memory operands use the canonical no-swizzle layout (8 x 16-byte
 // core matrices); TMEM holds P (128 cols), O_ext (80) and the f32 state
 // (3 tiles x 80).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "sanatan_internal.h"
 #include "sanatan_math.cuh"
 #include "tc_ptx.cuh"
@@ -118,6 +121,10 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
 constexpr bool kSinPoly = SANATAN_SINPOLY != 0;  // sine/cosine of the angle on the FMA pipe
 
 struct TcParams {
+  // f32 outputs in forward time: the tensor map of o as [B*H][T][64] floats,
+  // boxes of 64 rows x 32 columns with the 128-byte swizzle (tma_out = 1)
+  CUtensorMap tmap_o;
+  int tma_out;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
@@ -189,7 +196,7 @@ __device__ __forceinline__ void prefetch_chunk(const TcParams& prm, int64_t seq_
 
 // ---------------------------------------------------------------------------
 template <bool kStateOnly>
-__global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
+__global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_constant__ TcParams prm) {
   extern __shared__ __align__(1024) unsigned char smem[];
   Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
   const uint32_t sQ = smem_u32(smem + kOffQ);
@@ -490,11 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         if (lane == 0) mbar_arrive(&m.bar[kPTilde]);
 
         // E2: snapshot of the state after this chunk, for the next chunk's
-        // Phi(Q)[S|z] (QFree: this chunk's Phi(Q)[S|z], the snapshot buffer's
-        // last reader, and the state update before it are complete).  It comes
-        // before the outputs so that the next chunk's tensor-core work does not
-        // wait for their stores.
-        wait_bar(m, kQFree, ci & 1);
+        // Phi(Q)[S|z] (StateDone: the state update and, issued before it, this
+        // chunk's Phi(Q)[S|z], the snapshot buffer's last reader, are
+        // complete).  It comes before the outputs so that the next chunk's
+        // tensor-core work does not wait for their stores.
+        wait_bar(m, kStateDone, ci & 1);
         tc_fence_after();
         if (ci + 1 < nloc) {
           epi_sync();  // every thread's outputs of the previous chunk have read vs[(ci + 1) & 1]
@@ -570,50 +577,84 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         }
         {
           const int et = tid - 32 * kEpiWarp0;
-          const int rows_per_pass = prm.out_bf16 ? kC : kC / 2;
-          const uint32_t row_bytes = prm.out_bf16 ? 128u : 256u;
-          const uint32_t pitch = prm.out_bf16 ? kStagePitchH : kStagePitch;
-          for (int pass = 0; pass * rows_per_pass < kC; ++pass) {
-            const int u0 = pass * rows_per_pass;                    // first chunk row
-            const int n = max(0, min(rows_per_pass, nrow - u0));    // rows in this pass
-            if (n == 0) break;
-            const int lr = row - u0;
-            if (lr >= 0 && lr < n) {
-              const uint32_t srow = sV + static_cast<uint32_t>(lr) * pitch;
-              if (prm.out_bf16) {
+          if (prm.tma_out) {
+            // Two passes of 64 rows; per pass two boxes of 32 columns (8 KB,
+            // 128-byte rows whose 16-byte pieces are swizzled by row % 8, the
+            // layout of the tensor map's 128-byte swizzle, so a warp's
+            // row-per-lane stores spread over all banks) and two tensor stores.
+            // Rows past the end of the sequence are clipped by the copy.
+            for (int pass = 0; pass < 2; ++pass) {
+              const int u0 = 64 * pass;
+              if (u0 >= nrow) break;
+              const int lr = row - u0;
+              if (lr >= 0 && lr < 64) {
+                const uint32_t srow = sV + static_cast<uint32_t>(lr) * 128u;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  st_shared_v4(srow + 16 * j, pack_bf16x2(ov[8 * j], ov[8 * j + 1]),
-                               pack_bf16x2(ov[8 * j + 2], ov[8 * j + 3]),
-                               pack_bf16x2(ov[8 * j + 4], ov[8 * j + 5]),
-                               pack_bf16x2(ov[8 * j + 6], ov[8 * j + 7]));
-              } else {
+                for (int bx = 0; bx < 2; ++bx)
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  st_shared_v4(srow + 16 * j, __float_as_uint(ov[4 * j]),
-                               __float_as_uint(ov[4 * j + 1]), __float_as_uint(ov[4 * j + 2]),
-                               __float_as_uint(ov[4 * j + 3]));
+                  for (int c = 0; c < 8; ++c)
+                    st_shared_v4(srow + 8192u * bx + 16u * (c ^ (lr & 7)),
+                                 __float_as_uint(ov[32 * bx + 4 * c]),
+                                 __float_as_uint(ov[32 * bx + 4 * c + 1]),
+                                 __float_as_uint(ov[32 * bx + 4 * c + 2]),
+                                 __float_as_uint(ov[32 * bx + 4 * c + 3]));
               }
+              fence_proxy_async_smem();
+              epi_sync();
+              if (et == 0) {
+                tma_store_3d(&prm.tmap_o, sV, 0, tok0 + u0, bh);
+                tma_store_3d(&prm.tmap_o, sV + 8192u, 32, tok0 + u0, bh);
+                bulk_commit();
+                bulk_wait_read_all();   // the staging has been read
+              }
+              epi_sync();
             }
-            fence_proxy_async_smem();
-            epi_sync();
-            if (warp == kEpiWarp0) {
-              // one bulk copy per staged row, issued by the 32 lanes of one warp
-              unsigned char* obase = reinterpret_cast<unsigned char*>(prm.o);
-              for (int r2 = lane; r2 < n; r2 += 32)
-                bulk_store_s2g(obase + (seq_row0 + orow(prm, tok0 + u0 + r2)) *
-                                           static_cast<int64_t>(row_bytes),
-                               sV + static_cast<uint32_t>(r2) * pitch, row_bytes);
-              bulk_commit();
-              bulk_wait_read_all();   // this lane's staged rows have been read
+          } else {
+            // Reverse time or bf16 outputs (the backward's uses): staged rows
+            // (272 / 144-byte pitch) and coalesced 16-byte stores.
+            const int rows_per_pass = prm.out_bf16 ? kC : kC / 2;
+            const int lg = prm.out_bf16 ? 3 : 4;   // log2 of 16-byte pieces per row
+            const uint32_t pitch = prm.out_bf16 ? kStagePitchH : kStagePitch;
+            unsigned char* obase = reinterpret_cast<unsigned char*>(prm.o);
+            const int64_t row_bytes = int64_t{16} << lg;
+            for (int pass = 0; pass * rows_per_pass < kC; ++pass) {
+              const int u0 = pass * rows_per_pass;
+              const int n = max(0, min(rows_per_pass, nrow - u0));
+              if (n == 0) break;
+              const int lr = row - u0;
+              if (lr >= 0 && lr < n) {
+                const uint32_t srow = sV + static_cast<uint32_t>(lr) * pitch;
+                if (prm.out_bf16) {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j)
+                    st_shared_v4(srow + 16 * j, pack_bf16x2(ov[8 * j], ov[8 * j + 1]),
+                                 pack_bf16x2(ov[8 * j + 2], ov[8 * j + 3]),
+                                 pack_bf16x2(ov[8 * j + 4], ov[8 * j + 5]),
+                                 pack_bf16x2(ov[8 * j + 6], ov[8 * j + 7]));
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j)
+                    st_shared_v4(srow + 16 * j, __float_as_uint(ov[4 * j]),
+                                 __float_as_uint(ov[4 * j + 1]), __float_as_uint(ov[4 * j + 2]),
+                                 __float_as_uint(ov[4 * j + 3]));
+                }
+              }
+              epi_sync();
+              for (int pc = et; pc < (n << lg); pc += 128) {
+                const int rr = pc >> lg, cc = pc & ((1 << lg) - 1);
+                const uint4 val =
+                    *reinterpret_cast<const uint4*>(smem + kOffV + rr * pitch + 16 * cc);
+                *reinterpret_cast<uint4*>(obase + (seq_row0 + orow(prm, tok0 + u0 + rr)) * row_bytes +
+                                          16 * cc) = val;
+              }
+              epi_sync();
             }
-            epi_sync();
           }
           if (et == 0) mbar_arrive(&m.bar[kStageFree]);
         }
       }
-      // the last bulk output copies have landed
-      if (warp == kEpiWarp0) bulk_wait_all();
+      // the last tensor stores of the outputs have landed
+      if (tid == 32 * kEpiWarp0) bulk_wait_all();
     } else {
       // One wait on the single-phase drain barrier: a wait on the last
       // state_done phase could alias an earlier phase of the same parity.
@@ -747,24 +788,34 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
         dVl = smem_desc(smem_u32(smem + ((ci & 1) ? kSoV1 : kSoV0)), kLBO_SV, 128);
       }
       asm volatile("" : "+l"(dQl), "+l"(dKbl), "+l"(dKal), "+l"(dSl), "+l"(dVl));
+      // Order per chunk: Phi(Q)[S|z] from the previous chunk's snapshot, the
+      // scores (Phi(Q) is free after them), the state update (Phi(K) is free
+      // after it), then P~[V|1].  The query buffer is released one product
+      // before the key buffer, and each featuriser group gets the other
+      // group's products as head start.
       if constexpr (kStateOnly) {
         wait_bar(m, (ci & 1) ? kFeatK1 : kFeatK, (ci >> 1) & 1);
+        if (ci == 0) wait_bar(m, kSnapReady, 0);  // the initial state is in TMEM
       } else {
         wait_bar(m, kFeatQ, ci & 1);
+        wait_bar(m, kSnapReady, ci & 1);  // snapshot of the state before this chunk
+        wait_bar(m, kOFree, ci & 1);      // previous outputs drained from TMEM
+        tc_fence_after();
+        asm volatile("" : "+l"(dQl), "+l"(dSl));
+#pragma unroll
+        for (int s = 0; s < 20; ++s)
+          mma_ss(tmem + kTO, dQl + 16 * s, dSl + (2 * kLBO_SV / 16) * s, idIN, s > 0);
         wait_bar(m, kFeatK, ci & 1);
-      }
-      tc_fence_after();
-      // Order: scores, state update (the key buffer is free after it), then
-      // Phi(Q)[S|z] from the previous chunk's snapshot, then P~[V|1].
-      if constexpr (!kStateOnly) {
+        // the scores overwrite P~ of the previous chunk: its P~[V|1] is done
+        if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
+        tc_fence_after();
+        asm volatile("" : "+l"(dQl), "+l"(dKbl));
 #pragma unroll
         for (int s = 0; s < 20; ++s)
           mma_ss(tmem + kTP, dQl + 16 * s, dKbl + 16 * s, idQK, s > 0);
         mma_commit(&m.bar[kPFull]);
+        mma_commit(&m.bar[kQFree]);
       }
-      // the state may change once the previous snapshot has been taken (at
-      // ci = 0: once the initial state is in TMEM)
-      if (!kStateOnly || ci == 0) wait_bar(m, kSnapReady, ci & 1);
       if constexpr (kStateOnly)
         wait_bar(m, (ci & 1) ? kFeatV1 : kFeatV, (ci >> 1) & 1);
       else
@@ -779,13 +830,6 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
                  dVl + (2 * kLBO_SV / 16) * s, idST, true);
       mma_commit(&m.bar[(kStateOnly && (ci & 1)) ? kStateDone1 : kStateDone]);
       if constexpr (!kStateOnly) {
-        wait_bar(m, kOFree, ci & 1);      // previous outputs drained from TMEM
-        tc_fence_after();
-        asm volatile("" : "+l"(dQl), "+l"(dSl));
-#pragma unroll
-        for (int s = 0; s < 20; ++s)
-          mma_ss(tmem + kTO, dQl + 16 * s, dSl + (2 * kLBO_SV / 16) * s, idIN, s > 0);
-        mma_commit(&m.bar[kQFree]);
         wait_bar(m, kPTilde, ci & 1);
         tc_fence_after();
         asm volatile("" : "+l"(dVl));
@@ -919,10 +963,47 @@ cudaError_t tc_state_pass(const TcJob& job, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// The output o [B*H][T][64] f32 as a 3-D tensor for the epilogue's tensor
+// stores: boxes of 32 columns x 64 rows, 128-byte swizzle.
+cudaError_t encode_output_map(CUtensorMap* map, float* o, int bhn, int T) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(bhn)};
+  const cuuint64_t strides[2] = {64 * sizeof(float), static_cast<cuuint64_t>(T) * 64 * sizeof(float)};
+  const cuuint32_t box[3] = {32, 64, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, o, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t tc_attention(const TcJob& job, cudaStream_t st) {
   cudaError_t e = tc_set_smem();
   if (e != cudaSuccess) return e;
   TcParams p = tc_params(job);
+  if (!job.reverse && !job.out_bf16 && job.T > 0 && job.B * job.H > 0) {
+    if ((e = encode_output_map(&p.tmap_o, static_cast<float*>(job.o), job.B * job.H, job.T)) !=
+        cudaSuccess)
+      return e;
+    p.tma_out = 1;
+  }
   const bool state_pass = p.nseg > 1 && !job.deltas_ready;
   if (state_pass) {
     if ((e = tc_state_pass(job, st)) != cudaSuccess) return e;

@@ -41,7 +41,26 @@ cudaError_t launch(const void* u, const float* gamma, const float* omega, const 
   return cudaGetLastError();
 }
 
+// The rotation rate from its unconstrained parameter (reading notes §2.2,
+// eq. (4)): phi = scale tanh(lambda_raw), and the pull-back of a rate
+// gradient, dlambda_raw = dphi scale (1 - tanh^2(lambda_raw)).
+__global__ void __launch_bounds__(256) rate_kernel(const float* __restrict__ raw,
+                                                   const float* __restrict__ dphi, int n,
+                                                   float scale, float* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float t = tanhf(raw[i]);
+  out[i] = dphi == nullptr ? scale * t : dphi[i] * scale * (1.0f - t * t);
+}
+
 }  // namespace
+
+cudaError_t rate_launch(const float* raw, const float* dphi, int n, float scale, float* out,
+                        cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  rate_kernel<<<(n + 255) / 256, 256, 0, st>>>(raw, dphi, n, scale, out);
+  return cudaGetLastError();
+}
 
 cudaError_t featurize_launch(const void* u, int u_dtype, const float* gamma,
                              const float* omega, const float* phi, int B, int H, int T, int d,

@@ -57,6 +57,10 @@ cudaError_t featurize_launch(const void* u, int u_dtype, const float* gamma, con
                              const float* phi, int B, int H, int T, int d, int64_t pos0,
                              void* out, int out_dtype, cudaStream_t st);
 
+// phi = scale tanh(raw) (dphi == null) or dphi scale (1 - tanh^2(raw)).
+cudaError_t rate_launch(const float* raw, const float* dphi, int n, float scale, float* out,
+                        cudaStream_t st);
+
 cudaError_t decode_step_launch(float* S, float* z, const float* q, const float* k,
                                const float* v, const float* gamma, const float* omega,
                                const float* phi, const int64_t* pos, int N, int G, float eps,

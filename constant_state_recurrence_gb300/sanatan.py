@@ -29,6 +29,9 @@ _SIGS = {
     "sanatan_state_bytes": (_c_sz, [_c_int] * 4),
     "sanatan_featurize": (_c_int, [_c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int, _c_int,
                                    _c_i64, _c_p, _c_int, _c_p]),
+    "sanatan_rate_from_raw": (_c_int, [_c_p, _c_int, _c_f, _c_p, _c_p]),
+    "sanatan_rate_from_raw_bwd": (_c_int, [_c_p, _c_p, _c_int, _c_f, _c_p, _c_p]),
+    "sanatan_eps_raw": (_c_f, [_c_f, _c_int, _c_int]),
     "sanatan_chunk_fwd_workspace_size": (_c_sz, [_c_int] * 6),
     "sanatan_chunk_fwd_plan": (_c_int, [_c_int] * 5 + [_c_p, _c_p]),
     "sanatan_chunk_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int,
@@ -174,6 +177,36 @@ def sanatan_featurize(u, gamma, omega, phi, pos0=0, out_dtype=None, out=None):
                                  _stream(u.device))
     _check("sanatan_featurize", st)
     return out
+
+
+RATE_SCALE = 0.01   # the pages' lambda = 0.01 tanh(lambda_raw)
+
+
+def rate_from_raw(lambda_raw, scale=RATE_SCALE, out=None):
+    """phi = scale * tanh(lambda_raw) (float32, on the device)."""
+    _need(lambda_raw, "lambda_raw", (torch.float32,))
+    out = torch.empty_like(lambda_raw) if out is None else out
+    _need(out, "phi", (torch.float32,), tuple(lambda_raw.shape))
+    _check("sanatan_rate_from_raw",
+           lib().sanatan_rate_from_raw(_ptr(lambda_raw), lambda_raw.numel(), float(scale),
+                                       _ptr(out), _stream(lambda_raw.device)))
+    return out
+
+
+def rate_from_raw_bwd(lambda_raw, dphi, scale=RATE_SCALE, out=None):
+    """dlambda_raw = dphi * scale * (1 - tanh^2(lambda_raw))."""
+    _need(lambda_raw, "lambda_raw", (torch.float32,))
+    _need(dphi, "dphi", (torch.float32,), tuple(lambda_raw.shape))
+    out = torch.empty_like(lambda_raw) if out is None else out
+    _check("sanatan_rate_from_raw_bwd",
+           lib().sanatan_rate_from_raw_bwd(_ptr(lambda_raw), _ptr(dphi), lambda_raw.numel(),
+                                           float(scale), _ptr(out), _stream(lambda_raw.device)))
+    return out
+
+
+def eps_raw(eps, d=64, convention=0):
+    """c * eps with c = 4d + 1e-6 (convention 0) or 4d * 1e-6 (convention 1)."""
+    return float(lib().sanatan_eps_raw(float(eps), int(d), int(convention)))
 
 
 def chunk_fwd_workspace_size(B, H, T, d=64, dv=64, dtype=torch.bfloat16):

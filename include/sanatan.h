@@ -88,6 +88,31 @@ SANATAN_API int sanatan_featurize(const void* u, int u_dtype, const float* gamma
                       int out_dtype, void* stream);
 
 /*
+ * sanatan_rate_from_raw -- the rotation rate of eq. (4) from its unconstrained
+ * parameter, as the notes give it (§2.2): phi = scale * tanh(lambda_raw) with
+ * scale = 0.01 on the pages (any scale is accepted).  lambda_raw and phi are
+ * n float32 values on the device (e.g. [H, d]); phi may be passed to every
+ * call that takes phi.  SANATAN_ERR_INVALID for n < 0 or a null/misaligned
+ * pointer (n = 0 does nothing).
+ * sanatan_rate_from_raw_bwd -- the gradient of the same map:
+ * dlambda_raw = dphi * scale * (1 - tanh^2(lambda_raw)), e.g. for the dphi of
+ * sanatan_chunk_bwd.
+ */
+SANATAN_API int sanatan_rate_from_raw(const float* lambda_raw, int n, float scale, float* phi,
+                                      void* stream);
+SANATAN_API int sanatan_rate_from_raw_bwd(const float* lambda_raw, const float* dphi, int n,
+                                          float scale, float* dlambda_raw, void* stream);
+
+/*
+ * sanatan_eps_raw -- the raw-score eps that reproduces a parallel form which
+ * divides scores by c before adding eps (notes §2.7: eps_raw = c * eps):
+ * convention 0 takes the authors' parallel code's c = 4d + 1e-6, convention 1
+ * the recurrence notebook's approximation c = 4d * 1e-6.  Host-only
+ * arithmetic; returns -1 for d <= 0 or another convention.
+ */
+SANATAN_API float sanatan_eps_raw(float eps, int d, int convention);
+
+/*
  * sanatan_chunk_fwd -- causal normalised attention at p = 1 over whole
  * sequences (eq. (9) evaluated chunk-parallel; the exact re-association of the
  * sums in Notes §2.7), optionally continuing from a state (S0, z0).

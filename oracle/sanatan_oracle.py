@@ -489,6 +489,30 @@ def attn_ablation(q, k, v, gamma, omega, phi, p, channels, shift=0.0, pos0=0, ep
 
 
 # ---------------------------------------------------------------------------
+# Rate parameterisation (Notes §2.2, eq. (4)) and the eps scale (Notes §2.7)
+# ---------------------------------------------------------------------------
+
+
+def rate_from_raw(lambda_raw, scale=0.01):
+    """The rotation rate lambda = 0.01 tanh(lambda_raw) of eq. (4)."""
+    return scale * np.tanh(np.asarray(lambda_raw, dtype=np.float64))
+
+
+def rate_from_raw_grad(lambda_raw, dphi, scale=0.01):
+    """d loss / d lambda_raw from d loss / d lambda (chain rule of tanh)."""
+    t = np.tanh(np.asarray(lambda_raw, dtype=np.float64))
+    return np.asarray(dphi, dtype=np.float64) * scale * (1.0 - t * t)
+
+
+def eps_raw(eps, d, convention=0):
+    """Notes §2.7: a parallel form that divides by c and then adds eps equals
+    the raw-score form with eps_raw = c eps; the authors' parallel code uses
+    c = 4d + 1e-6 (convention 0), their recurrence notebook 4d * 1e-6 (1)."""
+    c = 4.0 * d + 1e-6 if convention == 0 else 4.0 * d * 1e-6
+    return c * eps
+
+
+# ---------------------------------------------------------------------------
 # Memory accounting: Notes §4.5 [paper §4.4]
 # ---------------------------------------------------------------------------
 

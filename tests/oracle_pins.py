@@ -551,3 +551,41 @@ ALL_CHECKS += [
     check_three_channel_p1_is_linear_attention,
     check_ablation_single_token_and_constant_values,
 ]
+
+
+# --------------------------------------------------------------------------
+# Rate parameterisation lambda = 0.01 tanh(lambda_raw) (Notes §2.2) and the
+# eps scale of the two normalisation conventions (Notes §2.7)
+# --------------------------------------------------------------------------
+
+def check_rate_parameterisation():
+    x = np.array([0.0, 1e-8, -1e-8, 40.0, -40.0, 0.5493061443340549])  # atanh(0.5) last
+    lam = O.rate_from_raw(x)
+    assert lam[0] == 0.0 and abs(lam[1] - 1e-10) < 1e-20      # slope 0.01 at the origin
+    assert abs(lam[3] - 0.01) < 1e-15 and abs(lam[4] + 0.01) < 1e-15   # saturates at +-0.01
+    assert abs(lam[5] - 0.005) < 1e-15
+    g = _rng(21)
+    raw = g.standard_normal(50)
+    dphi = g.standard_normal(50)
+    h = 1e-6
+    fd = (O.rate_from_raw(raw + h) - O.rate_from_raw(raw - h)) / (2 * h) * dphi
+    assert np.allclose(O.rate_from_raw_grad(raw, dphi), fd, rtol=1e-7, atol=1e-14)
+
+
+def check_eps_conventions():
+    # c = 4d + 1e-6 (parallel code) and 4d x 1e-6 (recurrence notebook), d = 64
+    assert abs(O.eps_raw(1.0, 64, 0) - 256.000001) < 1e-9
+    assert abs(O.eps_raw(1.0, 64, 1) - 2.56e-4) < 1e-16
+    # the raw-score form with eps_raw equals the scaled form with eps (p = 1)
+    c = _small_case(seed=22, T=6)
+    d = c["q"].shape[-1]
+    cc = 4.0 * d + 1e-6
+    o_raw, _ = O.attn_quadratic(**c, eps=O.eps_raw(0.3, d, 0))
+    pq = O.featurize(c["q"], c["gamma"], c["omega"], c["phi"])[0, 0]
+    pk = O.featurize(c["k"], c["gamma"], c["omega"], c["phi"])[0, 0]
+    w = (pq @ pk.T) / cc * np.tril(np.ones((6, 6)))
+    o_scaled = (w @ c["v"][0, 0]) / (w.sum(1) + 0.3)[:, None]
+    assert np.allclose(o_raw[0, 0], o_scaled, atol=1e-12)
+
+
+ALL_CHECKS += [check_rate_parameterisation, check_eps_conventions]

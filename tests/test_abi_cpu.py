@@ -126,3 +126,11 @@ def test_ablation_argument_errors_before_any_launch(lib):
     assert lib.sanatan_ablation_fwd(*args(2, 3, -1.0)) == 1     # negative shift
     assert lib.sanatan_ablation_fwd(*args(3, 3, 0.0)) == 2      # unsupported power
     del P
+
+
+def test_eps_raw_conventions(lib):
+    assert abs(lib.sanatan_eps_raw(1.0, 64, 0) - 256.000001) < 1e-4
+    assert abs(lib.sanatan_eps_raw(2.0, 64, 1) - 5.12e-4) < 1e-9
+    assert lib.sanatan_eps_raw(1.0, 0, 0) == -1.0 and lib.sanatan_eps_raw(1.0, 64, 2) == -1.0
+    assert lib.sanatan_rate_from_raw(None, -1, 0.01, None, None) == 1
+    assert lib.sanatan_rate_from_raw_bwd(None, None, -1, 0.01, None, None) == 1
