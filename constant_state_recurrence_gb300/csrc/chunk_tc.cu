@@ -33,9 +33,6 @@
 // Shared-memory operands use the canonical no-swizzle layout (8 x 16-byte
 // core matrices); TMEM holds P (128 cols), O_ext (80) and the f32 state
 // (3 tiles x 80).
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "sanatan_internal.h"
 #include "sanatan_math.cuh"
 #include "tc_ptx.cuh"
@@ -60,10 +57,9 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + 16 * kXQ;
 constexpr int kOffS = kOffK + 16 * kXK;
 constexpr int kOffV = kOffS + 40 * kLBO_SV;
-// The MMAs read up to 128 B past S'bf16 and V (the ignored padding columns
-// 72..79 of their N = 80): past V they read the start of Misc, the
-// featuriser constants, never written while MMAs run.
-constexpr int kOffMisc = kOffV + 16 * kLBO_SV;
+// The MMAs read up to 128 B past S'bf16 and V (ignored padding columns); the
+// pad keeps those reads inside this layout and away from the mbarriers.
+constexpr int kOffMisc = kOffV + 16 * kLBO_SV + 128;
 // The state-only pass needs no Phi(Q) and no snapshot: it double-buffers
 // Phi(K) and V instead, so that the keys of chunk c + 1 are featurised while
 // the tensor core accumulates chunk c.
@@ -74,7 +70,7 @@ static_assert(kSoV1 + 16 * kLBO_SV + 128 <= kOffMisc, "state-only buffers must f
 
 enum Bar {
   kFeatQ = 0, kFeatK, kFeatV, kPFull, kPTilde, kQFree, kStateDone, kPVDone, kSnapReady, kOFree,
-  kDrain, kInitDone, kStageFree,
+  kDrain,
   // second buffer of Phi(K) / V in the state-only pass
   kFeatK1, kFeatV1, kStateDone1,
   kNumBars
@@ -82,20 +78,20 @@ enum Bar {
 
 struct Misc {
   float4 dimc[64];   // per dim: gamma*sqrt2*cos(omega+pi/4), gamma*sqrt2*sin(omega+pi/4),
-                     //          cos(8 phi), sin(8 phi)  (first: the MMAs' over-read lands here)
-  float vs[2][68];   // state row 320 before chunk ci, in vs[ci & 1]: sum v (64), count
+                     //          cos(8 phi), sin(8 phi)
+  float vs[68];      // state row 320 before the current chunk: sum v (64), count
   float a0[68];      // constant-channel part of S0: sum_a S0[6a] (64), sum_a z0[6a]
   uint64_t bar[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(float4) * 8 <= sizeof(Misc::dimc), "the over-read must stay in dimc");
-// Output staging in the value buffer: 64 f32 rows at a 272-B pitch or 128 bf16
-// rows at 144 B (the pitches spread a warp's row-per-lane stores over the banks).
-constexpr uint32_t kStagePitch = 272;
-constexpr uint32_t kStagePitchH = 144;
-static_assert(64 * kStagePitch <= 16 * kLBO_SV && 128 * kStagePitchH <= 16 * kLBO_SV,
-              "output staging must fit the value buffer");
+// Output staging: rows at a 272-B (f32) or 144-B (bf16) pitch, so that the
+// row-per-thread writes spread over the banks.  It lives in the bf16 state
+// snapshot buffer, which is free between the chunk's Phi(Q)[S|z] product and
+// the next snapshot.
+constexpr int kStagePitch = 272;
+constexpr int kStagePitchH = 144;
+static_assert(kC * kStagePitch <= 40 * kLBO_SV, "output staging must fit the snapshot buffer");
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kSmemBytes <= 232448, "shared memory layout exceeds 227 KB");
 
@@ -115,16 +111,8 @@ constexpr int kMmaWarp = 20;   // warp 20: MMA issue (one thread)
 constexpr int kVWarp0 = 21;    // warps 21-22: value loads
 constexpr int kVWarps = 2;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
-#ifndef SANATAN_SINPOLY
-#define SANATAN_SINPOLY 0
-#endif
-constexpr bool kSinPoly = SANATAN_SINPOLY != 0;  // sine/cosine of the angle on the FMA pipe
 
 struct TcParams {
-  // f32 outputs in forward time: the tensor map of o as [B*H][T][64] floats,
-  // boxes of 64 rows x 32 columns with the 128-byte swizzle (tma_out = 1)
-  CUtensorMap tmap_o;
-  int tma_out;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
@@ -168,18 +156,6 @@ __device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
 }
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-// Warps 8-23 (key featurisers, epilogue, MMA and value loaders).
-__device__ __forceinline__ void upper_sync() { asm volatile("bar.sync 2, 512;" ::: "memory"); }
-
-// Initial state of a later segment, gathered by warps 8-23 before the roles
-// start: the sums of the earlier segments (the compact slot layout, 68 x 321
-// floats) are added up with 16-byte loads into a shared-memory copy of one
-// slot.  It lives in the Phi(K) buffer and the start of the snapshot buffer;
-// the query featurisers, which write only Phi(Q), proceed meanwhile.
-constexpr int kOffInit = kOffK;
-constexpr int kSlotUsed4 = kSCUsedCols * kSCRows / 4;     // float4 per slot actually used
-constexpr int kSlot4 = kSCRows * kSCCols / 4;             // float4 stride between slots
-static_assert(kOffInit + kSlotUsed4 * 16 <= kOffV, "initial-state copy must fit before V");
 
 // L2 prefetch of one chunk's rows of q (unless state-only), k and v.
 template <bool kStateOnly>
@@ -196,7 +172,7 @@ __device__ __forceinline__ void prefetch_chunk(const TcParams& prm, int64_t seq_
 
 // ---------------------------------------------------------------------------
 template <bool kStateOnly>
-__global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_constant__ TcParams prm) {
+__global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
   extern __shared__ __align__(1024) unsigned char smem[];
   Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
   const uint32_t sQ = smem_u32(smem + kOffQ);
@@ -235,9 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
       const uint32_t cnt = (b == kFeatQ) ? kQWarps
                            : (b == kFeatK || b == kFeatK1) ? (kStateOnly ? 16u : 8u)
                            : (b == kFeatV || b == kFeatV1) ? static_cast<uint32_t>(kVWarps)
-                           : (b == kPTilde || b == kSnapReady || b == kOFree || b == kInitDone)
-                               ? 4u
-                               : 1u;
+                           : (b == kPTilde || b == kSnapReady || b == kOFree) ? 4u : 1u;
       mbar_init(&m.bar[b], cnt);
     }
     m.abort_flag = 0;
@@ -274,30 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
       st_shared_v4(sV + kg * kLBO_SV + 8 * 128 + row * 16, 0x3F80u, 0u, 0u, 0u);
     }
   }
+  if (tid < 8) st_shared_v4(sV + 16 * kLBO_SV + 16 * tid, 0u, 0u, 0u, 0u);  // over-read pad
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = m.tmem_base;
-
-  // A later segment starts from the sums of the earlier ones (written by the
-  // state-only pass): warps 8-23 add them up into shared memory.
-  const bool init_copy = !kStateOnly && prm.deltas != nullptr && seg > 0;
-  if (init_copy && warp >= kKWarp0) {
-    if (prm.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");  // the state-only pass is complete
-    const float4* d0 = reinterpret_cast<const float4*>(
-        prm.deltas + static_cast<int64_t>(bh) * prm.nseg * kSCRows * kSCCols);
-    float4* dst = reinterpret_cast<float4*>(smem + kOffInit);
-#pragma unroll 4
-    for (int i = tid - 32 * kKWarp0; i < kSlotUsed4; i += 512) {
-      float4 acc = d0[i];
-      for (int sp = 1; sp < seg; ++sp) {
-        const float4 x = d0[static_cast<int64_t>(sp) * kSlot4 + i];
-        acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
-      }
-      dst[i] = acc;
-    }
-    upper_sync();
-  }
 
   if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ featurisers
@@ -335,8 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
       const int chunk = c_begin + ci;
       const int tok0 = chunk * kC;
       if (tid == 0 && ci + 2 < nloc) prefetch_chunk<kStateOnly>(prm, seq_row0, chunk + 2);
-      // rotation factors cos, sin(t phi) of the thread's first token (exact
-      // product, reduction mod 2 pi), then rotated by 8 phi per token
       float cb[8], sb[8];
       {
         const int64_t tabs = prm.pos0 + orow(prm, tok0 + tq);
@@ -350,23 +303,32 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
         if (ci > 1) wait_bar(m, (ci & 1) ? kStateDone1 : kStateDone, ((ci >> 1) - 1) & 1);
       } else {
         if (ci > 0) wait_bar(m, kgrp ? kStateDone : kQFree, (ci - 1) & 1);
-        // the initial-state copy in the Phi(K) buffer has been read
-        if (ci == 0 && kgrp && init_copy) wait_bar(m, kInitDone, 0);
       }
 #pragma unroll
       for (int i = 0; i < kNI; ++i) {
         const int t = tq + 8 * i;
         const bool valid = tok0 + t < prm.T;
         uint32_t f[5][4];
-        // (raw is zero past the end, so the math stays finite; the rotation
-        // advances for every token)
-        features8_rot<kSinPoly>(raw[i], dimc, cb, sb, f);
+        if (valid) {
+          features8(raw[i], dimc, cb, sb, f);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 5; ++c)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) f[c][p] = 0u;
+        }
         const uint32_t base = sdst + (t >> 3) * pitch + (t & 7) * 16;
 #pragma unroll
         for (int c = 0; c < 5; ++c)
-          st_shared_v4_nc(base + feat_group(ag, c + 1) * 128, valid ? f[c][0] : 0u,
-                          valid ? f[c][1] : 0u, valid ? f[c][2] : 0u, valid ? f[c][3] : 0u);
-        if (kgrp && ag == 0) st_shared_v4_nc(base + 40 * 128, valid ? 0x3F80u : 0u, 0u, 0u, 0u);
+          st_shared_v4(base + feat_group(ag, c + 1) * 128, f[c][0], f[c][1], f[c][2], f[c][3]);
+        if (kgrp && ag == 0) st_shared_v4(base + 40 * 128, valid ? 0x3F80u : 0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 kc = dimc[j];
+          const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
+          sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
+          cb[j] = nc;
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -382,8 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
     // Initial state -> TMEM tiles (and the bf16 snapshot for the first chunk):
     // the caller's state (S0, z0) plus the sums of all earlier segments.
+    if (!kStateOnly && prm.pdl && seg > 0)
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the state-only pass is complete
     {
-      const float* init_sum = reinterpret_cast<const float*>(smem + kOffInit);
       for (int mt = 0; mt < 3; ++mt) {
         const int f = mt * 128 + row;
         if (mt == 2 && qd == 3) continue;  // rows 352..383 are never used
@@ -402,9 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
           }
           val[64] = prm.z0[rowi];
         }
-        if (init_copy && f < kSCRows) {
+        if (!kStateOnly && f < kSCRows && prm.deltas != nullptr) {
+          const float* d0 = prm.deltas + static_cast<int64_t>(bh) * prm.nseg * kSCRows * kSCCols;
+          for (int sp = 0; sp < seg; ++sp) {
+            const float* ds = d0 + static_cast<int64_t>(sp) * kSCRows * kSCCols;
 #pragma unroll
-          for (int e = 0; e < 65; ++e) val[e] += init_sum[sc_index(f, e)];
+            for (int e = 0; e < 65; ++e) val[e] += ds[sc_index(f, e)];
+          }
         }
 #pragma unroll
         for (int blk = 0; blk < 5; ++blk) {
@@ -414,42 +381,21 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
           tmem_st16(tmem + lane_off + kTS + mt * kN + 16 * blk, rr);
         }
         if constexpr (!kStateOnly) {
-          if (f == kNF) {
+          if (f < kNF) {
+            const uint32_t base = sS + (f >> 3) * kLBO_SV + (f & 7) * 16;
 #pragma unroll
-            for (int e = 0; e < 65; ++e) m.vs[0][e] = val[e];
+            for (int ng = 0; ng < kNG; ++ng)
+              st_shared_v4(base + ng * 128, pack_bf16x2(val[8 * ng], val[8 * ng + 1]),
+                           pack_bf16x2(val[8 * ng + 2], val[8 * ng + 3]),
+                           pack_bf16x2(val[8 * ng + 4], val[8 * ng + 5]),
+                           pack_bf16x2(val[8 * ng + 6], val[8 * ng + 7]));
+          } else if (f == kNF) {
+#pragma unroll
+            for (int e = 0; e < 65; ++e) m.vs[e] = val[e];
           }
         }
       }
       tmem_st_wait();
-      if constexpr (!kStateOnly) {
-        // The bf16 snapshot for the first chunk, from TMEM: its buffer overlaps
-        // the initial-state copy, which every epilogue thread has read by now.
-        tc_fence_before();
-        epi_sync();
-        tc_fence_after();
-        if (lane == 0 && init_copy) mbar_arrive(&m.bar[kInitDone]);
-        for (int mt = 0; mt < 3; ++mt) {
-          const int f = mt * 128 + row;
-          if (f >= kNF) continue;
-          float val[72];
-#pragma unroll
-          for (int blk = 0; blk < 5; ++blk) {
-            float x[16];
-            tmem_ld16(tmem + lane_off + kTS + mt * kN + 16 * blk, x);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (16 * blk + i < 72) val[16 * blk + i] = x[i];
-          }
-          tmem_ld_wait();
-          const uint32_t base = sS + (f >> 3) * kLBO_SV + (f & 7) * 16;
-#pragma unroll
-          for (int ng = 0; ng < kNG; ++ng)
-            st_shared_v4(base + ng * 128, pack_bf16x2(val[8 * ng], val[8 * ng + 1]),
-                         pack_bf16x2(val[8 * ng + 2], val[8 * ng + 3]),
-                         pack_bf16x2(val[8 * ng + 4], val[8 * ng + 5]),
-                         pack_bf16x2(val[8 * ng + 6], val[8 * ng + 7]));
-        }
-      }
       fence_proxy_async_smem();
       tc_fence_before();
       epi_sync();
@@ -496,15 +442,79 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
         __syncwarp();
         if (lane == 0) mbar_arrive(&m.bar[kPTilde]);
 
-        // E2: snapshot of the state after this chunk, for the next chunk's
-        // Phi(Q)[S|z] (StateDone: the state update and, issued before it, this
-        // chunk's Phi(Q)[S|z], the snapshot buffer's last reader, are
-        // complete).  It comes before the outputs so that the next chunk's
-        // tensor-core work does not wait for their stores.
+        // E3: outputs of this chunk (state row 320 in m.vs is still the pre-chunk one).
+        // Each row is normalised in registers and staged in the free snapshot
+        // buffer; the four warps then copy the staged tile out with coalesced
+        // 16-byte stores (each warp instruction writes whole rows).
+        wait_bar(m, kPVDone, ci & 1);
+        tc_fence_after();
+        const int nrow = min(kC, prm.T - tok0);
+        {
+          float ov[80];
+#pragma unroll
+          for (int blk = 0; blk < 5; ++blk) {
+            float x[16];
+            tmem_ld16(tmem + lane_off + kTO + 16 * blk, x);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[16 * blk + i] = x[i];
+          }
+          tmem_ld_wait();
+          if (row < nrow) {
+            const float den = ov[64] + 64.0f * m.vs[64] + m.a0[64];
+            const float inv = prm.normalize ? 1.0f / (den + prm.eps) : 1.0f;
+            const float4* vs4 = reinterpret_cast<const float4*>(m.vs);
+            const float4* a04 = reinterpret_cast<const float4*>(m.a0);
+#pragma unroll
+            for (int e4 = 0; e4 < 16; ++e4) {
+              const float4 w = vs4[e4];
+              const float4 c = a04[e4];
+              ov[4 * e4 + 0] = (fmaf(64.0f, w.x, ov[4 * e4 + 0]) + c.x) * inv;
+              ov[4 * e4 + 1] = (fmaf(64.0f, w.y, ov[4 * e4 + 1]) + c.y) * inv;
+              ov[4 * e4 + 2] = (fmaf(64.0f, w.z, ov[4 * e4 + 2]) + c.z) * inv;
+              ov[4 * e4 + 3] = (fmaf(64.0f, w.w, ov[4 * e4 + 3]) + c.w) * inv;
+            }
+            if (prm.out_bf16) {
+              const uint32_t srow = sS + row * kStagePitchH;
+#pragma unroll
+              for (int e8 = 0; e8 < 8; ++e8)
+                st_shared_v4(srow + 16 * e8, pack_bf16x2(ov[8 * e8], ov[8 * e8 + 1]),
+                             pack_bf16x2(ov[8 * e8 + 2], ov[8 * e8 + 3]),
+                             pack_bf16x2(ov[8 * e8 + 4], ov[8 * e8 + 5]),
+                             pack_bf16x2(ov[8 * e8 + 6], ov[8 * e8 + 7]));
+            } else {
+              const uint32_t srow = sS + row * kStagePitch;
+#pragma unroll
+              for (int e4 = 0; e4 < 16; ++e4)
+                st_shared_v4(srow + 16 * e4, __float_as_uint(ov[4 * e4]),
+                             __float_as_uint(ov[4 * e4 + 1]), __float_as_uint(ov[4 * e4 + 2]),
+                             __float_as_uint(ov[4 * e4 + 3]));
+            }
+            if (prm.Dn != nullptr) prm.Dn[seq_row0 + orow(prm, tok0 + row)] = den;
+          }
+        }
+        tc_fence_before();
+        epi_sync();  // every row staged, every thread done with m.vs and O
+        if (lane == 0) mbar_arrive(&m.bar[kOFree]);
+        {
+          // 16-byte pieces: piece p is column piece p % per_row of staged row p / per_row.
+          const int et = tid - 32 * kEpiWarp0;
+          const int lg = prm.out_bf16 ? 3 : 4;  // log2 of pieces per row
+          const int pitch = prm.out_bf16 ? kStagePitchH : kStagePitch;
+          unsigned char* obase = reinterpret_cast<unsigned char*>(prm.o);
+          const int64_t row_bytes = int64_t{16} << lg;
+          for (int pc = et; pc < (nrow << lg); pc += 128) {
+            const int rr = pc >> lg, cc = pc & ((1 << lg) - 1);
+            const uint4 val = *reinterpret_cast<const uint4*>(smem + kOffS + rr * pitch + 16 * cc);
+            *reinterpret_cast<uint4*>(obase + (seq_row0 + orow(prm, tok0 + rr)) * row_bytes +
+                                      16 * cc) = val;
+          }
+        }
+        epi_sync();  // staged tile read out before the snapshot overwrites it
+
+        // E2: snapshot of the state after this chunk, for the next chunk.
         wait_bar(m, kStateDone, ci & 1);
         tc_fence_after();
         if (ci + 1 < nloc) {
-          epi_sync();  // every thread's outputs of the previous chunk have read vs[(ci + 1) & 1]
           for (int mt = 0; mt < 3; ++mt) {
             if (mt == 2 && qd >= 3) continue;
             const int f = mt * 128 + row;
@@ -528,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
                              pack_bf16x2(val[8 * ng + 6], val[8 * ng + 7]));
             } else if (f == kNF) {
 #pragma unroll
-              for (int e = 0; e < 65; ++e) m.vs[(ci + 1) & 1][e] = val[e];
+              for (int e = 0; e < 65; ++e) m.vs[e] = val[e];
             }
           }
           fence_proxy_async_smem();
@@ -536,125 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
           epi_sync();
           if (lane == 0) mbar_arrive(&m.bar[kSnapReady]);
         }
-
-        // E3: outputs of this chunk (vs[ci & 1] holds state row 320 before it).
-        // Each warp hands the accumulator back as soon as its rows are in
-        // registers; the rows are normalised, staged in the value buffer (free
-        // once this chunk's P~[V|1] is done) and written with bulk copies
-        // (64 f32 rows or 128 bf16 rows per copy: a contiguous range of the
-        // output), so the output stores leave the load/store pipe alone.
-        wait_bar(m, kPVDone, ci & 1);
-        tc_fence_after();
-        const int nrow = min(kC, prm.T - tok0);
-        float ov[80];
-#pragma unroll
-        for (int blk = 0; blk < 5; ++blk) {
-          float x[16];
-          tmem_ld16(tmem + lane_off + kTO + 16 * blk, x);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) ov[16 * blk + i] = x[i];
-        }
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&m.bar[kOFree]);
-        if (row < nrow) {
-          const float* vsc = m.vs[ci & 1];
-          const float den = ov[64] + 64.0f * vsc[64] + m.a0[64];
-          const float inv = prm.normalize ? 1.0f / (den + prm.eps) : 1.0f;
-          const float4* vs4 = reinterpret_cast<const float4*>(vsc);
-          const float4* a04 = reinterpret_cast<const float4*>(m.a0);
-#pragma unroll
-          for (int e4 = 0; e4 < 16; ++e4) {
-            const float4 w = vs4[e4];
-            const float4 c = a04[e4];
-            ov[4 * e4 + 0] = (fmaf(64.0f, w.x, ov[4 * e4 + 0]) + c.x) * inv;
-            ov[4 * e4 + 1] = (fmaf(64.0f, w.y, ov[4 * e4 + 1]) + c.y) * inv;
-            ov[4 * e4 + 2] = (fmaf(64.0f, w.z, ov[4 * e4 + 2]) + c.z) * inv;
-            ov[4 * e4 + 3] = (fmaf(64.0f, w.w, ov[4 * e4 + 3]) + c.w) * inv;
-          }
-          if (prm.Dn != nullptr) prm.Dn[seq_row0 + orow(prm, tok0 + row)] = den;
-        }
-        {
-          const int et = tid - 32 * kEpiWarp0;
-          if (prm.tma_out) {
-            // Two passes of 64 rows; per pass two boxes of 32 columns (8 KB,
-            // 128-byte rows whose 16-byte pieces are swizzled by row % 8, the
-            // layout of the tensor map's 128-byte swizzle, so a warp's
-            // row-per-lane stores spread over all banks) and two tensor stores.
-            // Rows past the end of the sequence are clipped by the copy.
-            for (int pass = 0; pass < 2; ++pass) {
-              const int u0 = 64 * pass;
-              if (u0 >= nrow) break;
-              const int lr = row - u0;
-              if (lr >= 0 && lr < 64) {
-                const uint32_t srow = sV + static_cast<uint32_t>(lr) * 128u;
-#pragma unroll
-                for (int bx = 0; bx < 2; ++bx)
-#pragma unroll
-                  for (int c = 0; c < 8; ++c)
-                    st_shared_v4(srow + 8192u * bx + 16u * (c ^ (lr & 7)),
-                                 __float_as_uint(ov[32 * bx + 4 * c]),
-                                 __float_as_uint(ov[32 * bx + 4 * c + 1]),
-                                 __float_as_uint(ov[32 * bx + 4 * c + 2]),
-                                 __float_as_uint(ov[32 * bx + 4 * c + 3]));
-              }
-              fence_proxy_async_smem();
-              epi_sync();
-              if (et == 0) {
-                tma_store_3d(&prm.tmap_o, sV, 0, tok0 + u0, bh);
-                tma_store_3d(&prm.tmap_o, sV + 8192u, 32, tok0 + u0, bh);
-                bulk_commit();
-                bulk_wait_read_all();   // the staging has been read
-              }
-              epi_sync();
-            }
-          } else {
-            // Reverse time or bf16 outputs (the backward's uses): staged rows
-            // (272 / 144-byte pitch) and coalesced 16-byte stores.
-            const int rows_per_pass = prm.out_bf16 ? kC : kC / 2;
-            const int lg = prm.out_bf16 ? 3 : 4;   // log2 of 16-byte pieces per row
-            const uint32_t pitch = prm.out_bf16 ? kStagePitchH : kStagePitch;
-            unsigned char* obase = reinterpret_cast<unsigned char*>(prm.o);
-            const int64_t row_bytes = int64_t{16} << lg;
-            for (int pass = 0; pass * rows_per_pass < kC; ++pass) {
-              const int u0 = pass * rows_per_pass;
-              const int n = max(0, min(rows_per_pass, nrow - u0));
-              if (n == 0) break;
-              const int lr = row - u0;
-              if (lr >= 0 && lr < n) {
-                const uint32_t srow = sV + static_cast<uint32_t>(lr) * pitch;
-                if (prm.out_bf16) {
-#pragma unroll
-                  for (int j = 0; j < 8; ++j)
-                    st_shared_v4(srow + 16 * j, pack_bf16x2(ov[8 * j], ov[8 * j + 1]),
-                                 pack_bf16x2(ov[8 * j + 2], ov[8 * j + 3]),
-                                 pack_bf16x2(ov[8 * j + 4], ov[8 * j + 5]),
-                                 pack_bf16x2(ov[8 * j + 6], ov[8 * j + 7]));
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 16; ++j)
-                    st_shared_v4(srow + 16 * j, __float_as_uint(ov[4 * j]),
-                                 __float_as_uint(ov[4 * j + 1]), __float_as_uint(ov[4 * j + 2]),
-                                 __float_as_uint(ov[4 * j + 3]));
-                }
-              }
-              epi_sync();
-              for (int pc = et; pc < (n << lg); pc += 128) {
-                const int rr = pc >> lg, cc = pc & ((1 << lg) - 1);
-                const uint4 val =
-                    *reinterpret_cast<const uint4*>(smem + kOffV + rr * pitch + 16 * cc);
-                *reinterpret_cast<uint4*>(obase + (seq_row0 + orow(prm, tok0 + u0 + rr)) * row_bytes +
-                                          16 * cc) = val;
-              }
-              epi_sync();
-            }
-          }
-          if (et == 0) mbar_arrive(&m.bar[kStageFree]);
-        }
       }
-      // the last tensor stores of the outputs have landed
-      if (tid == 32 * kEpiWarp0) bulk_wait_all();
     } else {
       // One wait on the single-phase drain barrier: a wait on the last
       // state_done phase could alias an earlier phase of the same parity.
@@ -696,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
             prm.z_out[static_cast<int64_t>(bh) * 384 + 6 * a + c] = val[64];
           } else if (f == kNF) {
 #pragma unroll
-            for (int e = 0; e < 65; ++e) m.vs[nloc & 1][e] = val[e];
+            for (int e = 0; e < 65; ++e) m.vs[e] = val[e];
           }
         }
       }
@@ -709,10 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
           const int64_t rowi = static_cast<int64_t>(bh) * 384 + 6 * a;
           if (e < 64) {
             const float base = prm.S0 ? prm.S0[rowi * 64 + e] : 0.f;
-            prm.S_out[rowi * 64 + e] = base + m.vs[nloc & 1][e];
+            prm.S_out[rowi * 64 + e] = base + m.vs[e];
           } else {
             const float base = prm.z0 ? prm.z0[rowi] : 0.f;
-            prm.z_out[rowi] = base + m.vs[nloc & 1][64];
+            prm.z_out[rowi] = base + m.vs[64];
           }
         }
       }
@@ -734,9 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
         vdst = smem_u32(smem + ((ci & 1) ? kSoV1 : kSoV0));
         if (ci > 1) wait_bar(m, (ci & 1) ? kStateDone1 : kStateDone, ((ci >> 1) - 1) & 1);
       } else {
-        // the buffer is free once the previous chunk's outputs staged in it
-        // have been copied out (which follows its P~[V|1])
-        if (ci > 0) wait_bar(m, kStageFree, (ci - 1) & 1);
+        if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
       }
       for (int pc = vt; pc < kC * 8; pc += 32 * kVWarps) {
         const int t = pc >> 3, ng = pc & 7;
@@ -751,10 +641,6 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
           st_shared_v4(vdst + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16,
                        __bfloat16_as_ushort(__float2bfloat16_rn(x)), 0u, 0u, 0u);
         }
-      } else if (!kStateOnly && ci > 0) {
-        // the ones column (and its zero padding), overwritten by the staging
-        for (int t = vt; t < kC; t += 32 * kVWarps)
-          st_shared_v4(vdst + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16, 0x3F80u, 0u, 0u, 0u);
       }
       cp_async_wait_all();
       fence_proxy_async_smem();
@@ -788,33 +674,29 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
         dVl = smem_desc(smem_u32(smem + ((ci & 1) ? kSoV1 : kSoV0)), kLBO_SV, 128);
       }
       asm volatile("" : "+l"(dQl), "+l"(dKbl), "+l"(dKal), "+l"(dSl), "+l"(dVl));
-      // Order per chunk: Phi(Q)[S|z] from the previous chunk's snapshot, the
-      // scores (Phi(Q) is free after them), the state update (Phi(K) is free
-      // after it), then P~[V|1].  The query buffer is released one product
-      // before the key buffer, and each featuriser group gets the other
-      // group's products as head start.
       if constexpr (kStateOnly) {
         wait_bar(m, (ci & 1) ? kFeatK1 : kFeatK, (ci >> 1) & 1);
-        if (ci == 0) wait_bar(m, kSnapReady, 0);  // the initial state is in TMEM
       } else {
         wait_bar(m, kFeatQ, ci & 1);
-        wait_bar(m, kSnapReady, ci & 1);  // snapshot of the state before this chunk
+        wait_bar(m, kFeatK, ci & 1);
+      }
+      tc_fence_after();
+      if constexpr (!kStateOnly) {
+#pragma unroll
+        for (int s = 0; s < 20; ++s)
+          mma_ss(tmem + kTP, dQl + 16 * s, dKbl + 16 * s, idQK, s > 0);
+        mma_commit(&m.bar[kPFull]);
+        wait_bar(m, kSnapReady, ci & 1);  // bf16 state snapshot of the previous chunk
         wait_bar(m, kOFree, ci & 1);      // previous outputs drained from TMEM
         tc_fence_after();
         asm volatile("" : "+l"(dQl), "+l"(dSl));
 #pragma unroll
         for (int s = 0; s < 20; ++s)
           mma_ss(tmem + kTO, dQl + 16 * s, dSl + (2 * kLBO_SV / 16) * s, idIN, s > 0);
-        wait_bar(m, kFeatK, ci & 1);
-        // the scores overwrite P~ of the previous chunk: its P~[V|1] is done
-        if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
-        tc_fence_after();
-        asm volatile("" : "+l"(dQl), "+l"(dKbl));
-#pragma unroll
-        for (int s = 0; s < 20; ++s)
-          mma_ss(tmem + kTP, dQl + 16 * s, dKbl + 16 * s, idQK, s > 0);
-        mma_commit(&m.bar[kPFull]);
         mma_commit(&m.bar[kQFree]);
+      } else if (ci == 0) {
+        wait_bar(m, kSnapReady, 0);  // initial state is in TMEM
+        tc_fence_after();
       }
       if constexpr (kStateOnly)
         wait_bar(m, (ci & 1) ? kFeatV1 : kFeatV, (ci >> 1) & 1);
@@ -963,47 +845,10 @@ cudaError_t tc_state_pass(const TcJob& job, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// cuTensorMapEncodeTiled, looked up once through the runtime.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
-// The output o [B*H][T][64] f32 as a 3-D tensor for the epilogue's tensor
-// stores: boxes of 32 columns x 64 rows, 128-byte swizzle.
-cudaError_t encode_output_map(CUtensorMap* map, float* o, int bhn, int T) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (enc == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(bhn)};
-  const cuuint64_t strides[2] = {64 * sizeof(float), static_cast<cuuint64_t>(T) * 64 * sizeof(float)};
-  const cuuint32_t box[3] = {32, 64, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, o, dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 cudaError_t tc_attention(const TcJob& job, cudaStream_t st) {
   cudaError_t e = tc_set_smem();
   if (e != cudaSuccess) return e;
   TcParams p = tc_params(job);
-  if (!job.reverse && !job.out_bf16 && job.T > 0 && job.B * job.H > 0) {
-    if ((e = encode_output_map(&p.tmap_o, static_cast<float*>(job.o), job.B * job.H, job.T)) !=
-        cudaSuccess)
-      return e;
-    p.tma_out = 1;
-  }
   const bool state_pass = p.nseg > 1 && !job.deltas_ready;
   if (state_pass) {
     if ((e = tc_state_pass(job, st)) != cudaSuccess) return e;

@@ -83,68 +83,6 @@ __device__ __forceinline__ void features8(uint4 raw, const float4* __restrict__ 
   }
 }
 
-// sin(pi x) and cos(pi x) for |x| <= 1 on the FMA pipe: x is folded into
-// b = min(|x|, 1 - |x|) in [0, 1/2] (sin(pi (1 - a)) = sin(pi a),
-// cos(pi (1 - a)) = -cos(pi a)), then least-squares polynomials in b^2 fitted
-// on Chebyshev nodes of [0, 1/2] (degree 7 odd for the sine, degree 6 even
-// for the cosine; float32 evaluation error below 1e-5, far under the bf16
-// rounding of the features).
-__device__ __forceinline__ void sincospi_poly(float x, float& s, float& c) {
-  const float a = fabsf(x);
-  const float b = fminf(a, 1.0f - a);
-  const float b2 = b * b;
-  float ps = fmaf(-0.5594624280929565f, b2, 2.5440104007720947f);
-  ps = fmaf(ps, b2, -5.1674065589904785f);
-  ps = fmaf(ps, b2, 3.1415903568267822f);
-  float pc = fmaf(-1.2220317125320435f, b2, 4.041248321533203f);
-  pc = fmaf(pc, b2, -4.933934688568115f);
-  pc = fmaf(pc, b2, 0.9999932646751404f);
-  s = copysignf(ps * b, x);
-  c = (a > 0.5f) ? -pc : pc;
-}
-
-// features8 followed by the rotation of (cb, sb) to the thread's next token
-// (by dimc[j].z, .w), reading each dimension's constants once.  With kPoly
-// the sine and cosine of the squashed angle come from sincospi_poly (FMA pipe)
-// instead of the special-function unit.
-template <bool kPoly>
-__device__ __forceinline__ void features8_rot(uint4 raw, const float4* __restrict__ dimc,
-                                              float (&cb)[8], float (&sb)[8],
-                                              uint32_t (&out)[5][4]) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    float ch[5][2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = 2 * p + h;
-      const float u = __uint_as_float((h == 0 ? (w[p] << 16) : (w[p] & 0xffff0000u)));
-      float s, c;
-      if constexpr (kPoly) {
-        sincospi_poly(__fdividef(u, 1.0f + fabsf(u)), s, c);
-      } else {
-        // theta = pi u / (1 + |u|) = u / ((1 + |u|) / pi)
-        const float th = __fdividef(u, fmaf(fabsf(u), 0.318309886183790672f, 0.318309886183790672f));
-        __sincosf(th, &s, &c);
-      }
-      const float4 kc = dimc[j];
-      const float r = tanh_fast(fmaf(kc.x, c, -kc.y * s));
-      const float cr = fmaf(c, cb[j], -s * sb[j]);
-      const float sr = fmaf(s, cb[j], c * sb[j]);
-      ch[0][h] = cr;
-      ch[1][h] = sr;
-      ch[2][h] = r;
-      ch[3][h] = r * cr;
-      ch[4][h] = r * sr;
-      const float nc = fmaf(cb[j], kc.z, -sb[j] * kc.w);
-      sb[j] = fmaf(sb[j], kc.z, cb[j] * kc.w);
-      cb[j] = nc;
-    }
-#pragma unroll
-    for (int c = 0; c < 5; ++c) out[c][p] = pack_bf16x2(ch[c][0], ch[c][1]);
-  }
-}
-
 // The non-constant channels of eight dimensions of one token for the
 // feature map with CH channels per dimension, packed as bf16 pairs
 // (out[c][j/2] holds dims j, j+1 of channel c), then the rotation of
@@ -203,15 +141,6 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
-}
-
-// A shared-memory store that does not act as a compiler memory barrier (so
-// loads of unrelated shared data are not re-issued around it); its order with
-// other volatile asm (fences, barrier arrivals) is kept.
-__device__ __forceinline__ void st_shared_v4_nc(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                                uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

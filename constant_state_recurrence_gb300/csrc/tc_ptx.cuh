@@ -143,20 +143,6 @@ __device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32
                "r"(ssrc), "r"(bytes)
                : "memory");
 }
-// Tensor store (TMA) of a 3-D box from shared memory at `ssrc` to the tensor
-// described by `tmap` (a CUtensorMap in kernel-parameter space) at element
-// coordinates (c0 innermost, c1, c2); tracked by the thread's bulk group.
-// Coordinates past the tensor's extent are clipped by the hardware; none may
-// be negative.
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t ssrc, int c0, int c1,
-                                             int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(ssrc), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
