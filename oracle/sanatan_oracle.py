@@ -1,7 +1,7 @@
 """Float64 CPU oracle for SANATAN root-parity gated angular attention: the
 feature map, the p = 1 causal attention in its quadratic and recurrent forms,
 the power-sharpened attention of eq. (8) at integer p, and their gradients,
-and the four- and three-channel ablation kernels.
+the four- and three-channel ablation kernels, and the harmonic feature map.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
@@ -486,6 +486,110 @@ def attn_ablation(q, k, v, gamma, omega, phi, p, channels, shift=0.0, pos0=0, ep
             o[b, h] = (w @ v[b, h]) / (den + eps)[:, None]
             D[b, h] = den
     return o, D
+
+
+# ---------------------------------------------------------------------------
+# Harmonic features (Notes, "附录 B 的频谱展望": adding cos(n theta), sin(n theta)
+# keeps the p = 1 form explicitly expandable, with more features and state)
+# ---------------------------------------------------------------------------
+
+
+def harmonic_channels(N):
+    """Channels per dimension of the map with harmonics 1..N: the label block
+    [1, r] times the angle block [1, cos th, sin th, ..., cos N th, sin N th]."""
+    return 2 * (2 * N + 1)
+
+
+def features_harmonic_from_angles(theta_rot, r, N):
+    """Per dimension [A, r A] with A = [1, cos th, sin th, cos 2th, sin 2th, ...,
+    cos N th, sin N th] of the rotated angle (channel l (2N + 1) + m of
+    dimension a at index a * 2(2N+1) + l (2N + 1) + m).  N = 1 is the
+    six-channel block of eq. (6)."""
+    th = np.asarray(theta_rot, dtype=np.float64)
+    ang = [np.ones_like(th)]
+    for n in range(1, N + 1):
+        ang += [np.cos(n * th), np.sin(n * th)]
+    A = np.stack(ang, axis=-1)
+    blk = np.concatenate([A, np.asarray(r)[..., None] * A], axis=-1)
+    return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * blk.shape[-1],))
+
+
+def featurize_harmonic(u, gamma, omega, phi, N, pos0=0):
+    """The harmonic features of a [B, H, T, d] tensor: squash, soft root from
+    the un-rotated angle, rotation, then features_harmonic_from_angles."""
+    u = np.asarray(u, dtype=np.float64)
+    B, H, T, d = u.shape
+    g = np.asarray(gamma, dtype=np.float64).reshape(1, H, 1, 1)
+    om = np.asarray(omega, dtype=np.float64).reshape(1, H, 1, d)
+    ph = np.asarray(phi, dtype=np.float64).reshape(1, H, 1, d)
+    t = positions(T, pos0).astype(np.float64).reshape(1, 1, T, 1)
+    theta = squash(u)
+    return features_harmonic_from_angles(rotate(theta, t, ph), soft_root(theta, g, om), N)
+
+
+def attn_harmonic(q, k, v, gamma, omega, phi, N, pos0=0, eps=0.0, S0=None, z0=None):
+    """Causal normalised attention at p = 1 with the harmonic map (the
+    quadratic form of eq. (9)'s attention, s_tj = Phi_N(q_t).Phi_N(k_j)),
+    with the history of a state (S0, z0) added as in attn_quadratic."""
+    pq = featurize_harmonic(q, gamma, omega, phi, N, pos0)
+    pk = featurize_harmonic(k, gamma, omega, phi, N, pos0)
+    v = _heads(v)
+    B, H, T, _ = pq.shape
+    mask = np.tril(np.ones((T, T)))
+    o = np.zeros((B, H, T, v.shape[-1]))
+    D = np.zeros((B, H, T))
+    for b in range(B):
+        for h in range(H):
+            s = (pq[b, h] @ pk[b, h].T) * mask
+            num = s @ v[b, h]
+            den = s.sum(axis=1)
+            if S0 is not None:
+                num = num + pq[b, h] @ _heads(S0)[b, h]
+                den = den + pq[b, h] @ _heads(z0)[b, h]
+            o[b, h] = num / (den + eps)[:, None]
+            D[b, h] = den
+    return o, D
+
+
+def final_state_harmonic(k, v, gamma, omega, phi, N, pos0=0, S0=None, z0=None):
+    """S = S0 + sum_t Phi_N(k_t) v_t^T, z = z0 + sum_t Phi_N(k_t)."""
+    pk = featurize_harmonic(k, gamma, omega, phi, N, pos0)
+    S = np.matmul(np.swapaxes(pk, -1, -2), _heads(v))
+    z = pk.sum(axis=2)
+    if S0 is not None:
+        S = S + _heads(S0)
+        z = z + _heads(z0)
+    return S, z
+
+
+def decode_step_harmonic(S, z, q, k, v, gamma, omega, phi, pos, N, eps=0.0):
+    """One token of the recurrence with the harmonic map for N slots (the
+    arguments of decode_step; S [n, F_N, dv], z [n, F_N])."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    n, d = q.shape
+    g = np.asarray(gamma, dtype=np.float64).reshape(n, 1)
+    om = np.asarray(omega, dtype=np.float64)
+    ph = np.asarray(phi, dtype=np.float64)
+    t = np.asarray(pos, dtype=np.int64).astype(np.float64).reshape(n, 1)
+
+    def phi_of(u):
+        th = squash(u)
+        return features_harmonic_from_angles(rotate(th, t, ph), soft_root(th, g, om), N)
+
+    pq, pk = phi_of(q), phi_of(k)
+    S = _heads(S) + pk[:, :, None] * np.asarray(v, dtype=np.float64)[:, None, :]
+    z = _heads(z) + pk
+    num = np.einsum("nf,nfe->ne", pq, S)
+    den = np.einsum("nf,nf->n", pq, z)
+    return S, z, num / (den + eps)[:, None]
+
+
+def state_bytes_harmonic(layers, heads, d, dv, N, bytes_per_float=4):
+    """Recurrent state with harmonics 1..N: per head S (F_N x dv) and z (F_N),
+    F_N = 2(2N + 1) d (N = 1: the six-channel 6 d^2 + 6 d of Notes §2.7)."""
+    F = harmonic_channels(N) * d
+    return layers * heads * (F * dv + F) * bytes_per_float
 
 
 # ---------------------------------------------------------------------------

@@ -589,3 +589,79 @@ def check_eps_conventions():
 
 
 ALL_CHECKS += [check_rate_parameterisation, check_eps_conventions]
+
+
+# --------------------------------------------------------------------------
+# Harmonic features (Appendix B of the notes)
+# --------------------------------------------------------------------------
+
+def check_harmonic_one_is_six_channel():
+    c = _small_case(seed=31, T=7, d=4)
+    a = O.featurize_harmonic(c["q"], c["gamma"], c["omega"], c["phi"], 1, pos0=5)
+    b = O.featurize(c["q"], c["gamma"], c["omega"], c["phi"], pos0=5)
+    assert np.allclose(a, b, atol=1e-15)
+    assert O.harmonic_channels(1) == 6 and O.harmonic_channels(3) == 14
+
+
+def check_harmonic_kernel_closed_form():
+    # Phi_N(q).Phi_N(k) = sum_a (1 + r_q r_k)(1 + sum_{n<=N} cos(n dtheta_a))
+    c = _small_case(seed=32, T=6, d=3)
+    for N in (2, 3):
+        pq = O.featurize_harmonic(c["q"], c["gamma"], c["omega"], c["phi"], N)[0, 0]
+        pk = O.featurize_harmonic(c["k"], c["gamma"], c["omega"], c["phi"], N)[0, 0]
+        tq, rq = _angles(c, c["q"][0, 0])
+        tk, rk = _angles(c, c["k"][0, 0])
+        for i in range(6):
+            for j in range(6):
+                dth = tq[i] - tk[j]
+                ang = 1.0 + sum(np.cos(n * dth) for n in range(1, N + 1))
+                want = np.sum((1.0 + rq[i] * rk[j]) * ang)
+                assert abs(pq[i] @ pk[j] - want) < 1e-12, (N, i, j)
+
+
+def check_harmonic_quadratic_equals_recurrent_and_decode():
+    c = _small_case(seed=33, B=2, T=9, d=3)
+    for N in (2, 3):
+        o, D = O.attn_harmonic(**c, N=N, eps=0.4, pos0=3)
+        F = O.harmonic_channels(N) * 3
+        Sx = np.zeros((2, 2, F, 2))
+        zx = np.zeros((2, 2, F))
+        for t in range(9):
+            g = np.repeat(c["gamma"][None], 2, 0).reshape(-1)
+            om = np.repeat(c["omega"][None], 2, 0).reshape(-1, 3)
+            ph = np.repeat(c["phi"][None], 2, 0).reshape(-1, 3)
+            Sn, zn, on = O.decode_step_harmonic(
+                Sx.reshape(4, F, 2), zx.reshape(4, F), c["q"][:, :, t].reshape(4, 3),
+                c["k"][:, :, t].reshape(4, 3), c["v"][:, :, t].reshape(4, 2), g, om, ph,
+                np.full(4, 3 + t), N, eps=0.4)
+            Sx, zx = Sn.reshape(2, 2, F, 2), zn.reshape(2, 2, F)
+            assert np.allclose(on.reshape(2, 2, 2), o[:, :, t], atol=1e-12), (N, t)
+        S_ref, z_ref = O.final_state_harmonic(c["k"], c["v"], c["gamma"], c["omega"], c["phi"], N,
+                                              pos0=3)
+        assert np.allclose(Sx, S_ref, atol=1e-12) and np.allclose(zx, z_ref, atol=1e-12)
+
+
+def check_harmonic_channels_double_angle():
+    # the second harmonic channels obey cos 2x = 2 cos^2 x - 1 and sin 2x =
+    # 2 sin x cos x in terms of the first ones, and the root block is r times
+    # the angle block (channel order [A, r A] per dimension)
+    c = _small_case(seed=34, T=5, d=3)
+    f = O.featurize_harmonic(c["k"], c["gamma"], c["omega"], c["phi"], 2, pos0=11)
+    f = f.reshape(f.shape[:-1] + (3, 10))
+    cos1, sin1, cos2, sin2 = f[..., 1], f[..., 2], f[..., 3], f[..., 4]
+    assert np.allclose(cos2, 2 * cos1 ** 2 - 1, atol=1e-13)
+    assert np.allclose(sin2, 2 * sin1 * cos1, atol=1e-13)
+    assert np.allclose(f[..., 0], 1.0)
+    r = f[..., 5]
+    assert np.allclose(f[..., 5:], r[..., None] * f[..., :5], atol=1e-15)
+
+
+def check_harmonic_state_size():
+    # N = 1 is the paper's 14,376,960 bytes; each harmonic adds 4d features
+    assert O.state_bytes_harmonic(12, 12, 64, 64, 1) == 14376960
+    assert O.state_bytes_harmonic(12, 12, 64, 64, 2) == 12 * 12 * (640 * 64 + 640) * 4
+
+
+ALL_CHECKS += [check_harmonic_one_is_six_channel, check_harmonic_kernel_closed_form,
+               check_harmonic_quadratic_equals_recurrent_and_decode, check_harmonic_state_size,
+               check_harmonic_channels_double_angle]

@@ -14,7 +14,8 @@ _orig = {n: getattr(O, n) for n in ("squash", "soft_root", "rotate", "features_f
                                      "attn_quadratic", "attn_recurrent", "attn_backward",
                                      "_feature_vjp", "state_bytes", "featurize", "attn_power",
                                      "attn_power_backward", "attn_ablation",
-                                     "features4_from_angles", "ablation_scale")}
+                                     "features4_from_angles", "ablation_scale",
+                                     "features_harmonic_from_angles")}
 
 
 def m_squash_no_abs(u):
@@ -224,6 +225,29 @@ def m_ablation_scale_4d(channels, d, shift=0.0):
     return 4.0 * d
 
 
+def m_harmonic_unrotated_multiple(theta_rot, r, N):
+    # a plausible slip: the n-th harmonic of the rotated angle taken as
+    # n theta + t phi (rotation not multiplied) -- emulated by using n = 1 rotation
+    th = np.asarray(theta_rot, dtype=np.float64)
+    ang = [np.ones_like(th)]
+    for n in range(1, N + 1):
+        ang += [np.cos(th * (1 if n == 1 else n) + (0.1 if n > 1 else 0.0)),
+                np.sin(th * (1 if n == 1 else n) + (0.1 if n > 1 else 0.0))]
+    A = np.stack(ang, axis=-1)
+    blk = np.concatenate([A, np.asarray(r)[..., None] * A], axis=-1)
+    return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * blk.shape[-1],))
+
+
+def m_harmonic_no_label_block(theta_rot, r, N):
+    th = np.asarray(theta_rot, dtype=np.float64)
+    ang = [np.ones_like(th)]
+    for n in range(1, N + 1):
+        ang += [np.cos(n * th), np.sin(n * th)]
+    A = np.stack(ang, axis=-1)
+    blk = np.concatenate([A, A], axis=-1)
+    return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * blk.shape[-1],))
+
+
 MUTANTS = {
     "squash_no_abs": ("squash", m_squash_no_abs),
     "squash_square": ("squash", m_squash_square),
@@ -251,6 +275,8 @@ MUTANTS = {
     "three_channel_shift_ignored": ("attn_ablation", _ablation_mutant("shift_ignored")),
     "four_channel_angles_unrooted": ("features4_from_angles", m_features4_unrooted),
     "ablation_scale_4d": ("ablation_scale", m_ablation_scale_4d),
+    "harmonic_phase_slip": ("features_harmonic_from_angles", m_harmonic_unrotated_multiple),
+    "harmonic_without_root_label": ("features_harmonic_from_angles", m_harmonic_no_label_block),
 }
 
 
