@@ -391,6 +391,67 @@ int sanatan_device_status(void* stream) {
   return h ? SANATAN_ERR_TIMEOUT : SANATAN_OK;
 }
 
+size_t sanatan_state_bytes_harmonic(int layers, int heads, int d, int dv, int harmonics) {
+  if (layers < 0 || heads < 0 || d < 0 || dv < 0 || harmonics < 1) return 0;
+  const size_t F = static_cast<size_t>(2 * (2 * harmonics + 1)) * d;
+  return static_cast<size_t>(layers) * heads * (F * dv + F) * sizeof(float);
+}
+
+int sanatan_featurize_harmonic(const void* u, int u_dtype, const float* gamma, const float* omega,
+                               const float* phi, int B, int H, int T, int d, int64_t pos0,
+                               int harmonics, void* out, int out_dtype, void* stream) {
+  if (!ok_dtype(u_dtype) || !ok_dtype(out_dtype)) return SANATAN_ERR_INVALID;
+  if (B < 0 || H < 0 || T < 0 || d <= 0 || harmonics < 1) return SANATAN_ERR_INVALID;
+  if (d != 64 || harmonics > 3) return SANATAN_ERR_UNSUPPORTED;
+  const int64_t n = static_cast<int64_t>(B) * H * T;
+  if (n == 0) return SANATAN_OK;
+  if (!ok_ptr(u) || !ok_ptr(out)) return SANATAN_ERR_INVALID;
+  if (int s = check_params(gamma, omega, phi)) return s;
+  if (n * d / 256 + 1 > 0x7fffffffLL) return SANATAN_ERR_UNSUPPORTED;
+  if (int s = check_arch()) return s;
+  HarmonicFeatArgs a{u, u_dtype, gamma, omega, phi, B, H, T, pos0, harmonics, out, out_dtype};
+  return from_cuda(featurize_harmonic_launch(a, static_cast<cudaStream_t>(stream)));
+}
+
+int sanatan_chunk_fwd_harmonic(const void* q, const void* k, const void* v, int in_dtype,
+                               const float* gamma, const float* omega, const float* phi, int B,
+                               int H, int T, int d, int dv, int64_t pos0, int harmonics,
+                               float eps, const float* S0, const float* z0, float* o, float* D,
+                               float* S_out, float* z_out, void* stream) {
+  if (!ok_dtype(in_dtype) || harmonics < 1) return SANATAN_ERR_INVALID;
+  if (int s = check_sizes(B, H, T, d, dv)) return s;
+  if (harmonics > 2) return SANATAN_ERR_UNSUPPORTED;
+  if ((S0 == nullptr) != (z0 == nullptr)) return SANATAN_ERR_INVALID;
+  if ((S_out == nullptr) != (z_out == nullptr)) return SANATAN_ERR_INVALID;
+  if (!ok_nullable(S0) || !ok_nullable(z0) || !ok_nullable(S_out) || !ok_nullable(z_out) ||
+      !ok_nullable(D))
+    return SANATAN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * H == 0) return SANATAN_OK;
+  if (T > 0 && (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(o))) return SANATAN_ERR_INVALID;
+  if (int s = check_params(gamma, omega, phi)) return s;
+  if (int s = check_arch()) return s;
+  ChunkFwdArgs a{q, k, v, in_dtype, gamma, omega, phi, B, H, T, d, dv, pos0, eps,
+                 S0, z0, o, D, S_out, z_out, nullptr, 0};
+  return from_cuda(chunk_fwd_harmonic_launch(a, harmonics, static_cast<cudaStream_t>(stream)));
+}
+
+int sanatan_decode_step_harmonic(float* S, float* z, const float* q, const float* k,
+                                 const float* v, const float* gamma, const float* omega,
+                                 const float* phi, const int64_t* pos, int N, int G, int d, int dv,
+                                 int harmonics, float eps, float* o, void* stream) {
+  if (N < 0 || G <= 0 || d < 0 || dv < 0 || harmonics < 1) return SANATAN_ERR_INVALID;
+  if (d != 64 || dv != 64 || harmonics > 3) return SANATAN_ERR_UNSUPPORTED;
+  if (N == 0) return SANATAN_OK;
+  if (!ok_ptr(S) || !ok_ptr(z) || !ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(pos) ||
+      !ok_ptr(o))
+    return SANATAN_ERR_INVALID;
+  if (int s = check_params(gamma, omega, phi)) return s;
+  if (static_cast<int64_t>(N) * 4 > 0x7fffffffLL) return SANATAN_ERR_UNSUPPORTED;
+  if (int s = check_arch()) return s;
+  return from_cuda(decode_harmonic_launch(S, z, q, k, v, gamma, omega, phi, pos, N, G, eps,
+                                          harmonics, o, static_cast<cudaStream_t>(stream)));
+}
+
 int sanatan_selftest_wait_timeout(uint64_t timeout_ns, int arrive, void* stream) {
   if (timeout_ns < 1000ull || timeout_ns > 1000000000ull) return SANATAN_ERR_INVALID;
   if (arrive != 0 && arrive != 1) return SANATAN_ERR_INVALID;

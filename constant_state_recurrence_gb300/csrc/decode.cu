@@ -208,8 +208,14 @@ cudaError_t decode_step_launch(float* S, float* z, const float* q, const float* 
                                const float* phi, const int64_t* pos, int N, int G, float eps,
                                float* o, cudaStream_t st) {
   if (N == 0) return cudaSuccess;
-  // Fewer slots than about four per SM: split each slot over a 4-CTA cluster
-  // so that every SM streams part of the state.
+  // Up to two slots per SM: one 1024-thread CTA per slot (six state loads in
+  // flight per thread); up to four: a 4-CTA cluster per slot so that every SM
+  // streams part of the state; more: one 256-thread CTA per slot.
+  if (static_cast<int64_t>(N) <= 2LL * sm_count_decode()) {
+    decode_step_kernel<1, 1024><<<N, 1024, 0, st>>>(S, z, q, k, v, gamma, omega, phi, pos, G, eps,
+                                                    o);
+    return cudaGetLastError();
+  }
   if (static_cast<int64_t>(N) < 4LL * sm_count_decode()) {
     constexpr int kR = 4;
     cudaLaunchConfig_t cfg{};

@@ -66,6 +66,27 @@ cudaError_t decode_step_launch(float* S, float* z, const float* q, const float* 
                                const float* phi, const int64_t* pos, int N, int G, float eps,
                                float* o, cudaStream_t st);
 
+// Harmonic feature map (harmonics n = 1..N, N <= 3).
+struct HarmonicFeatArgs {
+  const void* u;
+  int u_dtype;
+  const float* gamma;
+  const float* omega;
+  const float* phi;
+  int B, H, T;
+  int64_t pos0;
+  int harmonics;
+  void* out;
+  int out_dtype;
+};
+cudaError_t featurize_harmonic_launch(const HarmonicFeatArgs& a, cudaStream_t st);
+// f32 chunked forward with the harmonic map (N <= 2; bf16 or f32 loads).
+cudaError_t chunk_fwd_harmonic_launch(const ChunkFwdArgs& a, int harmonics, cudaStream_t st);
+cudaError_t decode_harmonic_launch(float* S, float* z, const float* q, const float* k,
+                                   const float* v, const float* gamma, const float* omega,
+                                   const float* phi, const int64_t* pos, int N, int G, float eps,
+                                   int harmonics, float* o, cudaStream_t st);
+
 size_t chunk_fwd_simt_smem_bytes();
 size_t chunk_bwd_simt_smem_bytes();
 cudaError_t chunk_bwd_simt_launch(const ChunkBwdArgs& a, cudaStream_t st);

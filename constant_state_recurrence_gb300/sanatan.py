@@ -60,6 +60,15 @@ _SIGS = {
     "sanatan_device_status": (_c_int, [_c_p]),
     "sanatan_set_profile_events": (_c_int, [_c_p, _c_p]),
     "sanatan_selftest_wait_timeout": (_c_int, [ctypes.c_uint64, _c_int, _c_p]),
+    "sanatan_state_bytes_harmonic": (_c_sz, [_c_int] * 5),
+    "sanatan_featurize_harmonic": (_c_int, [_c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int,
+                                            _c_int, _c_i64, _c_int, _c_p, _c_int, _c_p]),
+    "sanatan_chunk_fwd_harmonic": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_int,
+                                            _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_f,
+                                            _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "sanatan_decode_step_harmonic": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                              _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f,
+                                              _c_p, _c_p]),
     "sanatan_decode_step": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_int,
                                      _c_int, _c_int, _c_int, _c_f, _c_p, _c_p]),
 }
@@ -522,6 +531,76 @@ def sanatan_decode_step(S, z, q, k, v, gamma, omega, phi, pos, eps=0.0, out=None
                                    _ptr(omega), _ptr(phi), _ptr(pos), N, G, d, dv, float(eps),
                                    _ptr(o), _stream(q.device))
     _check("sanatan_decode_step", st)
+    return o
+
+
+def harmonic_features(harmonics, d=64):
+    """F_N = 2 (2N + 1) d features of the harmonic map."""
+    return 2 * (2 * harmonics + 1) * d
+
+
+def sanatan_featurize_harmonic(u, gamma, omega, phi, harmonics, pos0=0, out_dtype=None):
+    """Phi_N(u) [B, H, T, F_N] of the harmonic map."""
+    _need(u, "u", (torch.float32, torch.bfloat16))
+    B, H, T, d = u.shape
+    _need_params(gamma, omega, phi, H, d)
+    out = torch.empty(B, H, T, harmonic_features(harmonics, d), dtype=out_dtype or torch.float32,
+                      device=u.device)
+    _check("sanatan_featurize_harmonic",
+           lib().sanatan_featurize_harmonic(_ptr(u), _DT[u.dtype], _ptr(gamma), _ptr(omega),
+                                            _ptr(phi), B, H, T, d, int(pos0), int(harmonics),
+                                            _ptr(out), _DT[out.dtype], _stream(u.device)))
+    return out
+
+
+def sanatan_chunk_fwd_harmonic(q, k, v, gamma, omega, phi, harmonics, pos0=0, eps=0.0, S0=None,
+                               z0=None, want_D=True, want_state=False):
+    """Causal p=1 attention with the harmonic map (float32 on the CUDA cores).
+    Returns (o, D or None, S [B,H,F_N,dv] or None, z [B,H,F_N] or None)."""
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    B, H, T, d = q.shape
+    _need(k, "k", (q.dtype,), (B, H, T, d))
+    dv = v.shape[-1]
+    _need(v, "v", (q.dtype,), (B, H, T, dv))
+    _need_params(gamma, omega, phi, H, d)
+    F = harmonic_features(harmonics, d)
+    dev = q.device
+    o = torch.empty(B, H, T, dv, dtype=torch.float32, device=dev)
+    D = torch.empty(B, H, T, dtype=torch.float32, device=dev) if want_D else None
+    Sx = zx = None
+    if want_state:
+        Sx = torch.empty(B, H, F, dv, dtype=torch.float32, device=dev)
+        zx = torch.empty(B, H, F, dtype=torch.float32, device=dev)
+    if S0 is not None:
+        _need(S0, "S0", (torch.float32,), (B, H, F, dv))
+        _need(z0, "z0", (torch.float32,), (B, H, F))
+    _check("sanatan_chunk_fwd_harmonic",
+           lib().sanatan_chunk_fwd_harmonic(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(gamma),
+                                            _ptr(omega), _ptr(phi), B, H, T, d, dv, int(pos0),
+                                            int(harmonics), float(eps), _ptr(S0), _ptr(z0),
+                                            _ptr(o), _ptr(D), _ptr(Sx), _ptr(zx), _stream(dev)))
+    return o, D, Sx, zx
+
+
+def sanatan_decode_step_harmonic(S, z, q, k, v, gamma, omega, phi, pos, harmonics, eps=0.0):
+    """One decode token with the harmonic map; S [N,F_N,dv], z [N,F_N] in place."""
+    _need(q, "q", (torch.float32,))
+    N, d = q.shape
+    _need(k, "k", (torch.float32,), (N, d))
+    dv = v.shape[-1]
+    _need(v, "v", (torch.float32,), (N, dv))
+    F = harmonic_features(harmonics, d)
+    _need(S, "S", (torch.float32,), (N, F, dv))
+    _need(z, "z", (torch.float32,), (N, F))
+    _need(pos, "pos", (torch.int64,), (N,))
+    G = gamma.shape[0]
+    _need_params(gamma, omega, phi, G, d)
+    o = torch.empty(N, dv, dtype=torch.float32, device=q.device)
+    _check("sanatan_decode_step_harmonic",
+           lib().sanatan_decode_step_harmonic(_ptr(S), _ptr(z), _ptr(q), _ptr(k), _ptr(v),
+                                              _ptr(gamma), _ptr(omega), _ptr(phi), _ptr(pos), N,
+                                              G, d, dv, int(harmonics), float(eps), _ptr(o),
+                                              _stream(q.device)))
     return o
 
 

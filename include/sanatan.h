@@ -293,6 +293,47 @@ SANATAN_API int sanatan_set_profile_events(void* start, void* stop);
 SANATAN_API int sanatan_device_status(void* stream);
 
 /*
+ * Harmonic feature map (the notes' Appendix B, "附录 B 的频谱展望"): harmonics
+ * cos(n th), sin(n th), n = 1..N, added to the angle block; at p = 1 the
+ * attention stays an explicit feature-map attention with a constant-size state
+ * of F_N = 2(2N + 1) d features (N = 1: the six-channel map).  Per dimension a
+ * the channels are [A, r A], A = [1, cos th, sin th, ..., cos N th, sin N th]
+ * with th the rotated angle and r the root of the un-rotated one; channel
+ * l (2N + 1) + m of dimension a sits at a * 2(2N + 1) + l (2N + 1) + m.  The
+ * kernel is sum_a (1 + r_q r_k)(1 + sum_n cos(n dtheta_a)).  These calls run in
+ * float32 on the CUDA cores.
+ *
+ * sanatan_state_bytes_harmonic -- bytes of S (F_N x dv) and z (F_N) float32 of
+ *   layers x heads heads (host arithmetic; 0 for harmonics < 1).
+ * sanatan_featurize_harmonic -- Phi_N(u) [B, H, T, F_N] in out_dtype for u
+ *   [B, H, T, d]; harmonics 1..3 (SANATAN_ERR_UNSUPPORTED above 3).
+ * sanatan_chunk_fwd_harmonic -- the causal normalised attention of
+ *   sanatan_chunk_fwd with Phi_N (arguments, layouts and outputs as there with
+ *   6d replaced by F_N; no workspace); q, k, v f32 or bf16 (converted to f32);
+ *   harmonics 1..2 (the state of one sequence lives in shared memory).
+ * sanatan_decode_step_harmonic -- one token of the recurrence with Phi_N for N
+ *   slots, as sanatan_decode_step with S [N, F_N, dv] and z [N, F_N];
+ *   harmonics 1..3.
+ */
+SANATAN_API size_t sanatan_state_bytes_harmonic(int layers, int heads, int d, int dv,
+                                                int harmonics);
+SANATAN_API int sanatan_featurize_harmonic(const void* u, int u_dtype, const float* gamma,
+                                           const float* omega, const float* phi, int B, int H,
+                                           int T, int d, int64_t pos0, int harmonics, void* out,
+                                           int out_dtype, void* stream);
+SANATAN_API int sanatan_chunk_fwd_harmonic(const void* q, const void* k, const void* v,
+                                           int in_dtype, const float* gamma, const float* omega,
+                                           const float* phi, int B, int H, int T, int d, int dv,
+                                           int64_t pos0, int harmonics, float eps, const float* S0,
+                                           const float* z0, float* o, float* D, float* S_out,
+                                           float* z_out, void* stream);
+SANATAN_API int sanatan_decode_step_harmonic(float* S, float* z, const float* q, const float* k,
+                                             const float* v, const float* gamma,
+                                             const float* omega, const float* phi,
+                                             const int64_t* pos, int N, int G, int d, int dv,
+                                             int harmonics, float eps, float* o, void* stream);
+
+/*
  * sanatan_selftest_wait_timeout -- failure-detection self-test (the paper has
  * no counterpart).  Enqueues one small kernel whose thread waits, with the
  * same bounded mbarrier wait the tensor-core kernels use, on a barrier that

@@ -134,3 +134,13 @@ def test_eps_raw_conventions(lib):
     assert lib.sanatan_eps_raw(1.0, 0, 0) == -1.0 and lib.sanatan_eps_raw(1.0, 64, 2) == -1.0
     assert lib.sanatan_rate_from_raw(None, -1, 0.01, None, None) == 1
     assert lib.sanatan_rate_from_raw_bwd(None, None, -1, 0.01, None, None) == 1
+
+
+def test_harmonic_state_bytes_and_argument_errors(lib):
+    assert lib.sanatan_state_bytes_harmonic(12, 12, 64, 64, 1) == 14376960
+    assert lib.sanatan_state_bytes_harmonic(12, 12, 64, 64, 2) == 12 * 12 * (640 * 64 + 640) * 4
+    assert lib.sanatan_state_bytes_harmonic(1, 1, 64, 64, 0) == 0
+    assert lib.sanatan_featurize_harmonic(None, 0, None, None, None, 1, 1, 1, 64, 0, 0, None, 0,
+                                          None) == 1
+    assert lib.sanatan_featurize_harmonic(None, 0, None, None, None, 1, 1, 1, 64, 0, 4, None, 0,
+                                          None) == 2

@@ -1,0 +1,114 @@
+"""The harmonic feature map (Appendix B of the notes) on the GPU against the
+float64 oracle: features (f32 <= 1e-5 abs), the chunked p=1 forward (f32:
+<= 1e-5 on o, state relative <= 1e-5), the decode step (<= 1e-5), chunked vs
+decode (<= 1e-4), and N = 1 against the six-channel entry points."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.sanatan_oracle as O
+from constant_state_recurrence_gb300 import sanatan as S
+from constant_state_recurrence_gb300 import workloads as W
+from gpu_util import dev, f64, max_abs, ref_args, rel_fro, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("N", [1, 2, 3])
+def test_features(N):
+    x = W.make(W.TINY, B=1, H=2, T=50)
+    x["phi"] = W.rates(2, 64, "geometric")
+    g = to_dev(x)
+    f = S.sanatan_featurize_harmonic(g["q"], g["gamma"], g["omega"], g["phi"], N, pos0=300)
+    torch.cuda.synchronize()
+    ra = ref_args(x)
+    ref = O.featurize_harmonic(ra["q"], ra["gamma"], ra["omega"], ra["phi"], N, pos0=300)
+    assert max_abs(f64(f), ref) <= 1e-5
+
+
+@pytest.mark.parametrize("T", [1, 7, 8, 9, 100])
+def test_chunked_forward_two_harmonics(T):
+    x = W.make(W.TINY, B=2, H=2, T=T)
+    x["phi"] = W.rates(2, 64, "geometric")
+    g = to_dev(x)
+    o, D, Sx, zx = S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
+                                                g["phi"], 2, pos0=40, eps=0.2, want_state=True)
+    torch.cuda.synchronize()
+    ra = ref_args(x)
+    o_ref, D_ref = O.attn_harmonic(**ra, N=2, pos0=40, eps=0.2)
+    S_ref, z_ref = O.final_state_harmonic(ra["k"], ra["v"], ra["gamma"], ra["omega"], ra["phi"], 2,
+                                          pos0=40)
+    assert max_abs(f64(o), o_ref) <= 1e-5
+    assert rel_fro(f64(D), D_ref) <= 1e-5
+    assert rel_fro(f64(Sx), S_ref) <= 1e-5 and rel_fro(f64(zx), z_ref) <= 1e-5
+
+
+def test_chunked_forward_bf16_inputs_and_initial_state():
+    x = W.make(W.LAYER, B=1, H=3, T=77)
+    g = to_dev(x)
+    ra = ref_args(x)
+    rng = np.random.default_rng(4)
+    S0, z0 = O.final_state_harmonic(rng.standard_normal((1, 3, 30, 64)),
+                                    rng.standard_normal((1, 3, 30, 64)), ra["gamma"], ra["omega"],
+                                    ra["phi"], 2, pos0=500)
+    S0t, z0t = torch.tensor(S0, dtype=torch.float32), torch.tensor(z0, dtype=torch.float32)
+    o, _, _, _ = S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
+                                              g["phi"], 2, pos0=530, S0=S0t.to(dev()),
+                                              z0=z0t.to(dev()))
+    torch.cuda.synchronize()
+    o_ref, _ = O.attn_harmonic(**ra, N=2, pos0=530, S0=f64(S0t), z0=f64(z0t))
+    assert max_abs(f64(o), o_ref) <= 1e-5
+
+
+@pytest.mark.parametrize("N", [1, 2, 3])
+def test_decode_steps_match_oracle_and_chunked(N):
+    """T single-token steps from the zero state reproduce the oracle (1e-5) and,
+    for N <= 2, the chunked forward (1e-4)."""
+    x = W.make(W.TINY, B=1, H=3, T=40)
+    x["phi"] = W.rates(3, 64, "geometric")
+    g = to_dev(x)
+    F = S.harmonic_features(N)
+    Sd = torch.zeros(3, F, 64, device=dev())
+    zd = torch.zeros(3, F, device=dev())
+    outs = []
+    for t in range(40):
+        pos = torch.full((3,), 900 + t, dtype=torch.int64, device=dev())
+        outs.append(S.sanatan_decode_step_harmonic(Sd, zd, g["q"][0, :, t].contiguous(),
+                                                   g["k"][0, :, t].contiguous(),
+                                                   g["v"][0, :, t].contiguous(), g["gamma"],
+                                                   g["omega"], g["phi"], pos, N, eps=0.1))
+    od = torch.stack(outs, 1).unsqueeze(0)
+    torch.cuda.synchronize()
+    o_ref, _ = O.attn_harmonic(**ref_args(x), N=N, pos0=900, eps=0.1)
+    assert max_abs(f64(od), o_ref) <= 1e-5
+    if N <= 2:
+        oc, _, Sc, zc = S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
+                                                     g["phi"], N, pos0=900, eps=0.1,
+                                                     want_state=True)
+        torch.cuda.synchronize()
+        assert max_abs(f64(od), f64(oc)) <= 1e-4
+        assert rel_fro(f64(Sd), f64(Sc)[0]) <= 1e-5
+
+
+def test_one_harmonic_is_the_six_channel_path():
+    x = W.make(W.TINY, B=1, H=2, T=64)
+    g = to_dev(x)
+    a, _, _, _ = S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
+                                              g["phi"], 1)
+    b, _, _, _ = S.sanatan_chunk_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"])
+    fa = S.sanatan_featurize_harmonic(g["q"], g["gamma"], g["omega"], g["phi"], 1)
+    fb = S.sanatan_featurize(g["q"], g["gamma"], g["omega"], g["phi"])
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert (fa - fb).abs().max().item() <= 1e-6
+
+
+def test_argument_errors():
+    x = W.make(W.TINY, B=1, H=1, T=4)
+    g = to_dev(x)
+    with pytest.raises(S.SanatanError) as e:
+        S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], 3)
+    assert e.value.status == 2
+    with pytest.raises(S.SanatanError) as e:
+        S.sanatan_featurize_harmonic(g["q"], g["gamma"], g["omega"], g["phi"], 4)
+    assert e.value.status == 2
