@@ -3,8 +3,9 @@
 //   S <- S + Phi(k) v^T,  z <- z + Phi(k),  o = Phi(q)^T S / (Phi(q)^T z + eps).
 // The step streams each slot's 6d x dv float32 state once (read + write).
 //
-// A slot is split over a cluster of R CTAs by feature rows (R = 4 when there
-// are too few slots to fill the GPU, else 1).  Each CTA issues the loads of
+// A slot is handled by one CTA (1024 threads when there are at most two slots
+// per SM, 256 when there are more than four) or split over a cluster of R = 4
+// CTAs by feature rows (in between).  Each CTA issues the loads of
 // its whole row block first and featurises q and k for its rows while they
 // are in flight; the readout partial sums (numerator and denominator) are
 // reduced with warp shuffles, a shared-memory tree and, across the cluster,
