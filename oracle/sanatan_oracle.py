@@ -1,7 +1,8 @@
 """Float64 CPU oracle for SANATAN root-parity gated angular attention: the
 feature map, the p = 1 causal attention in its quadratic and recurrent forms,
 the power-sharpened attention of eq. (8) at integer p, and their gradients,
-the four- and three-channel ablation kernels, and the harmonic feature map.
+the four- and three-channel ablation kernels, the harmonic feature map, and
+the attention stack of several layers (parallel form and decode step).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
@@ -590,6 +591,59 @@ def state_bytes_harmonic(layers, heads, d, dv, N, bytes_per_float=4):
     F_N = 2(2N + 1) d (N = 1: the six-channel 6 d^2 + 6 d of Notes §2.7)."""
     F = harmonic_channels(N) * d
     return layers * heads * (F * dv + F) * bytes_per_float
+
+
+# ---------------------------------------------------------------------------
+# Multi-layer attention stack (Notes §2.7: the whole-model recurrence updates
+# the layers' states in order, each layer with its own weights, at the same
+# positions; §3.1: 12 layers x 12 heads x d = 64).  The attention path only:
+# per layer x -> q, k, v = x Wq, x Wk, x Wv, the p = 1 attention of every
+# head, x <- x + a Wo (no normalisation layers or MLP).
+# ---------------------------------------------------------------------------
+
+
+def stack_parallel(X, Wqkv, Wo, gamma, omega, phi, heads, pos0=0, eps=0.0):
+    """The attention stack over a whole sequence in the parallel form:
+    X [B, T, heads*d]; Wqkv [L, heads*d, 3*heads*d] (columns: q | k | v);
+    Wo [L, heads*d, heads*d]; gamma [L, heads]; omega, phi [L, heads, d].
+    Every layer's attention is attn_quadratic over the whole prefix.
+    Returns the last layer's output X [B, T, heads*d]."""
+    X = np.asarray(X, dtype=np.float64)
+    B, T, Dm = X.shape
+    L = np.asarray(Wqkv).shape[0]
+    d = Dm // heads
+    for l in range(L):
+        qkv = X @ np.asarray(Wqkv[l], dtype=np.float64)
+        sp = lambda m: m.reshape(B, T, heads, d).transpose(0, 2, 1, 3)  # noqa: E731
+        q, k, v = sp(qkv[..., :Dm]), sp(qkv[..., Dm:2 * Dm]), sp(qkv[..., 2 * Dm:])
+        o, _ = attn_quadratic(q, k, v, gamma[l], omega[l], phi[l], pos0=pos0, eps=eps)
+        A = o.transpose(0, 2, 1, 3).reshape(B, T, Dm)
+        X = X + A @ np.asarray(Wo[l], dtype=np.float64)
+    return X
+
+
+def stack_decode_step(x, Wqkv, Wo, S, z, gamma, omega, phi, heads, pos, eps=0.0):
+    """One token through the attention stack with the constant-state
+    recurrence: x [B, heads*d]; S [L, B*heads, 6d, d], z [L, B*heads, 6d]
+    (slot b * heads + h); pos [B] integer positions.  Returns (x, S, z)."""
+    x = np.asarray(x, dtype=np.float64)
+    B, Dm = x.shape
+    L = np.asarray(Wqkv).shape[0]
+    d = Dm // heads
+    S = np.array(S, dtype=np.float64)
+    z = np.array(z, dtype=np.float64)
+    slot_pos = np.repeat(np.asarray(pos, dtype=np.int64), heads)
+    for l in range(L):
+        qkv = x @ np.asarray(Wqkv[l], dtype=np.float64)
+        q = qkv[:, :Dm].reshape(B * heads, d)
+        k = qkv[:, Dm:2 * Dm].reshape(B * heads, d)
+        v = qkv[:, 2 * Dm:].reshape(B * heads, d)
+        g = np.tile(np.asarray(gamma[l], dtype=np.float64), B)
+        om = np.tile(np.asarray(omega[l], dtype=np.float64), (B, 1))
+        ph = np.tile(np.asarray(phi[l], dtype=np.float64), (B, 1))
+        S[l], z[l], o = decode_step(S[l], z[l], q, k, v, g, om, ph, slot_pos, eps=eps)
+        x = x + o.reshape(B, Dm) @ np.asarray(Wo[l], dtype=np.float64)
+    return x, S, z
 
 
 # ---------------------------------------------------------------------------

@@ -665,3 +665,49 @@ def check_harmonic_state_size():
 ALL_CHECKS += [check_harmonic_one_is_six_channel, check_harmonic_kernel_closed_form,
                check_harmonic_quadratic_equals_recurrent_and_decode, check_harmonic_state_size,
                check_harmonic_channels_double_angle]
+
+
+# --------------------------------------------------------------------------
+# Attention stack: the stepped recurrence through all layers equals the
+# parallel form (the pages' parallel-vs-recurrent agreement, Notes §2.7)
+# --------------------------------------------------------------------------
+
+def _stack_case(seed=41, B=2, T=6, L=3, heads=2, d=3):
+    g = _rng(seed)
+    Dm = heads * d
+    return dict(X=g.standard_normal((B, T, Dm)),
+                Wqkv=g.standard_normal((L, Dm, 3 * Dm)) / math.sqrt(Dm),
+                Wo=g.standard_normal((L, Dm, Dm)) / math.sqrt(Dm),
+                gamma=g.uniform(1.0, 5.0, (L, heads)),
+                omega=g.uniform(-math.pi, math.pi, (L, heads, d)),
+                phi=g.uniform(0.0, 0.3, (L, heads, d)), heads=heads)
+
+
+def check_stack_recurrent_equals_parallel():
+    c = _stack_case()
+    B, T, Dm = c["X"].shape
+    L, heads = c["Wqkv"].shape[0], c["heads"]
+    d = Dm // heads
+    Y = O.stack_parallel(**c, pos0=7, eps=0.3)
+    S = np.zeros((L, B * heads, 6 * d, d))
+    z = np.zeros((L, B * heads, 6 * d))
+    for t in range(T):
+        y, S, z = O.stack_decode_step(c["X"][:, t], c["Wqkv"], c["Wo"], S, z, c["gamma"],
+                                      c["omega"], c["phi"], heads, np.full(B, 7 + t), eps=0.3)
+        assert np.allclose(y, Y[:, t], atol=1e-12), t
+
+
+def check_stack_single_layer_is_one_attention():
+    # one layer with identity-like projections: x + attention(x) Wo, directly
+    c = _stack_case(seed=42, L=1)
+    B, T, Dm = c["X"].shape
+    heads, d = c["heads"], Dm // c["heads"]
+    qkv = c["X"] @ c["Wqkv"][0]
+    sp = lambda m: m.reshape(B, T, heads, d).transpose(0, 2, 1, 3)  # noqa: E731
+    o, _ = O.attn_recurrent(sp(qkv[..., :Dm]), sp(qkv[..., Dm:2 * Dm]), sp(qkv[..., 2 * Dm:]),
+                            c["gamma"][0], c["omega"][0], c["phi"][0])[:2]
+    want = c["X"] + o.transpose(0, 2, 1, 3).reshape(B, T, Dm) @ c["Wo"][0]
+    assert np.allclose(O.stack_parallel(**c), want, atol=1e-12)
+
+
+ALL_CHECKS += [check_stack_recurrent_equals_parallel, check_stack_single_layer_is_one_attention]

@@ -15,7 +15,7 @@ _orig = {n: getattr(O, n) for n in ("squash", "soft_root", "rotate", "features_f
                                      "_feature_vjp", "state_bytes", "featurize", "attn_power",
                                      "attn_power_backward", "attn_ablation",
                                      "features4_from_angles", "ablation_scale",
-                                     "features_harmonic_from_angles")}
+                                     "features_harmonic_from_angles", "stack_decode_step")}
 
 
 def m_squash_no_abs(u):
@@ -248,6 +248,26 @@ def m_harmonic_no_label_block(theta_rot, r, N):
     return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * blk.shape[-1],))
 
 
+def m_stack_no_residual(x, Wqkv, Wo, S, z, gamma, omega, phi, heads, pos, eps=0.0):
+    # the residual dropped: x <- a Wo
+    x = np.asarray(x, dtype=np.float64)
+    B, Dm = x.shape
+    d = Dm // heads
+    S = np.array(S, dtype=np.float64)
+    z = np.array(z, dtype=np.float64)
+    sp_ = np.repeat(np.asarray(pos, dtype=np.int64), heads)
+    for l in range(np.asarray(Wqkv).shape[0]):
+        qkv = x @ Wqkv[l]
+        g = np.tile(gamma[l], B)
+        om = np.tile(omega[l], (B, 1))
+        ph = np.tile(phi[l], (B, 1))
+        S[l], z[l], o = O.decode_step(S[l], z[l], qkv[:, :Dm].reshape(-1, d),
+                                      qkv[:, Dm:2 * Dm].reshape(-1, d),
+                                      qkv[:, 2 * Dm:].reshape(-1, d), g, om, ph, sp_, eps=eps)
+        x = o.reshape(B, Dm) @ Wo[l]
+    return x, S, z
+
+
 MUTANTS = {
     "squash_no_abs": ("squash", m_squash_no_abs),
     "squash_square": ("squash", m_squash_square),
@@ -277,6 +297,7 @@ MUTANTS = {
     "ablation_scale_4d": ("ablation_scale", m_ablation_scale_4d),
     "harmonic_phase_slip": ("features_harmonic_from_angles", m_harmonic_unrotated_multiple),
     "harmonic_without_root_label": ("features_harmonic_from_angles", m_harmonic_no_label_block),
+    "stack_without_residual": ("stack_decode_step", m_stack_no_residual),
 }
 
 
