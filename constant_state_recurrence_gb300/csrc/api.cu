@@ -452,6 +452,28 @@ int sanatan_decode_step_harmonic(float* S, float* z, const float* q, const float
                                           harmonics, o, static_cast<cudaStream_t>(stream)));
 }
 
+size_t sanatan_stack_decode_workspace_size(int B, int heads, int d) {
+  if (B < 0 || heads < 0 || d != 64) return 0;
+  return stack_workspace_bytes(B, heads, d);
+}
+
+int sanatan_stack_decode_step(float* x, const float* Wqkv, const float* Wo, float* S, float* z,
+                              const float* gamma, const float* omega, const float* phi,
+                              const int64_t* pos, int B, int L, int heads, int d, float eps,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || L < 0 || heads < 0 || d < 0) return SANATAN_ERR_INVALID;
+  if (d != 64 || B > stack_max_batch() || (heads * d) % 128 != 0) return SANATAN_ERR_UNSUPPORTED;
+  if (B == 0 || L == 0 || heads == 0) return SANATAN_OK;
+  if (!ok_ptr(x) || !ok_ptr(Wqkv) || !ok_ptr(Wo) || !ok_ptr(S) || !ok_ptr(z) || !ok_ptr(pos) ||
+      !ok_ptr(workspace))
+    return SANATAN_ERR_INVALID;
+  if (int s = check_params(gamma, omega, phi)) return s;
+  if (workspace_bytes < stack_workspace_bytes(B, heads, d)) return SANATAN_ERR_INVALID;
+  if (int s = check_arch()) return s;
+  StackArgs a{x, Wqkv, Wo, S, z, gamma, omega, phi, pos, B, L, heads, eps, workspace};
+  return from_cuda(stack_decode_launch(a, static_cast<cudaStream_t>(stream)));
+}
+
 int sanatan_selftest_wait_timeout(uint64_t timeout_ns, int arrive, void* stream) {
   if (timeout_ns < 1000ull || timeout_ns > 1000000000ull) return SANATAN_ERR_INVALID;
   if (arrive != 0 && arrive != 1) return SANATAN_ERR_INVALID;

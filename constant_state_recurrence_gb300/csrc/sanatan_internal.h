@@ -87,6 +87,25 @@ cudaError_t decode_harmonic_launch(float* S, float* z, const float* q, const flo
                                    const float* phi, const int64_t* pos, int N, int G, float eps,
                                    int harmonics, float* o, cudaStream_t st);
 
+// One token through L attention layers (stack.cu).
+struct StackArgs {
+  float* x;              // [B, heads * 64], updated in place
+  const float* Wqkv;     // [L, heads * 64, 3 * heads * 64]
+  const float* Wo;       // [L, heads * 64, heads * 64]
+  float* S;              // [L, B * heads, 384, 64]
+  float* z;              // [L, B * heads, 384]
+  const float* gamma;    // [L, heads]
+  const float* omega;    // [L, heads, 64]
+  const float* phi;      // [L, heads, 64]
+  const int64_t* pos;    // [B * heads]
+  int B, L, heads;
+  float eps;
+  void* workspace;       // stack_workspace_bytes
+};
+size_t stack_workspace_bytes(int B, int heads, int d);
+int stack_max_batch();
+cudaError_t stack_decode_launch(const StackArgs& a, cudaStream_t st);
+
 size_t chunk_fwd_simt_smem_bytes();
 size_t chunk_bwd_simt_smem_bytes();
 cudaError_t chunk_bwd_simt_launch(const ChunkBwdArgs& a, cudaStream_t st);

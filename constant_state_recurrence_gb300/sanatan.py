@@ -60,6 +60,10 @@ _SIGS = {
     "sanatan_device_status": (_c_int, [_c_p]),
     "sanatan_set_profile_events": (_c_int, [_c_p, _c_p]),
     "sanatan_selftest_wait_timeout": (_c_int, [ctypes.c_uint64, _c_int, _c_p]),
+    "sanatan_stack_decode_workspace_size": (_c_sz, [_c_int] * 3),
+    "sanatan_stack_decode_step": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                           _c_int, _c_int, _c_int, _c_int, _c_f, _c_p, _c_sz,
+                                           _c_p]),
     "sanatan_state_bytes_harmonic": (_c_sz, [_c_int] * 5),
     "sanatan_featurize_harmonic": (_c_int, [_c_p, _c_int, _c_p, _c_p, _c_p, _c_int, _c_int, _c_int,
                                             _c_int, _c_i64, _c_int, _c_p, _c_int, _c_p]),
@@ -532,6 +536,34 @@ def sanatan_decode_step(S, z, q, k, v, gamma, omega, phi, pos, eps=0.0, out=None
                                    _ptr(o), _stream(q.device))
     _check("sanatan_decode_step", st)
     return o
+
+
+def sanatan_stack_decode_step(x, Wqkv, Wo, S, z, gamma, omega, phi, pos, eps=0.0,
+                              workspace=None):
+    """One token through L attention layers; x [B, heads*64] is updated in
+    place (and returned), S [L, B*heads, 384, 64] and z [L, B*heads, 384] too.
+    gamma [L, heads], omega and phi [L, heads, 64], pos [B*heads] int64."""
+    _need(x, "x", (torch.float32,))
+    B, Dm = x.shape
+    L, heads = gamma.shape
+    d = Dm // heads
+    _need(Wqkv, "Wqkv", (torch.float32,), (L, Dm, 3 * Dm))
+    _need(Wo, "Wo", (torch.float32,), (L, Dm, Dm))
+    _need(S, "S", (torch.float32,), (L, B * heads, 6 * d, d))
+    _need(z, "z", (torch.float32,), (L, B * heads, 6 * d))
+    _need(gamma, "gamma", (torch.float32,), (L, heads))
+    _need(omega, "omega", (torch.float32,), (L, heads, d))
+    _need(phi, "phi", (torch.float32,), (L, heads, d))
+    _need(pos, "pos", (torch.int64,), (B * heads,))
+    ws_n = int(lib().sanatan_stack_decode_workspace_size(B, heads, d))
+    if workspace is None:
+        workspace = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=x.device)
+    _check("sanatan_stack_decode_step",
+           lib().sanatan_stack_decode_step(_ptr(x), _ptr(Wqkv), _ptr(Wo), _ptr(S), _ptr(z),
+                                           _ptr(gamma), _ptr(omega), _ptr(phi), _ptr(pos), B, L,
+                                           heads, d, float(eps), _ptr(workspace),
+                                           workspace.numel(), _stream(x.device)))
+    return x
 
 
 def harmonic_features(harmonics, d=64):

@@ -334,6 +334,33 @@ SANATAN_API int sanatan_decode_step_harmonic(float* S, float* z, const float* q,
                                              int harmonics, float eps, float* o, void* stream);
 
 /*
+ * sanatan_stack_decode_step -- one decode token through L attention layers of
+ * `heads` heads (the notes §2.7: the whole-model recurrence updates the layers'
+ * states in order, each layer with its own weights, at the same positions;
+ * §3.1: 12 layers x 12 heads x d = 64).  The attention path only, float32:
+ * per layer l
+ *     [q | k | v] = x Wqkv[l],  o = sanatan_decode_step of the layer's slots,
+ *     x <- x + o Wo[l].
+ *   x     [B, heads * d] f32, read and written (the token's input, then output)
+ *   Wqkv  [L, heads * d, 3 * heads * d] f32 (columns: q | k | v, head-major)
+ *   Wo    [L, heads * d, heads * d] f32
+ *   S     [L, B * heads, 6d, d] f32 and z [L, B * heads, 6d] f32, updated in
+ *         place (slot b * heads + h of layer l)
+ *   gamma [L, heads], omega, phi [L, heads, d] f32
+ *   pos   [B * heads] int64: the position of the token, per slot
+ *   workspace: sanatan_stack_decode_workspace_size(B, heads, d) bytes.
+ * B <= 8 and heads * d a multiple of 128 (SANATAN_ERR_UNSUPPORTED otherwise).
+ * The projections accumulate with float atomics, so results can differ in the
+ * last bits from run to run.
+ */
+SANATAN_API size_t sanatan_stack_decode_workspace_size(int B, int heads, int d);
+SANATAN_API int sanatan_stack_decode_step(float* x, const float* Wqkv, const float* Wo, float* S,
+                                          float* z, const float* gamma, const float* omega,
+                                          const float* phi, const int64_t* pos, int B, int L,
+                                          int heads, int d, float eps, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/*
  * sanatan_selftest_wait_timeout -- failure-detection self-test (the paper has
  * no counterpart).  Enqueues one small kernel whose thread waits, with the
  * same bounded mbarrier wait the tensor-core kernels use, on a barrier that
