@@ -33,6 +33,9 @@
 // Shared-memory operands use the canonical no-swizzle layout (8 x 16-byte
 // core matrices); TMEM holds P (128 cols), O_ext (80) and the f32 state
 // (3 tiles x 80).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "sanatan_internal.h"
 #include "sanatan_math.cuh"
 #include "tc_ptx.cuh"
@@ -113,6 +116,12 @@ constexpr int kVWarps = 2;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
 
 struct TcParams {
+  // v as a 4-D tensor {8 columns of a group, token, column group, sequence}
+  // (element strides 1, 64, 8, 64 T): one box of 8 x 8 x 8 is the eight 8 x 8
+  // core matrices of a token group of [V | 1], in that order (tma_v = 1;
+  // forward time only).
+  CUtensorMap tmap_v;
+  int tma_v;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
@@ -172,7 +181,7 @@ __device__ __forceinline__ void prefetch_chunk(const TcParams& prm, int64_t seq_
 
 // ---------------------------------------------------------------------------
 template <bool kStateOnly>
-__global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
+__global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_constant__ TcParams prm) {
   extern __shared__ __align__(1024) unsigned char smem[];
   Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
   const uint32_t sQ = smem_u32(smem + kOffQ);
@@ -622,11 +631,32 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(TcParams prm) {
       const int tok0 = (c_begin + ci) * kC;
       const int nrow = min(kC, prm.T - tok0);
       uint32_t vdst = sV;
+      uint64_t* vbar = &m.bar[(kStateOnly && (ci & 1)) ? kFeatV1 : kFeatV];
       if constexpr (kStateOnly) {
         vdst = smem_u32(smem + ((ci & 1) ? kSoV1 : kSoV0));
         if (ci > 1) wait_bar(m, (ci & 1) ? kStateDone1 : kStateDone, ((ci >> 1) - 1) & 1);
       } else {
         if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
+      }
+      if (prm.tma_v) {
+        // 16 tensor loads of one token group each (rows past the end read as
+        // zero); the first value-loader thread's arrival carries their bytes
+        if (vt == 0) {
+          mbar_arrive_expect_tx(vbar, 16u * 8u * 128u);
+          for (int kg = 0; kg < 16; ++kg)
+            tma_load_4d(vdst + kg * kLBO_SV, &prm.tmap_v, 0, tok0 + 8 * kg, 0, bh, vbar);
+        }
+        if (prm.extra != nullptr) {
+          for (int t = vt; t < kC; t += 32 * kVWarps) {
+            const float x = t < nrow ? prm.extra[seq_row0 + orow(prm, tok0 + t)] : 0.f;
+            st_shared_v4(vdst + (t >> 3) * kLBO_SV + 8 * 128 + (t & 7) * 16,
+                         __bfloat16_as_ushort(__float2bfloat16_rn(x)), 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && vt != 0) mbar_arrive(vbar);
+        continue;
       }
       for (int pc = vt; pc < kC * 8; pc += 32 * kVWarps) {
         const int t = pc >> 3, ng = pc & 7;
@@ -808,8 +838,42 @@ cudaError_t tc_set_smem() {
   return e;
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// The tensor map of v for the value loads (see TcParams::tmap_v); false when
+// it cannot be encoded (the loads then use cp.async).
+bool encode_value_map(CUtensorMap* map, const void* v, int bhn, int T) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {8, static_cast<cuuint64_t>(T), 8, static_cast<cuuint64_t>(bhn)};
+  const cuuint64_t strides[3] = {kD * 2, 16, static_cast<cuuint64_t>(T) * kD * 2};
+  const cuuint32_t box[4] = {8, 8, 8, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(v), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 TcParams tc_params(const TcJob& job) {
   TcParams p{};
+  // value loads by tensor copies in forward time (the reversed rows of the
+  // backward's passes keep the row-by-row copies)
+  if (!job.reverse && job.T > 0 && job.B * job.H > 0)
+    p.tma_v = encode_value_map(&p.tmap_v, job.v, job.B * job.H, job.T) ? 1 : 0;
   p.q = static_cast<const __nv_bfloat16*>(job.q);
   p.k = static_cast<const __nv_bfloat16*>(job.k);
   p.v = static_cast<const __nv_bfloat16*>(job.v);

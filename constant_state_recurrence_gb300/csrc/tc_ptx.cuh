@@ -59,6 +59,20 @@ __device__ __forceinline__ void bulk_load_g2s(uint32_t sdst, const void* gsrc, u
       : "memory");
 }
 
+// Tensor load (TMA) of a 4-D box into shared memory at `sdst` from the tensor
+// described by `tmap` (a CUtensorMap in kernel-parameter space) at element
+// coordinates (c0 innermost .. c3); completion is counted on `bar` (bytes).
+// Coordinates past the tensor's extent read zeros.
+__device__ __forceinline__ void tma_load_4d(uint32_t sdst, const void* tmap, int c0, int c1,
+                                            int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(sdst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Arrive without release semantics: the thread does not wait for its earlier
 // global loads and stores.  Only for hand-offs that order nothing but work the
 // thread has already waited for (e.g. TMEM loads after tcgen05.wait::ld).
