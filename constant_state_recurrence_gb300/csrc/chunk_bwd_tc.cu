@@ -401,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float uu = __uint_as_float((j & 1) ? (w[j >> 1] & 0xffff0000u) : (w[j >> 1] << 16));
-          const float den = 1.0f + fabsf(uu);
-          const float th = kPi * __fdividef(uu, den);
+          const float inv = __fdividef(1.0f, 1.0f + fabsf(uu));
+          const float th = kPi * (uu * inv);
           float st, ct;
           __sincosf(th, &st, &ct);
           const float4 pc = m.pc[a0 + j];
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
           const float dth_rot = ds * cr - dc * sr;
           const float dpre = dr * (1.0f - rr * rr);
           const float dtheta = fmaf(dpre * gam, gpx, dth_rot);
-          const float du = rvalid ? __fdividef(dtheta * kPi, den * den) : 0.f;
+          const float du = rvalid ? dtheta * (kPi * inv * inv) : 0.f;
           if (j & 1)
             outp[j >> 1] |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(du))) << 16;
           else

@@ -211,23 +211,66 @@ __device__ __forceinline__ bool wait_bar(Misc& m, int b, uint32_t parity) {
 // The weights ((s / 4d)^p) of 32 keys of one row from their scores,
 // split into bf16 pairs hi (the truncated value) + lo (the rounded rest), keys
 // 2i and 2i + 1 in word i.  MASK: keys after `lim` get weight 0.
+// Packed f32x2 arithmetic (two float32 lanes in one 64-bit register; each
+// lane rounds as the scalar instruction does).
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+template <int P>
+__device__ __forceinline__ uint64_t pow_int2(uint64_t x) {
+  if constexpr (P <= 1) {
+    return x;
+  } else {
+    const uint64_t h = pow_int2<P / 2>(x);
+    const uint64_t h2 = fmul2(h, h);
+    return (P & 1) ? fmul2(h2, x) : h2;
+  }
+}
+
+// The weights ((s / 4d)^p) of 32 keys of one row from their scores, split
+// into bf16 pairs hi (the truncated value) + lo (the rounded rest), keys 2i and
+// 2i + 1 in word i.  MASK: keys after `lim` get weight 0.  Two keys per
+// packed instruction.
 template <int P, bool MASK>
 __device__ __forceinline__ void weights32(const float* pv, int lim, uint32_t (&hi)[16],
                                           uint32_t (&lo)[16]) {
   constexpr float kInv4d = 1.0f / (4.0f * kD);
   constexpr float kConst = 64.0f * kInv4d;   // the constant channel's share of s / 4d
+  const uint64_t scale = pk2(kInv4d, kInv4d), shift = pk2(kConst, kConst);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    float x0 = pow_int<P>(fmaf(pv[2 * i], kInv4d, kConst));
-    float x1 = pow_int<P>(fmaf(pv[2 * i + 1], kInv4d, kConst));
+    float x0, x1;
+    upk2(pow_int2<P>(ffma2(pk2(pv[2 * i], pv[2 * i + 1]), scale, shift)), x0, x1);
     if (MASK) {
       if (2 * i > lim) x0 = 0.f;
       if (2 * i + 1 > lim) x1 = 0.f;
     }
     const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
     hi[i] = __byte_perm(b0, b1, 0x7632);
-    lo[i] = pack_bf16x2(x0 - __uint_as_float(b0 & 0xffff0000u),
-                        x1 - __uint_as_float(b1 & 0xffff0000u));
+    float r0, r1;
+    upk2(fsub2(pk2(x0, x1), pk2(__uint_as_float(b0 & 0xffff0000u),
+                                __uint_as_float(b1 & 0xffff0000u))), r0, r1);
+    lo[i] = pack_bf16x2(r0, r1);
   }
 }
 

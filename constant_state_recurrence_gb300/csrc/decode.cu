@@ -4,8 +4,9 @@
 // The step streams each slot's 6d x dv float32 state once (read + write).
 //
 // A slot is handled by one CTA (1024 threads when there are at most two slots
-// per SM, 256 when there are more than four) or split over a cluster of R = 4
-// CTAs by feature rows (in between).  Each CTA issues the loads of
+// per SM, 256 when there are more than four) or split over a cluster of R
+// CTAs by feature rows (R = 4 in between, R = 8 when there are at most one
+// slot per eight SMs).  Each CTA issues the loads of
 // its whole row block first and featurises q and k for its rows while they
 // are in flight; the readout partial sums (numerator and denominator) are
 // reduced with warp shuffles, a shared-memory tree and, across the cluster,
@@ -202,6 +203,27 @@ int sm_count_decode() {
   return cached;
 }
 
+// One slot per cluster of R CTAs of 128 threads (rows split by CTA rank).
+template <int R>
+cudaError_t launch_cluster(float* S, float* z, const float* q, const float* k, const float* v,
+                           const float* gamma, const float* omega, const float* phi,
+                           const int64_t* pos, int N, int G, float eps, float* o, cudaStream_t st) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(N) * R);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = R;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_step_kernel<R, 128>, S, z, q, k, v, gamma, omega, phi,
+                            pos, G, eps, o);
+}
+
 }  // namespace
 
 cudaError_t decode_step_launch(float* S, float* z, const float* q, const float* k,
@@ -209,6 +231,10 @@ cudaError_t decode_step_launch(float* S, float* z, const float* q, const float* 
                                const float* phi, const int64_t* pos, int N, int G, float eps,
                                float* o, cudaStream_t st) {
   if (N == 0) return cudaSuccess;
+  // At most one slot per eight SMs (the layers of a batch-1 stack step): an
+  // 8-CTA cluster per slot, so that many SMs stream each slot's state.
+  if (8LL * N <= sm_count_decode())
+    return launch_cluster<8>(S, z, q, k, v, gamma, omega, phi, pos, N, G, eps, o, st);
   // Up to two slots per SM: one 1024-thread CTA per slot (six state loads in
   // flight per thread); up to four: a 4-CTA cluster per slot so that every SM
   // streams part of the state; more: one 256-thread CTA per slot.
@@ -217,23 +243,8 @@ cudaError_t decode_step_launch(float* S, float* z, const float* q, const float* 
                                                     o);
     return cudaGetLastError();
   }
-  if (static_cast<int64_t>(N) < 4LL * sm_count_decode()) {
-    constexpr int kR = 4;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(N) * kR);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kR;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_step_kernel<kR, 128>, S, z, q, k, v, gamma, omega, phi,
-                              pos, G, eps, o);
-  }
+  if (static_cast<int64_t>(N) < 4LL * sm_count_decode())
+    return launch_cluster<4>(S, z, q, k, v, gamma, omega, phi, pos, N, G, eps, o, st);
   decode_step_kernel<1, 256><<<N, 256, 0, st>>>(S, z, q, k, v, gamma, omega, phi, pos, G, eps, o);
   return cudaGetLastError();
 }

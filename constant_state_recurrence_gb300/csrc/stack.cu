@@ -36,17 +36,22 @@ __global__ void __launch_bounds__(32) gemv_acc_kernel(const float* __restrict__ 
   for (int b = 0; b < kMaxB; ++b)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[b][j] = 0.f;
-#pragma unroll 8
+  // Every row's load is issued before the first product, so that a CTA keeps
+  // its whole 16 KB block of W in flight.
+  float4 w[kRowsPerCta];
+#pragma unroll
+  for (int r = 0; r < kRowsPerCta; ++r)
+    w[r] = r < nk ? __ldg(reinterpret_cast<const float4*>(W + static_cast<int64_t>(k0 + r) * N + c0))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
   for (int r = 0; r < kRowsPerCta; ++r) {
-    if (r >= nk) break;
-    const float4 w = __ldg(reinterpret_cast<const float4*>(W + static_cast<int64_t>(k0 + r) * N + c0));
 #pragma unroll
     for (int b = 0; b < kMaxB; ++b) {
       const float xv = xs[b][r];
-      acc[b][0] = fmaf(xv, w.x, acc[b][0]);
-      acc[b][1] = fmaf(xv, w.y, acc[b][1]);
-      acc[b][2] = fmaf(xv, w.z, acc[b][2]);
-      acc[b][3] = fmaf(xv, w.w, acc[b][3]);
+      acc[b][0] = fmaf(xv, w[r].x, acc[b][0]);
+      acc[b][1] = fmaf(xv, w[r].y, acc[b][1]);
+      acc[b][2] = fmaf(xv, w[r].z, acc[b][2]);
+      acc[b][3] = fmaf(xv, w[r].w, acc[b][3]);
     }
   }
 #pragma unroll

@@ -35,7 +35,10 @@ def test_decode_over_tiny_sequence_matches_chunked_and_oracle():
     assert rel_fro(f64(Sd), f64(Sc)[0]) <= 1e-5 and rel_fro(f64(zd), f64(zc)[0]) <= 1e-5
 
 
-@pytest.mark.parametrize("N,G", [(144, 144), (300, 144), (7, 3), (400, 144), (700, 144)])
+# (7, 3), (19, 12): 8-CTA clusters; (20, 12), (144, 144), (300, 144): one
+# 1024-thread CTA per slot; (400, 144): 4-CTA clusters; (700, 144): 256 threads
+@pytest.mark.parametrize("N,G", [(144, 144), (300, 144), (7, 3), (19, 12), (20, 12), (400, 144),
+                                 (700, 144)])
 def test_decode_many_slots_from_random_state(N, G):
     rng = np.random.default_rng(N)
     gen = W.generator(4000 + N)
