@@ -386,8 +386,9 @@ int sanatan_device_status(void* stream) {
   const int hb = bwd_tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
   const int hp = pow_tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
   const int hpb = pow_bwd_tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
-  if (h < 0 || hb < 0 || hp < 0 || hpb < 0) return SANATAN_ERR_CUDA;
-  if (hb || hp || hpb) return SANATAN_ERR_TIMEOUT;
+  const int hs = stack_read_and_clear_error(static_cast<cudaStream_t>(stream));
+  if (h < 0 || hb < 0 || hp < 0 || hpb < 0 || hs < 0) return SANATAN_ERR_CUDA;
+  if (hb || hp || hpb || hs) return SANATAN_ERR_TIMEOUT;
   return h ? SANATAN_ERR_TIMEOUT : SANATAN_OK;
 }
 

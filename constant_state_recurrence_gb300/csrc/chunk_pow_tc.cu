@@ -307,6 +307,8 @@ __device__ __forceinline__ void weights_for(const float* pv, int lim, const PowP
 // ---------------------------------------------------------------------------
 // CH: channels per dimension of the feature map (6; 4 and 3 for the ablation
 // maps, whose 8 (CH - 1) feature groups shorten the score products).
+constexpr int kSeqGroup = 8;
+
 template <int P, int CH>
 __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
   constexpr int kNFG = 8 * (CH - 1);   // non-constant feature groups
@@ -318,11 +320,18 @@ __global__ void __launch_bounds__(kThreads, 1) pow_attn_kernel(PowParams prm) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  // query chunk qi of sequence bh; the late (heavier) chunks first
-  const int qi = prm.nchunks - 1 - static_cast<int>(blockIdx.x) / prm.bhn;
-  // sequences in reverse order: the preparation kernel wrote the last ones
-  // most recently, so they are the likeliest to still be in L2
-  const int bh = prm.bhn - 1 - static_cast<int>(blockIdx.x) % prm.bhn;
+  // Query chunk qi of sequence bh.  CTAs run in groups of kSeqGroup
+  // sequences, within a group the late (heavier) query chunks first, so that
+  // the CTAs resident at a time read the key chunks of a few sequences, which
+  // stay in L2 between their readers; groups from the last sequence down (the
+  // preparation kernel wrote the last ones most recently).
+  const int b = static_cast<int>(blockIdx.x);
+  const int gsz_full = min(kSeqGroup, prm.bhn);
+  const int grp = b / (gsz_full * prm.nchunks);
+  const int gsz = min(gsz_full, prm.bhn - grp * gsz_full);
+  const int r = b - grp * gsz_full * prm.nchunks;
+  const int qi = prm.nchunks - 1 - r / gsz;
+  const int bh = prm.bhn - 1 - (grp * gsz_full + r % gsz);
   const int nk = qi + 1;
 
   if (warp == kMmaWarp) {

@@ -87,7 +87,7 @@ cudaError_t decode_harmonic_launch(float* S, float* z, const float* q, const flo
                                    const float* phi, const int64_t* pos, int N, int G, float eps,
                                    int harmonics, float* o, cudaStream_t st);
 
-// One token through L attention layers (stack.cu).
+// One token through L attention layers (stack.cu): one cooperative launch.
 struct StackArgs {
   float* x;              // [B, heads * 64], updated in place
   const float* Wqkv;     // [L, heads * 64, 3 * heads * 64]
@@ -105,6 +105,7 @@ struct StackArgs {
 size_t stack_workspace_bytes(int B, int heads, int d);
 int stack_max_batch();
 cudaError_t stack_decode_launch(const StackArgs& a, cudaStream_t st);
+int stack_read_and_clear_error(cudaStream_t st);
 
 size_t chunk_fwd_simt_smem_bytes();
 size_t chunk_bwd_simt_smem_bytes();

@@ -26,9 +26,9 @@ def _case(B, L, heads, seed=0):
         phi=torch.tensor([10000.0 ** (-a / 64) for a in range(64)]).repeat(L, heads, 1).float())
 
 
-@pytest.mark.parametrize("B,L", [(1, 3), (2, 2), (8, 1)])
-def test_stack_steps_match_the_parallel_form(B, L):
-    heads, T = 12, 12
+@pytest.mark.parametrize("B,L,heads", [(1, 3, 12), (2, 2, 12), (8, 1, 12), (3, 2, 2), (5, 2, 4)])
+def test_stack_steps_match_the_parallel_form(B, L, heads):
+    T = 12
     c = _case(B, L, heads)
     Dm = heads * 64
     X = torch.randn(B, T, Dm, generator=torch.Generator().manual_seed(9))
