@@ -278,25 +278,34 @@ def sanatan_chunk_fwd(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=N
 
 class HostForward:
     """sanatan_chunk_fwd over pinned HOST tensors q, k, v (bf16 [B, H, T, d])
-    into a pinned host o (f32 [B, H, T, dv]), pipelined over slices of the
-    batch: the host-to-device copy of slice i + 1, the attention of slice i
-    and the device-to-host copy of slice i - 1 run on three CUDA streams at
-    once (one cudaMemcpyAsync per tensor slice).  Device staging (two slices
-    of q, k, v and o, and the workspace) is allocated once, here, with torch;
-    each call then allocates nothing.  The calling stream waits for the last
-    copy, so `o` is complete once that stream is synchronised."""
+    into a pinned host o (f32 [B, H, T, dv]), pipelined over slices of the B * H
+    sequences: the host-to-device copy of slice i + 1, the attention of slice
+    i and the device-to-host copy of slice i - 1 run on three CUDA streams at
+    once (one cudaMemcpyAsync per tensor slice).  A slice is m = B * H / slices
+    consecutive sequences: whole batch rows when H divides m, else m heads of
+    one batch row (then m must divide H), with the matching rows of gamma,
+    omega and phi.  Device staging (two slices of q, k, v and o, and the
+    workspace) is allocated once, here, with torch; each call then allocates
+    nothing.  The calling stream waits for the last copy, so `o` is complete
+    once that stream is synchronised."""
 
     def __init__(self, B, H, T, d=64, dv=64, slices=4, device=None):
-        if B % slices:
-            raise ValueError("B must be a multiple of slices")
+        n_seq = B * H
+        if slices < 1 or n_seq % slices:
+            raise ValueError("B * H must be a multiple of slices")
+        m = n_seq // slices
+        if not (m % H == 0 or H % m == 0):
+            raise ValueError("a slice must hold whole batch rows or divide one")
         self.dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
-        self.B, self.H, self.T, self.d, self.dv, self.n = B, H, T, d, dv, slices
-        b = B // slices
-        mk = lambda dt, last: [torch.empty(b, H, T, last, dtype=dt, device=self.dev)  # noqa: E731
+        self.B, self.H, self.T, self.d, self.dv, self.n, self.m = B, H, T, d, dv, slices, m
+        # device shape of one slice
+        self.shape = (m // H, H) if m % H == 0 else (1, m)
+        sb, sh = self.shape
+        mk = lambda dt, last: [torch.empty(sb, sh, T, last, dtype=dt, device=self.dev)  # noqa: E731
                                for _ in range(2)]
         self.q, self.k, self.v = mk(torch.bfloat16, d), mk(torch.bfloat16, d), mk(torch.bfloat16, dv)
         self.o = mk(torch.float32, dv)
-        ws = chunk_fwd_workspace_size(b, H, T, d, dv)
+        ws = chunk_fwd_workspace_size(sb, sh, T, d, dv)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=self.dev)
         self.s_in = torch.cuda.Stream(self.dev)
         self.s_run = torch.cuda.Stream(self.dev)
@@ -305,46 +314,84 @@ class HostForward:
         self.done = [torch.cuda.Event() for _ in range(2)]
         self.freed_in = [torch.cuda.Event() for _ in range(2)]
         self.freed_out = [torch.cuda.Event() for _ in range(2)]
+        # per head range of a sub-row slice: its own (16-byte aligned) copies of
+        # gamma, omega, phi, refreshed at every call
+        self.params = {}
+        if sh < H:
+            for h0 in range(0, H, sh):
+                self.params[h0] = (torch.empty(sh, device=self.dev),
+                                   torch.empty(sh, d, device=self.dev),
+                                   torch.empty(sh, d, device=self.dev))
+
+    def _part(self, t, i):
+        """Slice i of a [B, H, ...] host tensor, shaped like the device slice."""
+        sb, sh = self.shape
+        if sh == self.H:
+            return t[i * sb:(i + 1) * sb]
+        b, h0 = divmod(i * sh, self.H)
+        return t[b:b + 1, h0:h0 + sh]
+
 
     def __call__(self, qh, kh, vh, gamma, omega, phi, oh, pos0=0, eps=0.0):
         for t, n in ((qh, "q"), (kh, "k"), (vh, "v"), (oh, "o")):
             if t.is_cuda or not t.is_pinned():
                 raise ValueError(f"{n} must be a pinned host tensor")
-        b = self.B // self.n
         caller = torch.cuda.current_stream(self.dev)
         for st in (self.s_in, self.s_run, self.s_out):
             st.wait_stream(caller)
+        sh = self.shape[1]
+        if self.params:
+            with torch.cuda.stream(self.s_run):
+                for h0, (g, w, f) in self.params.items():
+                    g.copy_(gamma[h0:h0 + sh])
+                    w.copy_(omega[h0:h0 + sh])
+                    f.copy_(phi[h0:h0 + sh])
         for i in range(self.n + 2):
             j = i % 2
             if i < self.n:                      # H2D of slice i into buffer j
                 with torch.cuda.stream(self.s_in):
                     if i >= 2:
                         self.s_in.wait_event(self.freed_in[j])
-                    sl = slice(i * b, (i + 1) * b)
-                    self.q[j].copy_(qh[sl], non_blocking=True)
-                    self.k[j].copy_(kh[sl], non_blocking=True)
-                    self.v[j].copy_(vh[sl], non_blocking=True)
+                    self.q[j].copy_(self._part(qh, i), non_blocking=True)
+                    self.k[j].copy_(self._part(kh, i), non_blocking=True)
+                    self.v[j].copy_(self._part(vh, i), non_blocking=True)
                     self.loaded[j].record(self.s_in)
             if 1 <= i <= self.n:                # attention of slice i - 1
                 jj = (i - 1) % 2
+                g, w, f = (gamma, omega, phi) if not self.params else \
+                    self.params[((i - 1) * sh) % self.H]
                 with torch.cuda.stream(self.s_run):
                     self.s_run.wait_event(self.loaded[jj])
                     if i - 1 >= 2:
                         self.s_run.wait_event(self.freed_out[jj])
-                    sanatan_chunk_fwd(self.q[jj], self.k[jj], self.v[jj], gamma, omega, phi,
-                                      pos0=pos0, eps=eps, want_D=False, out=self.o[jj],
-                                      workspace=self.ws)
+                    sanatan_chunk_fwd(self.q[jj], self.k[jj], self.v[jj], g, w, f, pos0=pos0,
+                                      eps=eps, want_D=False, out=self.o[jj], workspace=self.ws)
                     self.freed_in[jj].record(self.s_run)
                     self.done[jj].record(self.s_run)
             if i >= 2:                          # D2H of slice i - 2
                 jj = (i - 2) % 2
                 with torch.cuda.stream(self.s_out):
                     self.s_out.wait_event(self.done[jj])
-                    sl = slice((i - 2) * b, (i - 1) * b)
-                    oh[sl].copy_(self.o[jj], non_blocking=True)
+                    self._part(oh, i - 2).copy_(self.o[jj], non_blocking=True)
                     self.freed_out[jj].record(self.s_out)
         caller.wait_stream(self.s_out)
         return oh
+
+    def capture(self, qh, kh, vh, gamma, omega, phi, oh, pos0=0, eps=0.0):
+        """Record one call on these (fixed) host and parameter tensors as a CUDA
+        graph -- every copy and kernel of the pipeline, on its three streams --
+        so that replay() enqueues the whole step with one launch.  The call is
+        run once first (warm-up outside the capture)."""
+        self(qh, kh, vh, gamma, omega, phi, oh, pos0, eps)
+        torch.cuda.current_stream(self.dev).synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self(qh, kh, vh, gamma, omega, phi, oh, pos0, eps)
+        return self
+
+    def replay(self):
+        """One step of the captured pipeline on the current stream."""
+        self.graph.replay()
 
 
 def sanatan_chunk_fwd_noalloc(q, k, v, gamma, omega, phi, pos0=0, eps=0.0, S0=None, z0=None,

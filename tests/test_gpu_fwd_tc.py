@@ -127,18 +127,28 @@ def test_training_shape_forward_full_size_whole_tensor():
     _whole_tensor_check(x)
 
 
-@pytest.mark.parametrize("slices", [1, 2, 4])
-def test_host_forward_pipeline(slices):
-    """HostForward: pinned host q, k, v in, host o out, pipelined over batch
-    slices on three streams; the outputs are those of the definition."""
-    x = W.make(W.LAYER, device="cpu", B=4, H=2, T=300)
+@pytest.mark.parametrize("H,slices", [(2, 1), (2, 2), (2, 4), (2, 8), (6, 8), (6, 12)])
+def test_host_forward_pipeline(H, slices):
+    """HostForward: pinned host q, k, v in, host o out, pipelined over slices
+    of the sequences (whole batch rows, or head ranges of one row with their
+    own gamma, omega, phi) on three streams; the outputs are those of the
+    definition."""
+    x = W.make(W.LAYER, device="cpu", B=4, H=H, T=300)
     hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
-    ho = torch.full((4, 2, 300, 64), float("nan")).pin_memory()
+    ho = torch.full((4, H, 300, 64), float("nan")).pin_memory()
     g = to_dev(x, ("gamma", "omega", "phi"))
-    hf = S.HostForward(4, 2, 300, slices=slices)
+    hf = S.HostForward(4, H, 300, slices=slices)
+    o_ref, _ = O.attn_quadratic(**ref_args(x))
     for _ in range(2):
         hf(hq, hk, hv, g["gamma"], g["omega"], g["phi"], ho)
         torch.cuda.current_stream().synchronize()
         S.device_status()
-        o_ref, _ = O.attn_quadratic(**ref_args(x))
+        assert max_abs(f64(ho), o_ref) <= TOL_BF16
+    # the same pipeline captured as one CUDA graph and replayed
+    hf.capture(hq, hk, hv, g["gamma"], g["omega"], g["phi"], ho)
+    for _ in range(2):
+        ho.fill_(float("nan"))
+        hf.replay()
+        torch.cuda.current_stream().synchronize()
+        S.device_status()
         assert max_abs(f64(ho), o_ref) <= TOL_BF16
