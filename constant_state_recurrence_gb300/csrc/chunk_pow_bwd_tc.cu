@@ -12,17 +12,20 @@
 //
 // Launches: the forward's preparation kernel (Phi(Q), Phi(K), [V | 1 | 0]
 // per chunk), a small kernel for dN (bf16, operand layout) and dD, then two
-// tensor-core passes, each one CTA per (sequence, chunk, feature half):
-//   query pass: per query chunk i, for key chunks j <= i: S = Phi(Q_i) Phi(K_j)^T,
-//     dW = dN_i V_j^T, the epilogue forms dS in TMEM, and
-//     dPhi(Q_i)[half] += dS Phi(K_j)[half];
-//   key pass: per key chunk j, for query chunks i >= j: S^T, dW^T likewise,
-//     dPhi(K_j)[half] += dS^T Phi(Q_i)[half] and (half 0) dv_j += W^T dN_i.
-// Each accumulator of 320 features is split into two halves of 160 (whole
-// dimensions: all five channels of 32 dimensions) so that scores, their
-// gradients and the feature gradient fit the 512 TMEM columns.  After its
-// last tile each CTA applies the feature map's chain rule to its half and
-// writes du, and adds its share of dgamma, domega, dphi with atomics.
+// tensor-core passes, each one CTA per (sequence, chunk) with all 320 features:
+//   query pass: per query chunk i, for the 64-key halves of the key chunks
+//     j <= i: S = Phi(Q_i) Phi(K_j,half)^T, dW = dN_i V_j,half^T, the epilogue
+//     forms dS in its own TMEM buffer while the next half's S and dW are
+//     computed, and dPhi(Q_i) += dS Phi(K_j,half);
+//   key pass: per key chunk j, for the 64-query halves of the query chunks
+//     i >= j: S^T, dW^T likewise, the weights W^T and dS^T in place, then
+//     dPhi(K_j) += dS^T Phi(Q_i,half) and dv_j += W^T dN_i,half.
+// Halves of 64 tokens keep scores, score gradients and the 320-column feature
+// gradient inside the 512 TMEM columns without splitting the features, so
+// every score is computed once per pass; the streamed halves are
+// double-buffered in shared memory.  After its last tile each CTA applies the
+// feature map's chain rule and writes du, and adds its share of dgamma,
+// domega, dphi with atomics.
 #include "pow_common.cuh"
 #include "sanatan_internal.h"
 #include "sanatan_math.cuh"
@@ -42,27 +45,42 @@ using namespace powc;
 constexpr uint32_t kDNBytes = 16 * 1024;   // dN of one chunk: [tg * 1024 + ng * 128 + r * 16]
 constexpr uint32_t kDDBytes = kC * 4;      // dD of one chunk (f32)
 
-// TMEM columns (both passes).
-constexpr uint32_t kTS = 0;       // scores (weights in place, key pass)
-constexpr uint32_t kTDW = 128;    // score gradients (dS in place)
-constexpr uint32_t kTF = 256;     // feature-gradient half (160 columns)
-constexpr uint32_t kTV = 416;     // dv (key pass, 64 columns)
+// TMEM columns (every access stays inside the 512 allocated).  Query pass:
+constexpr uint32_t kQTF = 0;      // dPhi(Q_i), 320 columns
+constexpr uint32_t kQTS = 320;    // scores of a 64-key half (f32)
+constexpr uint32_t kQTDW = 384;   // dW of the half (f32)
+constexpr uint32_t kQTDS = 448;   // dS of the half: bf16 hi | lo per 32-key block
+// Key pass:
+constexpr uint32_t kKTS = 0;      // S^T of a 64-query half, then W^T hi | lo in place
+constexpr uint32_t kKTDW = 64;    // dW^T, then dS^T hi | lo in place
+constexpr uint32_t kKTF = 128;    // dPhi(K_j), 320 columns
+constexpr uint32_t kKTV = 448;    // dv_j, 64 columns
 constexpr uint32_t kTmemCols = 512;
 
-enum Bar { kResFull = 0, kStrFull, kSDone, kDSReady, kTileDone, kNumBars };
+// Bytes of one 64-token half of a chunk's operands.
+constexpr uint32_t kHalfPhi = 8 * kXQ;      // Phi: eight token groups
+constexpr uint32_t kHalfV = 8 * kVGroup;    // [V | 1 | 0]
+constexpr uint32_t kHalfDN = 8 * 1024;      // dN
+constexpr uint32_t kHalfDD = 64 * 4;        // dD
+
+enum Bar {
+  kResFull = 0, kStrFull0, kStrFull1, kSDone, kSFree, kDSReady, kTileDone0, kTileDone1, kDrain,
+  kNumBars
+};
 
 constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kThreads = 32 * (kLoadWarp + 1);
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kSeqGroup = 8;    // CTAs run in groups of this many sequences (L2 reuse)
 
 struct Misc {
   uint64_t bar[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
-  float red_omega[32];   // this CTA's share of domega, dphi (its 32 dimensions) and dgamma
-  float red_phi[32];
+  float red_omega[64];   // this CTA's share of domega, dphi and dgamma
+  float red_phi[64];
   float red_gamma;
 };
 
@@ -200,10 +218,10 @@ __device__ __forceinline__ void chain_rule16(uint32_t trow, int fh, int ch, int 
 #pragma unroll
   for (int gi = 0; gi < 2; ++gi) {
     const int agl = 2 * ch + gi;   // dimension group inside the half
-    float dphi_ch[48];
+    float dphi_ch[40];   // exactly the group's 40 columns
     tmem_ld16(trow + 40 * agl, *reinterpret_cast<float(*)[16]>(&dphi_ch[0]));
     tmem_ld16(trow + 40 * agl + 16, *reinterpret_cast<float(*)[16]>(&dphi_ch[16]));
-    tmem_ld16(trow + 40 * agl + 32, *reinterpret_cast<float(*)[16]>(&dphi_ch[32]));
+    tmem_ld8(trow + 40 * agl + 32, *reinterpret_cast<float(*)[8]>(&dphi_ch[32]));
     tmem_ld_wait();
     const uint32_t w[4] = {raw[gi].x, raw[gi].y, raw[gi].z, raw[gi].w};
 #pragma unroll
@@ -237,8 +255,8 @@ __device__ __forceinline__ void chain_rule16(uint32_t trow, int fh, int ch, int 
         ph += __shfl_xor_sync(0xffffffffu, ph, sh);
       }
       if (lane == 0) {
-        atomicAdd(&m.red_omega[a - 32 * fh], om);
-        atomicAdd(&m.red_phi[a - 32 * fh], ph);
+        atomicAdd(&m.red_omega[a], om);
+        atomicAdd(&m.red_phi[a], ph);
       }
     }
   }
@@ -260,12 +278,25 @@ __device__ __forceinline__ void chain_rule16(uint32_t trow, int fh, int ch, int 
 // Adds the CTA's shares of dgamma, domega, dphi to the outputs (after every
 // epilogue thread has contributed).
 __device__ __forceinline__ void flush_param_grads(const Misc& m, const BwdParams& prm, int h,
-                                                  int fh, int tid) {
-  if (tid < 32) {
-    atomicAdd(&prm.domega[h * kD + 32 * fh + tid], m.red_omega[tid]);
-    if (prm.dphi != nullptr) atomicAdd(&prm.dphi[h * kD + 32 * fh + tid], m.red_phi[tid]);
+                                                  int tid) {
+  if (tid < 64) {
+    atomicAdd(&prm.domega[h * kD + tid], m.red_omega[tid]);
+    if (prm.dphi != nullptr) atomicAdd(&prm.dphi[h * kD + tid], m.red_phi[tid]);
   }
   if (tid == 0) atomicAdd(&prm.dgamma[h], m.red_gamma);
+}
+
+// (sequence, chunk) of CTA b: groups of kSeqGroup sequences, within a group
+// the heaviest chunks first (query pass: late query chunks; key pass: early
+// key chunks), groups from the last sequence down.
+__device__ __forceinline__ void cta_chunk(int b, int bhn, int nchunks, bool late_first, int& bh,
+                                          int& chunk) {
+  const int gf = min(kSeqGroup, bhn);
+  const int grp = b / (gf * nchunks);
+  const int gsz = min(gf, bhn - grp * gf);
+  const int r = b - grp * gf * nchunks;
+  chunk = late_first ? nchunks - 1 - r / gsz : r / gsz;
+  bh = bhn - 1 - (grp * gf + r % gsz);
 }
 
 // Score-gradient (and weight) pairs of 32 keys: ds = (dw + dd) p x^(p-1) / 4d
@@ -302,15 +333,21 @@ __device__ __forceinline__ void grads32(const float* sv, const float* dwv, const
 }
 
 // ---------------------------------------------------------------------------
-// Query pass.  Shared memory: Phi(Q_i) and dN_i resident, Phi(K_j) and
-// [V_j | 1 | 0] streamed (single buffer).
+// Query pass.  Shared memory: Phi(Q_i) and dN_i resident; Phi(K) and
+// [V | 1 | 0] halves streamed through two buffers.
 constexpr int kQOffQ = 0;
 constexpr int kQOffDN = kQOffQ + kPhiBytes;
-constexpr int kQOffK = kQOffDN + kDNBytes;
-constexpr int kQOffV = kQOffK + kPhiBytes;
-constexpr int kQOffMisc = kQOffV + kVBytes;
+constexpr int kQOffK = kQOffDN + kDNBytes;           // two halves
+constexpr int kQOffV = kQOffK + 2 * kHalfPhi;        // two halves
+constexpr int kQOffMisc = kQOffV + 2 * kHalfV;
 constexpr int kQSmem = kQOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kQSmem <= 232448, "query pass: shared memory exceeds 227 KB");
+
+__device__ __forceinline__ void bulk_load_pieces(uint32_t sdst, const unsigned char* src,
+                                                 uint32_t bytes, uint64_t* bar) {
+  for (uint32_t off = 0; off < bytes; off += 16384)
+    bulk_load_g2s(sdst + off, src + off, min(16384u, bytes - off), bar);
+}
 
 template <int P>
 __global__ void __launch_bounds__(kThreads, 1) pow_bwd_q_kernel(BwdParams prm) {
@@ -319,24 +356,24 @@ __global__ void __launch_bounds__(kThreads, 1) pow_bwd_q_kernel(BwdParams prm) {
   const uint32_t sQ = smem_u32(smem + kQOffQ), sDN = smem_u32(smem + kQOffDN);
   const uint32_t sK = smem_u32(smem + kQOffK), sV = smem_u32(smem + kQOffV);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int fh = static_cast<int>(blockIdx.x) & 1;
-  const int rest = static_cast<int>(blockIdx.x) >> 1;
-  const int qi = prm.nchunks - 1 - rest / prm.bhn;   // heavy (late) query chunks first
-  const int bh = rest % prm.bhn;
+  int bh, qi;
+  cta_chunk(static_cast<int>(blockIdx.x), prm.bhn, prm.nchunks, true, bh, qi);
   const int h = bh % prm.H;
-  const int ntiles = qi + 1;
+  const int ntiles = 2 * (qi + 1);   // 64-key halves of the key chunks 0..qi
 
   if (warp == kMmaWarp) {
     tmem_alloc(&m.tmem_base, kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int b = 0; b < kNumBars; ++b)
-      mbar_init(&m.bar[b], b == kDSReady ? static_cast<uint32_t>(kEpiWarps) : 1u);
+    for (int b = 0; b < kNumBars; ++b) {
+      const bool epi = b == kSFree || b == kDSReady;
+      mbar_init(&m.bar[b], epi ? static_cast<uint32_t>(kEpiWarps) : 1u);
+    }
     m.abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid < 32) { m.red_omega[tid] = 0.f; m.red_phi[tid] = 0.f; }
+  if (tid < 64) { m.red_omega[tid] = 0.f; m.red_phi[tid] = 0.f; }
   if (tid == 0) m.red_gamma = 0.f;
   tc_fence_before();
   __syncthreads();
@@ -348,107 +385,133 @@ __global__ void __launch_bounds__(kThreads, 1) pow_bwd_q_kernel(BwdParams prm) {
       const unsigned char* cq = chunk_base(prm.ws, bh, prm.nchunks, qi);
       const unsigned char* dq = prm.dn + (static_cast<int64_t>(bh) * prm.nchunks + qi) * kDNBytes;
       mbar_arrive_expect_tx(&m.bar[kResFull], kPhiBytes + kDNBytes);
-      for (uint32_t off = 0; off < kPhiBytes; off += 16384)
-        bulk_load_g2s(sQ + off, cq + off, 16384, &m.bar[kResFull]);
+      bulk_load_pieces(sQ, cq, kPhiBytes, &m.bar[kResFull]);
       bulk_load_g2s(sDN, dq, kDNBytes, &m.bar[kResFull]);
       int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        // the previous tile has read K, V; after an abandoned wait nothing more is issued
-        if (j > 0 && !wait_bar(m, kTileDone, (j - 1) & 1)) break;
-        const unsigned char* cj = chunk_base(prm.ws, bh, prm.nchunks, j);
-        mbar_arrive_expect_tx(&m.bar[kStrFull], kPhiBytes + kVBytes);
-        for (uint32_t off = 0; off < kPhiBytes; off += 16384)
-          bulk_load_g2s(sK + off, cj + kPhiBytes + off, 16384, &m.bar[kStrFull]);
-        bulk_load_g2s(sV, cj + 2 * kPhiBytes, kVBytes, &m.bar[kStrFull]);
-        issued = j + 1;
+      for (int t = 0; t < ntiles; ++t) {
+        const int b = t & 1;
+        // buffer b is free once the tile that used it before has completed
+        if (t >= 2 && !wait_bar(m, kTileDone0 + b, ((t - 2) >> 1) & 1)) break;
+        const unsigned char* cj = chunk_base(prm.ws, bh, prm.nchunks, t >> 1);
+        const uint32_t hk = static_cast<uint32_t>(t & 1);
+        mbar_arrive_expect_tx(&m.bar[kStrFull0 + b], kHalfPhi + kHalfV);
+        bulk_load_pieces(sK + b * kHalfPhi, cj + kPhiBytes + hk * kHalfPhi, kHalfPhi,
+                         &m.bar[kStrFull0 + b]);
+        bulk_load_g2s(sV + b * kHalfV, cj + 2 * kPhiBytes + hk * kHalfV, kHalfV,
+                      &m.bar[kStrFull0 + b]);
+        issued = t + 1;
       }
       // no copy may still be writing shared memory when the CTA exits
       mbar_wait_bounded(&m.bar[kResFull], 0, kWaitNs);
-      if (issued > 0) mbar_wait_bounded(&m.bar[kStrFull], (issued - 1) & 1, kWaitNs);
+      for (int t = max(0, issued - 2); t < issued; ++t)
+        mbar_wait_bounded(&m.bar[kStrFull0 + (t & 1)], (t >> 1) & 1, kWaitNs);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t idF = idesc_bf16_f32(128, 160, false, true);
-      wait_bar(m, kResFull, 0);
-      for (int j = 0; j < ntiles; ++j) {
-        wait_bar(m, kStrFull, j & 1);   // also implies the previous tile's MMAs are done
+      // dPhi(Q_i) += dS(t) Phi(K half of tile t): K = 64 keys, N = 2 x 160 features
+      auto issue_feature_grad = [&](int t) -> bool {
+        if (!wait_bar(m, kDSReady, t & 1)) return false;
         tc_fence_after();
-        uint64_t dQ = smem_desc(sQ, 128, kXQ);          // Phi(Q_i), K-major A
-        uint64_t dK = smem_desc(sK, 128, kXQ);          // Phi(K_j), K-major B (N = keys)
-        uint64_t dN = smem_desc(sDN, 128, 1024);        // dN_i, K-major A
-        uint64_t dV = smem_desc(sV, 128, kVGroup);      // V_j, K-major B (N = keys)
+        uint64_t dKf = smem_desc(sK + (t & 1) * kHalfPhi, kXQ, 128);   // MN-major B
+        asm volatile("" : "+l"(dKf));
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          const uint32_t hi = tmem + kQTDS + 32 * (st >> 1) + 8 * (st & 1);
+#pragma unroll
+          for (int nh = 0; nh < 2; ++nh) {
+            const uint64_t bd = dKf + 160 * nh + (2 * kXQ / 16) * st;
+            mma_ts(tmem + kQTF + 160 * nh, hi, bd, idF, (t | st) != 0);
+            mma_ts(tmem + kQTF + 160 * nh, hi + 16, bd, idF, true);
+          }
+        }
+        mma_commit(&m.bar[kTileDone0 + (t & 1)]);
+        return true;
+      };
+      bool ok = wait_bar(m, kResFull, 0);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int b = t & 1;
+        if (!wait_bar(m, kStrFull0 + b, (t >> 1) & 1)) break;
+        // the epilogue has read the previous scores and dW from TMEM
+        if (t > 0 && !wait_bar(m, kSFree, (t - 1) & 1)) break;
+        tc_fence_after();
+        uint64_t dQ = smem_desc(sQ, 128, kXQ);                   // Phi(Q_i), K-major A
+        uint64_t dK = smem_desc(sK + b * kHalfPhi, 128, kXQ);    // Phi(K half), K-major B
+        uint64_t dN = smem_desc(sDN, 128, 1024);                 // dN_i, K-major A
+        uint64_t dV = smem_desc(sV + b * kHalfV, 128, kVGroup);  // V half, K-major B
         asm volatile("" : "+l"(dQ), "+l"(dK), "+l"(dN), "+l"(dV));
 #pragma unroll
         for (int st = 0; st < 20; ++st)
-          mma_ss(tmem + kTS, dQ + 16 * st, dK + 16 * st, idS, st > 0);
+          mma_ss(tmem + kQTS, dQ + 16 * st, dK + 16 * st, idS, st > 0);
 #pragma unroll
         for (int st = 0; st < 4; ++st)
-          mma_ss(tmem + kTDW, dN + 16 * st, dV + 16 * st, idS, st > 0);
+          mma_ss(tmem + kQTDW, dN + 16 * st, dV + 16 * st, idS, st > 0);
         mma_commit(&m.bar[kSDone]);
-        wait_bar(m, kDSReady, j & 1);
-        tc_fence_after();
-        uint64_t dKf = smem_desc(sK + 20 * 128 * fh, kXQ, 128);   // Phi(K_j) half, MN-major B
-        asm volatile("" : "+l"(dKf));
-#pragma unroll
-        for (int st = 0; st < 8; ++st) {
-          const uint32_t hi = tmem + kTDW + 32 * (st >> 1) + 8 * (st & 1);
-          mma_ts(tmem + kTF, hi, dKf + (2 * kXQ / 16) * st, idF, (j | st) != 0);
-          mma_ts(tmem + kTF, hi + 16, dKf + (2 * kXQ / 16) * st, idF, true);
-        }
-        mma_commit(&m.bar[kTileDone]);
+        if (t > 0 && !issue_feature_grad(t - 1)) { ok = false; break; }
+        if (t == ntiles - 1) ok = issue_feature_grad(t);
       }
-      mbar_wait_bounded(&m.bar[kTileDone], (ntiles - 1) & 1, kWaitNs);
+      // wait (bounded) for every MMA issued, also after an abandoned wait
+      mma_commit(&m.bar[kDrain]);
+      mbar_wait_bounded(&m.bar[kDrain], 0, kWaitNs);
     }
   } else {
-    // epilogue: warp (qd, ch) owns query rows 32 qd .. + 31 and keys 64 ch .. + 63
-    const int qd = warp & 3, ch = warp >> 2;
+    // epilogue: warp (qd, cw) owns query rows 32 qd .. + 31 and keys 32 cw .. + 31
+    // of each 64-key half
+    const int qd = warp & 3, cw = warp >> 2;
     const int row = 32 * qd + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
     const float ddrow = prm.dd[(static_cast<int64_t>(bh) * prm.nchunks + qi) * kC + row];
     float ddv[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) ddv[k] = ddrow;
-    for (int j = 0; j < ntiles; ++j) {
-      wait_bar(m, kSDone, j & 1);
+    for (int t = 0; t < ntiles; ++t) {
+      if (!wait_bar(m, kSDone, t & 1)) break;
       tc_fence_after();
-      const bool diag = (j == qi);
-#pragma unroll 1
-      for (int bi = 0; bi < 2; ++bi) {
-        const int blk = 2 * ch + bi;
-        const uint32_t cs = tmem + lane_off + kTS + 32 * blk;
-        const uint32_t cd = tmem + lane_off + kTDW + 32 * blk;
-        uint32_t dhi[16], dlo[16], whi[16], wlo[16];
-        if (diag && blk > qd) {   // every key of the block is after every row of the warp
-#pragma unroll
-          for (int i = 0; i < 16; ++i) { dhi[i] = 0u; dlo[i] = 0u; }
-        } else {
-          float sv[32], dwv[32];
-          tmem_ld16(cs, *reinterpret_cast<float(*)[16]>(&sv[0]));
-          tmem_ld16(cs + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
-          tmem_ld16(cd, *reinterpret_cast<float(*)[16]>(&dwv[0]));
-          tmem_ld16(cd + 16, *reinterpret_cast<float(*)[16]>(&dwv[16]));
-          tmem_ld_wait();
-          const int lim = (diag && blk == qd) ? lane : 31;   // keys up to the row's own
-          grads32<P>(sv, dwv, ddv, [lim](int k) { return k <= lim; }, dhi, dlo, whi, wlo);
-        }
-        tmem_st16(cd, dhi);
-        tmem_st16(cd + 16, dlo);
+      const bool diag = (t >> 1) == qi;
+      const int blk = 2 * (t & 1) + cw;   // 32-key block of the chunk
+      const bool none = diag && blk > qd;  // every key of the block is after every row
+      float sv[32], dwv[32];
+      if (!none) {
+        tmem_ld16(tmem + lane_off + kQTS + 32 * cw, *reinterpret_cast<float(*)[16]>(&sv[0]));
+        tmem_ld16(tmem + lane_off + kQTS + 32 * cw + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
+        tmem_ld16(tmem + lane_off + kQTDW + 32 * cw, *reinterpret_cast<float(*)[16]>(&dwv[0]));
+        tmem_ld16(tmem + lane_off + kQTDW + 32 * cw + 16,
+                  *reinterpret_cast<float(*)[16]>(&dwv[16]));
+        tmem_ld_wait();
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&m.bar[kSFree]);   // the next half's MMAs may overwrite them
+      uint32_t dhi[16], dlo[16], whi[16], wlo[16];
+      if (none) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) { dhi[i] = 0u; dlo[i] = 0u; }
+      } else {
+        const int lim = (diag && blk == qd) ? lane : 31;   // keys up to the row's own
+        grads32<P>(sv, dwv, ddv, [lim](int k) { return k <= lim; }, dhi, dlo, whi, wlo);
+      }
+      // the previous half's feature-gradient MMAs have read the dS buffer
+      if (t > 0 && !wait_bar(m, kTileDone0 + ((t - 1) & 1), ((t - 1) >> 1) & 1)) break;
+      tc_fence_after();
+      tmem_st16(tmem + lane_off + kQTDS + 32 * cw, dhi);
+      tmem_st16(tmem + lane_off + kQTDS + 32 * cw + 16, dlo);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&m.bar[kDSReady]);
     }
-    wait_bar(m, kTileDone, (ntiles - 1) & 1);
+    wait_bar(m, kTileDone0 + ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1);
     tc_fence_after();
     const int t = qi * kC + row;
     const bool valid = t < prm.T;
     const int64_t grow = static_cast<int64_t>(bh) * prm.T + (valid ? t : 0);
-    chain_rule16(tmem + lane_off + kTF, fh, ch, h, prm.pos0 + t, valid, prm.u + grow * kD, prm,
-                 prm.du + grow * kD, m, lane);
+#pragma unroll 1
+    for (int ch = 0; ch < 2; ++ch)
+      chain_rule16(tmem + lane_off + kQTF + 160 * cw, cw, ch, h, prm.pos0 + t, valid,
+                   prm.u + grow * kD, prm, prm.du + grow * kD, m, lane);
     epi_sync();
-    flush_param_grads(m, prm, h, fh, tid);
+    flush_param_grads(m, prm, h, tid);
   }
   tc_fence_before();
   __syncthreads();
@@ -459,14 +522,14 @@ __global__ void __launch_bounds__(kThreads, 1) pow_bwd_q_kernel(BwdParams prm) {
 }
 
 // ---------------------------------------------------------------------------
-// Key pass.  Shared memory: Phi(K_j) and [V_j | 1 | 0] resident, Phi(Q_i), dN_i
-// and dD_i streamed (single buffer).
+// Key pass.  Shared memory: Phi(K_j) and [V_j | 1 | 0] resident; Phi(Q), dN
+// and dD halves streamed through two buffers.
 constexpr int kKOffK = 0;
 constexpr int kKOffV = kKOffK + kPhiBytes;
-constexpr int kKOffQ = kKOffV + kVBytes;
-constexpr int kKOffDN = kKOffQ + kPhiBytes;
-constexpr int kKOffDD = kKOffDN + kDNBytes;
-constexpr int kKOffMisc = kKOffDD + kDDBytes;
+constexpr int kKOffQ = kKOffV + kVBytes;             // two halves
+constexpr int kKOffDN = kKOffQ + 2 * kHalfPhi;       // two halves
+constexpr int kKOffDD = kKOffDN + 2 * kHalfDN;       // two halves
+constexpr int kKOffMisc = kKOffDD + 2 * kHalfDD;
 constexpr int kKSmem = kKOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kKSmem <= 232448, "key pass: shared memory exceeds 227 KB");
 
@@ -479,13 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1) pow_bwd_k_kernel(BwdParams prm) {
   const uint32_t sQ = smem_u32(smem + kKOffQ), sDN = smem_u32(smem + kKOffDN);
   const uint32_t sDD = smem_u32(smem + kKOffDD);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int fh = static_cast<int>(blockIdx.x) & 1;
-  const int rest = static_cast<int>(blockIdx.x) >> 1;
-  const int kj = rest / prm.bhn;   // early key chunks (the most query chunks) first
-  const int bh = rest % prm.bhn;
+  int bh, kj;
+  cta_chunk(static_cast<int>(blockIdx.x), prm.bhn, prm.nchunks, false, bh, kj);
   const int h = bh % prm.H;
-  const int ntiles = prm.nchunks - kj;
-  const bool with_dv = (fh == 0);
+  const int ntiles = 2 * (prm.nchunks - kj);   // 64-query halves of the chunks kj..
 
   if (warp == kMmaWarp) {
     tmem_alloc(&m.tmem_base, kTmemCols);
@@ -497,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) pow_bwd_k_kernel(BwdParams prm) {
     m.abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid < 32) { m.red_omega[tid] = 0.f; m.red_phi[tid] = 0.f; }
+  if (tid < 64) { m.red_omega[tid] = 0.f; m.red_phi[tid] = 0.f; }
   if (tid == 0) m.red_gamma = 0.f;
   tc_fence_before();
   __syncthreads();
@@ -508,122 +568,126 @@ __global__ void __launch_bounds__(kThreads, 1) pow_bwd_k_kernel(BwdParams prm) {
     if (lane == 0) {
       const unsigned char* ck = chunk_base(prm.ws, bh, prm.nchunks, kj);
       mbar_arrive_expect_tx(&m.bar[kResFull], kPhiBytes + kVBytes);
-      for (uint32_t off = 0; off < kPhiBytes; off += 16384)
-        bulk_load_g2s(sK + off, ck + kPhiBytes + off, 16384, &m.bar[kResFull]);
+      bulk_load_pieces(sK, ck + kPhiBytes, kPhiBytes, &m.bar[kResFull]);
       bulk_load_g2s(sV, ck + 2 * kPhiBytes, kVBytes, &m.bar[kResFull]);
       int issued = 0;
-      for (int n = 0; n < ntiles; ++n) {
-        const int qi = kj + n;
-        // the previous tile has read Q, dN, dD; after an abandoned wait nothing more is issued
-        if (n > 0 && !wait_bar(m, kTileDone, (n - 1) & 1)) break;
+      for (int t = 0; t < ntiles; ++t) {
+        const int b = t & 1;
+        if (t >= 2 && !wait_bar(m, kTileDone0 + b, ((t - 2) >> 1) & 1)) break;
+        const int qi = kj + (t >> 1);
+        const uint32_t hq = static_cast<uint32_t>(t & 1);
         const unsigned char* cq = chunk_base(prm.ws, bh, prm.nchunks, qi);
         const int64_t sc = static_cast<int64_t>(bh) * prm.nchunks + qi;
-        mbar_arrive_expect_tx(&m.bar[kStrFull], kPhiBytes + kDNBytes + kDDBytes);
-        for (uint32_t off = 0; off < kPhiBytes; off += 16384)
-          bulk_load_g2s(sQ + off, cq + off, 16384, &m.bar[kStrFull]);
-        bulk_load_g2s(sDN, prm.dn + sc * kDNBytes, kDNBytes, &m.bar[kStrFull]);
-        bulk_load_g2s(sDD, prm.dd + sc * kC, kDDBytes, &m.bar[kStrFull]);
-        issued = n + 1;
+        mbar_arrive_expect_tx(&m.bar[kStrFull0 + b], kHalfPhi + kHalfDN + kHalfDD);
+        bulk_load_pieces(sQ + b * kHalfPhi, cq + hq * kHalfPhi, kHalfPhi, &m.bar[kStrFull0 + b]);
+        bulk_load_g2s(sDN + b * kHalfDN, prm.dn + sc * kDNBytes + hq * kHalfDN, kHalfDN,
+                      &m.bar[kStrFull0 + b]);
+        bulk_load_g2s(sDD + b * kHalfDD, prm.dd + sc * kC + 64 * hq, kHalfDD,
+                      &m.bar[kStrFull0 + b]);
+        issued = t + 1;
       }
       mbar_wait_bounded(&m.bar[kResFull], 0, kWaitNs);
-      if (issued > 0) mbar_wait_bounded(&m.bar[kStrFull], (issued - 1) & 1, kWaitNs);
+      for (int t = max(0, issued - 2); t < issued; ++t)
+        mbar_wait_bounded(&m.bar[kStrFull0 + (t & 1)], (t >> 1) & 1, kWaitNs);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t idF = idesc_bf16_f32(128, 160, false, true);
       constexpr uint32_t idV = idesc_bf16_f32(128, 64, false, true);
-      wait_bar(m, kResFull, 0);
-      for (int n = 0; n < ntiles; ++n) {
-        wait_bar(m, kStrFull, n & 1);
+      bool ok = wait_bar(m, kResFull, 0);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int b = t & 1;
+        if (!wait_bar(m, kStrFull0 + b, (t >> 1) & 1)) break;
+        // the previous half's MMAs have read W^T and dS^T from the score columns
+        if (t > 0 && !wait_bar(m, kTileDone0 + ((t - 1) & 1), ((t - 1) >> 1) & 1)) break;
         tc_fence_after();
-        uint64_t dK = smem_desc(sK, 128, kXQ);          // Phi(K_j), K-major A (M = keys)
-        uint64_t dQ = smem_desc(sQ, 128, kXQ);          // Phi(Q_i), K-major B (N = queries)
-        uint64_t dV = smem_desc(sV, 128, kVGroup);      // V_j, K-major A
-        uint64_t dN = smem_desc(sDN, 128, 1024);        // dN_i, K-major B (N = queries)
+        uint64_t dK = smem_desc(sK, 128, kXQ);                    // Phi(K_j), K-major A
+        uint64_t dQ = smem_desc(sQ + b * kHalfPhi, 128, kXQ);     // Phi(Q half), K-major B
+        uint64_t dV = smem_desc(sV, 128, kVGroup);                // V_j, K-major A
+        uint64_t dN = smem_desc(sDN + b * kHalfDN, 128, 1024);    // dN half, K-major B
         asm volatile("" : "+l"(dK), "+l"(dQ), "+l"(dV), "+l"(dN));
 #pragma unroll
         for (int st = 0; st < 20; ++st)
-          mma_ss(tmem + kTS, dK + 16 * st, dQ + 16 * st, idS, st > 0);
+          mma_ss(tmem + kKTS, dK + 16 * st, dQ + 16 * st, idS, st > 0);
 #pragma unroll
         for (int st = 0; st < 4; ++st)
-          mma_ss(tmem + kTDW, dV + 16 * st, dN + 16 * st, idS, st > 0);
+          mma_ss(tmem + kKTDW, dV + 16 * st, dN + 16 * st, idS, st > 0);
         mma_commit(&m.bar[kSDone]);
-        wait_bar(m, kDSReady, n & 1);
+        if (!wait_bar(m, kDSReady, t & 1)) break;
         tc_fence_after();
-        uint64_t dQf = smem_desc(sQ + 20 * 128 * fh, kXQ, 128);   // Phi(Q_i) half, MN-major B
-        uint64_t dNv = smem_desc(sDN, 1024, 128);                 // dN_i, MN-major B
+        uint64_t dQf = smem_desc(sQ + b * kHalfPhi, kXQ, 128);    // Phi(Q half), MN-major B
+        uint64_t dNv = smem_desc(sDN + b * kHalfDN, 1024, 128);   // dN half, MN-major B
         asm volatile("" : "+l"(dQf), "+l"(dNv));
 #pragma unroll
-        for (int st = 0; st < 8; ++st) {
-          const uint32_t hi = tmem + kTDW + 32 * (st >> 1) + 8 * (st & 1);
-          mma_ts(tmem + kTF, hi, dQf + (2 * kXQ / 16) * st, idF, (n | st) != 0);
-          mma_ts(tmem + kTF, hi + 16, dQf + (2 * kXQ / 16) * st, idF, true);
-        }
-        if (with_dv) {
+        for (int st = 0; st < 4; ++st) {
+          const uint32_t hs = tmem + kKTDW + 32 * (st >> 1) + 8 * (st & 1);   // dS^T
+          const uint32_t hw = tmem + kKTS + 32 * (st >> 1) + 8 * (st & 1);    // W^T
 #pragma unroll
-          for (int st = 0; st < 8; ++st) {
-            const uint32_t hi = tmem + kTS + 32 * (st >> 1) + 8 * (st & 1);
-            mma_ts(tmem + kTV, hi, dNv + (2 * 1024 / 16) * st, idV, (n | st) != 0);
-            mma_ts(tmem + kTV, hi + 16, dNv + (2 * 1024 / 16) * st, idV, true);
+          for (int nh = 0; nh < 2; ++nh) {
+            const uint64_t bd = dQf + 160 * nh + (2 * kXQ / 16) * st;
+            mma_ts(tmem + kKTF + 160 * nh, hs, bd, idF, (t | st) != 0);
+            mma_ts(tmem + kKTF + 160 * nh, hs + 16, bd, idF, true);
           }
+          const uint64_t vd = dNv + (2 * 1024 / 16) * st;
+          mma_ts(tmem + kKTV, hw, vd, idV, (t | st) != 0);
+          mma_ts(tmem + kKTV, hw + 16, vd, idV, true);
         }
-        mma_commit(&m.bar[kTileDone]);
+        mma_commit(&m.bar[kTileDone0 + b]);
       }
-      mbar_wait_bounded(&m.bar[kTileDone], (ntiles - 1) & 1, kWaitNs);
+      mma_commit(&m.bar[kDrain]);
+      mbar_wait_bounded(&m.bar[kDrain], 0, kWaitNs);
     }
   } else {
-    // epilogue: warp (qd, ch) owns key rows 32 qd .. + 31 and queries 64 ch .. + 63
-    const int qd = warp & 3, ch = warp >> 2;
+    // epilogue: warp (qd, cw) owns key rows 32 qd .. + 31 and queries 32 cw .. + 31
+    // of each 64-query half
+    const int qd = warp & 3, cw = warp >> 2;
     const int row = 32 * qd + lane;
     const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
-    for (int n = 0; n < ntiles; ++n) {
-      wait_bar(m, kStrFull, n & 1);   // dD_i in shared memory (the bulk copy's own barrier)
-      wait_bar(m, kSDone, n & 1);
+    for (int t = 0; t < ntiles; ++t) {
+      const int b = t & 1;
+      if (!wait_bar(m, kStrFull0 + b, (t >> 1) & 1)) break;   // dD of the half in shared memory
+      if (!wait_bar(m, kSDone, t & 1)) break;
       tc_fence_after();
-      const bool diag = (n == 0);   // query chunk == key chunk
-#pragma unroll 1
-      for (int bi = 0; bi < 2; ++bi) {
-        const int blk = 2 * ch + bi;
-        const uint32_t cs = tmem + lane_off + kTS + 32 * blk;
-        const uint32_t cd = tmem + lane_off + kTDW + 32 * blk;
-        uint32_t dhi[16], dlo[16], whi[16], wlo[16];
-        if (diag && blk < qd) {   // every query of the block is before every key of the warp
+      const bool diag = (t >> 1) == 0;    // query chunk == key chunk
+      const int qblk = 2 * (t & 1) + cw;  // 32-query block of the chunk
+      uint32_t dhi[16], dlo[16], whi[16], wlo[16];
+      if (diag && qblk < qd) {   // every query of the block is before every key of the warp
 #pragma unroll
-          for (int i = 0; i < 16; ++i) { dhi[i] = 0u; dlo[i] = 0u; whi[i] = 0u; wlo[i] = 0u; }
-        } else {
-          float sv[32], dwv[32];
-          tmem_ld16(cs, *reinterpret_cast<float(*)[16]>(&sv[0]));
-          tmem_ld16(cs + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
-          tmem_ld16(cd, *reinterpret_cast<float(*)[16]>(&dwv[0]));
-          tmem_ld16(cd + 16, *reinterpret_cast<float(*)[16]>(&dwv[16]));
-          tmem_ld_wait();
-          const int first = (diag && blk == qd) ? lane : 0;   // queries from the key's own
-          grads32<P>(sv, dwv, sdd + 32 * blk, [first](int k) { return k >= first; }, dhi, dlo,
-                     whi, wlo);
-        }
-        tmem_st16(cs, whi);
-        tmem_st16(cs + 16, wlo);
-        tmem_st16(cd, dhi);
-        tmem_st16(cd + 16, dlo);
+        for (int i = 0; i < 16; ++i) { dhi[i] = 0u; dlo[i] = 0u; whi[i] = 0u; wlo[i] = 0u; }
+      } else {
+        float sv[32], dwv[32];
+        tmem_ld16(tmem + lane_off + kKTS + 32 * cw, *reinterpret_cast<float(*)[16]>(&sv[0]));
+        tmem_ld16(tmem + lane_off + kKTS + 32 * cw + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
+        tmem_ld16(tmem + lane_off + kKTDW + 32 * cw, *reinterpret_cast<float(*)[16]>(&dwv[0]));
+        tmem_ld16(tmem + lane_off + kKTDW + 32 * cw + 16,
+                  *reinterpret_cast<float(*)[16]>(&dwv[16]));
+        tmem_ld_wait();
+        const int first = (diag && qblk == qd) ? lane : 0;   // queries from the key's own
+        grads32<P>(sv, dwv, sdd + b * 64 + 32 * cw, [first](int k) { return k >= first; }, dhi,
+                   dlo, whi, wlo);
       }
+      tmem_st16(tmem + lane_off + kKTS + 32 * cw, whi);
+      tmem_st16(tmem + lane_off + kKTS + 32 * cw + 16, wlo);
+      tmem_st16(tmem + lane_off + kKTDW + 32 * cw, dhi);
+      tmem_st16(tmem + lane_off + kKTDW + 32 * cw + 16, dlo);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&m.bar[kDSReady]);
     }
-    wait_bar(m, kTileDone, (ntiles - 1) & 1);
+    wait_bar(m, kTileDone0 + ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1);
     tc_fence_after();
     const int t = kj * kC + row;
     const bool valid = t < prm.T;
     const int64_t grow = static_cast<int64_t>(bh) * prm.T + (valid ? t : 0);
-    if (with_dv) {
+    {
       float dvv[32];
-      tmem_ld16(tmem + lane_off + kTV + 32 * ch, *reinterpret_cast<float(*)[16]>(&dvv[0]));
-      tmem_ld16(tmem + lane_off + kTV + 32 * ch + 16, *reinterpret_cast<float(*)[16]>(&dvv[16]));
+      tmem_ld16(tmem + lane_off + kKTV + 32 * cw, *reinterpret_cast<float(*)[16]>(&dvv[0]));
+      tmem_ld16(tmem + lane_off + kKTV + 32 * cw + 16, *reinterpret_cast<float(*)[16]>(&dvv[16]));
       tmem_ld_wait();
       if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(prm.dv + grow * kD + 32 * ch);
+        uint4* dst = reinterpret_cast<uint4*>(prm.dv + grow * kD + 32 * cw);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
           dst[q4] = make_uint4(pack_bf16x2(dvv[8 * q4], dvv[8 * q4 + 1]),
@@ -632,10 +696,12 @@ __global__ void __launch_bounds__(kThreads, 1) pow_bwd_k_kernel(BwdParams prm) {
                                pack_bf16x2(dvv[8 * q4 + 6], dvv[8 * q4 + 7]));
       }
     }
-    chain_rule16(tmem + lane_off + kTF, fh, ch, h, prm.pos0 + t, valid, prm.u + grow * kD, prm,
-                 prm.du + grow * kD, m, lane);
+#pragma unroll 1
+    for (int ch = 0; ch < 2; ++ch)
+      chain_rule16(tmem + lane_off + kKTF + 160 * cw, cw, ch, h, prm.pos0 + t, valid,
+                   prm.u + grow * kD, prm, prm.du + grow * kD, m, lane);
     epi_sync();
-    flush_param_grads(m, prm, h, fh, tid);
+    flush_param_grads(m, prm, h, tid);
   }
   tc_fence_before();
   __syncthreads();
@@ -750,7 +816,7 @@ cudaError_t pow_bwd_tc_launch(const PowBwdArgs& a, cudaStream_t st) {
   bp.dgamma = a.dgamma;
   bp.domega = a.domega;
   bp.dphi = a.dphi;
-  const unsigned grid = static_cast<unsigned>(2 * nsc);
+  const unsigned grid = static_cast<unsigned>(nsc);
   bp.u = static_cast<const __nv_bfloat16*>(f.q);
   bp.du = static_cast<__nv_bfloat16*>(a.dq);
   bp.dv = nullptr;
