@@ -360,7 +360,8 @@ def decode_case(batch, dev, flush, steps, warmup, stream):
 
 def train_case(dev, flush, steps, warmup, stream):
     """Training step of the B=8, H=12, T=4096 workload: the chunked forward
-    (keeping o and D) then the backward to dq, dk, dv, dgamma, domega, dphi."""
+    (keeping o and D) then the backward to dq, dk, dv, dgamma, domega, dphi
+    (reusing the forward's per-segment state sums from its workspace)."""
     from constant_state_recurrence_gb300 import sanatan as S
     x = W.make(W.TRAIN, device=dev, with_grad_out=True, shard=SHARD)
     g = {n: x[n] for n in ("q", "k", "v", "gamma", "omega", "phi", "dO")}
@@ -376,7 +377,7 @@ def train_case(dev, flush, steps, warmup, stream):
         S.sanatan_chunk_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], out=o,
                             D_out=D, workspace=ws)
         S.sanatan_chunk_bwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], o, D,
-                            g["dO"], want_dphi=True, workspace=bws)
+                            g["dO"], want_dphi=True, workspace=bws, fwd_workspace=ws)
 
     for _ in range(warmup):
         flush.zero_()
@@ -684,7 +685,7 @@ def main():
                    "parallelism": f"{world} independent replica(s), sequences sharded by rank",
                    "l2": "256 MiB flush write before every timed step",
                    "launch": "each timed step replays a CUDA graph of one library call; "
-                             "e2e uses eager calls"},
+                             "e2e replays the host pipeline's CUDA graph"},
         "gpu_launches": steps * layer["launches"],
         "roofline": {"bound": "tensor", "kernel": "sanatan_tc_kernel (main pass)",
                      "achieved": achieved_tf, "peak": pk["bf16"], "unit": "TFLOP/s",

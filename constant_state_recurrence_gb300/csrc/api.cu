@@ -8,7 +8,7 @@ namespace {
 
 using namespace sanatan;
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr int kMaxPower = 8;   // largest p of sanatan_power_fwd
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -203,8 +203,9 @@ int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
                       const float* z0, const float* o, const float* D, const void* dO,
                       int grad_dtype, void* dq, void* dk, void* dv_out, float* dgamma,
                       float* domega, float* dphi, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+                      const void* fwd_workspace, size_t fwd_workspace_bytes, void* stream) {
   if (!ok_dtype(in_dtype) || !ok_dtype(grad_dtype)) return SANATAN_ERR_INVALID;
+  if (!ok_nullable(fwd_workspace)) return SANATAN_ERR_INVALID;
   if (int s = check_sizes(B, H, T, d, dv)) return s;
   if ((S0 == nullptr) != (z0 == nullptr)) return SANATAN_ERR_INVALID;
   if (!ok_nullable(S0) || !ok_nullable(z0) || !ok_nullable(dphi) || !ok_nullable(workspace))
@@ -236,6 +237,8 @@ int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
   a.dphi = dphi;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
+  a.fwd_workspace = fwd_workspace;
+  a.fwd_workspace_bytes = fwd_workspace == nullptr ? 0 : fwd_workspace_bytes;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (in_dtype == SANATAN_BF16) return from_cuda(chunk_bwd_tc_launch(a, st));
   return from_cuda(chunk_bwd_simt_launch(a, st));

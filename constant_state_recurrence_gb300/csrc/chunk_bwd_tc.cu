@@ -733,14 +733,19 @@ cudaError_t chunk_bwd_tc_launch(const ChunkBwdArgs& a, cudaStream_t st) {
   const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(f.v);
 
   // Per-segment sums: forward state sum Phi(k)[v|1] (for dq) and reverse-time
-  // sum Phi(q)[dN|dD] (for dk and dv).
+  // sum Phi(q)[dN|dD] (for dk and dv).  The forward-time sums are the ones the
+  // forward wrote at the start of its workspace when it used the same split.
   if (nseg > 1) {
     TcJob fs{};
     fs.q = nullptr; fs.k = k; fs.v = v; fs.extra = nullptr;
     fs.gamma = f.gamma; fs.omega = f.omega; fs.phi = f.phi;
     fs.B = B; fs.H = H; fs.T = T; fs.pos0 = f.pos0;
-    fs.deltas = fdeltas;
-    if ((e = tc_state_pass(fs, st)) != cudaSuccess) return e;
+    if (a.fwd_workspace != nullptr && tc_segments_fit(B, H, T, a.fwd_workspace_bytes) == nseg) {
+      fdeltas = static_cast<float*>(const_cast<void*>(a.fwd_workspace));
+    } else {
+      fs.deltas = fdeltas;
+      if ((e = tc_state_pass(fs, st)) != cudaSuccess) return e;
+    }
     TcJob rs = fs;
     rs.k = q; rs.v = dN; rs.extra = dD; rs.reverse = 1; rs.deltas = rdeltas;
     if ((e = tc_state_pass(rs, st)) != cudaSuccess) return e;

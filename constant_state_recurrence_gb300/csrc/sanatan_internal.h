@@ -43,6 +43,8 @@ struct ChunkBwdArgs {
   float* dphi;
   void* workspace;
   size_t workspace_bytes;
+  const void* fwd_workspace;   // the forward's workspace (its per-segment sums) or null
+  size_t fwd_workspace_bytes;
 };
 
 // Events recorded around the dominant kernel of a chunk_fwd / chunk_bwd call

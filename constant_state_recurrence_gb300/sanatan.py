@@ -529,8 +529,11 @@ def chunk_bwd_workspace_size(B, H, T, d=64, dv=64, dtype=torch.bfloat16):
 
 
 def sanatan_chunk_bwd(q, k, v, gamma, omega, phi, o, D, dO, pos0=0, eps=0.0, S0=None, z0=None,
-                      want_dphi=False, workspace=None):
-    """Gradients of sum(o * dO): dict(dq, dk, dv, dgamma, domega, dphi)."""
+                      want_dphi=False, workspace=None, fwd_workspace=None):
+    """Gradients of sum(o * dO): dict(dq, dk, dv, dgamma, domega, dphi).
+
+    fwd_workspace: the workspace the forward that produced o and D ran with (on
+    these same inputs), so that its per-segment state sums are reused."""
     _need(q, "q", (torch.float32, torch.bfloat16))
     B, H, T, d = q.shape
     dv = v.shape[-1]
@@ -555,7 +558,10 @@ def sanatan_chunk_bwd(q, k, v, gamma, omega, phi, o, D, dO, pos0=0, eps=0.0, S0=
                                  _ptr(omega), _ptr(phi), B, H, T, d, dv, int(pos0), float(eps),
                                  _ptr(S0), _ptr(z0), _ptr(o), _ptr(D), _ptr(dO), _DT[dO.dtype],
                                  _ptr(dq), _ptr(dk), _ptr(dvv), _ptr(dgamma), _ptr(domega),
-                                 _ptr(dphi), _ptr(workspace), ws_bytes, _stream(dev))
+                                 _ptr(dphi), _ptr(workspace), ws_bytes, _ptr(fwd_workspace),
+                                 0 if fwd_workspace is None else
+                                 fwd_workspace.numel() * fwd_workspace.element_size(),
+                                 _stream(dev))
     _check("sanatan_chunk_bwd", st)
     return dict(dq=dq, dk=dk, dv=dvv, dgamma=dgamma, domega=domega, dphi=dphi)
 
@@ -688,14 +694,19 @@ class SanatanAttention(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, v, gamma, omega, phi, pos0=0, eps=0.0):
-        o, D, _, _ = sanatan_chunk_fwd(q, k, v, gamma, omega, phi, pos0=pos0, eps=eps)
+        B, H, T, d = q.shape
+        ws_size = chunk_fwd_workspace_size(B, H, T, d, v.shape[-1], q.dtype)
+        ws = torch.empty(max(ws_size, 16), dtype=torch.uint8, device=q.device)
+        o, D, _, _ = sanatan_chunk_fwd(q, k, v, gamma, omega, phi, pos0=pos0, eps=eps,
+                                       workspace=ws)
         ctx.save_for_backward(q, k, v, gamma, omega, phi, o, D)
         ctx.pos0, ctx.eps = pos0, eps
+        ctx.fwd_ws = ws   # its per-segment state sums serve the backward
         return o
 
     @staticmethod
     def backward(ctx, dO):
         q, k, v, gamma, omega, phi, o, D = ctx.saved_tensors
         g = sanatan_chunk_bwd(q, k, v, gamma, omega, phi, o, D, dO.contiguous(), pos0=ctx.pos0,
-                              eps=ctx.eps, want_dphi=True)
+                              eps=ctx.eps, want_dphi=True, fwd_workspace=ctx.fwd_ws)
         return g["dq"], g["dk"], g["dv"], g["dgamma"], g["domega"], g["dphi"], None, None

@@ -187,6 +187,14 @@ SANATAN_API int sanatan_chunk_fwd_noalloc(const void* q, const void* k, const vo
  *   dgamma  [H] f32 output, domega [H, d] f32 output (overwritten, summed over
  *           the batch and both q and k), dphi [H, d] f32 output or NULL
  *   workspace: at least sanatan_chunk_bwd_workspace_size(...) bytes.
+ *   fwd_workspace / fwd_workspace_bytes: NULL / 0, or the workspace of the
+ *           sanatan_chunk_fwd call that produced o and D from these same q, k,
+ *           v, gamma, omega, phi and pos0, unchanged since.  On the bf16 path,
+ *           when that workspace holds the forward's per-segment state sums for
+ *           the backward's own split (the forward's preferred workspace size
+ *           or more), the backward reuses them instead of recomputing them
+ *           (one launch fewer); otherwise it is ignored.  Passing a workspace
+ *           of another call gives wrong gradients.
  */
 SANATAN_API size_t sanatan_chunk_bwd_workspace_size(int B, int H, int T, int d, int dv, int in_dtype);
 SANATAN_API int sanatan_chunk_bwd(const void* q, const void* k, const void* v, int in_dtype,
@@ -195,7 +203,7 @@ SANATAN_API int sanatan_chunk_bwd(const void* q, const void* k, const void* v, i
                       const float* z0, const float* o, const float* D, const void* dO,
                       int grad_dtype, void* dq, void* dk, void* dv_out, float* dgamma,
                       float* domega, float* dphi, void* workspace, size_t workspace_bytes,
-                      void* stream);
+                      const void* fwd_workspace, size_t fwd_workspace_bytes, void* stream);
 
 /*
  * sanatan_power_fwd -- power-sharpened causal attention, eq. (8) (Notes §2.6),
