@@ -17,9 +17,11 @@
 //      numerator and denominator accumulated with atomics),
 //   C  x += o Wo with o = numerator / (denominator + eps) (warp items of 128
 //      columns x 16 rows).
-// The barriers are bounded: a CTA that waits longer than a second records a
-// timeout in the library's error word, raises an abort flag that ends every
-// other CTA's wait, and returns.
+// Data produced inside the kernel (x, q | k | v, the readout sums) is read
+// through L2 (ld.global.cg), never from a possibly stale L1 line.  The barriers
+// are bounded: a CTA that waits longer than a second records a timeout in the
+// library's error word, raises an abort flag that ends every other CTA's wait,
+// and returns.
 #include "decode_math.cuh"
 #include "sanatan_internal.h"
 #include "sanatan_math.cuh"
@@ -177,7 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1) stack_fused_kernel(FusedParams p)
         const int c0 = cb * 128 + 4 * lane, k0 = rb * kRowsA;
         float xr[B];
 #pragma unroll
-        for (int b = 0; b < B; ++b) xr[b] = p.x[static_cast<int64_t>(b) * Dm + k0 + lane];
+        for (int b = 0; b < B; ++b)
+          xr[b] = __ldcg(p.x + static_cast<int64_t>(b) * Dm + k0 + lane);
         float acc[B][4];
         gemv_item<B, kRowsA>(W, 3 * Dm, k0, c0, xr, acc);
         const int blk = c0 / Dm, col = c0 % Dm;   // q | k | v block and column (Dm % 4 == 0)
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) stack_fused_kernel(FusedParams p)
         const float* qrow = qkv + static_cast<int64_t>(b) * Dm + h * 64;
         if (tid < 16) {
           const int a = part * 8 + (tid & 7);
-          const float u = (tid < 8 ? qrow : qrow + static_cast<int64_t>(B) * Dm)[a];
+          const float u = __ldcg((tid < 8 ? qrow : qrow + static_cast<int64_t>(B) * Dm) + a);
           const float ph = phase_mod_2pi(p.pos[n], p.phi[gh * 64 + a]);
           float ch[6];
           decm::feat_decode(u, p.gamma[gh], p.omega[gh * 64 + a], ph, ch);
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) stack_fused_kernel(FusedParams p)
 #pragma unroll
           for (int c = 0; c < 6; ++c) dst[c] = ch[c];
         } else if (tid < 16 + 64) {
-          s_v[tid - 16] = qrow[static_cast<int64_t>(2) * B * Dm + tid - 16];
+          s_v[tid - 16] = __ldcg(qrow + static_cast<int64_t>(2) * B * Dm + tid - 16);
         }
         __syncthreads();
         const float4 vv = reinterpret_cast<const float4*>(s_v)[cgp];
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) stack_fused_kernel(FusedParams p)
 #pragma unroll
         for (int b = 0; b < B; ++b) {
           const int n = b * p.heads + hh;
-          xr[b] = p.num[static_cast<int64_t>(n) * 64 + e] / (p.den[n] + p.eps);
+          xr[b] = __ldcg(p.num + static_cast<int64_t>(n) * 64 + e) / (__ldcg(p.den + n) + p.eps);
         }
         float acc[B][4];
         gemv_item<B, kRowsC>(W, Dm, k0, c0, xr, acc);
