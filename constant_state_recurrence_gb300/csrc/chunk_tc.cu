@@ -623,21 +623,25 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
   }
   if (warp >= kVWarp0 && warp < kVWarp0 + kVWarps) {
     // ------------------------------------------------------------ value loads
-    // v rows go straight to [V | 1] in shared memory through 16-byte cp.async
-    // copies (the ones column is constant; the optional extra column replaces
-    // it per token).
+    // v rows go straight to [V | 1] in shared memory, by TMA tensor copies in
+    // forward time and 16-byte cp.async copies otherwise (the ones column is
+    // constant; the optional extra column replaces it per token).
     const int vt = tid - 32 * kVWarp0;
+    int tma_issued = 0;   // chunks whose tensor copies have been issued
     for (int ci = 0; ci < nloc; ++ci) {
       const int tok0 = (c_begin + ci) * kC;
       const int nrow = min(kC, prm.T - tok0);
       uint32_t vdst = sV;
       uint64_t* vbar = &m.bar[(kStateOnly && (ci & 1)) ? kFeatV1 : kFeatV];
+      bool free_buf = true;
       if constexpr (kStateOnly) {
         vdst = smem_u32(smem + ((ci & 1) ? kSoV1 : kSoV0));
-        if (ci > 1) wait_bar(m, (ci & 1) ? kStateDone1 : kStateDone, ((ci >> 1) - 1) & 1);
+        if (ci > 1) free_buf = wait_bar(m, (ci & 1) ? kStateDone1 : kStateDone, ((ci >> 1) - 1) & 1);
       } else {
-        if (ci > 0) wait_bar(m, kPVDone, (ci - 1) & 1);
+        if (ci > 0) free_buf = wait_bar(m, kPVDone, (ci - 1) & 1);
       }
+      // after an abandoned wait no further asynchronous copy is issued
+      if (!free_buf && prm.tma_v) break;
       if (prm.tma_v) {
         // 16 tensor loads of one token group each (rows past the end read as
         // zero); the first value-loader thread's arrival carries their bytes
@@ -646,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
           for (int kg = 0; kg < 16; ++kg)
             tma_load_4d(vdst + kg * kLBO_SV, &prm.tmap_v, 0, tok0 + 8 * kg, 0, bh, vbar);
         }
+        tma_issued = ci + 1;
         if (prm.extra != nullptr) {
           for (int t = vt; t < kC; t += 32 * kVWarps) {
             const float x = t < nrow ? prm.extra[seq_row0 + orow(prm, tok0 + t)] : 0.f;
@@ -676,6 +681,16 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&m.bar[(kStateOnly && (ci & 1)) ? kFeatV1 : kFeatV]);
+    }
+    // No tensor copy may still be writing shared memory when the CTA exits,
+    // also after an abandoned wait: wait (bounded) for the last issued ones.
+    if (vt == 0) {
+      for (int ci = (tma_issued >= 2 ? tma_issued - 2 : 0); ci < tma_issued; ++ci) {
+        if (kStateOnly)
+          mbar_wait_bounded(&m.bar[(ci & 1) ? kFeatV1 : kFeatV], (ci >> 1) & 1, kWaitNs);
+        else if (ci == tma_issued - 1)
+          mbar_wait_bounded(&m.bar[kFeatV], ci & 1, kWaitNs);
+      }
     }
   }
   if (warp == kMmaWarp && lane == 0) {
