@@ -681,7 +681,11 @@ def main():
         "data": "synthetic (seeded N(0,1) bf16 q/k/v; gamma=4; omega~U(-pi,pi); "
                 "phi_a=10000^(-a/64))",
         "config": {"workload": W.LAYER.name, "B": 4, "H": 12, "T": 2048, "d": 64, "dv": 64,
-                   "chunk": 128, "segments_per_sequence": layer["segs"],
+                   "chunk": 128,
+                   "chunk_note": "128-token tensor-core chunk (the M of a full-rate tcgen05.mma); "
+                                 "the config's 64-token chunking gives the same sums up to "
+                                 "rounding order",
+                   "segments_per_sequence": layer["segs"],
                    "parallelism": f"{world} independent replica(s), sequences sharded by rank",
                    "l2": "256 MiB flush write before every timed step",
                    "launch": "each timed step replays a CUDA graph of one library call; "

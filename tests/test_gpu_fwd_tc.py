@@ -152,3 +152,22 @@ def test_host_forward_pipeline(H, slices):
         torch.cuda.current_stream().synchronize()
         S.device_status()
         assert max_abs(f64(ho), o_ref) <= TOL_BF16
+
+
+def test_empty_sequences_copy_the_initial_state():
+    """T = 0 on the bf16 path: no output rows; the exported state is (S0, z0),
+    or zeros without one."""
+    x = W.make(W.LAYER, device="cpu", B=2, H=3, T=0)
+    g = to_dev(x)
+    S0 = torch.randn(2, 3, 384, 64, device=dev())
+    z0 = torch.rand(2, 3, 384, device=dev())
+    o, D, Sx, zx = S.sanatan_chunk_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"],
+                                       S0=S0, z0=z0, want_state=True)
+    torch.cuda.synchronize()
+    S.device_status()
+    assert o.shape == (2, 3, 0, 64) and D.shape == (2, 3, 0)
+    assert torch.equal(Sx, S0) and torch.equal(zx, z0)
+    _, _, Sz, zz = S.sanatan_chunk_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"],
+                                       want_state=True)
+    torch.cuda.synchronize()
+    assert not Sz.any() and not zz.any()

@@ -12,7 +12,7 @@ import torch
 import oracle.sanatan_oracle as O
 from constant_state_recurrence_gb300 import sanatan as S
 from constant_state_recurrence_gb300 import workloads as W
-from gpu_util import f64, max_abs, ref_args, rel_fro, to_dev
+from gpu_util import dev, f64, max_abs, ref_args, rel_fro, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -117,3 +117,17 @@ def test_invalid_power_is_rejected():
         with pytest.raises(S.SanatanError) as e:
             S.sanatan_power_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], p)
         assert f"status {code}" in str(e.value)
+
+
+def test_empty_inputs_do_nothing():
+    """T = 0 and B * H = 0 are valid calls that write nothing."""
+    for B, H, T in ((2, 3, 0), (0, 3, 256)):
+        x = W.make(W.LAYER, device="cpu", B=max(B, 1), H=H, T=T)
+        g = {n: x[n].to(dev()) for n in ("q", "k", "v", "gamma", "omega", "phi")}
+        if B == 0:
+            for n in ("q", "k", "v"):
+                g[n] = g[n][:0]
+        o, D = S.sanatan_power_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], 2)[:2]
+        torch.cuda.synchronize()
+        S.device_status()
+        assert o.numel() == 0 and (D is None or D.numel() == 0)
