@@ -65,6 +65,9 @@ FLUSH_BYTES = 256 << 20
 # Both arms report this metric on the layer-forward workload (B=4 H=12 T=2048).
 METRIC = "SANATAN p=1 prefill tokens/s"
 POWER_P = 2          # power of the sharpened-attention leg (the pre-training stage's p)
+ABLATION_P = 2       # power of the ablation-map leg
+HARMONICS = 2        # harmonics of the harmonic-map leg
+FP32_LANES_PER_SM = 128   # FP32 FMA lanes per SM (the CUDA-core peak of the harmonic leg)
 
 # Data shard of this process: under torchrun every rank processes its own
 # sequences (same gamma, omega, phi), set in main().
@@ -76,9 +79,11 @@ def peaks():
         with open(PEAKS_FILE) as f:
             p = json.load(f)
         return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
-                    bf16_sustained=float(p["bf16_tflops_sustained"]), source="measured")
+                    bf16_sustained=float(p["bf16_tflops_sustained"]),
+                    sm_max_mhz=float(p.get("sm_max_mhz", 2070.0)), source="measured")
     except Exception:
-        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, sm_max_mhz=2070.0,
+                    source="fallback")
 
 
 def source_hash(path):
@@ -436,6 +441,65 @@ def power_train_case(p, dev, flush, steps, warmup, stream):
     return dict(step=step, B=B, H=H, T=T, p=p)
 
 
+def ablation_case(dev, flush, steps, warmup, stream):
+    """The ablation maps on the layer-forward workload at p = 2: the four-channel
+    map (clipped scores) and the three-channel map with the printed +d shift;
+    feature preparation plus the quadratic tensor-core kernel, as the power leg."""
+    from constant_state_recurrence_gb300 import sanatan as S
+    x = W.make(W.LAYER, device=dev, shard=SHARD)
+    g = {n: x[n] for n in ("q", "k", "v", "gamma", "omega", "phi")}
+    B, H, T = x["B"], x["H"], x["T"]
+    o = torch.empty(B, H, T, 64, dtype=torch.float32, device=dev)
+    D = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    ws = torch.empty(S.power_fwd_workspace_size(B, H, T), dtype=torch.uint8, device=dev)
+    cases = {}
+    for ch, shift in ((4, 0.0), (3, 64.0)):
+        def step(_i, ch=ch, shift=shift):
+            S.sanatan_ablation_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"],
+                                   ABLATION_P, ch, shift=shift, out=o, D_out=D, workspace=ws)
+        for _ in range(warmup):
+            flush.zero_()
+            step(0)
+        cases[ch] = dict(step=step, shift=shift)
+    torch.cuda.synchronize()
+    S.device_status()
+    return dict(cases=cases, B=B, H=H, T=T)
+
+
+def harmonic_case(dev, flush, steps, warmup, stream):
+    """The harmonic map (N = 2) on the CUDA cores: the chunked forward over the
+    layer-forward workload and one decode step of 144 slots (batch 1) from a
+    state of that size."""
+    from constant_state_recurrence_gb300 import sanatan as S
+    x = W.make(W.LAYER, device=dev, shard=SHARD)
+    g = {n: x[n] for n in ("q", "k", "v", "gamma", "omega", "phi")}
+    B, H, T = x["B"], x["H"], x["T"]
+    N = HARMONICS
+    F = S.harmonic_features(N)
+
+    def fwd(_i):
+        S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], N)
+
+    G = 144
+    gen = W.generator(W.DECODE.seed + 11, dev)
+    gd, od, pd = W.params(G, 64, "geometric", gen, device=dev)
+    Sx = torch.randn(G, F, 64, generator=gen, device=dev) * 0.1
+    zx = torch.rand(G, F, generator=gen, device=dev) + 1.0
+    q, k, v = (t[0] for t in W.decode_tokens(G, 64, 64, 1, gen))
+    pos = torch.full((G,), 4096, dtype=torch.int64, device=dev)
+
+    def dec(_i):
+        S.sanatan_decode_step_harmonic(Sx, zx, q, k, v, gd, od, pd, pos, N)
+
+    for _ in range(warmup):
+        flush.zero_()
+        fwd(0)
+        dec(0)
+    torch.cuda.synchronize()
+    S.device_status()
+    return dict(fwd=fwd, dec=dec, B=B, H=H, T=T, F=F, slots=G)
+
+
 STACK_LAYERS, STACK_HEADS = 12, 12   # the 184M model's attention stack (12 layers x 12 heads)
 STACK_STEPS_PER_GRAPH = 64
 
@@ -573,7 +637,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["layer", "long", "decode", "train", "power", "stack"],
+    ap.add_argument("--only", choices=["layer", "long", "decode", "train", "power", "stack",
+                                       "ablation", "harmonic"],
                     default=None,
                     help="run one workload only (profiling); the JSON line keeps its keys")
     args = ap.parse_args()
@@ -607,6 +672,9 @@ def main():
     power = power_case(POWER_P, dev, flush, pw_steps, warm, stream) if want("power") else None
     ptrain = power_train_case(POWER_P, dev, flush, pw_steps, warm, stream) if want("power") else None
     stack = stack_case(dev, flush) if want("stack") else None
+    abl = ablation_case(dev, flush, pw_steps, warm, stream) if want("ablation") else None
+    hs_steps = max(3, steps // 10)
+    harm = harmonic_case(dev, flush, hs_steps, warm, stream) if want("harmonic") else None
 
     gpu_idx = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -638,6 +706,14 @@ def main():
             pw_whole, pw_kern = timed_steps(power["step"], pw_steps, flush, stream, profile=True)
             pt_whole, pt_kern = timed_steps(ptrain["step"], pw_steps, flush, stream, profile=True)
         st_ms = timed_stack(stack, 16, stream) if stack else nan
+        abl_t = {}
+        if abl:
+            for ch, c in abl["cases"].items():
+                abl_t[ch] = timed_steps(c["step"], pw_steps, flush, stream, profile=True)
+        hf_whole = hd_whole = [nan]
+        if harm:
+            hf_whole, _ = timed_steps(harm["fwd"], hs_steps, flush, stream)
+            hd_whole, _ = timed_steps(harm["dec"], steps, flush, stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
     barrier(world)
@@ -773,6 +849,45 @@ def main():
                     "hardware (context)"},
         "timed_region_wall_s": t_wall,
     }
+    if abl:
+        ab = {}
+        for ch, (whole, kern) in abl_t.items():
+            fl = power_flops(4, 12, 2048, F=ch * 64)
+            ab[f"{ch}ch"] = {
+                "p": ABLATION_P, "shift": abl["cases"][ch]["shift"],
+                "tokens_per_s": 4 * 2048 / (statistics.mean(whole) * 1e-3),
+                "ms_per_step": statistics.mean(whole), "kernel_ms": statistics.mean(kern),
+                "flops_per_step": fl,
+                "tc_frac_kernel": fl / (statistics.mean(kern) * 1e-3) / 1e12 / pk["bf16"]}
+        line["ablation"] = dict(workload=W.LAYER.name, steps=pw_steps, **ab,
+                                note="ablation maps of the notes at p = 2 (four channels: clipped "
+                                     "scores, scale 3d; three channels: +d shift, scale 3d); "
+                                     "flops = pairs j<=t x (2 F + 2 dv), F = channels x 64")
+    if harm:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        alu_peak = sms * FP32_LANES_PER_SM * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        F = harm["F"]
+        fl_th = 4 * F * (64 + 1)   # state update + readout per token-head (recurrent minimum)
+        th = harm["B"] * harm["H"] * harm["T"]
+        hf_ms = statistics.mean(hf_whole)
+        hd_ms = statistics.mean(hd_whole)
+        dec_bytes = harm["slots"] * (2 * (F * 64 + F) * 4 + 4 * 64 * 4)
+        line["harmonic"] = {
+            "harmonics": HARMONICS, "features": F,
+            "forward": {"workload": W.LAYER.name, "steps": hs_steps, "ms_per_step": hf_ms,
+                        "tokens_per_s": harm["B"] * harm["T"] / (hf_ms * 1e-3),
+                        "roofline": {"bound": "alu", "achieved": fl_th * th / (hf_ms * 1e-3) / 1e12,
+                                     "peak": alu_peak, "unit": "TFLOP/s",
+                                     "frac": fl_th * th / (hf_ms * 1e-3) / 1e12 / alu_peak,
+                                     "flops_per_token_head": fl_th,
+                                     "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 FMA "
+                                                    "lanes x 2 flops x max SM clock"}},
+            "decode": {"slots": harm["slots"], "steps": steps, "us_per_step": 1e3 * hd_ms,
+                       "achieved_gbs": dec_bytes / (hd_ms * 1e-3) / 1e9,
+                       "hbm_frac": dec_bytes / (hd_ms * 1e-3) / 1e9 / pk["hbm"],
+                       "bytes_per_step": dec_bytes},
+            "note": "float32 on the CUDA cores (the tensor-core path keeps 320 + 1 features); "
+                    "L2 flushed before each step"}
     clocks = clk.summary()
     if clocks:
         line["clocks"] = clocks
