@@ -480,6 +480,9 @@ def harmonic_case(dev, flush, steps, warmup, stream):
     def fwd(_i):
         S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], N)
 
+    def fwd3(_i):
+        S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], 3)
+
     G = 144
     gen = W.generator(W.DECODE.seed + 11, dev)
     gd, od, pd = W.params(G, 64, "geometric", gen, device=dev)
@@ -494,10 +497,12 @@ def harmonic_case(dev, flush, steps, warmup, stream):
     for _ in range(warmup):
         flush.zero_()
         fwd(0)
+        fwd3(0)
         dec(0)
     torch.cuda.synchronize()
     S.device_status()
-    return dict(fwd=fwd, dec=dec, B=B, H=H, T=T, F=F, slots=G)
+    return dict(fwd=fwd, fwd3=fwd3, dec=dec, B=B, H=H, T=T, F=F, F3=S.harmonic_features(3),
+                slots=G)
 
 
 STACK_LAYERS, STACK_HEADS = 12, 12   # the 184M model's attention stack (12 layers x 12 heads)
@@ -710,9 +715,10 @@ def main():
         if abl:
             for ch, c in abl["cases"].items():
                 abl_t[ch] = timed_steps(c["step"], pw_steps, flush, stream, profile=True)
-        hf_whole = hd_whole = [nan]
+        hf_whole = hf3_whole = hd_whole = [nan]
         if harm:
             hf_whole, _ = timed_steps(harm["fwd"], hs_steps, flush, stream)
+            hf3_whole, _ = timed_steps(harm["fwd3"], hs_steps, flush, stream)
             hd_whole, _ = timed_steps(harm["dec"], steps, flush, stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
@@ -867,21 +873,26 @@ def main():
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         alu_peak = sms * FP32_LANES_PER_SM * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         F = harm["F"]
-        fl_th = 4 * F * (64 + 1)   # state update + readout per token-head (recurrent minimum)
         th = harm["B"] * harm["H"] * harm["T"]
-        hf_ms = statistics.mean(hf_whole)
         hd_ms = statistics.mean(hd_whole)
         dec_bytes = harm["slots"] * (2 * (F * 64 + F) * 4 + 4 * 64 * 4)
+
+        def harm_fwd(whole, nf):
+            ms = statistics.mean(whole)
+            fl = 4 * nf * (64 + 1)   # state update + readout per token-head (recurrent minimum)
+            ach = fl * th / (ms * 1e-3) / 1e12
+            return {"workload": W.LAYER.name, "features": nf, "steps": hs_steps,
+                    "ms_per_step": ms, "tokens_per_s": harm["B"] * harm["T"] / (ms * 1e-3),
+                    "roofline": {"bound": "alu", "achieved": ach, "peak": alu_peak,
+                                 "unit": "TFLOP/s", "frac": ach / alu_peak,
+                                 "flops_per_token_head": fl,
+                                 "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 FMA "
+                                                "lanes x 2 flops x max SM clock"}}
+
         line["harmonic"] = {
             "harmonics": HARMONICS, "features": F,
-            "forward": {"workload": W.LAYER.name, "steps": hs_steps, "ms_per_step": hf_ms,
-                        "tokens_per_s": harm["B"] * harm["T"] / (hf_ms * 1e-3),
-                        "roofline": {"bound": "alu", "achieved": fl_th * th / (hf_ms * 1e-3) / 1e12,
-                                     "peak": alu_peak, "unit": "TFLOP/s",
-                                     "frac": fl_th * th / (hf_ms * 1e-3) / 1e12 / alu_peak,
-                                     "flops_per_token_head": fl_th,
-                                     "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 FMA "
-                                                    "lanes x 2 flops x max SM clock"}},
+            "forward": harm_fwd(hf_whole, F),
+            "forward_N3": harm_fwd(hf3_whole, harm["F3"]),
             "decode": {"slots": harm["slots"], "steps": steps, "us_per_step": 1e3 * hd_ms,
                        "achieved_gbs": dec_bytes / (hd_ms * 1e-3) / 1e9,
                        "hbm_frac": dec_bytes / (hd_ms * 1e-3) / 1e9 / pk["hbm"],

@@ -424,7 +424,7 @@ int sanatan_chunk_fwd_harmonic(const void* q, const void* k, const void* v, int 
                                float* S_out, float* z_out, void* stream) {
   if (!ok_dtype(in_dtype) || harmonics < 1) return SANATAN_ERR_INVALID;
   if (int s = check_sizes(B, H, T, d, dv)) return s;
-  if (harmonics > 2) return SANATAN_ERR_UNSUPPORTED;
+  if (harmonics > 3) return SANATAN_ERR_UNSUPPORTED;
   if ((S0 == nullptr) != (z0 == nullptr)) return SANATAN_ERR_INVALID;
   if ((S_out == nullptr) != (z_out == nullptr)) return SANATAN_ERR_INVALID;
   if (!ok_nullable(S0) || !ok_nullable(z0) || !ok_nullable(S_out) || !ok_nullable(z_out) ||

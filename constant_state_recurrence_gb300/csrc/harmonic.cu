@@ -16,11 +16,15 @@
 
 #include "sanatan_internal.h"
 #include "sanatan_math.cuh"
+#include "f32x2.cuh"
 
 namespace sanatan {
 namespace {
 
 namespace cg = cooperative_groups;
+using f2::ffma2;
+using f2::pk2;
+using f2::upk2;
 
 constexpr int kD = 64;
 constexpr int kDv = 64;
@@ -76,143 +80,226 @@ __global__ void __launch_bounds__(256) featurize_harmonic_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Chunked forward (N = 2): per chunk of kC = 8 tokens, the masked scores from
-// the chunk's features, the outputs from them plus Phi(q) against the state of
-// the earlier chunks, then S += Phi(K)^T V, z += Phi(K)^T 1.
+// Chunked forward: a cluster of kRanks CTAs per sequence, CTA rank r holding
+// the state rows of dimensions 8r .. 8r + 7 (8 kCh rows x 64 columns) in
+// registers.  Scores, the intra-chunk weighted values and the state readout
+// are all sums over features, so per chunk of kCT tokens every CTA forms
+// complete partial numerators and denominators from its own rows:
+//   num_t = sum_{j<=t} (Phi(q_t) . Phi(k_j))_r v_j + Phi(q_t)_r S_r,
+//   den_t = sum_{j<=t} (Phi(q_t) . Phi(k_j))_r     + Phi(q_t)_r z_r,
+// and one cluster reduction through distributed shared memory (CTA rank r
+// sums tokens r and r + 8 over the cluster) gives o_t = num_t / (den_t + eps);
+// then S_r += Phi(K)_r^T V, z_r += Phi(K)_r^T 1 in registers.  Thread
+// (c, g) owns column c of the CTA's rows g kPT .. (g + 1) kPT - 1, read from
+// shared memory as 16-byte row pieces and multiplied in packed f32x2 pairs.
 constexpr int kThreads = 256;
+constexpr int kRanks = 8;      // CTAs per sequence: 8 dimensions each
+constexpr int kCT = 16;        // tokens per chunk (two per CTA in the reduction)
 
-template <int N, int C>
-struct HarmSmem {
-  static constexpr int kF = Harm<N>::kF;
-  static constexpr int kFP = kF + 1;   // padded row stride
-  float pq[C * kFP];
-  float pk[C * kFP];
-  float v[C * kDv];
-  float S[kF * kDv];
-  float z[kF];
-  float P[C * (C + 1)];
+template <int N>
+struct ClusterSmem {
+  static constexpr int kR = 8 * Harm<N>::kCh;   // state rows of this CTA
+  static constexpr int kRP = kR + 4;            // feature row pitch (16-byte rows)
+  alignas(16) float pq[kCT][kRP];
+  alignas(16) float pk[kCT][kRP];
+  float v[kCT][kDv];
+  float z[kR];
+  float P[kCT][kCT + 1];
+  float part[4][kCT][kDv];          // readout partials of the four row groups
+  float out[2][kCT][kDv + 1];       // this CTA's partial numerators | denominator (by chunk parity)
 };
 
-template <int N, int C, typename Tin>
-__global__ void __launch_bounds__(kThreads, 1) chunk_fwd_harmonic_kernel(
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int N, typename Tin>
+__global__ void __launch_bounds__(kThreads, 3) chunk_fwd_harmonic_kernel(
     const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
     const float* __restrict__ gamma, const float* __restrict__ omega,
     const float* __restrict__ phi, int H, int T, int64_t pos0, float eps,
     const float* __restrict__ S0, const float* __restrict__ z0, float* __restrict__ o,
     float* __restrict__ Dout, float* __restrict__ S_out, float* __restrict__ z_out) {
-  using Sm = HarmSmem<N, C>;
-  constexpr int kF = Sm::kF, kFP = Sm::kFP, kCh = Harm<N>::kCh;
-  constexpr int kPairLanes = kThreads / (C * C);   // threads per (t, j) score
-  constexpr int kRowLanes = kThreads / C;          // threads per output row
-  static_assert(kPairLanes >= 1 && (kPairLanes & (kPairLanes - 1)) == 0 && kRowLanes <= 32,
-                "thread mapping");
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
-  const int bh = blockIdx.x;
+  constexpr int kCh = Harm<N>::kCh, kF = Harm<N>::kF;
+  constexpr int kR = ClusterSmem<N>::kR;
+  constexpr int kPT = kR / 4;   // rows per thread
+  constexpr int kP4 = kPT / 4;  // 16-byte pieces of them
+  static_assert(kPT % 4 == 0 && kRanks * 8 == kD && 2 * kRanks == kCT, "shape");
+  static_assert(kThreads == 2 * kCT * 8 && kThreads == 4 * kDv, "thread map");
+  __shared__ ClusterSmem<N> sm;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int bh = blockIdx.x / kRanks;
   const int h = bh % H;
   const int tid = threadIdx.x;
+  const int c = tid & (kDv - 1), rg = tid >> 6;
   const int64_t seq = static_cast<int64_t>(bh) * T;
-  const float g = gamma[h];
+  const int64_t row0 = static_cast<int64_t>(bh) * kF + rank * kR;   // first state row of the CTA
+  const int f0 = rg * kPT;                                           // first row of the thread
 
-  for (int i = tid; i < kF * kDv; i += kThreads)
-    sm.S[i] = S0 ? S0[static_cast<int64_t>(bh) * kF * kDv + i] : 0.f;
-  for (int i = tid; i < kF; i += kThreads) sm.z[i] = z0 ? z0[static_cast<int64_t>(bh) * kF + i] : 0.f;
+  // feature thread map: (tensor, token, dimension of the CTA)
+  const int fw = tid >> 7, ft = (tid >> 3) & (kCT - 1), fa = rank * 8 + (tid & 7);
+  const Tin* fsrc = fw ? k : q;
+  const float g = gamma[h], om = omega[h * kD + fa], ph = phi[h * kD + fa];
 
-  for (int c0 = 0; c0 < T; c0 += C) {
-    const int nc = min(C, T - c0);
-    __syncthreads();  // the previous chunk is done with pq, pk, v, P and S
-    for (int e = tid; e < 2 * C * kD; e += kThreads) {
-      const int which = e / (C * kD);
-      const int t = (e / kD) % C;
-      const int a = e % kD;
-      float* dst = (which == 0 ? sm.pq : sm.pk) + t * kFP + kCh * a;
-      if (t < nc) {
-        const Tin* src = which == 0 ? q : k;
+  uint64_t Sr[kPT / 2];   // rows f0 + 2i, f0 + 2i + 1 of column c
+#pragma unroll
+  for (int i = 0; i < kPT / 2; ++i) {
+    const float a0 = S0 ? S0[(row0 + f0 + 2 * i) * kDv + c] : 0.f;
+    const float a1 = S0 ? S0[(row0 + f0 + 2 * i + 1) * kDv + c] : 0.f;
+    Sr[i] = pk2(a0, a1);
+  }
+  if (tid < kR) sm.z[tid] = z0 ? z0[row0 + tid] : 0.f;
+
+  // inputs of the next chunk, held in registers while the current one runs
+  float uf = 0.f, vr[4] = {0.f, 0.f, 0.f, 0.f};
+  auto prefetch = [&](int c0n) {
+    const int nn = min(kCT, T - c0n);
+    uf = ft < nn ? load_as_float(fsrc + (seq + c0n + ft) * kD + fa) : 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int t = rg + 4 * m;
+      vr[m] = t < nn ? load_as_float(v + (seq + c0n + t) * kDv + c) : 0.f;
+    }
+  };
+  if (T > 0) prefetch(0);
+
+  int buf = 0;
+  for (int c0 = 0; c0 < T; c0 += kCT, buf ^= 1) {
+    const int nc = min(kCT, T - c0);
+    __syncthreads();   // the previous chunk is done with pq, pk, v and z
+    {
+      float* dst = (fw ? &sm.pk[ft][0] : &sm.pq[ft][0]) + kCh * (tid & 7);
+      if (ft < nc) {
         float ch[kCh];
-        harmonic_channels<N>(load_as_float(src + (seq + c0 + t) * kD + a), g, omega[h * kD + a],
-                             phase_mod_2pi(pos0 + c0 + t, phi[h * kD + a]), ch);
+        harmonic_channels<N>(uf, g, om, phase_mod_2pi(pos0 + c0 + ft, ph), ch);
 #pragma unroll
         for (int cc = 0; cc < kCh; ++cc) dst[cc] = ch[cc];
       } else {
 #pragma unroll
         for (int cc = 0; cc < kCh; ++cc) dst[cc] = 0.f;
       }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) sm.v[rg + 4 * m][c] = vr[m];
     }
-    for (int e = tid; e < C * kDv; e += kThreads) {
-      const int t = e / kDv;
-      sm.v[e] = t < nc ? load_as_float(v + (seq + c0 + t) * kDv + (e % kDv)) : 0.f;
-    }
+    if (c0 + kCT < T) prefetch(c0 + kCT);
     __syncthreads();
-
-    // masked scores P[t][j], j <= t: kPairLanes threads per pair
     {
-      const int pair = tid / kPairLanes, part = tid % kPairLanes;
-      const int t = pair / C, j = pair % C;
-      float s = 0.f;
+      // partial scores over this CTA's rows: thread (t, j)
+      const int t = tid >> 4, j = tid & (kCT - 1);
       if (j <= t) {
-        const float* rq = sm.pq + t * kFP;
-        const float* rk = sm.pk + j * kFP;
-        for (int f = part; f < kF; f += kPairLanes) s = fmaf(rq[f], rk[f], s);
+        const ulonglong2* a = reinterpret_cast<const ulonglong2*>(&sm.pq[t][0]);
+        const ulonglong2* b = reinterpret_cast<const ulonglong2*>(&sm.pk[j][0]);
+        uint64_t s0 = 0, s1 = 0;
+#pragma unroll 4
+        for (int i = 0; i < kR / 4; ++i) {
+          const ulonglong2 x = a[i], y = b[i];
+          s0 = ffma2(x.x, y.x, s0);
+          s1 = ffma2(x.y, y.y, s1);
+        }
+        float p0, p1, p2, p3;
+        upk2(s0, p0, p1);
+        upk2(s1, p2, p3);
+        sm.P[t][j] = (p0 + p1) + (p2 + p3);
       }
-#pragma unroll
-      for (int off = kPairLanes / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (part == 0) sm.P[t * (C + 1) + j] = s;
     }
-    __syncthreads();
-
-    // outputs: kRowLanes threads per row, kDv / kRowLanes columns each
-    {
-      constexpr int kCols = kDv / kRowLanes;
-      const int t = tid / kRowLanes, lane = tid % kRowLanes;
-      const float* rq = sm.pq + t * kFP;
-      float num[kCols];
+#pragma unroll 1
+    for (int th = 0; th < kCT; th += 8) {
+      // readout partials of this thread's rows against the state before the chunk
+      uint64_t num[8];
 #pragma unroll
-      for (int m = 0; m < kCols; ++m) num[m] = 0.f;
-      for (int j = 0; j <= t; ++j) {
-        const float p = sm.P[t * (C + 1) + j];
+      for (int t = 0; t < 8; ++t) num[t] = 0;
 #pragma unroll
-        for (int m = 0; m < kCols; ++m) num[m] = fmaf(p, sm.v[j * kDv + lane + kRowLanes * m], num[m]);
+      for (int i = 0; i < kP4; ++i) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const ulonglong2 x = reinterpret_cast<const ulonglong2*>(&sm.pq[th + t][f0])[i];
+          num[t] = ffma2(x.x, Sr[2 * i], num[t]);
+          num[t] = ffma2(x.y, Sr[2 * i + 1], num[t]);
+        }
       }
-      for (int f = 0; f < kF; ++f) {
-        const float x = rq[f];
 #pragma unroll
-        for (int m = 0; m < kCols; ++m) num[m] = fmaf(x, sm.S[f * kDv + lane + kRowLanes * m], num[m]);
-      }
-      float den = 0.f;
-      for (int j = lane; j <= t; j += kRowLanes) den += sm.P[t * (C + 1) + j];
-      for (int f = lane; f < kF; f += kRowLanes) den = fmaf(rq[f], sm.z[f], den);
-#pragma unroll
-      for (int off = kRowLanes / 2; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-      if (t < nc) {
-        float* orow = o + (seq + c0 + t) * kDv;
-        const float inv = 1.0f / (den + eps);
-#pragma unroll
-        for (int m = 0; m < kCols; ++m) orow[lane + kRowLanes * m] = num[m] * inv;
-        if (Dout && lane == 0) Dout[seq + c0 + t] = den;
+      for (int t = 0; t < 8; ++t) {
+        float x0, x1;
+        upk2(num[t], x0, x1);
+        sm.part[rg][th + t][c] = x0 + x1;
       }
     }
     __syncthreads();
-
-    // state carry
     {
-      const int e = tid & (kDv - 1);
-      for (int f = tid >> 6; f < kF; f += kThreads / kDv) {
-        float acc = sm.S[f * kDv + e];
-        for (int j = 0; j < nc; ++j) acc = fmaf(sm.pk[j * kFP + f], sm.v[j * kDv + e], acc);
-        sm.S[f * kDv + e] = acc;
+      // this CTA's partial numerators and denominators: warp w, tokens w and w + 8
+      const int w = tid >> 5, lane = tid & 31;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int t = w + 8 * hh;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int col = lane + 32 * m;
+          float acc = (sm.part[0][t][col] + sm.part[1][t][col]) +
+                      (sm.part[2][t][col] + sm.part[3][t][col]);
+          for (int j = 0; j <= t; ++j) acc = fmaf(sm.P[t][j], sm.v[j][col], acc);
+          sm.out[buf][t][col] = acc;
+        }
+        float dn = (lane <= t) ? sm.P[t][lane] : 0.f;
+        for (int f = lane; f < kR; f += 32) dn = fmaf(sm.pq[t][f], sm.z[f], dn);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dn += __shfl_xor_sync(0xffffffffu, dn, off);
+        if (lane == 0) sm.out[buf][t][kDv] = dn;
       }
-      for (int f = tid; f < kF; f += kThreads) {
-        float acc = sm.z[f];
-        for (int j = 0; j < nc; ++j) acc += sm.pk[j * kFP + f];
-        sm.z[f] = acc;
+    }
+    cluster_arrive();  // this CTA's partials of the chunk are written
+    __syncthreads();   // z is read; the state may move on
+#pragma unroll 4
+    for (int j = 0; j < kCT; ++j) {
+      const float vj = sm.v[j][c];
+      const uint64_t vv = pk2(vj, vj);
+#pragma unroll
+      for (int i = 0; i < kP4; ++i) {
+        const ulonglong2 x = reinterpret_cast<const ulonglong2*>(&sm.pk[j][f0])[i];   // zero past T
+        Sr[2 * i] = ffma2(x.x, vv, Sr[2 * i]);
+        Sr[2 * i + 1] = ffma2(x.y, vv, Sr[2 * i + 1]);
+      }
+    }
+    if (tid < kR) {
+      float acc = sm.z[tid];
+#pragma unroll
+      for (int j = 0; j < kCT; ++j) acc += sm.pk[j][tid];
+      sm.z[tid] = acc;
+    }
+    cluster_wait();    // every CTA's partials of this chunk are in its shared memory
+    {
+      // tokens rank and rank + 8 of the chunk: the sums over the cluster
+      const int t = rank + kRanks * (tid >> 6), e = tid & (kDv - 1);
+      if (tid < 2 * kDv && t < nc) {
+        float nm = 0.f, dn = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < kRanks; ++rr) {
+          const float* rem = cluster.map_shared_rank(&sm.out[buf][t][0], rr);
+          nm += rem[e];
+          dn += rem[kDv];
+        }
+        const int64_t orow = seq + c0 + t;
+        o[orow * kDv + e] = nm / (dn + eps);
+        if (e == 0 && Dout) Dout[orow] = dn;
       }
     }
   }
   __syncthreads();
   if (S_out) {
-    for (int i = tid; i < kF * kDv; i += kThreads) S_out[static_cast<int64_t>(bh) * kF * kDv + i] = sm.S[i];
-    for (int i = tid; i < kF; i += kThreads) z_out[static_cast<int64_t>(bh) * kF + i] = sm.z[i];
+#pragma unroll
+    for (int i = 0; i < kPT / 2; ++i) {
+      float a0, a1;
+      upk2(Sr[i], a0, a1);
+      S_out[(row0 + f0 + 2 * i) * kDv + c] = a0;
+      S_out[(row0 + f0 + 2 * i + 1) * kDv + c] = a1;
+    }
+    if (tid < kR) z_out[row0 + tid] = sm.z[tid];
   }
+  cluster_arrive();    // no CTA leaves while another still reads its shared memory
+  cluster_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -356,17 +443,23 @@ cudaError_t featurize_n(const HarmonicFeatArgs& a, cudaStream_t st) {
   return featurize_h<N, __nv_bfloat16, __nv_bfloat16>(a, st);
 }
 
-template <int N, int C, typename Tin>
+template <int N, typename Tin>
 cudaError_t chunk_h(const ChunkFwdArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(HarmSmem<N, C>);
-  auto kern = chunk_fwd_harmonic_kernel<N, C, Tin>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  kern<<<a.B * a.H, kThreads, smem, st>>>(
-      static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
-      a.gamma, a.omega, a.phi, a.H, a.T, a.pos0, a.eps, a.S0, a.z0, a.o, a.D, a.S_out, a.z_out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.H) * kRanks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kRanks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chunk_fwd_harmonic_kernel<N, Tin>,
+                            static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k),
+                            static_cast<const Tin*>(a.v), a.gamma, a.omega, a.phi, a.H, a.T,
+                            a.pos0, a.eps, a.S0, a.z0, a.o, a.D, a.S_out, a.z_out);
 }
 
 template <int N>
@@ -406,7 +499,8 @@ cudaError_t chunk_fwd_harmonic_launch(const ChunkFwdArgs& a, int harmonics, cuda
   if (a.B * a.H == 0) return cudaSuccess;
   const bool f32 = a.in_dtype == SANATAN_F32;
   if (harmonics == 1) return chunk_fwd_simt_launch(a, st);  // the six-channel map itself
-  if (harmonics == 2) return f32 ? chunk_h<2, 8, float>(a, st) : chunk_h<2, 8, __nv_bfloat16>(a, st);
+  if (harmonics == 2) return f32 ? chunk_h<2, float>(a, st) : chunk_h<2, __nv_bfloat16>(a, st);
+  if (harmonics == 3) return f32 ? chunk_h<3, float>(a, st) : chunk_h<3, __nv_bfloat16>(a, st);
   return cudaErrorInvalidValue;
 }
 

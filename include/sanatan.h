@@ -318,7 +318,8 @@ SANATAN_API int sanatan_device_status(void* stream);
  * sanatan_chunk_fwd_harmonic -- the causal normalised attention of
  *   sanatan_chunk_fwd with Phi_N (arguments, layouts and outputs as there with
  *   6d replaced by F_N; no workspace); q, k, v f32 or bf16 (converted to f32);
- *   harmonics 1..2 (the state of one sequence lives in shared memory).
+ *   harmonics 1..3 (N >= 2: a cluster of eight CTAs per sequence, each
+ *   holding the state rows of eight dimensions in registers).
  * sanatan_decode_step_harmonic -- one token of the recurrence with Phi_N for N
  *   slots, as sanatan_decode_step with S [N, F_N, dv] and z [N, F_N];
  *   harmonics 1..3.

@@ -1,7 +1,8 @@
 """The harmonic feature map (Appendix B of the notes) on the GPU against the
 float64 oracle: features (f32 <= 1e-5 abs), the chunked p=1 forward (f32:
-<= 1e-5 on o, state relative <= 1e-5), the decode step (<= 1e-5), chunked vs
-decode (<= 1e-4), and N = 1 against the six-channel entry points."""
+<= 1e-5 on o, state relative <= 1e-5; at the full layer-forward size <= 1e-4
+on o), the decode step (<= 1e-5), chunked vs decode (<= 1e-4), and N = 1
+against the six-channel entry points."""
 import numpy as np
 import pytest
 import torch
@@ -26,17 +27,18 @@ def test_features(N):
     assert max_abs(f64(f), ref) <= 1e-5
 
 
-@pytest.mark.parametrize("T", [1, 7, 8, 9, 100])
-def test_chunked_forward_two_harmonics(T):
+@pytest.mark.parametrize("N,T", [(2, 1), (2, 7), (2, 8), (2, 9), (2, 100), (3, 1), (3, 13),
+                                 (3, 100)])
+def test_chunked_forward_harmonics(N, T):
     x = W.make(W.TINY, B=2, H=2, T=T)
     x["phi"] = W.rates(2, 64, "geometric")
     g = to_dev(x)
     o, D, Sx, zx = S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
-                                                g["phi"], 2, pos0=40, eps=0.2, want_state=True)
+                                                g["phi"], N, pos0=40, eps=0.2, want_state=True)
     torch.cuda.synchronize()
     ra = ref_args(x)
-    o_ref, D_ref = O.attn_harmonic(**ra, N=2, pos0=40, eps=0.2)
-    S_ref, z_ref = O.final_state_harmonic(ra["k"], ra["v"], ra["gamma"], ra["omega"], ra["phi"], 2,
+    o_ref, D_ref = O.attn_harmonic(**ra, N=N, pos0=40, eps=0.2)
+    S_ref, z_ref = O.final_state_harmonic(ra["k"], ra["v"], ra["gamma"], ra["omega"], ra["phi"], N,
                                           pos0=40)
     assert max_abs(f64(o), o_ref) <= 1e-5
     assert rel_fro(f64(D), D_ref) <= 1e-5
@@ -60,10 +62,34 @@ def test_chunked_forward_bf16_inputs_and_initial_state():
     assert max_abs(f64(o), o_ref) <= 1e-5
 
 
+@pytest.mark.parametrize("N", [2, 3])
+def test_chunked_forward_full_size_sampled_sequences(N):
+    """B=4, H=12, T=2048 bf16 (the layer-forward workload, all 48 sequences in
+    one launch): the outputs and final state of three sampled sequences, each
+    against the oracle's quadratic form (1e-4 on o, 1e-5 relative on D, S, z)."""
+    x = W.make(W.LAYER, device="cpu")
+    g = to_dev(x)
+    o, D, Sx, zx = S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
+                                                g["phi"], N, want_state=True)
+    torch.cuda.synchronize()
+    ra = ref_args(x)
+    og, Dg, Sg, zg = f64(o), f64(D), f64(Sx), f64(zx)
+    for b, h in ((0, 0), (1, 5), (3, 11)):
+        one = {n: ra[n][b:b + 1, h:h + 1] for n in ("q", "k", "v")}
+        one.update({n: ra[n][h:h + 1] for n in ("gamma", "omega", "phi")})
+        o_ref, D_ref = O.attn_harmonic(**one, N=N)
+        S_ref, z_ref = O.final_state_harmonic(one["k"], one["v"], one["gamma"], one["omega"],
+                                              one["phi"], N)
+        assert max_abs(og[b, h], o_ref[0, 0]) <= 1e-4, (b, h)
+        assert rel_fro(Dg[b, h], D_ref[0, 0]) <= 1e-5, (b, h)
+        assert rel_fro(Sg[b, h], S_ref[0, 0]) <= 1e-5, (b, h)
+        assert rel_fro(zg[b, h], z_ref[0, 0]) <= 1e-5, (b, h)
+
+
 @pytest.mark.parametrize("N", [1, 2, 3])
 def test_decode_steps_match_oracle_and_chunked(N):
-    """T single-token steps from the zero state reproduce the oracle (1e-5) and,
-    for N <= 2, the chunked forward (1e-4)."""
+    """T single-token steps from the zero state reproduce the oracle (1e-5) and
+    the chunked forward (1e-4)."""
     x = W.make(W.TINY, B=1, H=3, T=40)
     x["phi"] = W.rates(3, 64, "geometric")
     g = to_dev(x)
@@ -81,13 +107,11 @@ def test_decode_steps_match_oracle_and_chunked(N):
     torch.cuda.synchronize()
     o_ref, _ = O.attn_harmonic(**ref_args(x), N=N, pos0=900, eps=0.1)
     assert max_abs(f64(od), o_ref) <= 1e-5
-    if N <= 2:
-        oc, _, Sc, zc = S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
-                                                     g["phi"], N, pos0=900, eps=0.1,
-                                                     want_state=True)
-        torch.cuda.synchronize()
-        assert max_abs(f64(od), f64(oc)) <= 1e-4
-        assert rel_fro(f64(Sd), f64(Sc)[0]) <= 1e-5
+    oc, _, Sc, zc = S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
+                                                 g["phi"], N, pos0=900, eps=0.1, want_state=True)
+    torch.cuda.synchronize()
+    assert max_abs(f64(od), f64(oc)) <= 1e-4
+    assert rel_fro(f64(Sd), f64(Sc)[0]) <= 1e-5
 
 
 def test_one_harmonic_is_the_six_channel_path():
@@ -107,7 +131,7 @@ def test_argument_errors():
     x = W.make(W.TINY, B=1, H=1, T=4)
     g = to_dev(x)
     with pytest.raises(S.SanatanError) as e:
-        S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], 3)
+        S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], 4)
     assert e.value.status == 2
     with pytest.raises(S.SanatanError) as e:
         S.sanatan_featurize_harmonic(g["q"], g["gamma"], g["omega"], g["phi"], 4)
