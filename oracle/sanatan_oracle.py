@@ -586,6 +586,78 @@ def decode_step_harmonic(S, z, q, k, v, gamma, omega, phi, pos, N, eps=0.0):
     return S, z, num / (den + eps)[:, None]
 
 
+def _feature_vjp_harmonic(u, gamma, omega, phi, N, pos0, dphi):
+    """Pull a cotangent dPhi_N [B,H,T,F_N] of featurize_harmonic back to du and
+    the parameter gradients.  Per dimension, with the angle block A_m (A_0 = 1,
+    A_{2n-1} = cos n th, A_{2n} = sin n th of the rotated angle th) and the
+    label block r A_m:
+        dA_m  = dPhi[A_m] + r dPhi[r A_m],      dr = sum_m A_m dPhi[r A_m],
+        dth   = sum_n n (-sin(n th) dA_{2n-1} + cos(n th) dA_{2n}),
+    then through the soft root, the rotation and the squash exactly as the
+    six-channel map (which is N = 1)."""
+    parts = _feature_parts(u, gamma, omega, phi, pos0)
+    B, H, T, F = dphi.shape
+    kA = 2 * N + 1
+    d = F // (2 * kA)
+    dp = np.asarray(dphi, dtype=np.float64).reshape(B, H, T, d, 2, kA)
+    th = rotate(squash(parts["u"]), parts["t"], np.asarray(phi, dtype=np.float64).reshape(
+        1, H, 1, d))
+    r = parts["r"]
+    ang = [np.ones_like(th)]
+    for n in range(1, N + 1):
+        ang += [np.cos(n * th), np.sin(n * th)]
+    A = np.stack(ang, axis=-1)
+    dA = dp[..., 0, :] + r[..., None] * dp[..., 1, :]
+    dr = (A * dp[..., 1, :]).sum(axis=-1)
+    dth_rot = np.zeros_like(th)
+    for n in range(1, N + 1):
+        dth_rot += n * (-np.sin(n * th) * dA[..., 2 * n - 1] + np.cos(n * th) * dA[..., 2 * n])
+    dpre = dr * (1.0 - r * r)
+    dtheta = dth_rot + dpre * parts["g"] * parts["gpx"]
+    du = dtheta * np.pi / (1.0 + np.abs(parts["u"])) ** 2
+    dgamma = (dpre * parts["gx"]).sum(axis=(0, 2, 3))
+    domega = (dpre * parts["g"] * parts["gpx"]).sum(axis=(0, 2))
+    dphi_rate = (dth_rot * parts["t"]).sum(axis=(0, 2))
+    return du, dgamma, domega, dphi_rate
+
+
+def attn_harmonic_backward(q, k, v, gamma, omega, phi, dO, N, pos0=0, eps=0.0, S0=None, z0=None):
+    """Gradients of sum(o * dO) for ``attn_harmonic``: the equations of
+    ``attn_backward`` with Phi_N in place of Phi (s_tj = Phi_N(q_t).Phi_N(k_j)),
+    then through the harmonic map.  Returns the dict of ``attn_backward``."""
+    pq = featurize_harmonic(q, gamma, omega, phi, N, pos0)
+    pk = featurize_harmonic(k, gamma, omega, phi, N, pos0)
+    v = _heads(v)
+    dO = _heads(dO)
+    B, H, T, F = pq.shape
+    mask = np.tril(np.ones((T, T)))
+    dpq = np.zeros_like(pq)
+    dpk = np.zeros_like(pk)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            s = (pq[b, h] @ pk[b, h].T) * mask
+            num = s @ v[b, h]
+            den = s.sum(axis=1)
+            if S0 is not None:
+                num = num + pq[b, h] @ _heads(S0)[b, h]
+                den = den + pq[b, h] @ _heads(z0)[b, h]
+            dh = den + eps
+            o = num / dh[:, None]
+            dN = dO[b, h] / dh[:, None]
+            dD = -(dO[b, h] * o).sum(axis=1) / dh
+            ds = (dN @ v[b, h].T + dD[:, None]) * mask
+            dv[b, h] = s.T @ dN
+            dpq[b, h] = ds @ pk[b, h]
+            if S0 is not None:
+                dpq[b, h] += dN @ _heads(S0)[b, h].T + np.outer(dD, _heads(z0)[b, h])
+            dpk[b, h] = ds.T @ pq[b, h]
+    dq, dg_q, dom_q, dph_q = _feature_vjp_harmonic(q, gamma, omega, phi, N, pos0, dpq)
+    dk, dg_k, dom_k, dph_k = _feature_vjp_harmonic(k, gamma, omega, phi, N, pos0, dpk)
+    return dict(dq=dq, dk=dk, dv=dv, dgamma=dg_q + dg_k, domega=dom_q + dom_k,
+                dphi=dph_q + dph_k)
+
+
 def state_bytes_harmonic(layers, heads, d, dv, N, bytes_per_float=4):
     """Recurrent state with harmonics 1..N: per head S (F_N x dv) and z (F_N),
     F_N = 2(2N + 1) d (N = 1: the six-channel 6 d^2 + 6 d of Notes §2.7)."""

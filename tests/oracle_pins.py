@@ -662,9 +662,57 @@ def check_harmonic_state_size():
     assert O.state_bytes_harmonic(12, 12, 64, 64, 2) == 12 * 12 * (640 * 64 + 640) * 4
 
 
+def _harmonic_loss(c, N, dO, pos0, eps, S0, z0):
+    o, _ = O.attn_harmonic(c["q"], c["k"], c["v"], c["gamma"], c["omega"], c["phi"], N,
+                           pos0=pos0, eps=eps, S0=S0, z0=z0)
+    return float((o * dO).sum())
+
+
+def check_harmonic_backward_finite_differences():
+    # every gradient of the harmonic map's attention against central finite
+    # differences of the forward, for N = 2 and 3, with and without a history
+    c = _small_case(35, B=1, H=2, T=6, d=2, dv=2, phi_scale=0.8)
+    g = _rng(36)
+    dO = g.standard_normal(c["v"].shape)
+    for N in (2, 3):
+        S0, z0 = O.final_state_harmonic(g.standard_normal(c["k"].shape),
+                                        g.standard_normal(c["v"].shape), c["gamma"], c["omega"],
+                                        c["phi"], N, pos0=-6)
+        for pos0, eps, st in ((3, 0.0, False), (0, 0.3, True)):
+            S = S0 if st else None
+            Z = z0 if st else None
+            grads = O.attn_harmonic_backward(c["q"], c["k"], c["v"], c["gamma"], c["omega"],
+                                             c["phi"], dO, N, pos0=pos0, eps=eps, S0=S, z0=Z)
+            h = 1e-6
+            for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("gamma", "dgamma"),
+                                ("omega", "domega"), ("phi", "dphi")):
+                x = c[name]
+                num = np.zeros_like(x)
+                for idx in np.ndindex(x.shape):
+                    old = x[idx]
+                    x[idx] = old + h
+                    lp = _harmonic_loss(c, N, dO, pos0, eps, S, Z)
+                    x[idx] = old - h
+                    lm = _harmonic_loss(c, N, dO, pos0, eps, S, Z)
+                    x[idx] = old
+                    num[idx] = (lp - lm) / (2 * h)
+                err = np.abs(num - grads[gname]).max() / max(1e-3, np.abs(num).max())
+                assert err < 1e-6, (N, name, err)
+
+
+def check_harmonic_one_backward_is_six_channel_backward():
+    c = _small_case(37, B=2, H=2, T=8, d=3)
+    dO = _rng(38).standard_normal(c["v"].shape)
+    a = O.attn_harmonic_backward(**c, dO=dO, N=1, pos0=5, eps=0.2)
+    b = O.attn_backward(**c, dO=dO, pos0=5, eps=0.2)
+    for key in ("dq", "dk", "dv", "dgamma", "domega", "dphi"):
+        assert np.allclose(a[key], b[key], rtol=1e-12, atol=1e-12), key
+
+
 ALL_CHECKS += [check_harmonic_one_is_six_channel, check_harmonic_kernel_closed_form,
                check_harmonic_quadratic_equals_recurrent_and_decode, check_harmonic_state_size,
-               check_harmonic_channels_double_angle]
+               check_harmonic_channels_double_angle, check_harmonic_backward_finite_differences,
+               check_harmonic_one_backward_is_six_channel_backward]
 
 
 # --------------------------------------------------------------------------

@@ -15,7 +15,8 @@ _orig = {n: getattr(O, n) for n in ("squash", "soft_root", "rotate", "features_f
                                      "_feature_vjp", "state_bytes", "featurize", "attn_power",
                                      "attn_power_backward", "attn_ablation",
                                      "features4_from_angles", "ablation_scale",
-                                     "features_harmonic_from_angles", "stack_decode_step")}
+                                     "features_harmonic_from_angles", "stack_decode_step",
+                                     "_feature_vjp_harmonic", "attn_harmonic_backward")}
 
 
 def m_squash_no_abs(u):
@@ -248,6 +249,42 @@ def m_harmonic_no_label_block(theta_rot, r, N):
     return blk.reshape(blk.shape[:-2] + (blk.shape[-2] * blk.shape[-1],))
 
 
+def _harmonic_vjp_mutant(kind):
+    # the harmonic chain rule with one plausible slip, made by handing the
+    # correct chain rule a transformed cotangent:
+    #   no_multiple:    d(cos n th)/dth taken as -sin n th (the factor n dropped),
+    #   no_label_scale: the label block r A_m passed to dA_m without its r
+    def vjp(u, gamma, omega, phi, N, pos0, dphi):
+        dphi = np.asarray(dphi, dtype=np.float64)
+        B, H, T, F = dphi.shape
+        kA = 2 * N + 1
+        dp = dphi.reshape(B, H, T, F // (2 * kA), 2, kA).copy()
+        if kind == "no_multiple":
+            for n in range(2, N + 1):
+                dp[..., :, 2 * n - 1] /= n
+                dp[..., :, 2 * n] /= n
+        else:
+            r = O._feature_parts(u, gamma, omega, phi, pos0)["r"]
+            dp[..., 0, :] += (1.0 - r[..., None]) * dp[..., 1, :]
+        return _orig["_feature_vjp_harmonic"](u, gamma, omega, phi, N, pos0,
+                                              dp.reshape(dphi.shape))
+    return vjp
+
+
+def m_harmonic_backward_dv_unmasked(q, k, v, gamma, omega, phi, dO, N, pos0=0, eps=0.0, S0=None,
+                                    z0=None):
+    # dv summed over every query instead of the causal ones t >= j
+    g = dict(_orig["attn_harmonic_backward"](q, k, v, gamma, omega, phi, dO, N, pos0, eps, S0,
+                                             z0))
+    pq = O.featurize_harmonic(q, gamma, omega, phi, N, pos0)
+    pk = O.featurize_harmonic(k, gamma, omega, phi, N, pos0)
+    o, D = O.attn_harmonic(q, k, v, gamma, omega, phi, N, pos0=pos0, eps=eps, S0=S0, z0=z0)
+    dN = np.asarray(dO, dtype=np.float64) / (D + eps)[..., None]
+    s = np.matmul(pq, np.swapaxes(pk, -1, -2))
+    g["dv"] = np.matmul(np.swapaxes(s, -1, -2), dN)
+    return g
+
+
 def m_stack_no_residual(x, Wqkv, Wo, S, z, gamma, omega, phi, heads, pos, eps=0.0):
     # the residual dropped: x <- a Wo
     x = np.asarray(x, dtype=np.float64)
@@ -298,6 +335,10 @@ MUTANTS = {
     "harmonic_phase_slip": ("features_harmonic_from_angles", m_harmonic_unrotated_multiple),
     "harmonic_without_root_label": ("features_harmonic_from_angles", m_harmonic_no_label_block),
     "stack_without_residual": ("stack_decode_step", m_stack_no_residual),
+    "harmonic_vjp_without_multiple": ("_feature_vjp_harmonic", _harmonic_vjp_mutant("no_multiple")),
+    "harmonic_vjp_label_unscaled": ("_feature_vjp_harmonic",
+                                    _harmonic_vjp_mutant("no_label_scale")),
+    "harmonic_backward_dv_unmasked": ("attn_harmonic_backward", m_harmonic_backward_dv_unmasked),
 }
 
 
