@@ -483,6 +483,18 @@ def harmonic_case(dev, flush, steps, warmup, stream):
     def fwd3(_i):
         S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], 3)
 
+    dO = torch.randn(B, H, T, 64, generator=W.generator(W.LAYER.seed + 5, dev),
+                     device=dev).to(torch.bfloat16)
+    ws_b = torch.empty(max(int(S.lib().sanatan_chunk_bwd_harmonic_workspace_size(B, H, T, 64, 64,
+                                                                                 N)), 16),
+                       dtype=torch.uint8, device=dev)
+
+    def train(_i):
+        o, D, _, _ = S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
+                                                  g["phi"], N)
+        S.sanatan_chunk_bwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], N,
+                                     o, D, dO, want_dphi=True, workspace=ws_b)
+
     G = 144
     gen = W.generator(W.DECODE.seed + 11, dev)
     gd, od, pd = W.params(G, 64, "geometric", gen, device=dev)
@@ -498,11 +510,12 @@ def harmonic_case(dev, flush, steps, warmup, stream):
         flush.zero_()
         fwd(0)
         fwd3(0)
+        train(0)
         dec(0)
     torch.cuda.synchronize()
     S.device_status()
-    return dict(fwd=fwd, fwd3=fwd3, dec=dec, B=B, H=H, T=T, F=F, F3=S.harmonic_features(3),
-                slots=G)
+    return dict(fwd=fwd, fwd3=fwd3, train=train, dec=dec, B=B, H=H, T=T, F=F,
+                F3=S.harmonic_features(3), slots=G)
 
 
 STACK_LAYERS, STACK_HEADS = 12, 12   # the 184M model's attention stack (12 layers x 12 heads)
@@ -715,10 +728,11 @@ def main():
         if abl:
             for ch, c in abl["cases"].items():
                 abl_t[ch] = timed_steps(c["step"], pw_steps, flush, stream, profile=True)
-        hf_whole = hf3_whole = hd_whole = [nan]
+        hf_whole = hf3_whole = ht_whole = hd_whole = [nan]
         if harm:
             hf_whole, _ = timed_steps(harm["fwd"], hs_steps, flush, stream)
             hf3_whole, _ = timed_steps(harm["fwd3"], hs_steps, flush, stream)
+            ht_whole, _ = timed_steps(harm["train"], hs_steps, flush, stream)
             hd_whole, _ = timed_steps(harm["dec"], steps, flush, stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
@@ -893,6 +907,10 @@ def main():
             "harmonics": HARMONICS, "features": F,
             "forward": harm_fwd(hf_whole, F),
             "forward_N3": harm_fwd(hf3_whole, harm["F3"]),
+            "train": {"workload": W.LAYER.name, "steps": hs_steps,
+                      "ms_per_step": statistics.mean(ht_whole),
+                      "tokens_per_s": harm["B"] * harm["T"] / (statistics.mean(ht_whole) * 1e-3),
+                      "note": "forward + backward (dq, dk, dv, dgamma, domega, dphi) per step"},
             "decode": {"slots": harm["slots"], "steps": steps, "us_per_step": 1e3 * hd_ms,
                        "achieved_gbs": dec_bytes / (hd_ms * 1e-3) / 1e9,
                        "hbm_frac": dec_bytes / (hd_ms * 1e-3) / 1e9 / pk["hbm"],

@@ -439,6 +439,56 @@ int sanatan_chunk_fwd_harmonic(const void* q, const void* k, const void* v, int 
   return from_cuda(chunk_fwd_harmonic_launch(a, harmonics, static_cast<cudaStream_t>(stream)));
 }
 
+size_t sanatan_chunk_bwd_harmonic_workspace_size(int B, int H, int T, int d, int dv,
+                                                 int harmonics) {
+  if (B < 0 || H < 0 || T < 0 || d != 64 || dv != 64 || harmonics < 1 || harmonics > 3) return 0;
+  return chunk_bwd_harmonic_workspace_bytes(B, H, T, harmonics);
+}
+
+int sanatan_chunk_bwd_harmonic(const void* q, const void* k, const void* v, int in_dtype,
+                               const float* gamma, const float* omega, const float* phi, int B,
+                               int H, int T, int d, int dv, int64_t pos0, int harmonics,
+                               float eps, const float* S0, const float* z0, const float* o,
+                               const float* D, const void* dO, int grad_dtype, void* dq, void* dk,
+                               void* dv_out, float* dgamma, float* domega, float* dphi,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (!ok_dtype(in_dtype) || !ok_dtype(grad_dtype) || harmonics < 1) return SANATAN_ERR_INVALID;
+  if (int s = check_sizes(B, H, T, d, dv)) return s;
+  if (harmonics > 3) return SANATAN_ERR_UNSUPPORTED;
+  if ((S0 == nullptr) != (z0 == nullptr)) return SANATAN_ERR_INVALID;
+  if (!ok_nullable(S0) || !ok_nullable(z0) || !ok_nullable(dphi) || !ok_nullable(workspace))
+    return SANATAN_ERR_INVALID;
+  if (H > 0 && (!ok_ptr(dgamma) || !ok_ptr(domega))) return SANATAN_ERR_INVALID;
+  if (static_cast<int64_t>(B) * H * T > 0 &&
+      (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(o) || !ok_ptr(D) || !ok_ptr(dO) ||
+       !ok_ptr(dq) || !ok_ptr(dk) || !ok_ptr(dv_out)))
+    return SANATAN_ERR_INVALID;
+  if (H > 0) {
+    if (int s = check_params(gamma, omega, phi)) return s;
+  }
+  const size_t need = sanatan_chunk_bwd_harmonic_workspace_size(B, H, T, d, dv, harmonics);
+  if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return SANATAN_ERR_INVALID;
+  if (H == 0) return SANATAN_OK;
+  if (int s = check_arch()) return s;
+  ChunkBwdArgs a{};
+  a.f = ChunkFwdArgs{q, k, v, in_dtype, gamma, omega, phi, B, H, T, d, dv, pos0, eps,
+                     S0, z0, nullptr, nullptr, nullptr, nullptr, nullptr, 0};
+  a.o = o;
+  a.Dn = D;
+  a.dO = dO;
+  a.grad_dtype = grad_dtype;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv_out;
+  a.dgamma = dgamma;
+  a.domega = domega;
+  a.dphi = dphi;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  return from_cuda(
+      chunk_bwd_harmonic_launch(a, harmonics, static_cast<cudaStream_t>(stream)));
+}
+
 int sanatan_decode_step_harmonic(float* S, float* z, const float* q, const float* k,
                                  const float* v, const float* gamma, const float* omega,
                                  const float* phi, const int64_t* pos, int N, int G, int d, int dv,

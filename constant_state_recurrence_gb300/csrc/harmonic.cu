@@ -8,10 +8,12 @@
 // a * 2(2N + 1) + l (2N + 1) + m (N = 1 is the six-channel map of eq. (6)).
 // The kernel per dimension is (1 + r_q r_k)(1 + sum_n cos(n dtheta)).
 //
-// Three kernels, all float32 on the CUDA cores: the elementwise feature map,
-// the chunked causal forward (one CTA per sequence, the state in shared
-// memory, chunks of 8 tokens; N = 1 is the six-channel f32 path), and the decode step
-// (a cluster of 4 CTAs per slot splitting the state rows).
+// Kernels, all float32 on the CUDA cores: the elementwise feature map; the
+// chunked causal forward (a cluster of 8 CTAs per sequence, each holding the
+// state rows of 8 dimensions in registers; N = 1 is the six-channel f32 path);
+// its backward (a preparation kernel, the forward recurrence in reverse time for
+// dv, and the feature-space passes for dq and dk with the chain rule); and the
+// decode step (a cluster of 4 CTAs per slot splitting the state rows).
 #include <cooperative_groups.h>
 
 #include "sanatan_internal.h"
@@ -116,12 +118,16 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int N, typename Tin>
+// kGrad: the value gradient of the backward, dv_j = sum_{t>=j} s_tj dN_t, as
+// this same recurrence in reverse time (token u processed at step T-1-u, at its
+// own position) with queries k, keys q, values dN and no normalisation; the
+// output is written in Tout and D, S_out, z_out are not produced.
+template <int N, typename Tin, typename Tv, typename Tout, bool kGrad>
 __global__ void __launch_bounds__(kThreads, 3) chunk_fwd_harmonic_kernel(
-    const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+    const Tin* __restrict__ q, const Tin* __restrict__ k, const Tv* __restrict__ v,
     const float* __restrict__ gamma, const float* __restrict__ omega,
     const float* __restrict__ phi, int H, int T, int64_t pos0, float eps,
-    const float* __restrict__ S0, const float* __restrict__ z0, float* __restrict__ o,
+    const float* __restrict__ S0, const float* __restrict__ z0, Tout* __restrict__ o,
     float* __restrict__ Dout, float* __restrict__ S_out, float* __restrict__ z_out) {
   constexpr int kCh = Harm<N>::kCh, kF = Harm<N>::kF;
   constexpr int kR = ClusterSmem<N>::kR;
@@ -155,14 +161,16 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_fwd_harmonic_kernel(
   if (tid < kR) sm.z[tid] = z0 ? z0[row0 + tid] : 0.f;
 
   // inputs of the next chunk, held in registers while the current one runs
+  // step i of the recurrence reads token row(i)
+  auto row = [&](int i) -> int { return kGrad ? T - 1 - i : i; };
   float uf = 0.f, vr[4] = {0.f, 0.f, 0.f, 0.f};
   auto prefetch = [&](int c0n) {
     const int nn = min(kCT, T - c0n);
-    uf = ft < nn ? load_as_float(fsrc + (seq + c0n + ft) * kD + fa) : 0.f;
+    uf = ft < nn ? load_as_float(fsrc + (seq + row(c0n + ft)) * kD + fa) : 0.f;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int t = rg + 4 * m;
-      vr[m] = t < nn ? load_as_float(v + (seq + c0n + t) * kDv + c) : 0.f;
+      vr[m] = t < nn ? load_as_float(v + (seq + row(c0n + t)) * kDv + c) : 0.f;
     }
   };
   if (T > 0) prefetch(0);
@@ -175,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_fwd_harmonic_kernel(
       float* dst = (fw ? &sm.pk[ft][0] : &sm.pq[ft][0]) + kCh * (tid & 7);
       if (ft < nc) {
         float ch[kCh];
-        harmonic_channels<N>(uf, g, om, phase_mod_2pi(pos0 + c0 + ft, ph), ch);
+        harmonic_channels<N>(uf, g, om, phase_mod_2pi(pos0 + row(c0 + ft), ph), ch);
 #pragma unroll
         for (int cc = 0; cc < kCh; ++cc) dst[cc] = ch[cc];
       } else {
@@ -281,14 +289,18 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_fwd_harmonic_kernel(
           nm += rem[e];
           dn += rem[kDv];
         }
-        const int64_t orow = seq + c0 + t;
-        o[orow * kDv + e] = nm / (dn + eps);
-        if (e == 0 && Dout) Dout[orow] = dn;
+        const int64_t orow = seq + row(c0 + t);
+        if constexpr (kGrad) {
+          o[orow * kDv + e] = store_from_float<Tout>(nm);
+        } else {
+          o[orow * kDv + e] = nm / (dn + eps);
+          if (e == 0 && Dout) Dout[orow] = dn;
+        }
       }
     }
   }
   __syncthreads();
-  if (S_out) {
+  if (!kGrad && S_out) {
 #pragma unroll
     for (int i = 0; i < kPT / 2; ++i) {
       float a0, a1;
@@ -300,6 +312,357 @@ __global__ void __launch_bounds__(kThreads, 3) chunk_fwd_harmonic_kernel(
   }
   cluster_arrive();    // no CTA leaves while another still reads its shared memory
   cluster_wait();
+}
+
+// ---------------------------------------------------------------------------
+// Backward of the chunked forward (N >= 2).  With Dh_t = D_t + eps,
+// dN_t = dO_t / Dh_t and dD_t = -(dO_t . o_t) / Dh_t:
+//   dv_j       = sum_{t>=j} s_tj dN_t                       (the kGrad forward),
+//   dPhi(q_t)  = [S_t | z_t] [dN_t | dD_t]   (S_t, z_t inclusive of t, from S0, z0),
+//   dPhi(k_j)  = [G_j | g_j] [v_j | 1],      G_j = sum_{t>=j} Phi(q_t) dN_t^T,
+//                                             g_j = sum_{t>=j} Phi(q_t) dD_t,
+// then the chain rule through the harmonic map per (token, dimension).  The
+// two feature gradients are attentions in feature space: a 65-wide query
+// ([dN|dD] or [v|1]) reads a state of F rows x 65 columns, so every feature
+// row's gradient is a reduction over the 65 columns only and a CTA that owns
+// the rows of 8 dimensions finishes their chain rule on its own (no cluster).
+
+constexpr int kPrepRows = 8;   // tokens (warps) per block of the preparation kernel
+
+// dN [rows, 64] and dD [rows] from dO, o, D: one warp per token.
+template <typename Tg>
+__global__ void __launch_bounds__(256) harm_bwd_prep_kernel(const float* __restrict__ o,
+                                                            const float* __restrict__ D,
+                                                            const Tg* __restrict__ dO, float eps,
+                                                            int64_t rows, float* __restrict__ dN,
+                                                            float* __restrict__ dD) {
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * kPrepRows + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const float inv = 1.0f / (D[r] + eps);
+  const float g0 = load_as_float(dO + r * kDv + lane), g1 = load_as_float(dO + r * kDv + lane + 32);
+  float dot = g0 * o[r * kDv + lane] + g1 * o[r * kDv + lane + 32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+  dN[r * kDv + lane] = g0 * inv;
+  dN[r * kDv + lane + 32] = g1 * inv;
+  if (lane == 0) dD[r] = -dot * inv;
+}
+
+// Gradient of one dimension's channels back to u and the per-head parameters.
+struct HarmGrad {
+  float du, dgamma, domega, dphi;
+};
+
+template <int N>
+__device__ __forceinline__ HarmGrad harmonic_vjp(float u, float g, float om, float phase,
+                                                 float tpos, const float* dch) {
+  constexpr int kA = Harm<N>::kAng;
+  const float th = squash_exact(u);
+  float sx, cx;
+  sincosf(th + om, &sx, &cx);
+  const float gx = cx - sx;
+  const float gpx = -sx - cx;
+  const float r = tanhf(g * gx);
+  float s1, c1;
+  sincosf(th + phase, &s1, &c1);
+  // A_0 = 1 contributes only to dr
+  float dr = dch[kA];
+  float dth = 0.f;
+  float cn = c1, sn = s1;
+#pragma unroll
+  for (int n = 1; n <= N; ++n) {
+    if (n > 1) {
+      const float cm = fmaf(cn, c1, -sn * s1);
+      const float sm = fmaf(sn, c1, cn * s1);
+      cn = cm;
+      sn = sm;
+    }
+    const float dAc = fmaf(r, dch[kA + 2 * n - 1], dch[2 * n - 1]);
+    const float dAs = fmaf(r, dch[kA + 2 * n], dch[2 * n]);
+    dr = fmaf(cn, dch[kA + 2 * n - 1], fmaf(sn, dch[kA + 2 * n], dr));
+    dth = fmaf(static_cast<float>(n), fmaf(cn, dAs, -sn * dAc), dth);
+  }
+  const float dpre = dr * (1.0f - r * r);
+  const float den = 1.0f + fabsf(u);
+  HarmGrad e;
+  e.du = fmaf(dpre * g, gpx, dth) * kPi / (den * den);
+  e.dgamma = dpre * gx;
+  e.domega = dpre * g * gpx;
+  e.dphi = dth * tpos;
+  return e;
+}
+
+constexpr int kFsaCT = 16;     // tokens per chunk
+constexpr int kQP = 68;        // row pitch of the 65-wide query / key rows (16-byte rows)
+
+template <int N>
+struct FsaSmem {
+  static constexpr int kR = 8 * Harm<N>::kCh;
+  alignas(16) float qa[kFsaCT][kQP];        // query rows: [dN|dD] (dq pass) or [v|1] (dk pass)
+  alignas(16) float kb[kFsaCT][kQP];        // key rows:   [v|1] or [dN|dD]
+  float pv[kFsaCT][kR + 1];                 // value features Phi(k) or Phi(q) of the CTA's rows
+  // state readout per column quarter; quarter 0 then holds the chunk's feature
+  // gradient (each (t, f) is summed and rewritten by one thread)
+  float part[4][kFsaCT][kR];
+  float ds[kFsaCT][kFsaCT + 1];             // pair scores query . key (causal)
+  float red[4][8][3];                       // parameter-gradient partials per warp
+};
+
+// One CTA per (sequence, 8 dimensions, pass): blockIdx.y = 0 gives dq (forward
+// time, state from S0, z0), 1 gives dk (reverse time, state from zero).  Thread
+// (cq, f) = (tid / kR, tid % kR) holds columns 16 cq .. 16 cq + 15 of state row f
+// (and column 64, the ones / dD column, for cq = 3) as packed pairs, so the
+// lanes of a warp share one column quarter and read the 65-wide rows as
+// broadcasts; the four quarters' partial readouts meet in shared memory.
+template <int N, typename Tin, bool kKeys>
+__device__ __forceinline__ void fsa_pass(
+    const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+    const float* __restrict__ dN, const float* __restrict__ dD, const float* __restrict__ gamma,
+    const float* __restrict__ omega, const float* __restrict__ phi, int H, int T, int64_t pos0,
+    const float* __restrict__ S0, const float* __restrict__ z0, Tin* __restrict__ dout,
+    float* __restrict__ dgamma, float* __restrict__ domega, float* __restrict__ dphi,
+    FsaSmem<N>& sm) {
+  constexpr int kCh = Harm<N>::kCh, kF = Harm<N>::kF;
+  constexpr int kR = FsaSmem<N>::kR;
+  const int grp = blockIdx.x & 7;              // dimensions 8 grp .. 8 grp + 7
+  const int bh = blockIdx.x >> 3;
+  const int h = bh % H;
+  const int tid = threadIdx.x;
+  const int f = tid % kR, cq = tid / kR;
+  const int64_t seq = static_cast<int64_t>(bh) * T;
+  const int64_t frow = static_cast<int64_t>(bh) * kF + grp * kR + f;   // global state row
+  const float g = gamma[h];
+  auto row = [&](int i) -> int { return kKeys ? T - 1 - i : i; };
+
+  uint64_t W[8];
+  float w64 = 0.f;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    float a0 = 0.f, a1 = 0.f;
+    if (!kKeys && S0) {
+      a0 = S0[frow * kDv + 16 * cq + 2 * m];
+      a1 = S0[frow * kDv + 16 * cq + 2 * m + 1];
+    }
+    W[m] = pk2(a0, a1);
+  }
+  if (!kKeys && z0 && cq == 3) w64 = z0[frow];
+
+  // chain-rule thread map (tid < 128): token ct, dimension ca of the group
+  const int ct = tid >> 3, ca = grp * 8 + (tid & 7);
+  const float om = omega[h * kD + ca], ph = phi[h * kD + ca];
+  float acc_g = 0.f, acc_o = 0.f, acc_p = 0.f;
+  const Tin* vsrc = kKeys ? q : k;     // tensor whose features are the values
+  const Tin* usrc = kKeys ? k : q;     // tensor whose gradient this pass writes
+
+  for (int c0 = 0; c0 < T; c0 += kFsaCT) {
+    const int nc = min(kFsaCT, T - c0);
+    __syncthreads();   // the previous chunk is done with every buffer
+    for (int e = tid; e < kFsaCT * kQP; e += blockDim.x) {
+      const int t = e / kQP, col = e % kQP;
+      float gq = 0.f, vv = 0.f;
+      if (t < nc && col <= kDv) {
+        const int64_t r = seq + row(c0 + t);
+        gq = col < kDv ? dN[r * kDv + col] : dD[r];
+        vv = col < kDv ? load_as_float(v + r * kDv + col) : 1.0f;
+      }
+      sm.qa[t][col] = kKeys ? vv : gq;
+      sm.kb[t][col] = kKeys ? gq : vv;
+    }
+    if (tid < 128) {
+      float* dst = &sm.pv[ct][kCh * (tid & 7)];
+      if (ct < nc) {
+        const int r = row(c0 + ct);
+        float ch[kCh];
+        harmonic_channels<N>(load_as_float(vsrc + (seq + r) * kD + ca), g, om,
+                             phase_mod_2pi(pos0 + r, ph), ch);
+#pragma unroll
+        for (int cc = 0; cc < kCh; ++cc) dst[cc] = ch[cc];
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < kCh; ++cc) dst[cc] = 0.f;
+      }
+    }
+    __syncthreads();
+    if (tid < kFsaCT * kFsaCT) {
+      const int t = tid >> 4, j = tid & (kFsaCT - 1);
+      if (j <= t) {
+        const ulonglong2* a = reinterpret_cast<const ulonglong2*>(&sm.qa[t][0]);
+        const ulonglong2* b = reinterpret_cast<const ulonglong2*>(&sm.kb[j][0]);
+        uint64_t s0 = 0, s1 = 0;
+#pragma unroll
+        for (int i = 0; i < kQP / 4; ++i) {
+          const ulonglong2 x = a[i], y = b[i];
+          s0 = ffma2(x.x, y.x, s0);
+          s1 = ffma2(x.y, y.y, s1);
+        }
+        float p0, p1, p2, p3;
+        upk2(s0, p0, p1);
+        upk2(s1, p2, p3);
+        sm.ds[t][j] = (p0 + p1) + (p2 + p3);
+      }
+    }
+    // state readout of the chunk per column quarter (before this chunk's keys)
+#pragma unroll 2
+    for (int t = 0; t < kFsaCT; ++t) {
+      const ulonglong2* a = reinterpret_cast<const ulonglong2*>(&sm.qa[t][16 * cq]);
+      uint64_t acc2 = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const ulonglong2 x = a[i];
+        acc2 = ffma2(x.x, W[2 * i], acc2);
+        acc2 = ffma2(x.y, W[2 * i + 1], acc2);
+      }
+      float x0, x1;
+      upk2(acc2, x0, x1);
+      float acc = x0 + x1;
+      if (cq == 3) acc = fmaf(sm.qa[t][kDv], w64, acc);
+      sm.part[cq][t][f] = acc;
+    }
+    __syncthreads();
+    // feature gradients: the four quarters plus the intra-chunk pairs, tokens
+    // cq, cq + 4, cq + 8, cq + 12 of row f
+#pragma unroll
+    for (int m = 0; m < kFsaCT / 4; ++m) {
+      const int t = cq + 4 * m;
+      float acc = (sm.part[0][t][f] + sm.part[1][t][f]) + (sm.part[2][t][f] + sm.part[3][t][f]);
+      for (int j = 0; j <= t; ++j) acc = fmaf(sm.ds[t][j], sm.pv[j][f], acc);
+      sm.part[0][t][f] = acc;
+    }
+    __syncthreads();
+    // state update W += pv^T kb (pv and kb are zero past the end)
+#pragma unroll 4
+    for (int j = 0; j < kFsaCT; ++j) {
+      const float w = sm.pv[j][f];
+      const uint64_t w2 = pk2(w, w);
+      const ulonglong2* b = reinterpret_cast<const ulonglong2*>(&sm.kb[j][16 * cq]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const ulonglong2 x = b[i];
+        W[2 * i] = ffma2(x.x, w2, W[2 * i]);
+        W[2 * i + 1] = ffma2(x.y, w2, W[2 * i + 1]);
+      }
+      if (cq == 3) w64 = fmaf(w, sm.kb[j][kDv], w64);
+    }
+    // chain rule of the chunk's tokens for the group's dimensions
+    if (tid < 128 && ct < nc) {
+      const int r = row(c0 + ct);
+      const int64_t pos = pos0 + r;
+      const HarmGrad e = harmonic_vjp<N>(load_as_float(usrc + (seq + r) * kD + ca), g, om,
+                                         phase_mod_2pi(pos, ph), static_cast<float>(pos),
+                                         &sm.part[0][ct][kCh * (tid & 7)]);
+      dout[(seq + r) * kD + ca] = store_from_float<Tin>(e.du);
+      acc_g += e.dgamma;
+      acc_o += e.domega;
+      acc_p += e.dphi;
+    }
+  }
+  // parameter gradients: sum over the 16 tokens of each dimension, then atomics
+  if (tid < 128) {
+#pragma unroll
+    for (int off = 8; off < 32; off <<= 1) {
+      acc_g += __shfl_xor_sync(0xffffffffu, acc_g, off);
+      acc_o += __shfl_xor_sync(0xffffffffu, acc_o, off);
+      acc_p += __shfl_xor_sync(0xffffffffu, acc_p, off);
+    }
+    if ((tid & 31) < 8) {
+      sm.red[tid >> 5][tid & 7][0] = acc_g;
+      sm.red[tid >> 5][tid & 7][1] = acc_o;
+      sm.red[tid >> 5][tid & 7][2] = acc_p;
+    }
+  }
+  __syncthreads();
+  if (tid < 8) {
+    float sg = 0.f, so = 0.f, sp = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      sg += sm.red[w][tid][0];
+      so += sm.red[w][tid][1];
+      sp += sm.red[w][tid][2];
+    }
+    atomicAdd(&domega[h * kD + grp * 8 + tid], so);
+    if (dphi) atomicAdd(&dphi[h * kD + grp * 8 + tid], sp);
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) sg += __shfl_xor_sync(0xffu, sg, off);
+    if (tid == 0) atomicAdd(&dgamma[h], sg);
+  }
+}
+
+// resident CTAs per SM the register budget is set for (320 threads at N = 2,
+// 448 at N = 3)
+template <int N>
+constexpr int fsa_min_blocks() { return N == 2 ? 3 : 2; }
+
+template <int N, typename Tin>
+__global__ void __launch_bounds__(4 * 8 * Harm<N>::kCh, fsa_min_blocks<N>()) fsa_harmonic_kernel(
+    const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+    const float* __restrict__ dN, const float* __restrict__ dD, const float* __restrict__ gamma,
+    const float* __restrict__ omega, const float* __restrict__ phi, int H, int T, int64_t pos0,
+    const float* __restrict__ S0, const float* __restrict__ z0, Tin* __restrict__ dq,
+    Tin* __restrict__ dk, float* __restrict__ dgamma, float* __restrict__ domega,
+    float* __restrict__ dphi) {
+  __shared__ FsaSmem<N> sm;
+  if (blockIdx.y == 0)
+    fsa_pass<N, Tin, false>(q, k, v, dN, dD, gamma, omega, phi, H, T, pos0, S0, z0, dq, dgamma,
+                            domega, dphi, sm);
+  else
+    fsa_pass<N, Tin, true>(q, k, v, dN, dD, gamma, omega, phi, H, T, pos0, S0, z0, dk, dgamma,
+                           domega, dphi, sm);
+}
+
+template <int N, typename Tin, typename Tg>
+cudaError_t bwd_h(const ChunkBwdArgs& a, cudaStream_t st) {
+  const ChunkFwdArgs& f = a.f;
+  const int64_t rows = static_cast<int64_t>(f.B) * f.H * f.T;
+  float* dN = static_cast<float*>(a.workspace);
+  float* dD = dN + rows * kDv;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(a.dgamma, 0, sizeof(float) * f.H, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(a.domega, 0, sizeof(float) * f.H * kD, st)) != cudaSuccess) return e;
+  if (a.dphi && (e = cudaMemsetAsync(a.dphi, 0, sizeof(float) * f.H * kD, st)) != cudaSuccess)
+    return e;
+  if (rows == 0) return cudaSuccess;
+  harm_bwd_prep_kernel<Tg>
+      <<<static_cast<unsigned>((rows + kPrepRows - 1) / kPrepRows), 32 * kPrepRows, 0, st>>>(
+      a.o, a.Dn, static_cast<const Tg*>(a.dO), f.eps, rows, dN, dD);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // dv: the forward recurrence in reverse time with queries k, keys q, values dN
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(f.B * f.H) * kRanks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kRanks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, chunk_fwd_harmonic_kernel<N, Tin, float, Tin, true>,
+                         static_cast<const Tin*>(f.k), static_cast<const Tin*>(f.q),
+                         static_cast<const float*>(dN), f.gamma, f.omega, f.phi, f.H, f.T,
+                         f.pos0, 0.0f, static_cast<const float*>(nullptr),
+                         static_cast<const float*>(nullptr), static_cast<Tin*>(a.dv),
+                         static_cast<float*>(nullptr), static_cast<float*>(nullptr),
+                         static_cast<float*>(nullptr));
+  if (e != cudaSuccess) return e;
+  // dq and dk: the two feature-space passes in one launch
+  const dim3 grid(static_cast<unsigned>(f.B * f.H) * 8, 2);
+  fsa_harmonic_kernel<N, Tin><<<grid, 4 * 8 * Harm<N>::kCh, 0, st>>>(
+      static_cast<const Tin*>(f.q), static_cast<const Tin*>(f.k), static_cast<const Tin*>(f.v), dN,
+      dD, f.gamma, f.omega, f.phi, f.H, f.T, f.pos0, f.S0, f.z0, static_cast<Tin*>(a.dq),
+      static_cast<Tin*>(a.dk), a.dgamma, a.domega, a.dphi);
+  return cudaGetLastError();
+}
+
+template <int N>
+cudaError_t bwd_n(const ChunkBwdArgs& a, cudaStream_t st) {
+  const bool in_f32 = a.f.in_dtype == SANATAN_F32;
+  const bool g_f32 = a.grad_dtype == SANATAN_F32;
+  if (in_f32 && g_f32) return bwd_h<N, float, float>(a, st);
+  if (in_f32) return bwd_h<N, float, __nv_bfloat16>(a, st);
+  if (g_f32) return bwd_h<N, __nv_bfloat16, float>(a, st);
+  return bwd_h<N, __nv_bfloat16, __nv_bfloat16>(a, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -456,7 +819,7 @@ cudaError_t chunk_h(const ChunkFwdArgs& a, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, chunk_fwd_harmonic_kernel<N, Tin>,
+  return cudaLaunchKernelEx(&cfg, chunk_fwd_harmonic_kernel<N, Tin, Tin, float, false>,
                             static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k),
                             static_cast<const Tin*>(a.v), a.gamma, a.omega, a.phi, a.H, a.T,
                             a.pos0, a.eps, a.S0, a.z0, a.o, a.D, a.S_out, a.z_out);
@@ -501,6 +864,18 @@ cudaError_t chunk_fwd_harmonic_launch(const ChunkFwdArgs& a, int harmonics, cuda
   if (harmonics == 1) return chunk_fwd_simt_launch(a, st);  // the six-channel map itself
   if (harmonics == 2) return f32 ? chunk_h<2, float>(a, st) : chunk_h<2, __nv_bfloat16>(a, st);
   if (harmonics == 3) return f32 ? chunk_h<3, float>(a, st) : chunk_h<3, __nv_bfloat16>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+size_t chunk_bwd_harmonic_workspace_bytes(int B, int H, int T, int harmonics) {
+  if (harmonics < 2) return 0;
+  return static_cast<size_t>(B) * H * T * (kDv + 1) * sizeof(float);
+}
+
+cudaError_t chunk_bwd_harmonic_launch(const ChunkBwdArgs& a, int harmonics, cudaStream_t st) {
+  if (harmonics == 1) return chunk_bwd_simt_launch(a, st);
+  if (harmonics == 2) return bwd_n<2>(a, st);
+  if (harmonics == 3) return bwd_n<3>(a, st);
   return cudaErrorInvalidValue;
 }
 

@@ -82,8 +82,11 @@ struct HarmonicFeatArgs {
   int out_dtype;
 };
 cudaError_t featurize_harmonic_launch(const HarmonicFeatArgs& a, cudaStream_t st);
-// f32 chunked forward with the harmonic map (N <= 2; bf16 or f32 loads).
+// f32 chunked forward with the harmonic map (N <= 3; bf16 or f32 loads).
 cudaError_t chunk_fwd_harmonic_launch(const ChunkFwdArgs& a, int harmonics, cudaStream_t st);
+// Its backward (N <= 3); the workspace holds dN and dD (none for N = 1).
+size_t chunk_bwd_harmonic_workspace_bytes(int B, int H, int T, int harmonics);
+cudaError_t chunk_bwd_harmonic_launch(const ChunkBwdArgs& a, int harmonics, cudaStream_t st);
 cudaError_t decode_harmonic_launch(float* S, float* z, const float* q, const float* k,
                                    const float* v, const float* gamma, const float* omega,
                                    const float* phi, const int64_t* pos, int N, int G, float eps,

@@ -70,6 +70,11 @@ _SIGS = {
     "sanatan_chunk_fwd_harmonic": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_int,
                                             _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_f,
                                             _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]),
+    "sanatan_chunk_bwd_harmonic_workspace_size": (_c_sz, [_c_int] * 6),
+    "sanatan_chunk_bwd_harmonic": (_c_int, [_c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p, _c_int,
+                                            _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_f,
+                                            _c_p, _c_p, _c_p, _c_p, _c_p, _c_int, _c_p, _c_p, _c_p,
+                                            _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p]),
     "sanatan_decode_step_harmonic": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                                               _c_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f,
                                               _c_p, _c_p]),
@@ -665,6 +670,41 @@ def sanatan_chunk_fwd_harmonic(q, k, v, gamma, omega, phi, harmonics, pos0=0, ep
                                             int(harmonics), float(eps), _ptr(S0), _ptr(z0),
                                             _ptr(o), _ptr(D), _ptr(Sx), _ptr(zx), _stream(dev)))
     return o, D, Sx, zx
+
+
+def sanatan_chunk_bwd_harmonic(q, k, v, gamma, omega, phi, harmonics, o, D, dO, pos0=0, eps=0.0,
+                               S0=None, z0=None, want_dphi=False, workspace=None):
+    """Gradients of sum(o * dO) for sanatan_chunk_fwd_harmonic: dict(dq, dk, dv,
+    dgamma, domega, dphi)."""
+    _need(q, "q", (torch.float32, torch.bfloat16))
+    B, H, T, d = q.shape
+    dv = v.shape[-1]
+    _need(k, "k", (q.dtype,), (B, H, T, d))
+    _need(v, "v", (q.dtype,), (B, H, T, dv))
+    _need(o, "o", (torch.float32,), (B, H, T, dv))
+    _need(D, "D", (torch.float32,), (B, H, T))
+    _need(dO, "dO", (torch.float32, torch.bfloat16), (B, H, T, dv))
+    _need_params(gamma, omega, phi, H, d)
+    dev = q.device
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dvv = torch.empty_like(v)
+    dgamma = torch.empty(H, dtype=torch.float32, device=dev)
+    domega = torch.empty(H, d, dtype=torch.float32, device=dev)
+    dphi = torch.empty(H, d, dtype=torch.float32, device=dev) if want_dphi else None
+    ws_size = int(lib().sanatan_chunk_bwd_harmonic_workspace_size(B, H, T, d, dv,
+                                                                   int(harmonics)))
+    if workspace is None and ws_size > 0:
+        workspace = torch.empty(ws_size, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().sanatan_chunk_bwd_harmonic(_ptr(q), _ptr(k), _ptr(v), _DT[q.dtype], _ptr(gamma),
+                                          _ptr(omega), _ptr(phi), B, H, T, d, dv, int(pos0),
+                                          int(harmonics), float(eps), _ptr(S0), _ptr(z0), _ptr(o),
+                                          _ptr(D), _ptr(dO), _DT[dO.dtype], _ptr(dq), _ptr(dk),
+                                          _ptr(dvv), _ptr(dgamma), _ptr(domega), _ptr(dphi),
+                                          _ptr(workspace), ws_bytes, _stream(dev))
+    _check("sanatan_chunk_bwd_harmonic", st)
+    return dict(dq=dq, dk=dk, dv=dvv, dgamma=dgamma, domega=domega, dphi=dphi)
 
 
 def sanatan_decode_step_harmonic(S, z, q, k, v, gamma, omega, phi, pos, harmonics, eps=0.0):

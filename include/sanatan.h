@@ -320,6 +320,19 @@ SANATAN_API int sanatan_device_status(void* stream);
  *   6d replaced by F_N; no workspace); q, k, v f32 or bf16 (converted to f32);
  *   harmonics 1..3 (N >= 2: a cluster of eight CTAs per sequence, each
  *   holding the state rows of eight dimensions in registers).
+ * sanatan_chunk_bwd_harmonic -- gradients of sum(o * dO) for
+ *   sanatan_chunk_fwd_harmonic (the chain rule of the six-channel backward
+ *   with Phi_N; the pages give no backward).  Arguments, layouts and outputs
+ *   as sanatan_chunk_bwd (dq, dk, dv_out in in_dtype; dgamma [H], domega
+ *   [H, d] and dphi [H, d] (or NULL) float32, overwritten, summed over the
+ *   batch and both q and k), without the forward-workspace pair; harmonics
+ *   1..3.  workspace: at least sanatan_chunk_bwd_harmonic_workspace_size(...)
+ *   bytes (65 floats per token-head: dN = dO / (D + eps) and
+ *   dD = -(dO . o) / (D + eps); 0 for harmonics = 1, which runs the six-channel
+ *   float32 backward); its contents on entry do not matter.  Arithmetic in
+ *   float32 on the CUDA cores; float atomics make dgamma, domega, dphi vary in
+ *   their last bits between runs.  Errors as sanatan_chunk_bwd, and
+ *   SANATAN_ERR_INVALID for a workspace smaller than the size above.
  * sanatan_decode_step_harmonic -- one token of the recurrence with Phi_N for N
  *   slots, as sanatan_decode_step with S [N, F_N, dv] and z [N, F_N];
  *   harmonics 1..3.
@@ -336,6 +349,17 @@ SANATAN_API int sanatan_chunk_fwd_harmonic(const void* q, const void* k, const v
                                            int64_t pos0, int harmonics, float eps, const float* S0,
                                            const float* z0, float* o, float* D, float* S_out,
                                            float* z_out, void* stream);
+SANATAN_API size_t sanatan_chunk_bwd_harmonic_workspace_size(int B, int H, int T, int d, int dv,
+                                                             int harmonics);
+SANATAN_API int sanatan_chunk_bwd_harmonic(const void* q, const void* k, const void* v,
+                                           int in_dtype, const float* gamma, const float* omega,
+                                           const float* phi, int B, int H, int T, int d, int dv,
+                                           int64_t pos0, int harmonics, float eps,
+                                           const float* S0, const float* z0, const float* o,
+                                           const float* D, const void* dO, int grad_dtype,
+                                           void* dq, void* dk, void* dv_out, float* dgamma,
+                                           float* domega, float* dphi, void* workspace,
+                                           size_t workspace_bytes, void* stream);
 SANATAN_API int sanatan_decode_step_harmonic(float* S, float* z, const float* q, const float* k,
                                              const float* v, const float* gamma,
                                              const float* omega, const float* phi,

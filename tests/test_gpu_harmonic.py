@@ -1,8 +1,9 @@
 """The harmonic feature map (Appendix B of the notes) on the GPU against the
 float64 oracle: features (f32 <= 1e-5 abs), the chunked p=1 forward (f32:
 <= 1e-5 on o, state relative <= 1e-5; at the full layer-forward size <= 1e-4
-on o), the decode step (<= 1e-5), chunked vs decode (<= 1e-4), and N = 1
-against the six-channel entry points."""
+on o), the decode step (<= 1e-5), chunked vs decode (<= 1e-4), N = 1 against
+the six-channel entry points, and the backward (f32 gradients <= 1e-4
+relative; bf16 at the layer shape <= 1e-2, the gradient bar)."""
 import numpy as np
 import pytest
 import torch
@@ -136,3 +137,117 @@ def test_argument_errors():
     with pytest.raises(S.SanatanError) as e:
         S.sanatan_featurize_harmonic(g["q"], g["gamma"], g["omega"], g["phi"], 4)
     assert e.value.status == 2
+
+
+def _rel(a, b):
+    return rel_fro(f64(a), b)
+
+
+def _harmonic_grads(g, N, pos0, eps, S0=None, z0=None, dO=None, want_dphi=True):
+    o, D, _, _ = S.sanatan_chunk_fwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"],
+                                              g["phi"], N, pos0=pos0, eps=eps, S0=S0, z0=z0)
+    return S.sanatan_chunk_bwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"],
+                                        N, o, D, dO, pos0=pos0, eps=eps, S0=S0, z0=z0,
+                                        want_dphi=want_dphi)
+
+
+@pytest.mark.parametrize("N,T,hist", [(2, 1, False), (2, 17, True), (2, 100, False),
+                                      (3, 16, False), (3, 77, True)])
+def test_backward_matches_oracle(N, T, hist):
+    """f32 inputs: every gradient (dq, dk, dv, dgamma, domega, dphi) within 1e-4
+    relative (Frobenius) of the float64 oracle, with a history (S0, z0), eps and
+    a position offset."""
+    x = W.make(W.TINY, B=2, H=2, T=T)
+    x["phi"] = W.rates(2, 64, "geometric")
+    g = to_dev(x)
+    ra = ref_args(x)
+    rng = np.random.default_rng(5 + T)
+    dO = rng.standard_normal((2, 2, T, 64)).astype(np.float32)
+    S0 = z0 = S0t = z0t = None
+    if hist:
+        S0, z0 = O.final_state_harmonic(rng.standard_normal((2, 2, 12, 64)),
+                                        rng.standard_normal((2, 2, 12, 64)), ra["gamma"],
+                                        ra["omega"], ra["phi"], N, pos0=20)
+        S0t = torch.tensor(S0, dtype=torch.float32, device=dev())
+        z0t = torch.tensor(z0, dtype=torch.float32, device=dev())
+        S0, z0 = f64(S0t), f64(z0t)
+    gr = _harmonic_grads(g, N, 32, 0.3, S0t, z0t, torch.tensor(dO, device=dev()))
+    torch.cuda.synchronize()
+    ref = O.attn_harmonic_backward(**ra, dO=dO.astype(np.float64), N=N, pos0=32, eps=0.3, S0=S0,
+                                   z0=z0)
+    for key in ("dq", "dk", "dv", "dgamma", "domega"):
+        err = _rel(gr[key], ref[key])
+        assert err <= 1e-4, (key, err)
+    # dphi: the q and k shares (position x angle gradient) cancel up to the
+    # relative positions (exactly, at T = 1), so its error is measured against
+    # the larger of its own norm and the shares' size, position x |dq|, scaled
+    # to the 1e-6 relative accuracy of a float32 angle gradient (1e-2 x 1e-4)
+    scale = max(np.linalg.norm(ref["dphi"]), 1e-2 * (32 + T) * np.linalg.norm(ref["dq"]))
+    err = np.linalg.norm(f64(gr["dphi"]) - ref["dphi"]) / scale
+    assert err <= 1e-4, ("dphi", err)
+
+
+@pytest.mark.parametrize("N", [2, 3])
+def test_backward_full_size_sampled_heads(N):
+    """B=4, H=12, T=2048 bf16 (the layer-forward workload, one launch over all 48
+    sequences): for heads 0 and 11, dq, dk, dv of every sequence and the head's
+    dgamma, domega, dphi (sums over the batch) within 1e-2 relative of the
+    oracle (gradients are bf16 like the inputs)."""
+    x = W.make(W.LAYER, device="cpu")
+    g = to_dev(x)
+    dOt = torch.randn(x["q"].shape[:3] + (64,), generator=torch.Generator().manual_seed(77))
+    gr = _harmonic_grads(g, N, 0, 0.0, dO=dOt.to(torch.bfloat16).to(dev()))
+    torch.cuda.synchronize()
+    ra = ref_args(x)
+    dO = f64(dOt.to(torch.bfloat16))
+    for h in (0, 11):
+        one = {n: ra[n][:, h:h + 1] for n in ("q", "k", "v")}
+        one.update({n: ra[n][h:h + 1] for n in ("gamma", "omega", "phi")})
+        ref = O.attn_harmonic_backward(**one, dO=dO[:, h:h + 1], N=N)
+        for key in ("dq", "dk", "dv"):
+            err = rel_fro(f64(gr[key])[:, h:h + 1], ref[key])
+            assert err <= 1e-2, (h, key, err)
+        for key in ("dgamma", "domega", "dphi"):
+            err = rel_fro(f64(gr[key])[h:h + 1], ref[key])
+            assert err <= 1e-2, (h, key, err)
+
+
+def test_backward_one_harmonic_is_the_six_channel_path():
+    x = W.make(W.TINY, B=1, H=2, T=40)
+    g = to_dev(x)
+    dO = torch.randn(1, 2, 40, 64, generator=torch.Generator().manual_seed(3)).to(dev())
+    o, D, _, _ = S.sanatan_chunk_fwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"])
+    a = S.sanatan_chunk_bwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], 1,
+                                     o, D, dO, want_dphi=True)
+    b = S.sanatan_chunk_bwd(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], o, D, dO,
+                            want_dphi=True)
+    torch.cuda.synchronize()
+    for key in ("dq", "dk", "dv"):
+        assert torch.equal(a[key], b[key]), key
+    for key in ("dgamma", "domega", "dphi"):
+        assert (a[key] - b[key]).abs().max().item() <= 1e-5 * (1 + b[key].abs().max().item()), key
+
+
+def test_backward_empty_and_errors():
+    x = W.make(W.TINY, B=1, H=2, T=0)
+    g = to_dev(x)
+    o = torch.empty(1, 2, 0, 64, device=dev())
+    D = torch.empty(1, 2, 0, device=dev())
+    gr = S.sanatan_chunk_bwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], 2,
+                                      o, D, o, want_dphi=True)
+    torch.cuda.synchronize()
+    for key in ("dgamma", "domega", "dphi"):
+        assert torch.count_nonzero(gr[key]).item() == 0, key
+    x = W.make(W.TINY, B=1, H=1, T=4)
+    g = to_dev(x)
+    o = torch.zeros(1, 1, 4, 64, device=dev())
+    D = torch.ones(1, 1, 4, device=dev())
+    with pytest.raises(S.SanatanError) as e:
+        S.sanatan_chunk_bwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], 4,
+                                     o, D, o)
+    assert e.value.status == 2
+    with pytest.raises(S.SanatanError) as e:
+        S.sanatan_chunk_bwd_harmonic(g["q"], g["k"], g["v"], g["gamma"], g["omega"], g["phi"], 2,
+                                     o, D, o, workspace=torch.empty(16, dtype=torch.uint8,
+                                                                    device=dev()))
+    assert e.value.status == 1
