@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1) fsa_kernel(FsaParams prm) {
   const int bh = blockIdx.x / prm.seg_grid;
   const int seg = blockIdx.x % prm.seg_grid;
   const int h = bh % prm.H;
-  const int c_begin = static_cast<int>(static_cast<int64_t>(seg) * prm.nchunks / prm.nseg);
-  const int c_end = static_cast<int>(static_cast<int64_t>(seg + 1) * prm.nchunks / prm.nseg);
+  const int c_begin = seg_begin(seg, prm.nchunks, prm.nseg);
+  const int c_end = seg_begin(seg + 1, prm.nchunks, prm.nseg);
   const int nloc = c_end - c_begin;
   const int64_t seq_row0 = static_cast<int64_t>(bh) * prm.T;
 

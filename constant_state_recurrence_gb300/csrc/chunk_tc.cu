@@ -197,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1) sanatan_tc_kernel(const __grid_co
   const int seg = blockIdx.x / prm.bhn;
   const int bh = blockIdx.x % prm.bhn;
   const int h = bh % prm.H;
-  const int c_begin = static_cast<int>(static_cast<int64_t>(seg) * prm.nchunks / prm.nseg);
-  const int c_end = static_cast<int>(static_cast<int64_t>(seg + 1) * prm.nchunks / prm.nseg);
+  const int c_begin = seg_begin(seg, prm.nchunks, prm.nseg);
+  const int c_end = seg_begin(seg + 1, prm.nchunks, prm.nseg);
   const int nloc = c_end - c_begin;
   const int64_t seq_row0 = static_cast<int64_t>(bh) * prm.T;  // first token row of the sequence
   const bool last_seg = (seg == prm.nseg - 1);

@@ -24,6 +24,17 @@ constexpr int kSCCols = 80;          // compact state row stride (floats)
 // that the threads of a warp (one row each) read and write consecutive words.
 constexpr int kSCUsedCols = 68;
 __host__ __device__ constexpr int sc_tile_rows(int mt) { return mt < 2 ? 128 : kSCRows - 256; }
+// First chunk of segment `seg` when nchunks chunks are split into nseg
+// segments (nseg <= nchunks; seg = nseg gives nchunks).  Rounded up, so the
+// longer shares go to the first segments: segment 0 needs no earlier sums and
+// starts at once, while every later segment waits for the whole state-only
+// pass, so an extra chunk costs least there (16 chunks in 3 segments: 6, 5, 5).
+// Every kernel that reads or writes per-segment sums uses this split.
+__host__ __device__ constexpr int seg_begin(int seg, int nchunks, int nseg) {
+  return static_cast<int>((static_cast<long long>(seg) * nchunks + nseg - 1) / nseg);
+}
+static_assert(seg_begin(1, 16, 3) == 6 && seg_begin(2, 16, 3) == 11 && seg_begin(3, 16, 3) == 16,
+              "segment split");
 __host__ __device__ constexpr int sc_index(int f, int col) {
   return kSCUsedCols * (f & ~127) + col * sc_tile_rows(f >> 7) + (f & 127);
 }
